@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Decode throughput of the batch-invariant forward on GB300.
+
+One step = one greedy decode step of a Qwen3-8B-shaped random-init model (36
+layers, d 4096, 32/8 heads, head_dim 128, FFN 12288, vocab 151936) for a batch
+of 64 requests whose cached KV lengths are drawn uniform on [128, 4096]:
+embedding, per layer RMSNorm -> QKV GEMM -> RoPE + paged KV store -> split-KV
+attention + merge tree -> O GEMM (+residual) -> RMSNorm -> gate|up GEMM ->
+SwiGLU -> down GEMM (+residual), then final RMSNorm, lm-head (fp32 logits) and
+top-20.  All of it runs in libbi's kernels through bi_model_forward.
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
+on a bounded sample of the same workload instead.
+Multi-GPU: replicas only (every rank decodes its own batch; no collective on
+the data path); value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "invariant decode tok/s (8B-shape, B=1..64); GEMM TFLOP/s & attn GB/s vs peak"
+BATCH = 64
+KV_LO, KV_HI = 128, 4096
+TOPK = 20
+WORKLOAD = ("Qwen3-8B-shaped decode step (36 layers, d4096, 32/8 heads, hd128, FFN 12288, vocab 151936), "
+            "B=64 requests, cached KV lengths U{128..4096}, greedy top-20")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["invariant", "fast", "protected"], default="invariant")
+    ap.add_argument("--batch", type=int, default=BATCH)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import synth
+    import invariant_deterministic_02_gb300 as bi
+    from invariant_deterministic_02_gb300.model import QWEN3_8B, BiModel
+
+    torch.cuda.set_device(local_rank)
+    dev = "cuda"
+    mode = bi.MODES[args.mode]
+    B = args.batch
+    K, W = args.steps, args.warmup
+    shape = QWEN3_8B
+    Ls = synth.uniform_ints(B, KV_LO, KV_HI, args.seed + 17 * rank)  # KV length at the first step
+    total_steps = W + 2 * K + K  # warm-up, timed, profiled, end-to-end
+    pages = int(sum((int(L) + total_steps + 16) // 16 + 1 for L in Ls)) + 16
+    model = BiModel(shape, BiModel.random_weights(shape, seed=args.seed + 1000 * rank), num_pages=pages,
+                    page_seed=args.seed + 3)
+    for b in range(B):
+        model.install_history(b, int(Ls[b]) - 1, args.seed * 7919 + 131 * b + rank)
+    # block table covering every step; pos0 of step s is L_b - 1 + s
+    rows = [model.pool.ensure(b, int(Ls[b]) + total_steps) for b in range(B)]
+    max_pages = max(len(r) for r in rows)
+    bt = np.full((B, max_pages), -1, dtype=np.int32)
+    for b, r in enumerate(rows):
+        bt[b, :len(r)] = r
+    pos_all = (Ls[None, :].astype(np.int64) - 1 + np.arange(total_steps)[:, None]).astype(np.int32)
+    d_bt = torch.from_numpy(bt).to(dev)
+    d_qs = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    d_pos = torch.from_numpy(pos_all).to(dev)
+    ids = [torch.from_numpy(synth.token_ids(B, shape.vocab, args.seed + 5)).to(dev),
+           torch.empty(B, dtype=torch.int32, device=dev)]
+    logits = torch.empty((B, shape.vocab), dtype=torch.float32, device=dev)
+    tv = torch.empty((B, TOPK), dtype=torch.float32, device=dev)
+    ti = torch.empty((B, TOPK), dtype=torch.int32, device=dev)
+    target = 0 if args.mode == "protected" else -1
+
+    def batch_for(step):
+        return bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos[step].data_ptr(), d_bt.data_ptr(), max_pages, pages,
+                        target, 0 if target >= 0 else -1, 1 if target >= 0 else 0)
+
+    ws_bytes = bi.bi_model_workspace(model.dims, batch_for(0), mode)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    step = [0]
+
+    def one_step():
+        s = step[0]
+        src, dst = ids[s % 2], ids[(s + 1) % 2]
+        bi.bi_model_forward(model.dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s), model.k_ptrs,
+                            model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=dst, mode=mode, workspace=ws,
+                            ws_bytes=ws_bytes, stream=sp)
+        step[0] += 1
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    for _ in range(W):
+        one_step()
+    torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- timed region (device-resident inputs)
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ck = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / K
+    value = B * world * K / (ms / 1000.0)
+    assert bi.bi_device_error() == 0
+
+    # ---------------------------------------------------------------- profiled pass: per-kernel event timing
+    bi.bi_profile_start(K * 600)
+    p_step0 = step[0]
+    for _ in range(K):
+        one_step()
+    torch.cuda.synchronize()
+    bi.bi_profile_stop()
+    kern = {}
+    tot_ms = 0.0
+    for name in bi.bi_profile_kernels():
+        n, t = bi.bi_profile_read(name)
+        if n:
+            kern[name] = {"launches_per_step": n / K, "ms_per_step": t / K}
+            tot_ms += t / K
+    for v in kern.values():
+        v["share"] = v["ms_per_step"] / tot_ms if tot_ms > 0 else None
+    launches_per_step = sum(v["launches_per_step"] for v in kern.values())
+    # algorithmic bytes / flops of the profiled steps
+    L = shape.layer
+    kvlens = pos_all[p_step0:p_step0 + K] + 1  # [K][B]
+    kv_bytes_step = float(kvlens.sum(axis=1).mean()) * L.n_kv_heads * L.head_dim * 2 * 2 * shape.n_layers
+    q_bytes_step = B * L.n_q_heads * L.head_dim * 2 * shape.n_layers
+    gemm_shapes = [(L.qkv_dim, L.d_model), (L.d_model, L.n_q_heads * L.head_dim), (2 * L.ffn_dim, L.d_model),
+                   (L.d_model, L.ffn_dim)]
+    gemm_bytes_step, gemm_flops_step = 0.0, 0.0
+    for N, Kd in gemm_shapes:
+        gemm_bytes_step += shape.n_layers * (2 * (B * Kd + N * Kd) + 2 * B * N + (2 * B * N if N == L.d_model else 0))
+        gemm_flops_step += shape.n_layers * 2.0 * B * N * Kd
+    gemm_bytes_step += 2 * (B * L.d_model + shape.vocab * L.d_model) + 4 * B * shape.vocab
+    gemm_flops_step += 2.0 * B * shape.vocab * L.d_model
+    pk = peaks()
+    algo = {"attn_decode_split": (kv_bytes_step + q_bytes_step, "hbm"), "gemm": (gemm_bytes_step, "hbm")}
+    dom = max(kern.items(), key=lambda kv: kv[1]["ms_per_step"])[0]
+    roof_name = dom if dom in algo else max(algo, key=lambda n: kern.get(n, {}).get("ms_per_step", 0))
+    kb, bound = algo[roof_name]
+    kms = kern[roof_name]["ms_per_step"]
+    achieved = kb / (kms / 1000.0) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if os.path.exists(tpath):
+        tj = json.load(open(tpath))
+        ent = tj.get(roof_name)
+        if ent and ent.get("source_sha") == _source_sha(ent.get("source")) and ent.get("workload") == "bench":
+            traffic = ent.get("bytes_per_launch")
+    launches_roof = kern[roof_name]["launches_per_step"]
+    roofline = {"kernel": roof_name, "bound": bound, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": round(kb / launches_roof),
+                "launch_ms": round(kms / launches_roof, 5), "peak_src": pk["src"] + " hbm_gbs (STREAM-style copy)"}
+    others = {}
+    for n, (b_, _) in algo.items():
+        if n in kern and n != roof_name:
+            a = b_ / (kern[n]["ms_per_step"] / 1000.0) / 1e9
+            others[n] = {"achieved_GBs": round(a, 1), "frac_hbm": round(a / pk["hbm_gbs"], 4)}
+    if "gemm" in kern:
+        others.setdefault("gemm", {})["achieved_TFLOPs"] = round(gemm_flops_step / (kern["gemm"]["ms_per_step"] /
+                                                                                    1000.0) / 1e12, 2)
+
+    # ---------------------------------------------------------------- end to end through host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_ids = pin(synth.token_ids(B, shape.vocab, args.seed + 6))
+    h_qs = pin(np.arange(B + 1, dtype=np.int32))
+    h_bt = pin(bt)
+    h_out_i = torch.empty((B, TOPK), dtype=torch.int32).pin_memory()
+    h_out_v = torch.empty((B, TOPK), dtype=torch.float32).pin_memory()
+    h_pos_all = pin(pos_all)
+    d_ids = torch.empty(B, dtype=torch.int32, device=dev)
+    d_pos1 = torch.empty(B, dtype=torch.int32, device=dev)
+    h2d = d2h = 0
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        s = step[0]
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_pos1.copy_(h_pos_all[s], non_blocking=True)
+        d_qs.copy_(h_qs, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        h2d = 4 * (B + B + (B + 1)) + bt.nbytes
+        b_ = bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos1.data_ptr(), d_bt.data_ptr(), max_pages, pages, target,
+                      0 if target >= 0 else -1, 1 if target >= 0 else 0)
+        bi.bi_model_forward(model.dims, model.mw, model.rope_cos, model.rope_sin, d_ids, b_, model.k_ptrs,
+                            model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=None, mode=mode, workspace=ws,
+                            ws_bytes=ws_bytes, stream=sp)
+        h_out_i.copy_(ti, non_blocking=True)
+        h_out_v.copy_(tv, non_blocking=True)
+        d2h = h_out_i.numel() * 4 + h_out_v.numel() * 4
+        stream.synchronize()
+        h_ids[:] = h_out_i[:, 0]
+        step[0] += 1
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": round(B * world * K / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic: seeded random-init weights ~N(0,0.02), random token ids, "
+                                     "seeded N(0,1) KV history",
+            "config": {"workload": WORKLOAD, "batch_per_gpu": B, "kv_len": "U{%d..%d} seed %d" % (KV_LO, KV_HI,
+                                                                                            args.seed),
+                       "mode": args.mode, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2: ~15 GB weights + ~20 GB KV streamed per step"},
+            "clocks": ck, "e2e": e2e, "gpu_launches": int(round(launches_per_step * K)),
+            "roofline": roofline, "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
+                                                  for kk, vv in v.items()} for k, v in kern.items()},
+            "other_rooflines": others}
+    return line
+
+
+def _source_sha(rel):
+    import hashlib
+    if not rel:
+        return None
+    p = os.path.join(ROOT, rel)
+    if not os.path.exists(p):
+        return None
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------- oracle (CPU) arm
+class OracleSample:
+    """A bounded sample of the bench workload for the float64 CPU oracle.
+
+    One decode step of the same 64-request batch (same KV-length draw, seeded
+    weights and N(0,1) KV history) through one Qwen3-8B-shaped layer, plus the
+    lm-head and top-20 over a 1/16 slice of the vocabulary; the time is scaled
+    to 36 layers and the full vocabulary.
+    """
+
+    def __init__(self, args):
+        import oracle
+        import synth
+
+        self.oracle = oracle
+        self.shape = synth.QWEN3_8B_LAYER
+        self.B = args.batch
+        sh = self.shape
+        self.Ls = synth.uniform_ints(self.B, KV_LO, KV_HI, args.seed)
+        self.w = {k: v.double().numpy() for k, v in synth.layer_weights(sh, args.seed + 77).items()}
+        self.h = synth.normal((self.B, sh.d_model), args.seed + 78).double().numpy()
+        rng = np.random.default_rng(args.seed + 79)
+        self.hist = [(rng.standard_normal((int(L) - 1, sh.n_kv_heads, sh.head_dim)),
+                      rng.standard_normal((int(L) - 1, sh.n_kv_heads, sh.head_dim))) for L in self.Ls]
+        self.head = synth.normal((151936 // 16, sh.d_model), args.seed + 80, std=0.02).double().numpy()
+        self.text = ("one decode step of the %d-request batch through 1 of 36 Qwen3-8B-shaped layers plus "
+                     "lm-head/top-20 over 1/16 of the vocabulary (float64 numpy), time scaled x36 layers and "
+                     "x16 vocabulary" % self.B)
+
+    def step_seconds(self):
+        """Scaled seconds of one full decode step, and the CPU seconds actually spent."""
+        o, sh = self.oracle, self.shape
+        kv = o.OracleKV(1, sh.n_kv_heads, sh.head_dim)
+        for b, (K, V) in enumerate(self.hist):
+            kv.set(0, b, K, V)
+        a = time.perf_counter()
+        o.layer_forward(self.h, self.w, sh, kv, 0, [(b, 1) for b in range(self.B)], [int(L) - 1 for L in self.Ls])
+        t_layer = time.perf_counter() - a
+        a = time.perf_counter()
+        x = o.round_bf16(o.rmsnorm(self.h, np.ones(sh.d_model), sh.rms_eps))
+        o.topk(o.round_f32(o.gemm(x, self.head)), TOPK)
+        t_head = time.perf_counter() - a
+        return 36 * t_layer + 16 * t_head, t_layer + t_head
+
+
+def run_reference(args):
+    cores = len(os.sched_getaffinity(0))
+    smp = OracleSample(args)
+    for _ in range(max(0, args.warmup)):
+        smp.step_seconds()
+    scaled, spent = [], 0.0
+    for _ in range(args.steps):
+        t, c = smp.step_seconds()
+        scaled.append(t)
+        spent += c
+    value = args.batch / statistics.mean(scaled)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * statistics.mean(scaled), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded weights ~N(0,0.02), seeded N(0,1) KV history",
+            "config": {"workload": WORKLOAD, "batch_per_gpu": args.batch, "kv_len": "U{%d..%d} seed %d" % (
+                KV_LO, KV_HI, args.seed), "mode": "oracle (float64 definitions)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": smp.text + "; %.1f s of CPU work over %d steps" % (spent, args.steps)},
+            "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            smp = OracleSample(args)
+            runs = [smp.step_seconds() for _ in range(2)]
+            v = args.batch / statistics.mean(t for t, _ in runs)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
+                                    "kind": "oracle", "sample": smp.text + "; 2 steps, %.1f s of CPU work" %
+                                    sum(c for _, c in runs)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

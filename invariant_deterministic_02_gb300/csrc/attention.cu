@@ -1,0 +1,914 @@
+// Paged split-KV attention: decode and prefill share one split-reduction device function.
+//
+// Definition (devpress digest of "Defeating Nondeterminism in LLM Inference",
+// section 3.3; "Batch-Invariant Kernel" notes, section Flash Attention):
+//   out_h = sum_j softmax_j(q_h . k_j * scale) v_j   over keys j <= p (query position p)
+// The invariant schedule cuts the keys into fixed splits of 256 absolute
+// positions (never a fixed split COUNT), reduces every split at full width with
+// masked lanes contributing nothing, and combines the split states with a
+// pairwise tree over the split index padded to a constant depth.  Because the
+// cached and the new K/V of a request are one sequence in the paged cache, a
+// query's reduction order depends on its absolute position only: token-by-token
+// decode and any chunked prefill produce the same bits.
+//
+// Split state of one query head over a split: m = max z (log2 domain), l =
+// sum exp2(z - m), o = sum exp2(z - m) v, z = (q.k) * scale * log2(e).
+//
+// Thread mapping of the split function (one group of 128 threads = 4 warps):
+// warp w owns positions [64w, 64w+64) of the split; lane = 8*slot + c; slot is
+// the position within a step of 4, c picks dims {8c..8c+7} (and {64+8c..} for
+// head_dim 128).  Dot products: per-lane FMA chains in dim order, then a
+// xor-butterfly over the 8 lanes (offsets 4, 2, 1).  Sum of exponentials: lane
+// L adds positions 8L..8L+7 in order, then a 32-lane butterfly.  Weighted sum
+// of values: per-lane FMA chain over the slot's 16 positions in order, xor 8
+// then 16 across slots, then the four warp sums added warp 0 + 1 + 2 + 3.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace bi {
+namespace attn {
+
+constexpr int kGroupThreads = 128;
+constexpr int kSplit = BI_SPLIT_TOKENS;
+constexpr int kPage = BI_PAGE_SIZE;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxFastUnits = 64;
+constexpr int kPrefillQBlock = 16;
+constexpr int kPrefillGroups = 4;
+
+enum : int { kPlanInvariant = 0, kPlanFast = 1 };
+
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(kGroupThreads) : "memory");
+}
+
+// Per-group shared scratch of the split function.
+template <int HD, int G>
+struct SplitSmem {
+  float z[G][kSplit];        // scores (log2 domain), -inf where masked
+  float e[kSplit][G];        // exp2(z - m)
+  float o[4][G][HD];         // per-warp partial weighted sums
+  float m[G];
+  float l[G];
+  int page[kSplit / kPage + 1];  // physical pages of the split (global loader)
+};
+
+// Loaders return the 16-byte pieces of position `pp` (0..255 within the split)
+// that lane c owns: dims [8c, 8c+8) and, for head_dim 128, [64+8c, 64+8c+8).
+template <int HD>
+struct GlobalKV {
+  const __nv_bfloat16* kc;
+  const __nv_bfloat16* vc;
+  const int* page;  // smem: physical page of positions start + 16i ..
+  int start_off;    // start % 16
+  int hkv, g;
+  __device__ __forceinline__ const __nv_bfloat16* row(const __nv_bfloat16* base, int pp) const {
+    const int r = start_off + pp;
+    const int pg = page[r >> 4];
+    return base + ((static_cast<size_t>(pg) * hkv + g) * kPage + (r & 15)) * HD;
+  }
+  __device__ __forceinline__ void k(int pp, int c, uint4 (&out)[HD / 64]) const {
+    const __nv_bfloat16* p = row(kc, pp);
+#pragma unroll
+    for (int i = 0; i < HD / 64; ++i) out[i] = ld_stream(p + 64 * i + 8 * c);
+  }
+  __device__ __forceinline__ void v(int pp, int c, uint4 (&out)[HD / 64]) const {
+    const __nv_bfloat16* p = row(vc, pp);
+#pragma unroll
+    for (int i = 0; i < HD / 64; ++i) out[i] = ld_stream(p + 64 * i + 8 * c);
+  }
+};
+
+template <int HD>
+struct SmemKV {
+  const __nv_bfloat16* ks;  // [256][HD] positions start .. start+255
+  const __nv_bfloat16* vs;
+  __device__ __forceinline__ void k(int pp, int c, uint4 (&out)[HD / 64]) const {
+#pragma unroll
+    for (int i = 0; i < HD / 64; ++i) out[i] = *reinterpret_cast<const uint4*>(ks + pp * HD + 64 * i + 8 * c);
+  }
+  __device__ __forceinline__ void v(int pp, int c, uint4 (&out)[HD / 64]) const {
+#pragma unroll
+    for (int i = 0; i < HD / 64; ++i) out[i] = *reinterpret_cast<const uint4*>(vs + pp * HD + 64 * i + 8 * c);
+  }
+};
+
+// Query registers of one lane: q[hh][dims owned by lane c], as fp32.
+template <int HD, int G>
+struct QRegs {
+  float q[G][HD / 8];
+};
+
+template <int HD, int G>
+__device__ __forceinline__ void load_q(const __nv_bfloat16* qrow /* [Hq][HD] at head g*G */, int c, QRegs<HD, G>& qr) {
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+    for (int i = 0; i < HD / 64; ++i) {
+      const uint4 u = *reinterpret_cast<const uint4*>(qrow + hh * HD + 64 * i + 8 * c);
+      float f[8];
+      unpack8(u, f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qr.q[hh][8 * i + e] = f[e];
+    }
+  }
+}
+
+__host__ __device__ constexpr int outputs_per_thread(int HD, int G) { return (G * HD + kGroupThreads - 1) / kGroupThreads; }
+
+// The split reduction.  Executed by one 128-thread group; `valid` (1..256)
+// positions starting at the loader's origin take part.  On return every thread
+// holds its assigned weighted-sum outputs k = tid + 128*j (head k / HD, dim
+// k % HD) in `out`, and sm.m / sm.l hold the per-head max and sum.
+template <int HD, int G, class KV>
+__device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& kv, int valid, float scale_log2,
+                                             SplitSmem<HD, G>& sm, int group, float (&out)[outputs_per_thread(HD, G)]) {
+  constexpr int DPL = HD / 8;
+  const int tid = threadIdx.x % kGroupThreads;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int slot = lane >> 3;
+  const int c = lane & 7;
+
+  // ---- scores
+#pragma unroll 2
+  for (int i = 0; i < 16; ++i) {
+    const int pp = 64 * w + 4 * i + slot;
+    float dot[G];
+    if (pp < valid) {
+      uint4 kr[HD / 64];
+      kv.k(pp, c, kr);
+      float kf[DPL];
+#pragma unroll
+      for (int j = 0; j < HD / 64; ++j) {
+        float f[8];
+        unpack8(kr[j], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kf[8 * j + e] = f[e];
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        float a = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) a = __fmaf_rn(qr.q[hh][e], kf[e], a);
+        dot[hh] = a;
+      }
+    } else {
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) dot[hh] = 0.f;
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      float a = dot[hh];
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 4));
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      if (c == hh) sm.z[hh][pp] = (pp < valid) ? __fmul_rn(a, scale_log2) : -INFINITY;
+    }
+  }
+  group_sync(group);
+
+  // ---- per-head max (exact, order-free) and sum of exponentials (fixed order)
+  for (int hh = w; hh < G; hh += 4) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, sm.z[hh][8 * lane + j]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int pp = 8 * lane + j;
+      const float e = (pp < valid) ? exp2f(__fsub_rn(sm.z[hh][pp], mx)) : 0.f;
+      sm.e[pp][hh] = e;
+      s = __fadd_rn(s, e);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
+    if (lane == 0) {
+      sm.m[hh] = mx;
+      sm.l[hh] = s;
+    }
+  }
+  group_sync(group);
+
+  // ---- weighted sum of values
+  float acc[G][DPL];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.f;
+#pragma unroll 2
+  for (int i = 0; i < 16; ++i) {
+    const int pp = 64 * w + 4 * i + slot;
+    if (pp < valid) {
+      uint4 vr[HD / 64];
+      kv.v(pp, c, vr);
+      float vf[DPL];
+#pragma unroll
+      for (int j = 0; j < HD / 64; ++j) {
+        float f[8];
+        unpack8(vr[j], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vf[8 * j + e] = f[e];
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float p = sm.e[pp][hh];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[hh][e] = __fmaf_rn(p, vf[e], acc[hh][e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      float a = acc[hh][e];
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 8));
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 16));
+      acc[hh][e] = a;
+    }
+  if (slot == 0) {
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) sm.o[w][hh][64 * (e >> 3) + 8 * c + (e & 7)] = acc[hh][e];
+  }
+  group_sync(group);
+#pragma unroll
+  for (int j = 0; j < outputs_per_thread(HD, G); ++j) {
+    const int k = tid + kGroupThreads * j;
+    if (k < G * HD) {
+      const int hh = k / HD, d = k % HD;
+      out[j] = __fadd_rn(__fadd_rn(__fadd_rn(sm.o[0][hh][d], sm.o[1][hh][d]), sm.o[2][hh][d]), sm.o[3][hh][d]);
+    }
+  }
+}
+
+// Combination of two split states (a covers lower positions than b).  An empty
+// state (m = -inf) is an exact identity on either side.
+__device__ __forceinline__ void merge_state(float& m, float& l, float& o, float mb, float lb, float ob) {
+  if (mb == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = mb;
+    l = lb;
+    o = ob;
+    return;
+  }
+  const float mx = fmaxf(m, mb);
+  const float ea = exp2f(__fsub_rn(m, mx));
+  const float eb = exp2f(__fsub_rn(mb, mx));
+  l = __fadd_rn(__fmul_rn(ea, l), __fmul_rn(eb, lb));
+  o = __fadd_rn(__fmul_rn(ea, o), __fmul_rn(eb, ob));
+  m = mx;
+}
+
+// ------------------------------------------------------------------ decode
+// Plan per request b: geometry (invariant or fast), unit length, unit count,
+// exclusive prefix of unit counts.  One CTA; B may be large.
+struct DecodePlan {
+  int* mode;    // [B]
+  int* ulen;    // [B] positions per unit
+  int* nunits;  // [B]
+  int* prefix;  // [B+1]
+};
+
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict__ kv_lens, int B, int mode,
+                                                           int target, int fast_units_wanted, DecodePlan plan) {
+  __shared__ int part[1024];
+  const int t = threadIdx.x;
+  const int per = (B + 1023) / 1024;
+  const int b0 = min(B, t * per), b1 = min(B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int L = kv_lens[b];
+    const bool inv = (mode == BI_MODE_INVARIANT) || (mode == BI_MODE_PROTECTED && b == target);
+    int ul, n;
+    if (inv) {
+      ul = kSplit;
+      n = (L + kSplit - 1) / kSplit;
+    } else {
+      const int pages = (L + kPage - 1) / kPage;
+      int want = min(max(1, fast_units_wanted), min(kMaxFastUnits, max(1, pages)));
+      ul = kPage * ((pages + want - 1) / want);
+      n = (L + ul - 1) / ul;
+    }
+    if (L <= 0) n = 0;
+    plan.mode[b] = inv ? kPlanInvariant : kPlanFast;
+    plan.ulen[b] = ul;
+    plan.nunits[b] = n;
+    local += n;
+  }
+  part[t] = local;
+  __syncthreads();
+  // inclusive Hillis-Steele scan over the 1024 thread totals (integers: order-free)
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int v = (t >= off) ? part[t - off] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  int run = part[t] - local;
+  for (int b = b0; b < b1; ++b) {
+    plan.prefix[b] = run;
+    run += plan.nunits[b];
+  }
+  if (t == 1023) plan.prefix[B] = part[1023];
+}
+
+__device__ __forceinline__ int find_row(const int* prefix, int n, int u) {
+  // largest b with prefix[b] <= u (prefix is non-decreasing, prefix[n] > u)
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Partials {
+  float* m;  // [units][Hq]
+  float* l;  // [units][Hq]
+  float* o;  // [units][Hq][HD]
+};
+
+template <int HD, int G>
+__global__ void __launch_bounds__(kGroupThreads) decode_split_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vc,
+    const int* __restrict__ block_table, const int* __restrict__ kv_lens, int B, int hq, int hkv, int max_pages,
+    float scale_log2, DecodePlan plan, Partials part) {
+  __shared__ __align__(16) SplitSmem<HD, G> sm;
+  constexpr int OPT = outputs_per_thread(HD, G);
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int c = lane & 7;
+  const int total = plan.prefix[B] * hkv;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    const int u = item / hkv;
+    const int g = item % hkv;
+    const int b = find_row(plan.prefix, B, u);
+    const int s = u - plan.prefix[b];
+    const int L = kv_lens[b];
+    const int ul = plan.ulen[b];
+    const int ustart = s * ul;
+    const int uend = min(L, ustart + ul);
+    QRegs<HD, G> qr;
+    load_q<HD, G>(q + (static_cast<size_t>(b) * hq + g * G) * HD, c, qr);
+    float rm[G], rl[G], ro[OPT];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      rm[hh] = -INFINITY;
+      rl[hh] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < OPT; ++j) ro[j] = 0.f;
+    bool first = true;
+    for (int bs = ustart; bs < uend; bs += kSplit) {
+      const int valid = min(kSplit, uend - bs);
+      if (tid <= (kSplit / kPage)) {
+        const int pi = bs / kPage + tid;
+        sm.page[tid] = (pi * kPage < uend) ? block_table[static_cast<size_t>(b) * max_pages + pi] : 0;
+      }
+      group_sync(0);
+      GlobalKV<HD> kv{kc, vc, sm.page, bs % kPage, hkv, g};
+      float bo[OPT];
+      split_reduce<HD, G>(qr, kv, valid, scale_log2, sm, 0, bo);
+#pragma unroll
+      for (int j = 0; j < OPT; ++j) {
+        const int k = tid + kGroupThreads * j;
+        if (k < G * HD) {
+          const int hh = k / HD;
+          if (first) {
+            ro[j] = bo[j];
+          } else {
+            float mm = rm[hh], ll = rl[hh];
+            merge_state(mm, ll, ro[j], sm.m[hh], sm.l[hh], bo[j]);
+          }
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        if (first) {
+          rm[hh] = sm.m[hh];
+          rl[hh] = sm.l[hh];
+        } else {
+          float oo = 0.f;
+          merge_state(rm[hh], rl[hh], oo, sm.m[hh], sm.l[hh], 0.f);
+        }
+      }
+      first = false;
+      group_sync(0);  // smem reused by the next block / item
+    }
+    const size_t pidx = static_cast<size_t>(u) * hq + g * G;
+#pragma unroll
+    for (int j = 0; j < OPT; ++j) {
+      const int k = tid + kGroupThreads * j;
+      if (k < G * HD) part.o[(pidx + k / HD) * HD + (k % HD)] = ro[j];
+    }
+    if (tid < G) {
+      part.m[pidx + tid] = rm[tid];
+      part.l[pidx + tid] = rl[tid];
+    }
+  }
+}
+
+// Merge of the split states of one row (a decode request or a prefill token)
+// for all heads of one kv group: thread (hh, d).  INVARIANT rows combine the
+// states in a pairwise tree over the split index (binary-counter form: the same
+// tree as the level-by-level tree over 2^BI_MERGE_DEPTH leaves padded with
+// empty states, since an empty state is an exact identity); FAST rows combine
+// left to right.
+__device__ __forceinline__ void merge_row(const Partials& part, size_t first_unit, int n, bool tree, int hq, int hd,
+                                          int h, int d, float& out_m, float& out_l, float& out_o) {
+  float m = -INFINITY, l = 0.f, o = 0.f;
+  if (!tree) {
+    for (int s = 0; s < n; ++s) {
+      const size_t pi = (first_unit + s) * hq + h;
+      merge_state(m, l, o, part.m[pi], part.l[pi], part.o[pi * hd + d]);
+    }
+  } else {
+    float sm_[BI_MERGE_DEPTH + 1], sl_[BI_MERGE_DEPTH + 1], so_[BI_MERGE_DEPTH + 1];
+    unsigned occ = 0;
+    for (int s = 0; s < n; ++s) {
+      const size_t pi = (first_unit + s) * hq + h;
+      float cm = part.m[pi], cl = part.l[pi], co = part.o[pi * hd + d];
+      int lvl = 0;
+      while (occ & (1u << lvl)) {
+        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
+        merge_state(am, al, ao, cm, cl, co);  // stack entry covers the lower indices
+        cm = am; cl = al; co = ao;
+        occ &= ~(1u << lvl);
+        ++lvl;
+      }
+      sm_[lvl] = cm; sl_[lvl] = cl; so_[lvl] = co;
+      occ |= (1u << lvl);
+    }
+    // fold what is left, smallest (rightmost) subtree first: merge(stack[lvl], acc)
+    for (int lvl = 0; lvl <= BI_MERGE_DEPTH; ++lvl) {
+      if (occ & (1u << lvl)) {
+        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
+        merge_state(am, al, ao, m, l, o);
+        m = am; l = al; o = ao;
+      }
+    }
+  }
+  out_m = m;
+  out_l = l;
+  out_o = o;
+}
+
+__global__ void decode_merge_kernel(const Partials part, DecodePlan plan, __nv_bfloat16* __restrict__ out, int B,
+                                    int hq, int hkv, int hd) {
+  const int b = blockIdx.x / hkv;
+  const int g = blockIdx.x % hkv;
+  const int G = hq / hkv;
+  const int hh = threadIdx.x / hd;
+  const int d = threadIdx.x % hd;
+  if (b >= B || hh >= G) return;
+  const int h = g * G + hh;
+  float m, l, o;
+  merge_row(part, plan.prefix[b], plan.nunits[b], plan.mode[b] == kPlanInvariant, hq, hd, h, d, m, l, o);
+  const float r = (l > 0.f) ? __fdiv_rn(o, l) : 0.f;
+  reinterpret_cast<uint16_t*>(out)[(static_cast<size_t>(b) * hq + h) * hd + d] = to_bf16_bits(r);
+}
+
+// ------------------------------------------------------------------ prefill
+// Units are (q-block of up to 16 tokens of one request, split); the q-block's
+// tokens that see the split reduce it one after another with the same split
+// function as decode, reading the split's K/V from shared memory.
+//
+// INVARIANT splits of a token at position p: [256s, 256s+256) ∩ [0, p].
+// FAST splits (the non-invariant scheme in which cached and new tokens are
+// reduced separately): cached keys [0, pos0) cut at multiples of 256 from 0,
+// then new keys [pos0, p] cut at pos0 + multiples of 256.
+struct PrefillPlan {
+  int* tok_prefix;   // [T+1] exclusive prefix of per-token split counts
+  int* qb_req;       // [NQB]
+  int* qb_tok0;      // [NQB]
+  int* qb_ntok;      // [NQB]
+  int* qb_prefix;    // [NQB+1] exclusive prefix of per-q-block unit counts
+  int* counts;       // [2]: NQB, total units
+  int* req_mode;     // [B]
+};
+
+__device__ __forceinline__ int n_splits_token(bool inv, int pos0, int p) {
+  if (inv) return p / kSplit + 1;
+  return (pos0 + kSplit - 1) / kSplit + (p - pos0) / kSplit + 1;
+}
+
+// split index s of a token of request (pos0) -> [start, end) of keys, clipped to p
+__device__ __forceinline__ void split_range(bool inv, int pos0, int s, int p, int& start, int& end) {
+  if (inv) {
+    start = s * kSplit;
+    end = min(p + 1, start + kSplit);
+    return;
+  }
+  const int nc = (pos0 + kSplit - 1) / kSplit;
+  if (s < nc) {
+    start = s * kSplit;
+    end = min(pos0, start + kSplit);
+  } else {
+    start = pos0 + (s - nc) * kSplit;
+    end = min(p + 1, start + kSplit);
+  }
+}
+
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const int* __restrict__ q_start,
+                                                            const int* __restrict__ q_pos0, int B, int T, int mode,
+                                                            int target, PrefillPlan plan) {
+  __shared__ int part[1024];
+
+  const int t = threadIdx.x;
+  // phase 1: per-token split counts -> tok_prefix (tokens in order)
+  {
+    const int per = (T + 1023) / 1024;
+    const int t0 = min(T, t * per), t1 = min(T, t0 + per);
+    int local = 0;
+    int b = 0;
+    for (int tok = t0; tok < t1; ++tok) {
+      if (tok == t0) {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (q_start[mid] <= tok) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+      }
+      while (q_start[b + 1] <= tok) ++b;
+      const bool inv = (mode == BI_MODE_INVARIANT) || (mode == BI_MODE_PROTECTED && b == target);
+      const int p = q_pos0[b] + (tok - q_start[b]);
+      local += n_splits_token(inv, q_pos0[b], p);
+    }
+    part[t] = local;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      const int v = (t >= off) ? part[t - off] : 0;
+      __syncthreads();
+      part[t] += v;
+      __syncthreads();
+    }
+    int run = part[t] - local;
+    for (int tok = t0; tok < t1; ++tok) {
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (q_start[mid] <= tok) lo = mid; else hi = mid - 1;
+      }
+      const int bb = lo;
+      const bool inv = (mode == BI_MODE_INVARIANT) || (mode == BI_MODE_PROTECTED && bb == target);
+      const int p = q_pos0[bb] + (tok - q_start[bb]);
+      plan.tok_prefix[tok] = run;
+      run += n_splits_token(inv, q_pos0[bb], p);
+    }
+    if (t == 1023) plan.tok_prefix[T] = part[1023];
+    __syncthreads();
+  }
+  // phase 2: q-blocks of each request (sequential over requests in thread 0,
+  // then a parallel fill); counts per request are small integers.
+  if (t == 0) {
+    int nqb = 0, units = 0;
+    for (int b = 0; b < B; ++b) {
+      const bool inv = (mode == BI_MODE_INVARIANT) || (mode == BI_MODE_PROTECTED && b == target);
+      plan.req_mode[b] = inv ? kPlanInvariant : kPlanFast;
+      const int n = q_start[b + 1] - q_start[b];
+      for (int j = 0; j < n; j += kPrefillQBlock) {
+        const int cnt = min(kPrefillQBlock, n - j);
+        const int plast = q_pos0[b] + j + cnt - 1;
+        plan.qb_req[nqb] = b;
+        plan.qb_tok0[nqb] = q_start[b] + j;
+        plan.qb_ntok[nqb] = cnt;
+        plan.qb_prefix[nqb] = units;
+        units += n_splits_token(inv, q_pos0[b], plast);
+        ++nqb;
+      }
+    }
+    plan.qb_prefix[nqb] = units;
+    plan.counts[0] = nqb;
+    plan.counts[1] = units;
+
+  }
+}
+
+template <int HD, int G>
+struct PrefillSmem {
+  __nv_bfloat16 k[kSplit][HD];
+  __nv_bfloat16 v[kSplit][HD];
+  SplitSmem<HD, G> grp[kPrefillGroups];
+};
+
+template <int HD, int G>
+__global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vc,
+    const int* __restrict__ block_table, const int* __restrict__ q_pos0, const int* __restrict__ q_start, int hq,
+    int hkv, int max_pages, float scale_log2, PrefillPlan plan, Partials part) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  PrefillSmem<HD, G>& sm = *reinterpret_cast<PrefillSmem<HD, G>*>(smem_raw);
+  constexpr int OPT = outputs_per_thread(HD, G);
+  const int group = threadIdx.x / kGroupThreads;
+  const int tid = threadIdx.x % kGroupThreads;
+  const int c = (tid & 31) & 7;
+  const int nqb = plan.counts[0];
+  const int total = plan.counts[1] * hkv;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    const int u = item / hkv;
+    const int g = item % hkv;
+    const int qb = find_row(plan.qb_prefix, nqb, u);
+    const int s = u - plan.qb_prefix[qb];
+    const int b = plan.qb_req[qb];
+    const int tok0 = plan.qb_tok0[qb];
+    const int ntok = plan.qb_ntok[qb];
+    const int pos0 = q_pos0[b];
+    const int p_first = pos0 + (tok0 - q_start[b]);
+    const int p_last = p_first + ntok - 1;
+    const bool inv = plan.req_mode[b] == kPlanInvariant;
+    int st, en;
+    split_range(inv, pos0, s, p_last, st, en);
+    // stage keys/values [st, en) of kv head g
+    const int rows = en - st;
+    constexpr int CH = HD / 8;  // 16-byte chunks per row
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * CH; idx += blockDim.x) {
+      const int r = idx / CH, ch = idx % CH;
+      const int pos = st + r;
+      const int pg = block_table[static_cast<size_t>(b) * max_pages + pos / kPage];
+      const size_t off = ((static_cast<size_t>(pg) * hkv + g) * kPage + (pos % kPage)) * HD + ch * 8;
+      *reinterpret_cast<uint4*>(&sm.k[r][ch * 8]) = *reinterpret_cast<const uint4*>(kc + off);
+      *reinterpret_cast<uint4*>(&sm.v[r][ch * 8]) = *reinterpret_cast<const uint4*>(vc + off);
+    }
+    __syncthreads();
+    SmemKV<HD> kv{&sm.k[0][0], &sm.v[0][0]};
+    for (int qi = group; qi < ntok; qi += kPrefillGroups) {
+      const int tok = tok0 + qi;
+      const int p = p_first + qi;
+      if (s >= n_splits_token(inv, pos0, p)) continue;  // this split lies after the token
+      int st_t, en_t;
+      split_range(inv, pos0, s, p, st_t, en_t);
+      const int valid = en_t - st_t;  // >= 1; same origin st as the staged rows
+      QRegs<HD, G> qr;
+      load_q<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
+      float bo[OPT];
+      split_reduce<HD, G>(qr, kv, valid, scale_log2, sm.grp[group], group, bo);
+      const size_t pidx = (static_cast<size_t>(plan.tok_prefix[tok]) + s) * hq + g * G;
+#pragma unroll
+      for (int j = 0; j < OPT; ++j) {
+        const int k = tid + kGroupThreads * j;
+        if (k < G * HD) part.o[(pidx + k / HD) * HD + (k % HD)] = bo[j];
+      }
+      if (tid < G) {
+        part.m[pidx + tid] = sm.grp[group].m[tid];
+        part.l[pidx + tid] = sm.grp[group].l[tid];
+      }
+      group_sync(group);  // group scratch reused by the next token
+    }
+  }
+}
+
+__global__ void prefill_merge_kernel(const Partials part, PrefillPlan plan, const int* __restrict__ q_start,
+                                     const int* __restrict__ q_pos0, int B, __nv_bfloat16* __restrict__ out, int hq,
+                                     int hkv, int hd) {
+  const int tok = blockIdx.x / hkv;
+  const int g = blockIdx.x % hkv;
+  const int G = hq / hkv;
+  const int hh = threadIdx.x / hd;
+  const int d = threadIdx.x % hd;
+  if (hh >= G) return;
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (q_start[mid] <= tok) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int h = g * G + hh;
+  const int n = plan.tok_prefix[tok + 1] - plan.tok_prefix[tok];
+  float m, l, o;
+  merge_row(part, plan.tok_prefix[tok], n, plan.req_mode[b] == kPlanInvariant, hq, hd, h, d, m, l, o);
+  const float r = (l > 0.f) ? __fdiv_rn(o, l) : 0.f;
+  reinterpret_cast<uint16_t*>(out)[(static_cast<size_t>(tok) * hq + h) * hd + d] = to_bf16_bits(r);
+}
+
+// ------------------------------------------------------------------ host side
+bi_status check_dims(const bi_attn_dims* dm) {
+  BI_REQUIRE(dm != nullptr, BI_ERR_INVALID_ARG, "attention: null dims");
+  BI_REQUIRE(dm->head_dim == 64 || dm->head_dim == 128, BI_ERR_UNSUPPORTED, "attention: head_dim %d (64 or 128)",
+             dm->head_dim);
+  BI_REQUIRE(dm->num_kv_heads >= 1 && dm->num_q_heads >= dm->num_kv_heads &&
+                 dm->num_q_heads % dm->num_kv_heads == 0,
+             BI_ERR_INVALID_ARG, "attention: heads %d/%d", dm->num_q_heads, dm->num_kv_heads);
+  const int G = dm->num_q_heads / dm->num_kv_heads;
+  BI_REQUIRE(G == 1 || G == 2 || G == 4, BI_ERR_UNSUPPORTED, "attention: %d query heads per kv head (1, 2 or 4)", G);
+  BI_REQUIRE(dm->page_size == kPage, BI_ERR_UNSUPPORTED, "attention: page_size %d (must be %d)", dm->page_size, kPage);
+  BI_REQUIRE(dm->max_pages >= 1 && dm->num_pages >= 1, BI_ERR_INVALID_ARG, "attention: max_pages/num_pages");
+  BI_REQUIRE(dm->scale > 0.f && dm->scale == dm->scale, BI_ERR_INVALID_ARG, "attention: scale must be > 0");
+  const int64_t max_tokens = static_cast<int64_t>(dm->max_pages) * kPage;
+  BI_REQUIRE((max_tokens + kSplit - 1) / kSplit <= (int64_t(1) << BI_MERGE_DEPTH), BI_ERR_UNSUPPORTED,
+             "attention: max_pages*16 beyond the merge depth");
+  return BI_OK;
+}
+
+int max_units_per_request(const bi_attn_dims* dm) {
+  const int inv = (dm->max_pages * kPage + kSplit - 1) / kSplit;
+  return std::max(inv, kMaxFastUnits);
+}
+
+struct DecodeWs {
+  DecodePlan plan;
+  Partials part;
+  size_t bytes;
+};
+
+DecodeWs carve_decode(void* ws, size_t cap, int B, const bi_attn_dims* dm) {
+  WsCarver cv(ws, cap);
+  DecodeWs r;
+  r.plan.mode = cv.take<int>(B);
+  r.plan.ulen = cv.take<int>(B);
+  r.plan.nunits = cv.take<int>(B);
+  r.plan.prefix = cv.take<int>(B + 1);
+  const size_t units = static_cast<size_t>(B) * max_units_per_request(dm);
+  r.part.m = cv.take<float>(units * dm->num_q_heads);
+  r.part.l = cv.take<float>(units * dm->num_q_heads);
+  r.part.o = cv.take<float>(units * dm->num_q_heads * dm->head_dim);
+  r.bytes = cv.used;
+  return r;
+}
+
+struct PrefillWs {
+  PrefillPlan plan;
+  Partials part;
+  size_t bytes;
+};
+
+int64_t max_prefill_qblocks(int B, int T) { return static_cast<int64_t>(B) + T / kPrefillQBlock + 1; }
+
+PrefillWs carve_prefill(void* ws, size_t cap, int B, int T, const bi_attn_dims* dm) {
+  WsCarver cv(ws, cap);
+  PrefillWs r;
+  const int64_t nqb = max_prefill_qblocks(B, T);
+  r.plan.tok_prefix = cv.take<int>(T + 1);
+  r.plan.qb_req = cv.take<int>(nqb);
+  r.plan.qb_tok0 = cv.take<int>(nqb);
+  r.plan.qb_ntok = cv.take<int>(nqb);
+  r.plan.qb_prefix = cv.take<int>(nqb + 1);
+  r.plan.counts = cv.take<int>(2);
+  r.plan.req_mode = cv.take<int>(B);
+  // per token at most ceil(max_tokens/256) + 1 splits (FAST adds one cut at pos0)
+  const size_t per_tok = (static_cast<size_t>(dm->max_pages) * kPage + kSplit - 1) / kSplit + 1;
+  const size_t units = static_cast<size_t>(T) * per_tok;
+  r.part.m = cv.take<float>(units * dm->num_q_heads);
+  r.part.l = cv.take<float>(units * dm->num_q_heads);
+  r.part.o = cv.take<float>(units * dm->num_q_heads * dm->head_dim);
+  r.bytes = cv.used;
+  return r;
+}
+
+template <int HD, int G>
+int decode_grid() {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<HD, G>, kGroupThreads, 0) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  return per_sm * num_sms();
+}
+
+template <int HD, int G>
+bi_status decode_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* kv_lens,
+                        int B, const bi_attn_dims* dm, void* out, bi_mode mode, int target, const DecodeWs& w,
+                        cudaStream_t s) {
+  const int fast_units = std::max(1, (4 * num_sms() + B * dm->num_kv_heads - 1) / (B * dm->num_kv_heads));
+  BI_TIMED(::bi::kTagAttnPlan, s, decode_plan_kernel<<<1, 1024, 0, s>>>(kv_lens, B, static_cast<int>(mode), target, fast_units, w.plan));
+  BI_LAUNCH_CHECK();
+  const float sl2 = dm->scale * kLog2e;
+  BI_TIMED(::bi::kTagAttnDecodeSplit, s, decode_split_kernel<HD, G><<<decode_grid<HD, G>(), kGroupThreads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
+      static_cast<const __nv_bfloat16*>(vc), bt, kv_lens, B, dm->num_q_heads, dm->num_kv_heads, dm->max_pages, sl2,
+      w.plan, w.part));
+  BI_LAUNCH_CHECK();
+  BI_TIMED(::bi::kTagAttnDecodeMerge, s, decode_merge_kernel<<<B * dm->num_kv_heads, G * HD, 0, s>>>(w.part, w.plan, static_cast<__nv_bfloat16*>(out), B,
+                                                              dm->num_q_heads, dm->num_kv_heads, HD));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+template <int HD, int G>
+bi_status prefill_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* q_start,
+                         const int32_t* q_pos0, int B, int T, const bi_attn_dims* dm, void* out, bi_mode mode,
+                         int target, const PrefillWs& w, cudaStream_t s) {
+  BI_TIMED(::bi::kTagAttnPlan, s, prefill_plan_kernel<<<1, 1024, 0, s>>>(q_start, q_pos0, B, T, static_cast<int>(mode), target, w.plan));
+  BI_LAUNCH_CHECK();
+  const size_t smem = sizeof(PrefillSmem<HD, G>);
+  static bool attr_set = false;
+  if (!attr_set) {
+    BI_CUDA_TRY(cudaFuncSetAttribute(prefill_split_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)));
+    attr_set = true;
+  }
+  const float sl2 = dm->scale * kLog2e;
+  BI_TIMED(::bi::kTagAttnPrefillSplit, s, prefill_split_kernel<HD, G><<<num_sms(), kGroupThreads * kPrefillGroups, smem, s>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
+      static_cast<const __nv_bfloat16*>(vc), bt, q_pos0, q_start, dm->num_q_heads, dm->num_kv_heads, dm->max_pages,
+      sl2, w.plan, w.part));
+  BI_LAUNCH_CHECK();
+  BI_TIMED(::bi::kTagAttnPrefillMerge, s, prefill_merge_kernel<<<T * dm->num_kv_heads, G * HD, 0, s>>>(w.part, w.plan, q_start, q_pos0, B,
+                                                               static_cast<__nv_bfloat16*>(out), dm->num_q_heads,
+                                                               dm->num_kv_heads, HD));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+#define BI_ATTN_DISPATCH(FN, ...)                                           \
+  do {                                                                      \
+    const int G_ = dims->num_q_heads / dims->num_kv_heads;                  \
+    if (dims->head_dim == 128) {                                            \
+      if (G_ == 1) return FN<128, 1>(__VA_ARGS__);                          \
+      if (G_ == 2) return FN<128, 2>(__VA_ARGS__);                          \
+      return FN<128, 4>(__VA_ARGS__);                                       \
+    }                                                                       \
+    if (G_ == 1) return FN<64, 1>(__VA_ARGS__);                             \
+    if (G_ == 2) return FN<64, 2>(__VA_ARGS__);                             \
+    return FN<64, 4>(__VA_ARGS__);                                          \
+  } while (0)
+
+}  // namespace attn
+
+bi_status decode_attention_impl(const void* q, const void* kc, const void* vc, const int32_t* bt,
+                                const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, void* out, bi_mode mode,
+                                int32_t target, void* ws, size_t ws_bytes, cudaStream_t s) {
+  clear_error();
+  BI_TRY(attn::check_dims(dims));
+  BI_REQUIRE(B >= 0, BI_ERR_INVALID_ARG, "bi_decode_attention: B=%d", B);
+  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+             static_cast<int>(mode));
+  BI_REQUIRE(mode != BI_MODE_PROTECTED || target < B, BI_ERR_INVALID_ARG, "target_request %d >= B %d", target, B);
+  if (B == 0) return BI_OK;
+  BI_REQUIRE(q && kc && vc && bt && kv_lens && out, BI_ERR_INVALID_ARG, "bi_decode_attention: null pointer");
+  BI_REQUIRE(aligned16(q) && aligned16(kc) && aligned16(vc) && aligned16(out), BI_ERR_INVALID_ARG,
+             "bi_decode_attention: q/caches/out must be 16-byte aligned");
+  attn::DecodeWs w = attn::carve_decode(ws, ws_bytes, B, dims);
+  BI_REQUIRE(ws != nullptr && w.bytes <= ws_bytes, BI_ERR_WORKSPACE, "bi_decode_attention: workspace %zu < %zu",
+             ws_bytes, w.bytes);
+  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, out, mode,
+                   mode == BI_MODE_PROTECTED ? target : -1, w, s);
+}
+
+bi_status prefill_attention_impl(const void* q, const void* kc, const void* vc, const int32_t* bt,
+                                 const int32_t* q_start, const int32_t* q_pos0, int32_t B, int32_t T,
+                                 const bi_attn_dims* dims, void* out, bi_mode mode, int32_t target, void* ws,
+                                 size_t ws_bytes, cudaStream_t s) {
+  clear_error();
+  BI_TRY(attn::check_dims(dims));
+  BI_REQUIRE(B >= 0 && T >= 0 && (B > 0 || T == 0), BI_ERR_INVALID_ARG, "bi_prefill_attention: B=%d T=%d", B, T);
+  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+             static_cast<int>(mode));
+  BI_REQUIRE(mode != BI_MODE_PROTECTED || target < B, BI_ERR_INVALID_ARG, "target_request %d >= B %d", target, B);
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(q && kc && vc && bt && q_start && q_pos0 && out, BI_ERR_INVALID_ARG, "bi_prefill_attention: null pointer");
+  BI_REQUIRE(aligned16(q) && aligned16(kc) && aligned16(vc) && aligned16(out), BI_ERR_INVALID_ARG,
+             "bi_prefill_attention: q/caches/out must be 16-byte aligned");
+  attn::PrefillWs w = attn::carve_prefill(ws, ws_bytes, B, T, dims);
+  BI_REQUIRE(ws != nullptr && w.bytes <= ws_bytes, BI_ERR_WORKSPACE, "bi_prefill_attention: workspace %zu < %zu",
+             ws_bytes, w.bytes);
+  BI_ATTN_DISPATCH(attn::prefill_launch, q, kc, vc, bt, q_start, q_pos0, B, T, dims, out, mode,
+                   mode == BI_MODE_PROTECTED ? target : -1, w, s);
+}
+
+size_t decode_attention_ws(int32_t B, const bi_attn_dims* dims) {
+  if (B <= 0 || attn::check_dims(dims) != BI_OK) return 0;
+  return attn::carve_decode(nullptr, 0, B, dims).bytes;
+}
+
+size_t prefill_attention_ws(int32_t B, int32_t T, const bi_attn_dims* dims) {
+  if (B <= 0 || T <= 0 || attn::check_dims(dims) != BI_OK) return 0;
+  return attn::carve_prefill(nullptr, 0, B, T, dims).bytes;
+}
+
+}  // namespace bi
+
+extern "C" size_t bi_decode_attention_workspace(int32_t B, const bi_attn_dims* dims, bi_mode) {
+  return bi::decode_attention_ws(B, dims);
+}
+
+extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, const int32_t* kv_lens, int32_t B,
+                                         const bi_attn_dims* dims, void* out, bi_mode mode, int32_t target_request,
+                                         void* workspace, size_t ws_bytes, bi_stream s) {
+  return bi::decode_attention_impl(q, k_cache, v_cache, block_table, kv_lens, B, dims, out, mode, target_request,
+                                   workspace, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+extern "C" size_t bi_prefill_attention_workspace(int32_t B, int32_t T, const bi_attn_dims* dims, bi_mode) {
+  return bi::prefill_attention_ws(B, T, dims);
+}
+
+extern "C" bi_status bi_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_table, const int32_t* q_start, const int32_t* q_pos0,
+                                          int32_t B, int32_t T, const bi_attn_dims* dims, void* out, bi_mode mode,
+                                          int32_t target_request, void* workspace, size_t ws_bytes, bi_stream s) {
+  return bi::prefill_attention_impl(q, k_cache, v_cache, block_table, q_start, q_pos0, B, T, dims, out, mode,
+                                    target_request, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}

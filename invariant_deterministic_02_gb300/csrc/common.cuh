@@ -1,0 +1,142 @@
+// Shared host/device helpers of libbi.  Compiled for sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/bi.h"
+
+namespace bi {
+
+// ------------------------------------------------------------------ host-side error reporting
+void set_error(const char* fmt, ...);
+void clear_error();
+int num_sms();  // SM count of the current device (cached per device)
+
+#define BI_REQUIRE(cond, code, ...)     \
+  do {                                  \
+    if (!(cond)) {                      \
+      ::bi::set_error(__VA_ARGS__);     \
+      return code;                      \
+    }                                   \
+  } while (0)
+
+#define BI_CUDA_TRY(expr)                                                                        \
+  do {                                                                                           \
+    cudaError_t e_ = (expr);                                                                     \
+    if (e_ != cudaSuccess) {                                                                     \
+      ::bi::set_error("%s failed: %s (%s:%d)", #expr, cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return BI_ERR_CUDA;                                                                        \
+    }                                                                                            \
+  } while (0)
+
+#define BI_LAUNCH_CHECK()                                                                        \
+  do {                                                                                           \
+    cudaError_t e_ = cudaGetLastError();                                                         \
+    if (e_ != cudaSuccess) {                                                                     \
+      ::bi::set_error("kernel launch failed: %s (%s:%d)", cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return BI_ERR_CUDA;                                                                        \
+    }                                                                                            \
+  } while (0)
+
+#define BI_TRY(expr)              \
+  do {                            \
+    bi_status st_ = (expr);       \
+    if (st_ != BI_OK) return st_; \
+  } while (0)
+
+// Kernel tags of the optional launch timer (names in api.cu, same order).
+enum KernelTag : int {
+  kTagRmsnorm = 0,
+  kTagRmsnormSplit,
+  kTagGemm,
+  kTagSplitkReduce,
+  kTagAttnPlan,
+  kTagAttnDecodeSplit,
+  kTagAttnDecodeMerge,
+  kTagAttnPrefillSplit,
+  kTagAttnPrefillMerge,
+  kTagQkvRope,
+  kTagSwiglu,
+  kTagEmbed,
+  kTagTopk,
+  kTagBatchIndex,
+  kTagGather,
+  kTagRopeTable,
+  kTagCount
+};
+extern volatile int g_profiling;
+int prof_begin(int tag, cudaStream_t s);  // -1 when not recording
+void prof_end(int slot, cudaStream_t s);
+
+// Launch a kernel, bracketed by timing events when the launch timer is on.
+#define BI_TIMED(tag, stream, ...)                                            \
+  do {                                                                        \
+    const int prof_slot_ = ::bi::g_profiling ? ::bi::prof_begin((tag), (stream)) : -1; \
+    __VA_ARGS__;                                                              \
+    if (prof_slot_ >= 0) ::bi::prof_end(prof_slot_, (stream));                \
+  } while (0)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Bump allocator over a caller-owned workspace (host-side bookkeeping only).
+struct WsCarver {
+  char* base;
+  size_t cap;
+  size_t used = 0;
+  WsCarver(void* b, size_t c) : base(static_cast<char*>(b)), cap(c) {}
+  template <typename T>
+  T* take(size_t count) {
+    used = align_up(used, 256);
+    T* p = reinterpret_cast<T*>(base ? base + used : nullptr);
+    used += count * sizeof(T);
+    return p;
+  }
+  bool ok() const { return used <= cap; }
+};
+
+// ------------------------------------------------------------------ device helpers
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// fp32 -> bf16 with round-to-nearest-even (the hardware conversion).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float v) {
+  __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+  f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+  f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// Loads that bypass L1 allocation for streamed-once data.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+}  // namespace bi

@@ -1,0 +1,735 @@
+// Batch-invariant bf16 GEMM on the sm_103a tensor cores (tcgen05 + TMEM, fed by TMA).
+//
+// C[i][j] = sum_k A[i][k] * W[j][k]  (+ residual[i][j]), fp32 accumulation.
+// (devpress digest of "Defeating Nondeterminism in LLM Inference", section 3.2:
+// a matmul is pointwise products plus a reduction over k; it stays batch
+// invariant when every output tile reduces its whole K range inside one core
+// with one kernel configuration for every M, i.e. no split-K.  "Batch-Invariant
+// Kernel" notes, section GEMM: the K split may depend on K only.)
+//
+// Reduction geometry, identical for every M, N and CTA shape:
+//   * one tensor-core instruction shape: tcgen05.mma.cta_group::1.kind::f16,
+//     M=128, N=64, K=16, bf16 operands from shared memory (128-byte swizzled,
+//     K-major), fp32 accumulator in tensor memory;
+//   * the K range is consumed in 64-wide k-tiles in ascending order, four
+//     instructions of K=16 per k-tile in ascending order; the first
+//     instruction of an output tile overwrites the accumulator, all others add.
+// An output element therefore sees the same instruction sequence with the
+// same operands whatever M is, whichever CTA computes it and however many
+// 64-column instruction tiles a CTA covers.  The CTA column extent (64, 128 or
+// 256 columns = 1, 2 or 4 instructions per k-step) and the persistent
+// tile-to-CTA mapping are scheduling choices that never touch an element's
+// arithmetic.
+//
+// FAST mode (the non-invariant schedule used to measure the cost of
+// invariance): when there are fewer tiles than SMs the K range is split over
+// several CTAs and the fp32 partials are added in a second pass, so an
+// element's rounding depends on M.  PROTECTED: tiles holding target rows are
+// never split.
+//
+// Roles in a CTA of 192 threads: warp 0 issues TMA loads, warp 1 owns the tensor
+// memory and issues the MMAs (one thread), warps 2-5 drain the accumulator
+// (tcgen05.ld) and store.  Shared-memory stages and two tensor-memory
+// accumulators are handed between roles with mbarriers.  Every wait is bounded:
+// when one runs out the kernel records a site code in a device error word,
+// stops all roles, waits (bounded) for its own copies and MMAs, frees its
+// tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "common.cuh"
+
+namespace bi {
+namespace gemm {
+
+constexpr int kBM = 128;        // instruction / tile rows
+constexpr int kBN = 64;         // instruction columns
+constexpr int kBK = 64;         // k-tile (128 bytes of bf16: one swizzle row)
+constexpr int kUK = 16;         // instruction K
+constexpr int kThreads = 192;
+constexpr int kATileBytes = kBM * kBK * 2;  // 16 KiB
+constexpr int kBSubBytes = kBN * kBK * 2;   // 8 KiB per 64-column instruction tile
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxStages = 8;
+constexpr int kMaxSplitK = 16;
+
+__device__ unsigned int g_err_word = 0;
+
+enum OutKind : int { kOutBF16 = 0, kOutF32 = 1 };
+
+struct Args {
+  int M, N, K;
+  int m_tiles, n_tiles;  // n_tiles counts CTA-wide column tiles (64*W wide)
+  int splits;            // K splits of unprotected tiles
+  int tm0, tm1;          // m-tiles [tm0, tm1) are never split
+  int units;             // total work units
+  int kb_total;          // k-tiles in K
+  int kb_per;            // k-tiles per split
+  void* C;
+  const __nv_bfloat16* R;  // residual or null
+  float* partial;          // [splits][M][N] fp32 (split units only)
+  int out_kind;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded wait, slow path.  Returns false (after recording `site`) when the
+// limit runs out or another role has already aborted.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort_flag) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        atomicCAS(&g_err_word, 0u, static_cast<unsigned>(site));
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, site);
+}
+
+// Time-bounded wait that ignores the abort flag (used while draining after an abort).
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity) && global_ns() - t0 < kWaitLimitNs) {
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor
+// version 1, base offset 0 (tiles are 1024-byte aligned).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;    // leading byte offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;  // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;           // version
+  d |= static_cast<uint64_t>(2) << 61;           // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N=64, M=128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
+                            (static_cast<uint32_t>(kBM >> 4) << 24);
+
+// unit -> (m tile, n tile, split index, split count)
+__device__ __forceinline__ void unit_coords(const Args& a, int u, int& mt, int& nt, int& s, int& nsplit) {
+  const int prot = a.tm1 - a.tm0;
+  const int per_col = prot + (a.m_tiles - prot) * a.splits;
+  nt = u / per_col;
+  int r = u % per_col;
+  const int before = a.tm0 * a.splits;
+  if (r < before) {
+    mt = r / a.splits;
+    s = r % a.splits;
+    nsplit = a.splits;
+  } else if (r < before + prot) {
+    mt = a.tm0 + (r - before);
+    s = 0;
+    nsplit = 1;
+  } else {
+    r -= before + prot;
+    mt = a.tm1 + r / a.splits;
+    s = r % a.splits;
+    nsplit = a.splits;
+  }
+}
+
+__device__ __forceinline__ void k_range(const Args& a, int s, int nsplit, int& kb0, int& kb1) {
+  if (nsplit == 1) {
+    kb0 = 0;
+    kb1 = a.kb_total;
+  } else {
+    kb0 = s * a.kb_per;
+    kb1 = min(a.kb_total, kb0 + a.kb_per);
+  }
+}
+
+template <int W>
+struct Layout {
+  static constexpr int kStageBytes = kATileBytes + W * kBSubBytes;
+  static constexpr int kStages = (kSmemBudget / kStageBytes) < kMaxStages ? (kSmemBudget / kStageBytes) : kMaxStages;
+  static constexpr int kTmemCols = 2 * W * kBN;  // two accumulators (64, 128 or 256 columns each)
+  static constexpr int kBarBytes = 256;  // 2*kStages+5 mbarriers, tmem slot, abort flag
+  static constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + kBarBytes;
+};
+
+template <int W>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                              const __grid_constant__ CUtensorMap tmW, const Args a) {
+  using L = Layout<W>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* tiles = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages * L::kStageBytes);
+  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * L::kStages;
+  const uint32_t tfull0 = empty0 + 8 * L::kStages;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain_bar = tempty0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * L::kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::kStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(L::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      uint32_t issued_mask = 0;  // stages holding a load issued by this thread
+      uint32_t issued_par = 0;   // parity of the phase that load completes
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        int mt, nt, s, ns, kb0, kb1;
+        unit_coords(a, u, mt, nt, s, ns);
+        k_range(a, s, ns, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * st;
+          const uint32_t sa = smem_u32(tiles + st * L::kStageBytes);
+          mbar_expect_tx(fb, L::kStageBytes);
+          tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
+          tma_load_2d(sa + kATileBytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+          issued_mask |= 1u << st;
+          issued_par = (issued_par & ~(1u << st)) | (ph << st);
+          if (++st == L::kStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before shared memory is released
+        for (int i = 0; i < L::kStages; ++i)
+          if (issued_mask & (1u << i)) wait_drain(full0 + 8 * i, (issued_par >> i) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      bool any = false;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        int mt, nt, s, ns, kb0, kb1;
+        unit_coords(a, u, mt, nt, s, ns);
+        k_range(a, s, ns, kb0, kb1);
+        if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 2)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * W * kBN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tiles + st * L::kStageBytes);
+          const uint64_t adesc = sw128_desc(sa);
+#pragma unroll
+          for (int k = 0; k < kBK / kUK; ++k) {
+            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+#pragma unroll
+            for (int n = 0; n < W; ++n) {
+              const uint64_t bdesc = sw128_desc(sa + kATileBytes + n * kBSubBytes);
+              // advance 32 bytes (16 bf16) along K inside the swizzled row
+              tc_mma(d0 + n * kBN, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc,
+                     accum);
+            }
+          }
+          tc_commit(empty0 + 8 * st);  // stage free once these MMAs have read it
+          any = true;
+          if (++st == L::kStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
+      }
+      if (*abort_flag && any) {
+        // a commit arrives once every MMA issued above has completed
+        tc_commit(drain_bar);
+        wait_drain(drain_bar, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+      int mt, nt, s, ns;
+      unit_coords(a, u, mt, nt, s, ns);
+      if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 4)) break;
+      tc_fence_after();
+      const int row = mt * kBM + row_in_tile;
+      const bool row_ok = row < a.M;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * W * kBN;
+#pragma unroll 1
+      for (int ch = 0; ch < 2 * W; ++ch) {
+        uint32_t r[32];
+        tc_ld32(tbase + ch * 32, r);
+        const int col0 = nt * W * kBN + ch * 32;
+        if (!row_ok || col0 >= a.N) continue;
+        if (ns > 1) {
+          float* dst = a.partial + (static_cast<size_t>(s) * a.M + row) * a.N + col0;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (col0 + 4 * g < a.N)
+              *reinterpret_cast<float4*>(dst + 4 * g) =
+                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
+                              __uint_as_float(r[4 * g + 3]));
+        } else if (a.out_kind == kOutF32) {
+          float* dst = static_cast<float*>(a.C) + static_cast<size_t>(row) * a.N + col0;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (col0 + 4 * g < a.N)
+              *reinterpret_cast<float4*>(dst + 4 * g) =
+                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
+                              __uint_as_float(r[4 * g + 3]));
+        } else {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.C) + static_cast<size_t>(row) * a.N + col0;
+          const __nv_bfloat16* res = a.R ? a.R + static_cast<size_t>(row) * a.N + col0 : nullptr;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + 8 * g >= a.N) break;
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * g + e]);
+            if (res) {
+              float rv[8];
+              unpack8(*reinterpret_cast<const uint4*>(res + 8 * g), rv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __fadd_rn(f[e], rv[e]);
+            }
+            *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(f);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_ph ^= 1u;
+      }
+    }
+  }
+
+  // Normal exit: the epilogue has consumed the last accumulator commit, so every
+  // MMA has completed and every load was consumed.  After an abort the producer
+  // and the MMA thread drained their own work above.
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(L::kTmemCols)
+                 : "memory");
+  }
+}
+
+// Second pass of split-K: element (i, j) of an unprotected tile is the
+// left-to-right sum of its split partials (+ residual), rounded once.
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, void* C, const __nv_bfloat16* __restrict__ R,
+                                     int M, int N, int splits, int skip_r0, int skip_r1, int out_kind) {
+  const int64_t chunks = static_cast<int64_t>(N) / 8;
+  const int64_t n = static_cast<int64_t>(M) * chunks;
+  for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(k / chunks);
+    const int col = static_cast<int>(k % chunks) * 8;
+    if (row >= skip_r0 && row < skip_r1) continue;
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float* p = partial + (static_cast<size_t>(s) * M + row) * N + col;
+      const float4 a = *reinterpret_cast<const float4*>(p);
+      const float4 b = *reinterpret_cast<const float4*>(p + 4);
+      f[0] = __fadd_rn(f[0], a.x); f[1] = __fadd_rn(f[1], a.y); f[2] = __fadd_rn(f[2], a.z); f[3] = __fadd_rn(f[3], a.w);
+      f[4] = __fadd_rn(f[4], b.x); f[5] = __fadd_rn(f[5], b.y); f[6] = __fadd_rn(f[6], b.z); f[7] = __fadd_rn(f[7], b.w);
+    }
+    if (out_kind == kOutF32) {
+      float* dst = static_cast<float*>(C) + static_cast<size_t>(row) * N + col;
+      *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
+    } else {
+      if (R) {
+        float rv[8];
+        unpack8(*reinterpret_cast<const uint4*>(R + static_cast<size_t>(row) * N + col), rv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __fadd_rn(f[e], rv[e]);
+      }
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(C) + static_cast<size_t>(row) * N + col) = pack8(f);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  int64_t rows, K;
+  int box_rows;
+  int dev;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && dev == o.dev;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = reinterpret_cast<size_t>(k.ptr);
+    h ^= static_cast<size_t>(k.rows) * 0x9E3779B97F4A7C15ull;
+    h ^= static_cast<size_t>(k.K) * 0xC2B2AE3D27D4EB4Full;
+    h ^= static_cast<size_t>(k.box_rows * 131 + k.dev);
+    return h;
+  }
+};
+
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// Tensor map of a [rows][K] bf16 row-major matrix, box 64 (K) x box_rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, CUtensorMap* out) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  MapKey key{ptr, rows, K, box_rows, dev};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return BI_OK;
+    }
+  }
+  auto fn = encode_fn();
+  BI_REQUIRE(fn != nullptr, BI_ERR_CUDA, "bi_gemm: cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  BI_REQUIRE(r == CUDA_SUCCESS, BI_ERR_CUDA, "bi_gemm: cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  if (g_maps.size() > 4096) g_maps.clear();
+  g_maps[key] = *out;
+  return BI_OK;
+}
+
+struct Plan {
+  int W;
+  int splits;
+  int tm0, tm1;
+  int m_tiles, n_tiles, units, kb_total, kb_per;
+};
+
+int choose_width(int64_t M, int64_t N) {
+  const int sms = num_sms();
+  const int64_t mt = (M + kBM - 1) / kBM;
+  double best = -1.0;
+  int bw = 1;
+  const int widths[3] = {4, 2, 1};
+  const double penalty[3] = {1.0, 0.92, 0.80};  // shared-memory operand traffic per flop grows as W shrinks
+  for (int i = 0; i < 3; ++i) {
+    const int w = widths[i];
+    const int64_t tiles = mt * ((N + w * kBN - 1) / (w * kBN));
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double eff = static_cast<double>(tiles) / static_cast<double>(waves * sms) * penalty[i];
+    if (eff > best + 1e-9) {
+      best = eff;
+      bw = w;
+    }
+  }
+  return bw;
+}
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te) {
+  Plan p;
+  p.W = choose_width(M, N);
+  p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  p.n_tiles = static_cast<int>((N + p.W * kBN - 1) / (p.W * kBN));
+  p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
+  p.splits = 1;
+  p.tm0 = p.tm1 = 0;
+  if (mode != BI_MODE_INVARIANT) {
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int sms = num_sms();
+    int s = static_cast<int>(std::min<int64_t>(kMaxSplitK, std::max<int64_t>(1, sms / std::max<int64_t>(1, tiles))));
+    s = std::min(s, p.kb_total);
+    if (s > 1) {
+      const int per = (p.kb_total + s - 1) / s;
+      s = (p.kb_total + per - 1) / per;
+    }
+    p.splits = std::max(1, s);
+    if (mode == BI_MODE_PROTECTED && te > tb) {
+      p.tm0 = static_cast<int>(tb / kBM);
+      p.tm1 = static_cast<int>((te - 1) / kBM) + 1;
+    }
+  }
+  p.kb_per = (p.kb_total + p.splits - 1) / p.splits;
+  const int prot = p.tm1 - p.tm0;
+  p.units = p.n_tiles * (prot + (p.m_tiles - prot) * p.splits);
+  return p;
+}
+
+template <int W>
+bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
+  using L = Layout<W>;
+  static bool attr = false;
+  if (!attr) {
+    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(L::kSmemBytes)));
+    attr = true;
+  }
+  const int grid = std::min(args.units, num_sms());
+  BI_TIMED(::bi::kTagGemm, s, gemm_tc_kernel<W><<<grid, kThreads, L::kSmemBytes, s>>>(ma, mw, args));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+}  // namespace gemm
+
+int take_gemm_device_error(cudaStream_t s, int32_t* code) {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, gemm::g_err_word, sizeof(v), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess) return 1;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return 1;
+  if (v != 0) {
+    unsigned zero = 0;
+    if (cudaMemcpyToSymbolAsync(gemm::g_err_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return 1;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return 1;
+  }
+  *code = static_cast<int32_t>(v);
+  return 0;
+}
+
+size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode) {
+  if (mode == BI_MODE_INVARIANT || M <= 0 || N <= 0 || K <= 0) return 0;
+  gemm::Plan p = gemm::make_plan(M, N, K, mode, 0, 0);
+  if (p.splits <= 1) return 0;
+  return static_cast<size_t>(p.splits) * M * N * sizeof(float);
+}
+
+bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64_t M, int64_t N, int64_t K,
+                    bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count, void* ws,
+                    size_t ws_bytes, cudaStream_t s) {
+  clear_error();
+  BI_REQUIRE(M >= 0 && N >= 0 && K >= 8, BI_ERR_INVALID_ARG, "bi_gemm: M=%lld N=%lld K=%lld",
+             static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
+  BI_REQUIRE(K % 8 == 0 && N % 8 == 0, BI_ERR_UNSUPPORTED, "bi_gemm: K (%lld) and N (%lld) must be multiples of 8",
+             static_cast<long long>(K), static_cast<long long>(N));
+  BI_REQUIRE(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), BI_ERR_UNSUPPORTED,
+             "bi_gemm: sizes beyond int32");
+  BI_REQUIRE(out_dtype == BI_BF16 || out_dtype == BI_F32, BI_ERR_UNSUPPORTED, "bi_gemm: out dtype %d",
+             static_cast<int>(out_dtype));
+  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "bi_gemm: mode %d",
+             static_cast<int>(mode));
+  BI_REQUIRE(R == nullptr || out_dtype == BI_BF16, BI_ERR_UNSUPPORTED, "bi_gemm: residual needs bf16 output");
+  int64_t tb = 0, te = 0;
+  if (mode == BI_MODE_PROTECTED && target_row >= 0) {
+    BI_REQUIRE(target_count >= 1 && target_row + static_cast<int64_t>(target_count) <= M, BI_ERR_INVALID_ARG,
+               "bi_gemm: target rows [%d, %d) outside [0, %lld)", target_row, target_row + target_count,
+               static_cast<long long>(M));
+    tb = target_row;
+    te = target_row + static_cast<int64_t>(target_count);
+  }
+  if (M == 0 || N == 0) return BI_OK;
+  BI_REQUIRE(A && Wt && C, BI_ERR_INVALID_ARG, "bi_gemm: null pointer");
+  BI_REQUIRE(aligned16(A) && aligned16(Wt) && aligned16(C) && (R == nullptr || aligned16(R)), BI_ERR_INVALID_ARG,
+             "bi_gemm: pointers must be 16-byte aligned");
+  gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te);
+  gemm::Args args{};
+  args.M = static_cast<int>(M);
+  args.N = static_cast<int>(N);
+  args.K = static_cast<int>(K);
+  args.m_tiles = p.m_tiles;
+  args.n_tiles = p.n_tiles;
+  args.splits = p.splits;
+  args.tm0 = p.tm0;
+  args.tm1 = p.tm1;
+  args.units = p.units;
+  args.kb_total = p.kb_total;
+  args.kb_per = p.kb_per;
+  args.C = C;
+  args.R = static_cast<const __nv_bfloat16*>(R);
+  args.out_kind = out_dtype == BI_F32 ? gemm::kOutF32 : gemm::kOutBF16;
+  args.partial = nullptr;
+  if (p.splits > 1) {
+    const size_t need = static_cast<size_t>(p.splits) * M * N * sizeof(float);
+    BI_REQUIRE(ws != nullptr && ws_bytes >= need && aligned16(ws), BI_ERR_WORKSPACE,
+               "bi_gemm: workspace %zu < %zu bytes", ws_bytes, need);
+    args.partial = static_cast<float*>(ws);
+  }
+  CUtensorMap ma, mw;
+  BI_TRY(gemm::tensor_map(A, M, K, gemm::kBM, &ma));
+  BI_TRY(gemm::tensor_map(Wt, N, K, p.W * gemm::kBN, &mw));
+  bi_status st;
+  if (p.W == 4) st = gemm::launch_w<4>(ma, mw, args, s);
+  else if (p.W == 2) st = gemm::launch_w<2>(ma, mw, args, s);
+  else st = gemm::launch_w<1>(ma, mw, args, s);
+  if (st != BI_OK) return st;
+  if (p.splits > 1) {
+    const int64_t n = M * (N / 8);
+    const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
+    const int skip0 = p.tm0 * gemm::kBM, skip1 = static_cast<int>(std::min<int64_t>(M, int64_t(p.tm1) * gemm::kBM));
+    BI_TIMED(::bi::kTagSplitkReduce, s, gemm::splitk_reduce_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(args.partial, C, args.R, args.M, args.N,
+                                                                          p.splits, skip0, skip1, args.out_kind));
+    BI_LAUNCH_CHECK();
+  }
+  return BI_OK;
+}
+
+}  // namespace bi
+
+extern "C" size_t bi_gemm_workspace(int64_t M, int64_t N, int64_t K, bi_mode mode) {
+  return bi::gemm_ws(M, N, K, mode);
+}
+
+extern "C" bi_status bi_gemm(const void* A, const void* W, void* C, const void* residual, int64_t M, int64_t N,
+                             int64_t K, bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count,
+                             void* workspace, size_t ws_bytes, bi_stream s) {
+  return bi::gemm_impl(A, W, C, residual, M, N, K, out_dtype, mode, target_row, target_count, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(s));
+}

@@ -1,0 +1,190 @@
+// Pointwise steps of the decoder layer: embedding gather, RoPE tables, the QKV
+// split with rotary embedding and the paged K/V store, SwiGLU gating.
+// Each output element depends on its own inputs only, so these steps are batch
+// invariant as they stand (devpress digest of "Defeating Nondeterminism in LLM
+// Inference", section 3: pointwise operations need no change).
+#include <cmath>
+
+#include "common.cuh"
+
+namespace bi {
+namespace {
+
+__global__ void embed_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ table, uint4* __restrict__ out,
+                             int64_t T, int64_t chunks_per_row, int64_t vocab) {
+  const int64_t t = blockIdx.x;
+  if (t >= T) return;
+  const int64_t id = ids[t];
+  const bool ok = id >= 0 && id < vocab;
+  for (int64_t c = threadIdx.x; c < chunks_per_row; c += blockDim.x)
+    out[t * chunks_per_row + c] = ok ? table[id * chunks_per_row + c] : make_uint4(0, 0, 0, 0);
+}
+
+// cos/sin(p * theta^(-2i/hd)) in float64, rounded once to fp32.
+__global__ void rope_table_kernel(double theta, int hd, int max_pos, float* __restrict__ cs, float* __restrict__ sn) {
+  const int half = hd / 2;
+  const int64_t n = static_cast<int64_t>(max_pos) * half;
+  for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int p = static_cast<int>(k / half);
+    const int i = static_cast<int>(k % half);
+    const double f = pow(theta, -2.0 * i / hd);
+    double sv, cv;
+    sincos(static_cast<double>(p) * f, &sv, &cv);
+    cs[k] = static_cast<float>(cv);
+    sn[k] = static_cast<float>(sv);
+  }
+}
+
+// One CTA per token.  Work items: rotated pairs of q heads, rotated pairs of k
+// heads, v elements (8 at a time).
+__global__ void qkv_rope_store_kernel(const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ rc,
+                                      const float* __restrict__ rs, const int32_t* __restrict__ token_pos,
+                                      const int32_t* __restrict__ token_req, const int32_t* __restrict__ block_table,
+                                      int max_pages, int hq, int hkv, int hd, __nv_bfloat16* __restrict__ q_out,
+                                      __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc) {
+  const int t = blockIdx.x;
+  const int pos = token_pos[t];
+  const int req = token_req[t];
+  const int half = hd / 2;
+  const int width = (hq + 2 * hkv) * hd;
+  const uint16_t* row = reinterpret_cast<const uint16_t*>(qkv) + static_cast<size_t>(t) * width;
+  const float* c_row = rc + static_cast<size_t>(pos) * half;
+  const float* s_row = rs + static_cast<size_t>(pos) * half;
+  const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
+  const int slot = pos % BI_PAGE_SIZE;
+  uint16_t* qo = reinterpret_cast<uint16_t*>(q_out) + static_cast<size_t>(t) * hq * hd;
+  uint16_t* ko = reinterpret_cast<uint16_t*>(kc);
+  const int nq = hq * half, nk = hkv * half;
+  for (int it = threadIdx.x; it < nq + nk; it += blockDim.x) {
+    const bool is_q = it < nq;
+    const int k = is_q ? it : it - nq;
+    const int h = k / half, i = k % half;
+    const uint16_t* src = row + (is_q ? 0 : hq * hd) + h * hd;
+    const float a = __uint_as_float(static_cast<uint32_t>(src[i]) << 16);
+    const float b = __uint_as_float(static_cast<uint32_t>(src[i + half]) << 16);
+    const float c = c_row[i], s = s_row[i];
+    const float lo = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+    const float hi = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
+    uint16_t* dst = is_q ? qo + h * hd
+                         : ko + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE + slot) * hd;
+    dst[i] = to_bf16_bits(lo);
+    dst[i + half] = to_bf16_bits(hi);
+  }
+  const int nv = hkv * hd / 8;
+  const uint4* vsrc = reinterpret_cast<const uint4*>(row + (hq + hkv) * hd);
+  for (int it = threadIdx.x; it < nv; it += blockDim.x) {
+    const int h = (it * 8) / hd, d = (it * 8) % hd;
+    uint4* dst = reinterpret_cast<uint4*>(vc + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE + slot) * hd + d);
+    *dst = vsrc[it];
+  }
+}
+
+__global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloat16* __restrict__ out, int64_t T,
+                              int64_t F) {
+  const int64_t chunks = F / 8;
+  const int64_t n = T * chunks;
+  for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = k / chunks, c = k % chunks;
+    const uint4 gv = *reinterpret_cast<const uint4*>(gu + t * 2 * F + c * 8);
+    const uint4 uv = *reinterpret_cast<const uint4*>(gu + t * 2 * F + F + c * 8);
+    float g[8], u[8], o[8];
+    unpack8(gv, g);
+    unpack8(uv, u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float sg = __fdiv_rn(g[e], __fadd_rn(1.0f, expf(-g[e])));
+      o[e] = __fmul_rn(sg, u[e]);
+    }
+    *reinterpret_cast<uint4*>(out + t * F + c * 8) = pack8(o);
+  }
+}
+
+}  // namespace
+
+bi_status embed_impl(const int32_t* ids, const void* table, void* out, int64_t T, int64_t d, int64_t vocab,
+                     cudaStream_t s) {
+  BI_REQUIRE(T >= 0 && d > 0 && d % 8 == 0 && vocab > 0, BI_ERR_INVALID_ARG, "bi_embed: T=%lld d=%lld vocab=%lld",
+             static_cast<long long>(T), static_cast<long long>(d), static_cast<long long>(vocab));
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(ids && table && out && aligned16(table) && aligned16(out), BI_ERR_INVALID_ARG,
+             "bi_embed: null or misaligned pointer");
+  BI_TIMED(::bi::kTagEmbed, s, embed_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(ids, static_cast<const uint4*>(table), static_cast<uint4*>(out),
+                                                        T, d / 8, vocab));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs, const int32_t* token_pos,
+                              const int32_t* token_req, const int32_t* block_table, int32_t T,
+                              const bi_attn_dims* dm, void* q_out, void* kc, void* vc, cudaStream_t s) {
+  BI_REQUIRE(dm && T >= 0, BI_ERR_INVALID_ARG, "bi_qkv_rope_store: dims/T");
+  BI_REQUIRE(dm->head_dim % 16 == 0 && dm->head_dim >= 16 && dm->num_kv_heads >= 1 && dm->num_q_heads >= 1,
+             BI_ERR_UNSUPPORTED, "bi_qkv_rope_store: head_dim %d", dm->head_dim);
+  BI_REQUIRE(dm->page_size == BI_PAGE_SIZE, BI_ERR_UNSUPPORTED, "bi_qkv_rope_store: page_size %d", dm->page_size);
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(qkv && rc && rs && token_pos && token_req && block_table && q_out && kc && vc, BI_ERR_INVALID_ARG,
+             "bi_qkv_rope_store: null pointer");
+  BI_REQUIRE(aligned16(qkv) && aligned16(q_out) && aligned16(kc) && aligned16(vc), BI_ERR_INVALID_ARG,
+             "bi_qkv_rope_store: misaligned pointer");
+  BI_TIMED(::bi::kTagQkvRope, s, qkv_rope_store_kernel<<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
+                                          block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
+                                          static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(kc),
+                                          static_cast<__nv_bfloat16*>(vc)));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+bi_status swiglu_impl(const void* gu, void* out, int64_t T, int64_t F, cudaStream_t s) {
+  BI_REQUIRE(T >= 0 && F > 0 && F % 8 == 0, BI_ERR_INVALID_ARG, "bi_swiglu: T=%lld F=%lld", static_cast<long long>(T),
+             static_cast<long long>(F));
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(gu && out && aligned16(gu) && aligned16(out), BI_ERR_INVALID_ARG, "bi_swiglu: null or misaligned");
+  const int64_t n = T * (F / 8);
+  const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 16);
+  BI_TIMED(::bi::kTagSwiglu, s, swiglu_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(gu),
+                                                            static_cast<__nv_bfloat16*>(out), T, F));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+bi_status rope_table_impl(double theta, int32_t hd, int32_t max_pos, float* cs, float* sn, cudaStream_t s) {
+  BI_REQUIRE(theta > 1.0 && hd > 0 && hd % 2 == 0 && max_pos >= 0, BI_ERR_INVALID_ARG,
+             "bi_rope_table: theta=%g head_dim=%d max_pos=%d", theta, hd, max_pos);
+  if (max_pos == 0) return BI_OK;
+  BI_REQUIRE(cs && sn, BI_ERR_INVALID_ARG, "bi_rope_table: null pointer");
+  const int64_t n = static_cast<int64_t>(max_pos) * (hd / 2);
+  const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
+  BI_TIMED(::bi::kTagRopeTable, s, rope_table_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(theta, hd, max_pos, cs, sn));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+}  // namespace bi
+
+extern "C" bi_status bi_embed(const int32_t* ids, const void* table, void* out, int64_t T, int64_t d, int64_t vocab,
+                              bi_stream s) {
+  bi::clear_error();
+  return bi::embed_impl(ids, table, out, T, d, vocab, reinterpret_cast<cudaStream_t>(s));
+}
+
+extern "C" bi_status bi_rope_table(double theta, int32_t head_dim, int32_t max_pos, float* cos_out, float* sin_out,
+                                   bi_stream s) {
+  bi::clear_error();
+  return bi::rope_table_impl(theta, head_dim, max_pos, cos_out, sin_out, reinterpret_cast<cudaStream_t>(s));
+}
+
+extern "C" bi_status bi_qkv_rope_store(const void* qkv, const float* rope_cos, const float* rope_sin,
+                                       const int32_t* token_pos, const int32_t* token_req, const int32_t* block_table,
+                                       int32_t T, const bi_attn_dims* dims, void* q_out, void* k_cache, void* v_cache,
+                                       bi_stream s) {
+  bi::clear_error();
+  return bi::qkv_rope_store_impl(qkv, rope_cos, rope_sin, token_pos, token_req, block_table, T, dims, q_out, k_cache,
+                                 v_cache, reinterpret_cast<cudaStream_t>(s));
+}
+
+extern "C" bi_status bi_swiglu(const void* gu, void* out, int64_t T, int64_t F, bi_stream s) {
+  bi::clear_error();
+  return bi::swiglu_impl(gu, out, T, F, reinterpret_cast<cudaStream_t>(s));
+}

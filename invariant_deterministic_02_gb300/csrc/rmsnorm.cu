@@ -1,0 +1,269 @@
+// Batch-invariant RMSNorm.
+//
+// y[r][j] = x[r][j] * (1 / sqrt(mean_j x[r][j]^2 + eps)) * gamma[j]
+// ("Batch-Invariant Kernel" notes, section RMSNorm: the formula and the
+// data-parallel reduction in which one CTA owns a whole row; devpress digest of
+// "Defeating Nondeterminism in LLM Inference", section 3.1).
+//
+// INVARIANT: one CTA of 256 threads per row, whatever the number of rows.
+// Thread t loads 16-byte vectors t, t+256, t+512, ... of the row, accumulates
+// their squares in order with fused multiply-adds, the warp reduces with a
+// fixed xor-butterfly, and the eight warp sums are combined in a fixed pairwise
+// tree.  The whole order depends on d only.  A grid-stride loop over rows keeps
+// the grid a multiple of the SM count without touching any row's arithmetic.
+//
+// FAST (the non-invariant schedule the pages describe): when there are fewer
+// rows than SMs, each row is split over several CTAs whose partial sums are
+// combined in a second pass, so a row's reduction order depends on the batch.
+#include "common.cuh"
+
+namespace bi {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxChunks = 8;  // register-resident 16-byte vectors per thread
+constexpr int kSplitThreads = 128;
+
+template <typename T>
+struct VecOf;
+template <>
+struct VecOf<float> {
+  static constexpr int N = 4;
+};
+template <>
+struct VecOf<__nv_bfloat16> {
+  static constexpr int N = 8;
+};
+
+__device__ __forceinline__ void load_vec(const float* p, float (&f)[4]) {
+  float4 v = *reinterpret_cast<const float4*>(p);
+  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&f)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  unpack8(u, f);
+}
+__device__ __forceinline__ void store_vec(float* p, const float (&f)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+}
+__device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&f)[8]) {
+  *reinterpret_cast<uint4*>(p) = pack8(f);
+}
+
+// Fixed xor-butterfly: every lane ends with the same bits (fp add commutes).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// Sum of the eight warp partials in a fixed pairwise tree (every thread computes it).
+__device__ __forceinline__ float sum8(const float* r) {
+  float a = __fadd_rn(__fadd_rn(r[0], r[1]), __fadd_rn(r[2], r[3]));
+  float b = __fadd_rn(__fadd_rn(r[4], r[5]), __fadd_rn(r[6], r[7]));
+  return __fadd_rn(a, b);
+}
+
+__device__ __forceinline__ float inv_rms(float sumsq, int d, float eps) {
+  float mean = __fdiv_rn(sumsq, static_cast<float>(d));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+}
+
+// The invariant computation of one row by one CTA of kThreads threads.
+template <typename T>
+__device__ __forceinline__ void rms_row(const T* __restrict__ x, const T* __restrict__ gamma, T* y, int d, float eps,
+                                        float* red) {
+  constexpr int V = VecOf<T>::N;
+  const int nchunks = d / V;
+  const int t = threadIdx.x;
+  float xs[kMaxChunks][V];
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int c = t + i * kThreads;
+    if (c < nchunks) {
+      load_vec(x + static_cast<size_t>(c) * V, xs[i]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc = __fmaf_rn(xs[i][e], xs[i][e], acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if ((t & 31) == 0) red[t >> 5] = acc;
+  __syncthreads();
+  const float r = inv_rms(sum8(red), d, eps);
+  __syncthreads();  // red is reused by the next row
+#pragma unroll
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int c = t + i * kThreads;
+    if (c < nchunks) {
+      float g[V], o[V];
+      load_vec(gamma + static_cast<size_t>(c) * V, g);
+#pragma unroll
+      for (int e = 0; e < V; ++e) o[e] = __fmul_rn(__fmul_rn(xs[i][e], r), g[e]);
+      store_vec(y + static_cast<size_t>(c) * V, o);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) rms_invariant_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
+                                                                 T* y, int64_t row_begin, int64_t row_end, int d,
+                                                                 float eps) {
+  __shared__ float red[kWarps];
+  for (int64_t r = row_begin + blockIdx.x; r < row_end; r += gridDim.x)
+    rms_row(x + r * d, gamma, y + r * d, d, eps, red);
+}
+
+// FAST pass 1: CTA (row, s) sums the squares of chunk range s of its row.
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads) rms_split_partial_kernel(const T* __restrict__ x, float* partial,
+                                                                          int64_t rows, int d, int splits,
+                                                                          int64_t skip_begin, int64_t skip_end) {
+  constexpr int V = VecOf<T>::N;
+  const int64_t r = blockIdx.x / splits;
+  const int s = blockIdx.x % splits;
+  if (r >= rows || (r >= skip_begin && r < skip_end)) return;
+  const int nchunks = d / V;
+  const int per = (nchunks + splits - 1) / splits;
+  const int c0 = s * per, c1 = min(nchunks, c0 + per);
+  float acc = 0.f;
+  for (int c = c0 + threadIdx.x; c < c1; c += kSplitThreads) {
+    float f[V];
+    load_vec(x + r * d + static_cast<int64_t>(c) * V, f);
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc = __fmaf_rn(f[e], f[e], acc);
+  }
+  acc = warp_sum(acc);
+  __shared__ float red[kSplitThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < kSplitThreads / 32; ++w) tot = __fadd_rn(tot, red[w]);
+    partial[r * splits + s] = tot;
+  }
+}
+
+// FAST pass 2: one CTA per row; split rows add their partials left to right,
+// rows in [inv_begin, inv_end) run the invariant row function instead.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) rms_split_finish_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
+                                                                    T* y, const float* partial, int64_t rows, int d,
+                                                                    int splits, float eps, int64_t inv_begin,
+                                                                    int64_t inv_end) {
+  constexpr int V = VecOf<T>::N;
+  __shared__ float red[kWarps];
+  const int64_t r = blockIdx.x;
+  if (r >= rows) return;
+  if (r >= inv_begin && r < inv_end) {
+    rms_row(x + r * d, gamma, y + r * d, d, eps, red);
+    return;
+  }
+  float tot = 0.f;
+  for (int s = 0; s < splits; ++s) tot = __fadd_rn(tot, partial[r * splits + s]);
+  const float rr = inv_rms(tot, d, eps);
+  const int nchunks = d / V;
+  for (int c = threadIdx.x; c < nchunks; c += kThreads) {
+    float f[V], g[V], o[V];
+    load_vec(x + r * d + static_cast<int64_t>(c) * V, f);
+    load_vec(gamma + static_cast<int64_t>(c) * V, g);
+#pragma unroll
+    for (int e = 0; e < V; ++e) o[e] = __fmul_rn(__fmul_rn(f[e], rr), g[e]);
+    store_vec(y + r * d + static_cast<int64_t>(c) * V, o);
+  }
+}
+
+int fast_splits(int64_t rows, int d, int vec) {
+  const int sms = num_sms();
+  if (rows <= 0 || rows >= sms) return 1;
+  const int by_sms = static_cast<int>(sms / rows);
+  const int by_work = max(1, (d / vec) / kSplitThreads);
+  return max(1, min(by_sms, by_work));
+}
+
+template <typename T>
+bi_status launch(const void* xv, const void* gv, void* yv, int64_t rows, int d, float eps, bi_mode mode,
+                 int64_t tb, int64_t te, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const T* x = static_cast<const T*>(xv);
+  const T* g = static_cast<const T*>(gv);
+  T* y = static_cast<T*>(yv);
+  constexpr int V = VecOf<T>::N;
+  const int splits = (mode == BI_MODE_INVARIANT) ? 1 : fast_splits(rows, d, V);
+  if (splits == 1) {
+    // Unsplit: the data-parallel schedule, identical to INVARIANT for every row.
+    const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(num_sms()) * 8);
+    BI_TIMED(::bi::kTagRmsnorm, s, rms_invariant_kernel<T><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(x, g, y, 0, rows, d, eps));
+    BI_LAUNCH_CHECK();
+    return BI_OK;
+  }
+  const size_t need = static_cast<size_t>(rows) * splits * sizeof(float);
+  BI_REQUIRE(ws != nullptr && ws_bytes >= need, BI_ERR_WORKSPACE, "bi_rmsnorm: workspace %zu < %zu bytes", ws_bytes,
+             need);
+  float* partial = static_cast<float*>(ws);
+  BI_TIMED(::bi::kTagRmsnormSplit, s, rms_split_partial_kernel<T><<<static_cast<unsigned>(rows * splits), kSplitThreads, 0, s>>>(x, partial, rows, d,
+                                                                                             splits, tb, te));
+  BI_LAUNCH_CHECK();
+  BI_TIMED(::bi::kTagRmsnormSplit, s, rms_split_finish_kernel<T><<<static_cast<unsigned>(rows), kThreads, 0, s>>>(x, g, y, partial, rows, d, splits, eps,
+                                                                              tb, te));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+bi_status check_target(bi_mode mode, int64_t rows, int32_t target_row, int32_t target_count, int64_t* tb,
+                       int64_t* te) {
+  *tb = 0;
+  *te = 0;
+  if (mode != BI_MODE_PROTECTED || target_row < 0) return BI_OK;
+  BI_REQUIRE(target_count >= 1 && target_row + static_cast<int64_t>(target_count) <= rows, BI_ERR_INVALID_ARG,
+             "target rows [%d, %d) outside [0, %lld)", target_row, target_row + target_count,
+             static_cast<long long>(rows));
+  *tb = target_row;
+  *te = target_row + static_cast<int64_t>(target_count);
+  return BI_OK;
+}
+
+}  // namespace
+
+bi_status rmsnorm_impl(const void* x, const void* gamma, void* y, int64_t rows, int64_t d, bi_dtype dtype, float eps,
+                       bi_mode mode, int32_t target_row, int32_t target_count, void* ws, size_t ws_bytes,
+                       cudaStream_t s) {
+  clear_error();
+  BI_REQUIRE(rows >= 0 && d > 0, BI_ERR_INVALID_ARG, "bi_rmsnorm: rows=%lld d=%lld", static_cast<long long>(rows),
+             static_cast<long long>(d));
+  BI_REQUIRE(dtype == BI_F32 || dtype == BI_BF16, BI_ERR_UNSUPPORTED, "bi_rmsnorm: dtype %d", static_cast<int>(dtype));
+  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "bi_rmsnorm: mode %d",
+             static_cast<int>(mode));
+  const int vec = dtype == BI_F32 ? 4 : 8;
+  BI_REQUIRE(d % vec == 0 && d / vec <= kThreads * kMaxChunks, BI_ERR_UNSUPPORTED,
+             "bi_rmsnorm: d=%lld must be a multiple of %d and at most %d", static_cast<long long>(d), vec,
+             kThreads * kMaxChunks * vec);
+  BI_REQUIRE(eps >= 0.f && eps == eps, BI_ERR_INVALID_ARG, "bi_rmsnorm: eps must be >= 0");
+  int64_t tb, te;
+  BI_TRY(check_target(mode, rows, target_row, target_count, &tb, &te));
+  if (rows == 0) return BI_OK;
+  BI_REQUIRE(x && gamma && y, BI_ERR_INVALID_ARG, "bi_rmsnorm: null pointer");
+  BI_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(y), BI_ERR_INVALID_ARG,
+             "bi_rmsnorm: pointers must be 16-byte aligned");
+  if (dtype == BI_F32)
+    return launch<float>(x, gamma, y, rows, static_cast<int>(d), eps, mode, tb, te, ws, ws_bytes, s);
+  return launch<__nv_bfloat16>(x, gamma, y, rows, static_cast<int>(d), eps, mode, tb, te, ws, ws_bytes, s);
+}
+
+size_t rmsnorm_ws(int64_t rows, int64_t d, bi_mode mode) {
+  if (mode == BI_MODE_INVARIANT || rows <= 0) return 0;
+  const int sms = num_sms();
+  if (rows >= sms) return 0;
+  return static_cast<size_t>(rows) * sms * sizeof(float);
+}
+
+}  // namespace bi
+
+extern "C" size_t bi_rmsnorm_workspace(int64_t rows, int64_t d, bi_mode mode) { return bi::rmsnorm_ws(rows, d, mode); }
+
+extern "C" bi_status bi_rmsnorm(const void* x, const void* gamma, void* y, int64_t rows, int64_t d, bi_dtype dtype,
+                                float eps, bi_mode mode, int32_t target_row, int32_t target_count, void* workspace,
+                                size_t ws_bytes, bi_stream s) {
+  return bi::rmsnorm_impl(x, gamma, y, rows, d, dtype, eps, mode, target_row, target_count, workspace, ws_bytes,
+                          reinterpret_cast<cudaStream_t>(s));
+}

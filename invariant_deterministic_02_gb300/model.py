@@ -1,0 +1,190 @@
+"""Model driver over the C ABI: random-init weights, paged KV caches, batch descriptors.
+
+Everything numeric runs in libbi's kernels through ``bi_model_forward``; this
+module only owns device memory (via torch), hands out KV pages and builds the
+batch descriptor (request -> query rows, first position, block-table row).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import synth
+from . import (Batch, LayerWeights, ModelDims, ModelWeights, PAGE_SIZE, bi_model_forward, bi_model_workspace,
+               bi_rope_table, INVARIANT)
+
+
+@dataclass
+class ModelShape:
+    layer: synth.LayerShape
+    n_layers: int
+    vocab: int
+    max_pos: int = 32768
+
+
+QWEN3_8B = ModelShape(synth.QWEN3_8B_LAYER, 36, 151936)
+LLAMA31_8B = ModelShape(synth.LLAMA31_8B_LAYER, 32, 128256)
+
+
+@dataclass
+class ForwardOut:
+    logits: torch.Tensor  # [B][V] fp32
+    top_v: torch.Tensor   # [B][k]
+    top_i: torch.Tensor   # [B][k]
+
+
+class PagePool:
+    """Free list of physical KV pages; a request owns an ordered list of pages."""
+
+    def __init__(self, num_pages: int, seed: int | None = None):
+        order = np.arange(num_pages, dtype=np.int32)
+        if seed is not None:
+            order = np.random.default_rng(seed).permutation(num_pages).astype(np.int32)
+        self.free = list(order[::-1])
+        self.owned: dict[int, list[int]] = {}
+
+    def ensure(self, req: int, tokens: int):
+        pages = self.owned.setdefault(req, [])
+        need = (tokens + PAGE_SIZE - 1) // PAGE_SIZE
+        while len(pages) < need:
+            if not self.free:
+                raise MemoryError("KV page pool exhausted")
+            pages.append(int(self.free.pop()))
+        return pages
+
+    def release(self, req: int):
+        for p in reversed(self.owned.pop(req, [])):
+            self.free.append(p)
+
+
+class BiModel:
+    def __init__(self, shape: ModelShape, weights: dict, num_pages: int, device="cuda", page_seed: int | None = None):
+        self.shape = shape
+        self.device = device
+        L = shape.layer
+        self.w = weights
+        self.dims = ModelDims(L.d_model, L.n_q_heads, L.n_kv_heads, L.head_dim, L.ffn_dim, shape.vocab, PAGE_SIZE,
+                              shape.max_pos, L.rms_eps)
+        self.rope_cos = torch.empty((shape.max_pos, L.head_dim // 2), dtype=torch.float32, device=device)
+        self.rope_sin = torch.empty_like(self.rope_cos)
+        bi_rope_table(L.rope_theta, L.head_dim, shape.max_pos, self.rope_cos, self.rope_sin)
+        self.num_pages = num_pages
+        self.k_caches = [torch.zeros((num_pages, L.n_kv_heads, PAGE_SIZE, L.head_dim), dtype=torch.bfloat16,
+                                     device=device) for _ in range(shape.n_layers)]
+        self.v_caches = [torch.zeros_like(k) for k in self.k_caches]
+        self.k_ptrs = (ctypes.c_void_p * max(1, shape.n_layers))(*[k.data_ptr() for k in self.k_caches])
+        self.v_ptrs = (ctypes.c_void_p * max(1, shape.n_layers))(*[v.data_ptr() for v in self.v_caches])
+        self._layer_structs = (LayerWeights * max(1, shape.n_layers))(*[
+            LayerWeights(lw["attn_norm"].data_ptr(), lw["w_qkv"].data_ptr(), lw["w_o"].data_ptr(),
+                         lw["ffn_norm"].data_ptr(), lw["w_gate_up"].data_ptr(), lw["w_down"].data_ptr())
+            for lw in weights["layers"]])
+        self.mw = ModelWeights(weights["embed"].data_ptr(), self._layer_structs, shape.n_layers,
+                               weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr())
+        self.pool = PagePool(num_pages, seed=page_seed)
+        self.lengths: dict[int, int] = {}
+        self._ws = None
+
+    # ------------------------------------------------------------ construction
+    @staticmethod
+    def random_weights(shape: ModelShape, seed: int, device="cuda", std: float = 0.02, on_host: bool | None = None):
+        L = shape.layer
+        if on_host is None:
+            on_host = L.d_model * L.ffn_dim * shape.n_layers < 64 * 1024 * 1024
+        if on_host:
+            layers = []
+            for i in range(shape.n_layers):
+                lw = synth.layer_weights(L, seed + 100 * (i + 1), std=std)
+                layers.append({k: v.to(device) for k, v in lw.items()})
+            embed = synth.normal((shape.vocab, L.d_model), seed + 1, std=std).to(device)
+            head = synth.normal((shape.vocab, L.d_model), seed + 2, std=std).to(device)
+        else:
+            layers = []
+            for i in range(shape.n_layers):
+                s = seed + 100 * (i + 1)
+                layers.append({
+                    "attn_norm": torch.ones(L.d_model, dtype=torch.bfloat16, device=device),
+                    "w_qkv": synth.normal_device((L.qkv_dim, L.d_model), s + 2, std=std, device=device),
+                    "w_o": synth.normal_device((L.d_model, L.n_q_heads * L.head_dim), s + 3, std=std, device=device),
+                    "ffn_norm": torch.ones(L.d_model, dtype=torch.bfloat16, device=device),
+                    "w_gate_up": synth.normal_device((2 * L.ffn_dim, L.d_model), s + 5, std=std, device=device),
+                    "w_down": synth.normal_device((L.d_model, L.ffn_dim), s + 6, std=std, device=device),
+                })
+            embed = synth.normal_device((shape.vocab, L.d_model), seed + 1, std=std, device=device)
+            head = synth.normal_device((shape.vocab, L.d_model), seed + 2, std=std, device=device)
+        return {"embed": embed, "layers": layers, "final_norm": torch.ones(L.d_model, dtype=torch.bfloat16,
+                                                                            device=device), "lm_head": head}
+
+    @classmethod
+    def random(cls, shape: ModelShape, seed: int, device="cuda", num_pages: int = 512, page_seed: int | None = 3):
+        return cls(shape, cls.random_weights(shape, seed, device), num_pages, device, page_seed)
+
+    def host_weights(self):
+        """float64 numpy copies of the weights (for the oracle on small models)."""
+        f = lambda t: t.detach().cpu().double().numpy()
+        return {"embed": f(self.w["embed"]), "final_norm": f(self.w["final_norm"]), "lm_head": f(self.w["lm_head"]),
+                "layers": [{k: f(v) for k, v in lw.items()} for lw in self.w["layers"]]}
+
+    # ------------------------------------------------------------ batches
+    def make_batch(self, items, target_request: int = -1):
+        """items: list of (request id, int32 token array).  Returns (Batch, keep-alive tensors, ids)."""
+        B = len(items)
+        counts = [len(t) for _, t in items]
+        q_start = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        pos0 = np.array([self.lengths.get(r, 0) for r, _ in items], dtype=np.int32)
+        rows = [self.pool.ensure(r, int(p) + n) for (r, _), p, n in zip(items, pos0, counts)]
+        max_pages = max(1, max(len(r) for r in rows))
+        bt = np.full((B, max_pages), -1, dtype=np.int32)
+        for b, r in enumerate(rows):
+            bt[b, :len(r)] = r
+        ids = np.concatenate([np.asarray(t, dtype=np.int32) for _, t in items])
+        dev = lambda a: torch.from_numpy(a).to(self.device, non_blocking=False)
+        keep = {"q_start": dev(q_start), "pos0": dev(pos0), "bt": dev(bt), "ids": dev(ids)}
+        trow = int(q_start[target_request]) if target_request >= 0 else -1
+        tcnt = counts[target_request] if target_request >= 0 else 0
+        batch = Batch(B, int(q_start[-1]), max(counts), keep["q_start"].data_ptr(), keep["pos0"].data_ptr(),
+                      keep["bt"].data_ptr(), max_pages, self.num_pages, target_request, trow, tcnt)
+        return batch, keep
+
+    def forward_batch(self, items, k: int = 20, mode=INVARIANT, target_request: int = -1) -> ForwardOut:
+        batch, keep = self.make_batch(items, target_request)
+        B = len(items)
+        logits = torch.empty((B, self.shape.vocab), dtype=torch.float32, device=self.device)
+        tv = torch.empty((B, k), dtype=torch.float32, device=self.device)
+        ti = torch.empty((B, k), dtype=torch.int32, device=self.device)
+        need = bi_model_workspace(self.dims, batch, mode)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        bi_model_forward(self.dims, self.mw, self.rope_cos, self.rope_sin, keep["ids"], batch, self.k_ptrs,
+                         self.v_ptrs, logits, k, tv, ti, mode=mode, workspace=self._ws, ws_bytes=need)
+        for (r, t) in items:
+            self.lengths[r] = self.lengths.get(r, 0) + len(t)
+        torch.cuda.current_stream().synchronize()  # keep-alive tensors must outlive the launches
+        return ForwardOut(logits, tv, ti)
+
+    def install_history(self, req: int, length: int, seed: int):
+        """Give request `req` a cached history of `length` tokens whose K/V (every
+        layer) are seeded N(0, 1) bf16 values, as if it had been prefilled earlier."""
+        if length <= 0:
+            return
+        pages = self.pool.ensure(req, length)
+        L = self.shape.layer
+        idx = torch.tensor(pages, dtype=torch.int64, device=self.device)
+        n = len(pages)
+        g = torch.Generator(device=self.device)
+        for li in range(self.shape.n_layers):
+            for ci, cache in enumerate((self.k_caches[li], self.v_caches[li])):
+                g.manual_seed((seed * 1000003 + li * 2 + ci) & 0x7FFFFFFF)
+                vals = torch.randn((n, L.n_kv_heads, PAGE_SIZE, L.head_dim), generator=g, device=self.device)
+                cache[idx] = vals.to(torch.bfloat16)
+        self.lengths[req] = length
+
+    def reset(self):
+        for r in list(self.lengths.keys()) + list(self.pool.owned.keys()):
+            self.release(r)
+
+    def release(self, req: int):
+        self.pool.release(req)
+        self.lengths.pop(req, None)

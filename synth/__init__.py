@@ -149,3 +149,29 @@ def layer_weights(shape: LayerShape, seed: int, std: float = 0.02, gamma_std: fl
         "w_gate_up": normal((2 * F, d), seed + 5, std=std),
         "w_down": normal((d, F), seed + 6, std=std),
     }
+
+
+def normal_device(shape, seed: int, std: float = 1.0, mean: float = 0.0, dtype=BF16, device="cuda") -> torch.Tensor:
+    """Seeded N(mean, std^2) tensor drawn by torch's device generator (for full-size
+    weights too large to draw on the host quickly)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) & 0x7FFFFFFFFFFFFFFF)
+    t = torch.randn(tuple(shape), generator=g, dtype=F32, device=device)
+    if std != 1.0:
+        t.mul_(std)
+    if mean != 0.0:
+        t.add_(mean)
+    return t.to(dtype)
+
+
+def fill_paged(k_cache: torch.Tensor, v_cache: torch.Tensor, block_row, K: torch.Tensor, V: torch.Tensor, start: int = 0):
+    """Store K/V rows [L][Hkv][hd] of one request at positions start.. into paged caches
+    [num_pages][Hkv][page_size][hd] following its block-table row (pure data movement)."""
+    L = K.shape[0]
+    ps = k_cache.shape[2]
+    pos = torch.arange(start, start + L)
+    row = torch.as_tensor(np.asarray(block_row), dtype=torch.int64)
+    pages = row[pos // ps].to(k_cache.device)
+    slots = (pos % ps).to(k_cache.device)
+    k_cache[pages, :, slots, :] = K.to(k_cache.device, k_cache.dtype)
+    v_cache[pages, :, slots, :] = V.to(v_cache.device, v_cache.dtype)

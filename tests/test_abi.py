@@ -1,0 +1,68 @@
+"""The C ABI library builds, loads and exports every entry point include/bi.h declares (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bi.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bi_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from invariant_deterministic_02_gb300.build import build_library
+    return build_library()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ["bi_rmsnorm", "bi_gemm", "bi_decode_attention", "bi_prefill_attention", "bi_layer_forward",
+                 "bi_embed", "bi_topk", "bi_status_string", "bi_model_forward"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    out = subprocess.run(["nm", "-D", "--defined-only", libpath], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (bi_[a-z0-9_]+)$", out, flags=re.M))
+    missing = [s for s in declared_symbols() if s not in exported]
+    assert not missing, missing
+
+
+def test_library_loads_and_answers_without_gpu(libpath):
+    import invariant_deterministic_02_gb300 as bi
+    l = bi.lib()
+    for name in declared_symbols():
+        assert hasattr(l, name)
+    assert l.bi_status_string(0) == b"BI_OK"
+    assert l.bi_status_string(3) == b"BI_ERR_WORKSPACE"
+    assert l.bi_version() >= 100
+
+
+def test_host_validation_rejects_bad_arguments_before_launch(libpath):
+    # every check below fails on the host, so nothing reaches a GPU
+    import invariant_deterministic_02_gb300 as bi
+    l = bi.lib()
+    assert l.bi_gemm(None, None, None, None, 4, 8, 7, bi.BI_BF16, 0, -1, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert l.bi_gemm(None, None, None, None, 4, 12, 16, bi.BI_BF16, 0, -1, 0, None, 0, None) == bi.BI_ERR_UNSUPPORTED
+    assert b"multiples of 8" in l.bi_last_error_message()
+    assert l.bi_rmsnorm(None, None, None, 4, 12, bi.BI_BF16, 1e-5, 0, -1, 0, None, 0, None) == bi.BI_ERR_UNSUPPORTED
+    assert l.bi_rmsnorm(None, None, None, 4, 16, bi.BI_BF16, 1e-5, 7, -1, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert l.bi_rmsnorm(None, None, None, 4, 16, bi.BI_BF16, 1e-5, 2, 3, 5, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    d = bi.attn_dims(32, 8, 96, 4, 4)
+    assert l.bi_decode_attention(None, None, None, None, None, 1, ctypes.byref(d), None, 0, -1, None, 0,
+                                 None) == bi.BI_ERR_UNSUPPORTED
+    d = bi.attn_dims(32, 4, 128, 4, 4)  # 8 query heads per kv head is not built
+    assert l.bi_decode_attention(None, None, None, None, None, 1, ctypes.byref(d), None, 0, -1, None, 0,
+                                 None) == bi.BI_ERR_UNSUPPORTED
+    assert l.bi_topk(None, 2, 10, 40, None, None, None) == bi.BI_ERR_UNSUPPORTED
+    # zero-size work is a no-op that succeeds without touching pointers
+    assert l.bi_rmsnorm(None, None, None, 0, 16, bi.BI_BF16, 1e-5, 0, -1, 0, None, 0, None) == bi.BI_OK
+    assert l.bi_gemm(None, None, None, None, 0, 8, 16, bi.BI_BF16, 0, -1, 0, None, 0, None) == bi.BI_OK

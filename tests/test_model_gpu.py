@@ -1,0 +1,129 @@
+"""Whole model through bi_model_forward: oracle parity on a tiny model, and the
+target request's greedy tokens and top-20 logits bit-exact across every batch
+composition tried (neighbour count and lengths, slot index, prefill chunking)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.helpers import max_rel_err
+
+pytestmark = pytest.mark.gpu
+bi = pytest.importorskip("invariant_deterministic_02_gb300")
+from invariant_deterministic_02_gb300.model import QWEN3_8B, BiModel, ModelShape  # noqa: E402
+
+
+def tiny_shape():
+    return ModelShape(layer=synth.TINY_LAYER, n_layers=2, vocab=512, max_pos=2048)
+
+
+def test_tiny_model_prefill_and_decode_parity():
+    shape = tiny_shape()
+    m = BiModel.random(shape, seed=11, num_pages=256)
+    prompts = [synth.token_ids(n, shape.vocab, 90 + n) for n in (37, 5, 120)]
+    out = m.forward_batch([(i, p) for i, p in enumerate(prompts)])
+    w = m.host_weights()
+    kv = oracle.OracleKV(shape.n_layers, shape.layer.n_kv_heads, shape.layer.head_dim)
+    lens = [len(p) for p in prompts]
+    logits = oracle.model_forward(np.concatenate(prompts), w["embed"], w["layers"], w["final_norm"], w["lm_head"],
+                                  shape.layer, kv, [(i, n) for i, n in enumerate(lens)], [0, 0, 0])
+    last = np.cumsum(lens) - 1
+    got = out.logits.double().cpu().numpy()
+    assert max_rel_err(got, logits[last]) <= 2e-2
+    nxt = out.top_i[:, 0].cpu().numpy().astype(np.int32)
+    out2 = m.forward_batch([(i, nxt[i:i + 1]) for i in range(3)])
+    logits2 = oracle.model_forward(nxt, w["embed"], w["layers"], w["final_norm"], w["lm_head"], shape.layer, kv,
+                                   [(i, 1) for i in range(3)], lens)
+    assert max_rel_err(out2.logits.double().cpu().numpy(), logits2) <= 2e-2
+    # top-k of the GPU logits is exactly the oracle's selection on those same fp32 values
+    tv, ti = oracle.topk(out2.logits.double().cpu().numpy(), 20)
+    assert np.array_equal(out2.top_i.cpu().numpy(), ti)
+    assert np.array_equal(out2.top_v.double().cpu().numpy(), tv)
+
+
+def greedy_run(m: BiModel, prompt, steps, prefill_chunks, neighbours, target_slot, decode_neighbours, seed,
+               mode=bi.INVARIANT):
+    """Prefill the target prompt in the given chunks (each chunk batched with
+    prefilling neighbours), then greedy-decode `steps` tokens batched with
+    decode neighbours that carry random cached histories.  Returns the target's
+    tokens and per-step top-20 (values, indices)."""
+    m.reset()
+    rng = np.random.default_rng(seed)
+    V = m.shape.vocab
+    T = "target"
+    # prefill
+    p = 0
+    out = None
+    for ci, n in enumerate(prefill_chunks):
+        items = []
+        for j in range(neighbours):
+            r = ("pre", ci, j)
+            L = int(rng.integers(100, 1200))
+            items.append((r, synth.token_ids(L, V, seed * 31 + ci * 7 + j)))
+        slot = min(target_slot, len(items))
+        items.insert(slot, (T, prompt[p:p + n]))
+        res = m.forward_batch(items, k=20, mode=mode, target_request=slot if mode == bi.PROTECTED else -1)
+        out = (res, slot)
+        for r, _ in items:
+            if r != T:
+                m.release(r)
+        p += n
+    res, slot = out
+    tokens, tops = [], []
+    tok = int(res.top_i[slot, 0])
+    tokens.append(tok)
+    tops.append((res.top_v[slot].cpu().numpy().view(np.uint32).copy(), res.top_i[slot].cpu().numpy().copy()))
+    # decode
+    hist = synth.uniform_ints(decode_neighbours, 100, 8000, seed + 5)
+    nb_tok = {}
+    for j in range(decode_neighbours):
+        m.install_history(("dec", j), int(hist[j]), seed * 1000 + j)
+        nb_tok[("dec", j)] = int(rng.integers(0, V))
+    for s in range(steps - 1):
+        items = [(("dec", j), np.array([nb_tok[("dec", j)]], dtype=np.int32)) for j in range(decode_neighbours)]
+        slot = min(target_slot, len(items))
+        items.insert(slot, (T, np.array([tok], dtype=np.int32)))
+        res = m.forward_batch(items, k=20, mode=mode, target_request=slot if mode == bi.PROTECTED else -1)
+        ti = res.top_i[:, 0].cpu().numpy()
+        for b, (r, _) in enumerate(items):
+            if r != T:
+                nb_tok[r] = int(ti[b])
+        tok = int(ti[slot])
+        tokens.append(tok)
+        tops.append((res.top_v[slot].cpu().numpy().view(np.uint32).copy(), res.top_i[slot].cpu().numpy().copy()))
+    return tokens, tops
+
+
+def assert_same(a, b, what):
+    ta, pa = a
+    tb, pb = b
+    assert ta == tb, "%s: token sequences differ (first at %d)" % (
+        what, next(i for i, (x, y) in enumerate(zip(ta, tb)) if x != y))
+    for s, ((va, ia), (vb, ib)) in enumerate(zip(pa, pb)):
+        assert np.array_equal(ia, ib) and np.array_equal(va, vb), "%s: top-20 differs at step %d" % (what, s)
+
+
+def test_tiny_model_greedy_bit_exact_across_compositions():
+    shape = tiny_shape()
+    m = BiModel.random(shape, seed=12, num_pages=16384, page_seed=5)
+    prompt = synth.token_ids(64, shape.vocab, 1234)
+    ref = greedy_run(m, prompt, 30, [64], 0, 0, 0, seed=1)
+    for i, (chunks, nb, slot, dnb) in enumerate([([64], 3, 1, 5), ([32, 32], 1, 0, 15), ([7, 57], 2, 2, 63),
+                                                 ([1] * 4 + [60], 0, 0, 1)]):
+        got = greedy_run(m, prompt, 30, chunks, nb, slot, dnb, seed=10 + i)
+        assert_same(ref, got, "composition %d" % i)
+    got = greedy_run(m, prompt, 30, [40, 24], 3, 1, 7, seed=50, mode=bi.PROTECTED)
+    assert_same(ref, got, "protected")
+
+
+@pytest.mark.slow
+def test_qwen3_8b_greedy_200_tokens_bit_exact_across_compositions():
+    """Full Qwen3-8B-shaped random-init model: a 512-token seeded prompt, greedy 200 tokens."""
+    m = BiModel(QWEN3_8B, BiModel.random_weights(QWEN3_8B, seed=5), num_pages=36000, page_seed=9)
+    prompt = synth.token_ids(512, QWEN3_8B.vocab, 1234)
+    ref = greedy_run(m, prompt, 200, [512], 0, 0, 0, seed=1)
+    trials = [([97] * 5 + [27], 3, 2, 7), ([512], 1, 1, 63), ([256, 256], 2, 0, 31)]
+    for i, (chunks, nb, slot, dnb) in enumerate(trials):
+        got = greedy_run(m, prompt, 200, chunks, nb, slot, dnb, seed=20 + i)
+        assert_same(ref, got, "composition %d" % i)
