@@ -169,6 +169,30 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
                               const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, void* out, bi_mode mode,
                               int32_t target_request, void* workspace, size_t ws_bytes, bi_stream s);
 
+/* Decode attention for callers that cannot allocate device memory at call time
+ * (for example a plugin inside a host framework whose caching allocator owns all
+ * of the GPU's memory, or a serving loop that must never call cudaMalloc, which
+ * can synchronise the device).  Same arguments, computation and bits as
+ * bi_decode_attention, but no workspace: the scratch is a fixed 16 MiB array in
+ * the library's own device data, which every GPU that loads the library holds
+ * until the process exits.  The pages have no counterpart of this call.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Batches whose scratch need exceeds 16 MiB are rejected with
+ *     BI_ERR_UNSUPPORTED and a message naming the need (INVARIANT needs
+ *     B * ceil(max_pages*16/256) * num_q_heads * (head_dim+2) * 4 bytes plus a
+ *     few int32 per request; FAST/PROTECTED plan up to 64 splits per request).
+ *   - All calls share the one array and each call writes every scratch byte it
+ *     reads, so nothing needs clearing between calls; calls whose kernels
+ *     overlap on the GPU (e.g. on two streams) race on the array and must be
+ *     serialised by the caller. */
+bi_status bi_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_table, const int32_t* kv_lens, int32_t B,
+                                      const bi_attn_dims* dims, void* out, bi_mode mode, int32_t target_request,
+                                      bi_stream s);
+
 /* Prefill (any number of query tokens per request, causal by absolute position).
  * q: device [T][num_q_heads][head_dim] bf16, tokens of request b at rows
  * q_start[b] .. q_start[b+1]-1 (q_start device int32 [B+1], q_start[0] = 0,

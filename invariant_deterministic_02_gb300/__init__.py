@@ -38,7 +38,8 @@ TOPK_MAX = 32
 EXPORTED = [
     "bi_status_string", "bi_last_error_message", "bi_version", "bi_num_sms", "bi_device_error",
     "bi_rmsnorm_workspace", "bi_rmsnorm", "bi_gemm_workspace", "bi_gemm",
-    "bi_decode_attention_workspace", "bi_decode_attention", "bi_prefill_attention_workspace",
+    "bi_decode_attention_workspace", "bi_decode_attention", "bi_decode_attention_noalloc",
+    "bi_prefill_attention_workspace",
     "bi_prefill_attention", "bi_embed", "bi_rope_table", "bi_qkv_rope_store", "bi_swiglu", "bi_topk",
     "bi_layer_workspace", "bi_layer_forward", "bi_model_workspace", "bi_model_forward",
     "bi_profile_start", "bi_profile_stop", "bi_profile_read", "bi_profile_kernel_name", "bi_profile_kernel_count",
@@ -106,6 +107,7 @@ def _declare(lib):
         "bi_gemm": (c_i32, [vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i32, c_i32, c_i32, c_i32, vp, c_sz, vp]),
         "bi_decode_attention_workspace": (c_sz, [c_i32, P(AttnDims), c_i32]),
         "bi_decode_attention": (c_i32, [vp, vp, vp, vp, vp, c_i32, P(AttnDims), vp, c_i32, c_i32, vp, c_sz, vp]),
+        "bi_decode_attention_noalloc": (c_i32, [vp, vp, vp, vp, vp, c_i32, P(AttnDims), vp, c_i32, c_i32, vp]),
         "bi_prefill_attention_workspace": (c_sz, [c_i32, c_i32, P(AttnDims), c_i32]),
         "bi_prefill_attention": (c_i32, [vp, vp, vp, vp, vp, vp, c_i32, c_i32, P(AttnDims), vp, c_i32, c_i32, vp,
                                          c_sz, vp]),
@@ -229,6 +231,16 @@ def bi_decode_attention(q, k_cache, v_cache, block_table, kv_lens, dims: AttnDim
     _check(lib().bi_decode_attention(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(kv_lens), B,
                                      ctypes.byref(dims), _p(out), m, target_request, _p(ws), nb, _stream(stream)),
            "bi_decode_attention")
+    return out
+
+
+def bi_decode_attention_noalloc(q, k_cache, v_cache, block_table, kv_lens, dims: AttnDims, out, mode=INVARIANT,
+                                target_request=-1, stream=None):
+    """bi_decode_attention without a workspace: the library serves the scratch from a
+    fixed 16 MiB device array of its own (for callers that cannot allocate)."""
+    _check(lib().bi_decode_attention_noalloc(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(kv_lens),
+                                             q.shape[0], ctypes.byref(dims), _p(out), _mode(mode), target_request,
+                                             _stream(stream)), "bi_decode_attention_noalloc")
     return out
 
 

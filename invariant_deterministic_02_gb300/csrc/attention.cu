@@ -23,6 +23,8 @@
 // of values: per-lane FMA chain over the slot's 16 positions in order, xor 8
 // then 16 across slots, then the four warp sums added warp 0 + 1 + 2 + 3.
 #include <algorithm>
+#include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -877,6 +879,83 @@ bi_status prefill_attention_impl(const void* q, const void* kc, const void* vc, 
                    mode == BI_MODE_PROTECTED ? target : -1, w, s);
 }
 
+// ------------------------------------------------------------------ decode without a caller workspace
+// Some callers cannot allocate device memory when they call attention: a plugin
+// inside a host framework whose caching allocator owns all of the GPU's memory,
+// or a serving loop that must never call cudaMalloc (it can synchronise the
+// device).  bi_decode_attention_noalloc serves them from a fixed scratch array
+// that lives in this library's device data for as long as the library is loaded.
+namespace attn {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per GPU that loads the library
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+std::vector<void*> g_noalloc_address;  // device address of the scratch, per device
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+bi_status noalloc_scratch_address(void** out) {
+  int dev = 0;
+  BI_CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (dev >= static_cast<int>(g_noalloc_address.size())) g_noalloc_address.resize(dev + 1, nullptr);
+  if (g_noalloc_address[dev] == nullptr) {
+    void* p = nullptr;
+    BI_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    g_noalloc_address[dev] = p;
+  }
+  *out = g_noalloc_address[dev];
+  return BI_OK;
+}
+
+// Scratch layout of one call: the same plan and partial-state arrays as the
+// workspace path, with the partial states sized for the units `mode` can plan
+// (INVARIANT: one per 256 tokens of the longest allowed request).
+DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode mode) {
+  WsCarver cv(base, kNoAllocScratchBytes);
+  DecodeWs r;
+  r.plan.mode = cv.take<int>(B);
+  r.plan.ulen = cv.take<int>(B);
+  r.plan.nunits = cv.take<int>(B);
+  r.plan.prefix = cv.take<int>(B + 1);
+  const int inv = (dm->max_pages * kPage + kSplit - 1) / kSplit;
+  const size_t units = static_cast<size_t>(B) * (mode == BI_MODE_INVARIANT ? inv : std::max(inv, kMaxFastUnits));
+  r.part.m = cv.take<float>(units * dm->num_q_heads);
+  r.part.l = cv.take<float>(units * dm->num_q_heads);
+  r.part.o = cv.take<float>(units * dm->num_q_heads * dm->head_dim);
+  r.bytes = cv.used;
+  return r;
+}
+
+}  // namespace attn
+
+bi_status decode_attention_noalloc_impl(const void* q, const void* kc, const void* vc, const int32_t* bt,
+                                        const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, void* out,
+                                        bi_mode mode, int32_t target, cudaStream_t s) {
+  clear_error();
+  BI_TRY(attn::check_dims(dims));
+  BI_REQUIRE(B >= 0, BI_ERR_INVALID_ARG, "bi_decode_attention_noalloc: B=%d", B);
+  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+             static_cast<int>(mode));
+  BI_REQUIRE(mode != BI_MODE_PROTECTED || target < B, BI_ERR_INVALID_ARG, "target_request %d >= B %d", target, B);
+  if (B == 0) return BI_OK;
+  BI_REQUIRE(q && kc && vc && bt && kv_lens && out, BI_ERR_INVALID_ARG, "bi_decode_attention_noalloc: null pointer");
+  BI_REQUIRE(aligned16(q) && aligned16(kc) && aligned16(vc) && aligned16(out), BI_ERR_INVALID_ARG,
+             "bi_decode_attention_noalloc: q/caches/out must be 16-byte aligned");
+  const size_t need = attn::carve_decode_noalloc(nullptr, B, dims, mode).bytes;
+  BI_REQUIRE(need <= attn::kNoAllocScratchBytes, BI_ERR_UNSUPPORTED,
+             "bi_decode_attention_noalloc: this batch needs %zu bytes of scratch but the fixed scratch holds %zu "
+             "bytes; use bi_decode_attention with a caller workspace",
+             need, attn::kNoAllocScratchBytes);
+  void* base = nullptr;
+  BI_TRY(attn::noalloc_scratch_address(&base));
+  attn::DecodeWs w = attn::carve_decode_noalloc(base, B, dims, mode);
+  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, out, mode,
+                   mode == BI_MODE_PROTECTED ? target : -1, w, s);
+}
+
 size_t decode_attention_ws(int32_t B, const bi_attn_dims* dims) {
   if (B <= 0 || attn::check_dims(dims) != BI_OK) return 0;
   return attn::carve_decode(nullptr, 0, B, dims).bytes;
@@ -899,6 +978,14 @@ extern "C" bi_status bi_decode_attention(const void* q, const void* k_cache, con
                                          void* workspace, size_t ws_bytes, bi_stream s) {
   return bi::decode_attention_impl(q, k_cache, v_cache, block_table, kv_lens, B, dims, out, mode, target_request,
                                    workspace, ws_bytes, reinterpret_cast<cudaStream_t>(s));
+}
+
+extern "C" bi_status bi_decode_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                 const int32_t* block_table, const int32_t* kv_lens, int32_t B,
+                                                 const bi_attn_dims* dims, void* out, bi_mode mode,
+                                                 int32_t target_request, bi_stream s) {
+  return bi::decode_attention_noalloc_impl(q, k_cache, v_cache, block_table, kv_lens, B, dims, out, mode,
+                                           target_request, reinterpret_cast<cudaStream_t>(s));
 }
 
 extern "C" size_t bi_prefill_attention_workspace(int32_t B, int32_t T, const bi_attn_dims* dims, bi_mode) {
