@@ -49,6 +49,10 @@ def parse():
     ap.add_argument("--batch", type=int, default=BATCH)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["model", "attn", "gemm", "topk"], default="model",
+                    help="model: the decode-step workload; attn/gemm/topk: one kernel on a small single-layer "
+                         "case (for profiler captures), printing that kernel's timing")
+    ap.add_argument("--gemm-shape", default="64,24576,4096", help="M,N,K of --case gemm")
     return ap.parse_args()
 
 
@@ -391,8 +395,76 @@ def run_reference(args):
     return line
 
 
+def run_case(args):
+    """One kernel on a small case: decode attention over one layer's paged cache
+    (B requests, KV U{128..4096}), one GEMM, or top-k over B lm-head rows."""
+    import torch
+
+    import synth
+    import invariant_deterministic_02_gb300 as bi
+
+    dev = "cuda"
+    mode = bi.MODES[args.mode]
+    B = args.batch
+    K, W = args.steps, args.warmup
+    pk = peaks()
+    if args.case == "attn":
+        hq, hkv, hd = 32, 8, 128
+        Ls = synth.uniform_ints(B, KV_LO, KV_HI, args.seed)
+        lay = synth.paged_layout(Ls, 16, args.seed + 1)
+        kc = synth.normal_device((lay.num_pages, hkv, 16, hd), args.seed + 2)
+        vc = synth.normal_device((lay.num_pages, hkv, 16, hd), args.seed + 3)
+        q = synth.normal_device((B, hq, hd), args.seed + 4)
+        bt = torch.from_numpy(lay.block_table).to(dev)
+        kl = torch.from_numpy(Ls).to(dev)
+        dims = bi.attn_dims(hq, hkv, hd, lay.max_pages, lay.num_pages)
+        out = torch.empty_like(q)
+        ws = torch.empty(bi.lib().bi_decode_attention_workspace(B, ctypes.byref(dims), mode), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: bi.bi_decode_attention(q, kc, vc, bt, kl, dims, out, mode=mode, workspace=ws)
+        kernel, work, unit = "attn_decode_split", float(Ls.sum()) * hkv * hd * 2 * 2 + 2 * B * hq * hd * 2, "GB/s"
+        peak = pk["hbm_gbs"]
+    elif args.case == "gemm":
+        M, N, Kd = (int(v) for v in args.gemm_shape.split(","))
+        A = synth.normal_device((M, Kd), args.seed + 5)
+        Wt = synth.normal_device((N, Kd), args.seed + 6, std=0.02)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: bi.bi_gemm(A, Wt, C, mode=mode)
+        flops = 2.0 * M * N * Kd
+        byts = 2.0 * (M * Kd + N * Kd + M * N)
+        if flops / byts > pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9):
+            kernel, work, unit, peak = "gemm", flops, "TFLOP/s", pk["bf16_tflops"]
+        else:
+            kernel, work, unit, peak = "gemm", byts, "GB/s", pk["hbm_gbs"]
+    else:
+        V = 151936
+        x = synth.normal_device((B, V), args.seed + 7, dtype=torch.float32)
+        tv = torch.empty((B, TOPK), dtype=torch.float32, device=dev)
+        ti = torch.empty((B, TOPK), dtype=torch.int32, device=dev)
+        fn = lambda: bi.bi_topk(x, TOPK, tv, ti)
+        kernel, work, unit, peak = "topk", 4.0 * B * V, "GB/s", pk["hbm_gbs"]
+    for _ in range(W):
+        fn()
+    torch.cuda.synchronize()
+    bi.bi_profile_start(K * 8)
+    for _ in range(K):
+        fn()
+    torch.cuda.synchronize()
+    bi.bi_profile_stop()
+    n, ms = bi.bi_profile_read(kernel)
+    per = ms / n
+    achieved = work / (per / 1000.0) / (1e12 if unit == "TFLOP/s" else 1e9)
+    return {"case": args.case, "kernel": kernel, "launches": n, "launch_ms": round(per, 5),
+            "achieved": round(achieved, 2), "unit": unit, "peak": peak, "frac": round(achieved / peak, 4),
+            "work_per_launch": work, "batch": B, "mode": args.mode,
+            "shape": args.gemm_shape if args.case == "gemm" else None}
+
+
 def main():
     args = parse()
+    if args.case != "model":
+        print(json.dumps(run_case(args)), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -38,6 +38,7 @@ int num_sms() {
 
 // Defined next to the kernels that own a device error word.
 int take_gemm_device_error(cudaStream_t s, int32_t* code);
+int take_attn_device_error(cudaStream_t s, int32_t* code);
 
 // ------------------------------------------------------------------ launch timer
 volatile int g_profiling = 0;
@@ -148,11 +149,12 @@ extern "C" bi_status bi_device_error(int32_t* code, bi_stream s) {
   *code = 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   BI_CUDA_TRY(cudaStreamSynchronize(st));
-  int32_t c = 0;
-  if (bi::take_gemm_device_error(st, &c) != 0) {
+  int32_t c = 0, ca = 0;
+  if (bi::take_gemm_device_error(st, &c) != 0 || bi::take_attn_device_error(st, &ca) != 0) {
     bi::set_error("bi_device_error: reading the device error word failed");
     return BI_ERR_CUDA;
   }
+  if (c == 0) c = ca;
   *code = c;
   if (c != 0) {
     bi::set_error("an in-kernel wait ran out (site code %d)", c);

@@ -48,59 +48,165 @@ __device__ __forceinline__ void group_sync(int group) {
 // Per-group shared scratch of the split function.
 template <int HD, int G>
 struct SplitSmem {
-  float z[G][kSplit];        // scores (log2 domain), -inf where masked
-  float e[kSplit][G];        // exp2(z - m)
-  float o[4][G][HD];         // per-warp partial weighted sums
+  float z[G][kSplit];               // scores (log2 domain), -inf where masked
+  __align__(16) float e[kSplit][4]; // exp2(z - m), position-major, heads padded to 4
+  __align__(16) float o[4][G][HD];  // per-warp partial weighted sums
   float m[G];
   float l[G];
-  int page[kSplit / kPage + 1];  // physical pages of the split (global loader)
 };
+
+// ------------------------------------------------------------------ mbarrier / bulk-copy helpers
+__device__ unsigned int g_attn_err_word = 0;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: after 2 s (or once another thread of the CTA has given up) it
+// records `site` in the error word and returns false; callers then carry on
+// with whatever shared memory holds, so no thread is ever left waiting on a
+// barrier and the kernel always finishes (with wrong values, reported by
+// bi_device_error).
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort_flag) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        atomicCAS(&g_attn_err_word, 0u, static_cast<unsigned>(site));
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, site);
+}
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity) && global_ns() - t0 < kWaitLimitNs) {
+  }
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
 // Loaders return the 16-byte pieces of position `pp` (0..255 within the split)
 // that lane c owns: dims [8c, 8c+8) and, for head_dim 128, [64+8c, 64+8c+8).
+// The before_*/after_* hooks bracket a warp's reads of its quarter (positions
+// [64w, 64w+64)); they synchronise with the copy engine but do no arithmetic.
+//
+// Decode: quarters of the split stream through a ring of shared-memory stages,
+// filled page by page with bulk copies; order K0..K3, V0..V3 per split.
 template <int HD>
-struct GlobalKV {
-  const __nv_bfloat16* kc;
-  const __nv_bfloat16* vc;
-  const int* page;  // smem: physical page of positions start + 16i ..
-  int start_off;    // start % 16
-  int hkv, g;
-  __device__ __forceinline__ const __nv_bfloat16* row(const __nv_bfloat16* base, int pp) const {
-    const int r = start_off + pp;
-    const int pg = page[r >> 4];
-    return base + ((static_cast<size_t>(pg) * hkv + g) * kPage + (r & 15)) * HD;
-  }
+struct RingKV {
+  const __nv_bfloat16* ring;  // [stages][64*HD]
+  uint32_t full0, empty0;     // mbarrier arrays
+  int n0;                     // linear stage index of K0 of this split
+  int stages;
+  volatile int* abort_flag;
+  __device__ __forceinline__ int slot(int j) const { return (n0 + j) % stages; }
+  __device__ __forceinline__ uint32_t parity(int j) const { return static_cast<uint32_t>(((n0 + j) / stages) & 1); }
   __device__ __forceinline__ void k(int pp, int c, uint4 (&out)[HD / 64]) const {
-    const __nv_bfloat16* p = row(kc, pp);
+    const __nv_bfloat16* r = ring + static_cast<size_t>(slot(pp >> 6)) * 64 * HD + (pp & 63) * HD;
 #pragma unroll
-    for (int i = 0; i < HD / 64; ++i) out[i] = ld_stream(p + 64 * i + 8 * c);
+    for (int i = 0; i < HD / 64; ++i) out[i] = *reinterpret_cast<const uint4*>(r + 64 * i + 8 * c);
   }
-  __device__ __forceinline__ void v(int pp, int c, uint4 (&out)[HD / 64]) const {
-    const __nv_bfloat16* p = row(vc, pp);
-#pragma unroll
-    for (int i = 0; i < HD / 64; ++i) out[i] = ld_stream(p + 64 * i + 8 * c);
+  // the HD/64 words (HD/32 values) of value row pp that lane `lane` owns in the weighted sum
+  __device__ __forceinline__ void vpiece(int pp, int lane, uint32_t (&w)[HD / 64]) const {
+    const __nv_bfloat16* r =
+        ring + static_cast<size_t>(slot(4 + (pp >> 6))) * 64 * HD + (pp & 63) * HD + lane * (HD / 32);
+    if constexpr (HD == 128) {
+      const uint2 u = *reinterpret_cast<const uint2*>(r);
+      w[0] = u.x;
+      w[1] = u.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t*>(r);
+    }
+  }
+  __device__ __forceinline__ void before_k(int w) const { wait_bounded(full0 + 8 * slot(w), parity(w), abort_flag, 11); }
+  __device__ __forceinline__ void after_k(int w) const {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty0 + 8 * slot(w));
+  }
+  __device__ __forceinline__ void before_v(int w) const {
+    wait_bounded(full0 + 8 * slot(4 + w), parity(4 + w), abort_flag, 12);
+  }
+  __device__ __forceinline__ void after_v(int w) const {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(empty0 + 8 * slot(4 + w));
   }
 };
 
+// Prefill: the split's keys and values are staged whole in shared memory.
 template <int HD>
 struct SmemKV {
   const __nv_bfloat16* ks;  // [256][HD] positions start .. start+255
   const __nv_bfloat16* vs;
+  __device__ __forceinline__ void before_k(int) const {}
+  __device__ __forceinline__ void after_k(int) const {}
+  __device__ __forceinline__ void before_v(int) const {}
+  __device__ __forceinline__ void after_v(int) const {}
   __device__ __forceinline__ void k(int pp, int c, uint4 (&out)[HD / 64]) const {
 #pragma unroll
     for (int i = 0; i < HD / 64; ++i) out[i] = *reinterpret_cast<const uint4*>(ks + pp * HD + 64 * i + 8 * c);
   }
-  __device__ __forceinline__ void v(int pp, int c, uint4 (&out)[HD / 64]) const {
-#pragma unroll
-    for (int i = 0; i < HD / 64; ++i) out[i] = *reinterpret_cast<const uint4*>(vs + pp * HD + 64 * i + 8 * c);
+  __device__ __forceinline__ void vpiece(int pp, int lane, uint32_t (&w)[HD / 64]) const {
+    const __nv_bfloat16* r = vs + pp * HD + lane * (HD / 32);
+    if constexpr (HD == 128) {
+      const uint2 u = *reinterpret_cast<const uint2*>(r);
+      w[0] = u.x;
+      w[1] = u.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t*>(r);
+    }
   }
 };
 
-// Query registers of one lane: q[hh][dims owned by lane c], as fp32.
+// Query registers of one lane for the score phase: the dims lane c owns
+// (64i + 8c + 2m, 64i + 8c + 2m + 1) of each head, as fp32 pairs.
 template <int HD, int G>
 struct QRegs {
-  float q[G][HD / 8];
+  float2 q[G][HD / 16];
 };
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
 
 template <int HD, int G>
 __device__ __forceinline__ void load_q(const __nv_bfloat16* qrow /* [Hq][HD] at head g*G */, int c, QRegs<HD, G>& qr) {
@@ -109,12 +215,56 @@ __device__ __forceinline__ void load_q(const __nv_bfloat16* qrow /* [Hq][HD] at 
 #pragma unroll
     for (int i = 0; i < HD / 64; ++i) {
       const uint4 u = *reinterpret_cast<const uint4*>(qrow + hh * HD + 64 * i + 8 * c);
-      float f[8];
-      unpack8(u, f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qr.q[hh][8 * i + e] = f[e];
+      qr.q[hh][4 * i + 0] = bf16x2_to_float2(u.x);
+      qr.q[hh][4 * i + 1] = bf16x2_to_float2(u.y);
+      qr.q[hh][4 * i + 2] = bf16x2_to_float2(u.z);
+      qr.q[hh][4 * i + 3] = bf16x2_to_float2(u.w);
     }
   }
+}
+
+// Sum of the 8 partial dot products of one position held by lanes 8s..8s+7
+// (one per head in dot[]), reduced with halving exchanges: lane c ends with the
+// full sum of head head_of_lane(c).  The additions are those of a xor-butterfly
+// (offsets 4, 2, 1), so every lane that holds a head's sum holds the same bits.
+template <int G>
+__device__ __forceinline__ float reduce_scatter8(const float (&dot)[G], int c) {
+  if constexpr (G == 4) {
+    const bool hi = (c & 4) != 0;
+    const float k0 = hi ? dot[2] : dot[0], k1 = hi ? dot[3] : dot[1];
+    const float s0 = hi ? dot[0] : dot[2], s1 = hi ? dot[1] : dot[3];
+    const float a0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, s0, 4));
+    const float a1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, s1, 4));
+    const bool mid = (c & 2) != 0;
+    const float k = mid ? a1 : a0, snd = mid ? a0 : a1;
+    const float b = __fadd_rn(k, __shfl_xor_sync(0xffffffffu, snd, 2));
+    return __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 1));
+  } else if constexpr (G == 2) {
+    const bool hi = (c & 4) != 0;
+    const float k = hi ? dot[1] : dot[0], snd = hi ? dot[0] : dot[1];
+    float a = __fadd_rn(k, __shfl_xor_sync(0xffffffffu, snd, 4));
+    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    return __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  } else {
+    float a = dot[0];
+    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    return __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  }
+}
+
+template <int G>
+__device__ __forceinline__ int head_of_lane(int c) {
+  if constexpr (G == 4) return ((c >> 2) & 1) * 2 + ((c >> 1) & 1);
+  else if constexpr (G == 2) return (c >> 2) & 1;
+  else return 0;
+}
+
+template <int G>
+__device__ __forceinline__ bool writes_score(int c) {
+  if constexpr (G == 4) return (c & 1) == 0;
+  else if constexpr (G == 2) return (c & 3) == 0;
+  else return c == 0;
 }
 
 __host__ __device__ constexpr int outputs_per_thread(int HD, int G) { return (G * HD + kGroupThreads - 1) / kGroupThreads; }
@@ -123,10 +273,21 @@ __host__ __device__ constexpr int outputs_per_thread(int HD, int G) { return (G 
 // positions starting at the loader's origin take part.  On return every thread
 // holds its assigned weighted-sum outputs k = tid + 128*j (head k / HD, dim
 // k % HD) in `out`, and sm.m / sm.l hold the per-head max and sum.
+//
+// Fixed arithmetic order (the same whoever calls it):
+//  * score of position pp, head h: lane (slot, c) with pp = 64w + 4i + slot
+//    forms two interleaved FMA chains over its 16 (8 for head_dim 64) dims,
+//    even and odd dims (packed fp32 FMA), adds them, then the 8 lanes of the
+//    position are summed as a xor-butterfly 4, 2, 1; times scale*log2(e);
+//  * m = max of the scores (exact); e = exp2(z - m); l: lane L adds positions
+//    L, L+32, ..., L+224 in order, then a 32-lane butterfly;
+//  * o[h][d]: lane L owns dims (HD/32)L .. +HD/32; warp w adds e*v over its
+//    positions 64w .. 64w+63 in order; the four warp sums are added 0+1+2+3.
 template <int HD, int G, class KV>
 __device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& kv, int valid, float scale_log2,
                                              SplitSmem<HD, G>& sm, int group, float (&out)[outputs_per_thread(HD, G)]) {
-  constexpr int DPL = HD / 8;
+  constexpr int NW = HD / 16;  // bf16 pairs per lane in the score phase
+  constexpr int DPO = HD / 32; // dims per lane in the weighted sum
   const int tid = threadIdx.x % kGroupThreads;
   const int w = tid >> 5;
   const int lane = tid & 31;
@@ -134,54 +295,50 @@ __device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& k
   const int c = lane & 7;
 
   // ---- scores
-#pragma unroll 2
+  kv.before_k(w);
+#pragma unroll 4
   for (int i = 0; i < 16; ++i) {
     const int pp = 64 * w + 4 * i + slot;
     float dot[G];
     if (pp < valid) {
       uint4 kr[HD / 64];
       kv.k(pp, c, kr);
-      float kf[DPL];
+      float2 kf[NW];
 #pragma unroll
       for (int j = 0; j < HD / 64; ++j) {
-        float f[8];
-        unpack8(kr[j], f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) kf[8 * j + e] = f[e];
+        kf[4 * j + 0] = bf16x2_to_float2(kr[j].x);
+        kf[4 * j + 1] = bf16x2_to_float2(kr[j].y);
+        kf[4 * j + 2] = bf16x2_to_float2(kr[j].z);
+        kf[4 * j + 3] = bf16x2_to_float2(kr[j].w);
       }
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        float a = 0.f;
+        float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) a = __fmaf_rn(qr.q[hh][e], kf[e], a);
-        dot[hh] = a;
+        for (int e = 0; e < NW; ++e) a = __ffma2_rn(qr.q[hh][e], kf[e], a);
+        dot[hh] = __fadd_rn(a.x, a.y);
       }
     } else {
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) dot[hh] = 0.f;
     }
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      float a = dot[hh];
-      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 4));
-      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
-      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
-      if (c == hh) sm.z[hh][pp] = (pp < valid) ? __fmul_rn(a, scale_log2) : -INFINITY;
-    }
+    const float full = reduce_scatter8<G>(dot, c);
+    if (writes_score<G>(c)) sm.z[head_of_lane<G>(c)][pp] = (pp < valid) ? __fmul_rn(full, scale_log2) : -INFINITY;
   }
+  kv.after_k(w);
   group_sync(group);
 
   // ---- per-head max (exact, order-free) and sum of exponentials (fixed order)
   for (int hh = w; hh < G; hh += 4) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, sm.z[hh][8 * lane + j]);
+    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, sm.z[hh][lane + 32 * j]);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int pp = 8 * lane + j;
+      const int pp = lane + 32 * j;
       const float e = (pp < valid) ? exp2f(__fsub_rn(sm.z[hh][pp], mx)) : 0.f;
       sm.e[pp][hh] = e;
       s = __fadd_rn(s, e);
@@ -196,47 +353,36 @@ __device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& k
   group_sync(group);
 
   // ---- weighted sum of values
-  float acc[G][DPL];
+  float2 acc[G][DPO / 2];
 #pragma unroll
   for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.f;
-#pragma unroll 2
-  for (int i = 0; i < 16; ++i) {
-    const int pp = 64 * w + 4 * i + slot;
-    if (pp < valid) {
-      uint4 vr[HD / 64];
-      kv.v(pp, c, vr);
-      float vf[DPL];
+    for (int e = 0; e < DPO / 2; ++e) acc[hh][e] = make_float2(0.f, 0.f);
+  kv.before_v(w);
+  const int nv = min(64, valid - 64 * w);  // positions of this warp (uniform across the warp)
+#pragma unroll 4
+  for (int j = 0; j < nv; ++j) {
+    const int pp = 64 * w + j;
+    uint32_t vw[HD / 64];
+    kv.vpiece(pp, lane, vw);
+    const float4 e4 = *reinterpret_cast<const float4*>(&sm.e[pp][0]);
+    const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
-      for (int j = 0; j < HD / 64; ++j) {
-        float f[8];
-        unpack8(vr[j], f);
+    for (int hh = 0; hh < G; ++hh) {
+      const float2 p2 = make_float2(ev[hh], ev[hh]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) vf[8 * j + e] = f[e];
-      }
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const float p = sm.e[pp][hh];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[hh][e] = __fmaf_rn(p, vf[e], acc[hh][e]);
-      }
+      for (int e = 0; e < DPO / 2; ++e) acc[hh][e] = __ffma2_rn(p2, bf16x2_to_float2(vw[e]), acc[hh][e]);
     }
   }
+  kv.after_v(w);
 #pragma unroll
-  for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      float a = acc[hh][e];
-      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 8));
-      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 16));
-      acc[hh][e] = a;
+  for (int hh = 0; hh < G; ++hh) {
+    float* dst = &sm.o[w][hh][lane * DPO];
+    if constexpr (DPO == 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
+    } else {
+      *reinterpret_cast<float2*>(dst) = acc[hh][0];
     }
-  if (slot == 0) {
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) sm.o[w][hh][64 * (e >> 3) + 8 * c + (e & 7)] = acc[hh][e];
   }
   group_sync(group);
 #pragma unroll
@@ -267,18 +413,73 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float& o, float 
   m = mx;
 }
 
+struct Partials {
+  float* m;  // [units][Hq]
+  float* l;  // [units][Hq]
+  float* o;  // [units][Hq][HD]
+};
+
+// Merge of the split states of one row (a decode request or a prefill token)
+// for all heads of one kv group: thread (hh, d).  INVARIANT rows combine the
+// states in a pairwise tree over the split index (binary-counter form: the same
+// tree as the level-by-level tree over 2^BI_MERGE_DEPTH leaves padded with
+// empty states, since an empty state is an exact identity); FAST rows combine
+// left to right.
+// Partial states are read through L2 (__ldcg): in the decode kernel they were
+// written by other CTAs of the same launch.
+__device__ __forceinline__ void merge_row(const Partials& part, size_t first_unit, int n, bool tree, int hq, int hd,
+                                          int h, int d, float& out_m, float& out_l, float& out_o) {
+  float m = -INFINITY, l = 0.f, o = 0.f;
+  if (!tree) {
+    for (int s = 0; s < n; ++s) {
+      const size_t pi = (first_unit + s) * hq + h;
+      merge_state(m, l, o, __ldcg(part.m + pi), __ldcg(part.l + pi), __ldcg(part.o + pi * hd + d));
+    }
+  } else {
+    float sm_[BI_MERGE_DEPTH + 1], sl_[BI_MERGE_DEPTH + 1], so_[BI_MERGE_DEPTH + 1];
+    unsigned occ = 0;
+    for (int s = 0; s < n; ++s) {
+      const size_t pi = (first_unit + s) * hq + h;
+      float cm = __ldcg(part.m + pi), cl = __ldcg(part.l + pi), co = __ldcg(part.o + pi * hd + d);
+      int lvl = 0;
+      while (occ & (1u << lvl)) {
+        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
+        merge_state(am, al, ao, cm, cl, co);  // stack entry covers the lower indices
+        cm = am; cl = al; co = ao;
+        occ &= ~(1u << lvl);
+        ++lvl;
+      }
+      sm_[lvl] = cm; sl_[lvl] = cl; so_[lvl] = co;
+      occ |= (1u << lvl);
+    }
+    // fold what is left, smallest (rightmost) subtree first: merge(stack[lvl], acc)
+    for (int lvl = 0; lvl <= BI_MERGE_DEPTH; ++lvl) {
+      if (occ & (1u << lvl)) {
+        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
+        merge_state(am, al, ao, m, l, o);
+        m = am; l = al; o = ao;
+      }
+    }
+  }
+  out_m = m;
+  out_l = l;
+  out_o = o;
+}
+
 // ------------------------------------------------------------------ decode
 // Plan per request b: geometry (invariant or fast), unit length, unit count,
 // exclusive prefix of unit counts.  One CTA; B may be large.
 struct DecodePlan {
-  int* mode;    // [B]
-  int* ulen;    // [B] positions per unit
-  int* nunits;  // [B]
-  int* prefix;  // [B+1]
+  int* mode;     // [B]
+  int* ulen;     // [B] positions per unit
+  int* nunits;   // [B]
+  int* prefix;   // [B+1]
 };
 
-__global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict__ kv_lens, int B, int mode,
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict__ kv_lens, int B, int hkv, int mode,
                                                            int target, int fast_units_wanted, DecodePlan plan) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int part[1024];
   const int t = threadIdx.x;
   const int per = (B + 1023) / 1024;
@@ -330,23 +531,103 @@ __device__ __forceinline__ int find_row(const int* prefix, int n, int u) {
   return lo;
 }
 
-struct Partials {
-  float* m;  // [units][Hq]
-  float* l;  // [units][Hq]
-  float* o;  // [units][Hq][HD]
+// Decode split kernel: a persistent CTA of one 128-thread consumer group plus a
+// producer warp.  The producer streams every split's K and V (in quarters of
+// 64 positions = 4 pages of one kv head, one bulk copy per page) into a ring of
+// shared-memory stages; the consumers run split_reduce on each split as soon as
+// its quarters land.  A unit (one request, one kv head, one planned range) is
+// one 256-position split under the invariant plan, or several consecutive
+// 256-position blocks combined left to right under the FAST plan.
+constexpr int kDecodeStages = 5;
+constexpr int kDecodeThreads = kGroupThreads + 32;
+
+template <int HD, int G>
+struct DecodeSmem {
+  __nv_bfloat16 ring[kDecodeStages][64 * HD];
+  SplitSmem<HD, G> sm;
+  unsigned long long full[kDecodeStages];
+  unsigned long long empty[kDecodeStages];
+  int abort_flag;
 };
 
 template <int HD, int G>
-__global__ void __launch_bounds__(kGroupThreads) decode_split_kernel(
+__global__ void __launch_bounds__(kDecodeThreads, 2) decode_split_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vc,
     const int* __restrict__ block_table, const int* __restrict__ kv_lens, int B, int hq, int hkv, int max_pages,
     float scale_log2, DecodePlan plan, Partials part) {
-  __shared__ __align__(16) SplitSmem<HD, G> sm;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>(smem_raw);
+  const uint32_t full0 = smem_u32(&S.full[0]);
+  const uint32_t empty0 = smem_u32(&S.empty[0]);
+  volatile int* abort_flag = &S.abort_flag;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecodeStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int total = plan.prefix[B] * hkv;
+
+  if (threadIdx.x >= kGroupThreads) {
+    // ---------------------------------------------------------------- producer warp
+    // Lane 0 claims each stage (waits for it to be free, arms its barrier with
+    // the byte count); lanes 0..3 then issue one page copy each, so the copies
+    // of a stage are in flight together.
+    const int plane = threadIdx.x - kGroupThreads;
+    int n = 0;
+    uint32_t issued = 0, ipar = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+      const int u = item / hkv;
+      const int g = item % hkv;
+      const int b = find_row(plan.prefix, B, u);
+      const int s = u - plan.prefix[b];
+      const int L = kv_lens[b];
+      const int ul = plan.ulen[b];
+      const int ustart = s * ul;
+      const int uend = min(L, ustart + ul);
+      const int* brow = block_table + static_cast<size_t>(b) * max_pages;
+      for (int bs = ustart; bs < uend; bs += kSplit) {
+        const int valid = min(kSplit, uend - bs);
+        for (int j = 0; j < 8; ++j, ++n) {
+          const int st = n % kDecodeStages;
+          const uint32_t ph = static_cast<uint32_t>((n / kDecodeStages) & 1);
+          const int q0 = (j & 3) * 64;
+          const int nv = max(0, min(64, valid - q0));
+          const int npg = (nv + kPage - 1) / kPage;
+          const uint32_t fb = full0 + 8 * st;
+          if (plane == 0) {
+            wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 13);
+            mbar_expect_tx(fb, static_cast<uint32_t>(npg * kPage * HD * 2));
+          }
+          __syncwarp();
+          if (plane < npg) {
+            const __nv_bfloat16* cache = (j < 4) ? kc : vc;
+            const int page = brow[(bs + q0) / kPage + plane];
+            const __nv_bfloat16* src = cache + (static_cast<size_t>(page) * hkv + g) * kPage * HD;
+            bulk_g2s(smem_u32(&S.ring[st][plane * kPage * HD]), src, kPage * HD * 2, fb);
+          }
+          issued |= 1u << st;
+          ipar = (ipar & ~(1u << st)) | (ph << st);
+        }
+      }
+    }
+    // keep the CTA resident until every copy it issued has landed
+    if (plane == 0)
+      for (int i = 0; i < kDecodeStages; ++i)
+        if (issued & (1u << i)) wait_drain(full0 + 8 * i, (ipar >> i) & 1u);
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
   constexpr int OPT = outputs_per_thread(HD, G);
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int c = lane & 7;
-  const int total = plan.prefix[B] * hkv;
+  const int c = (tid & 31) & 7;
+  int n0 = 0;
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
     const int u = item / hkv;
     const int g = item % hkv;
@@ -367,16 +648,11 @@ __global__ void __launch_bounds__(kGroupThreads) decode_split_kernel(
 #pragma unroll
     for (int j = 0; j < OPT; ++j) ro[j] = 0.f;
     bool first = true;
-    for (int bs = ustart; bs < uend; bs += kSplit) {
+    for (int bs = ustart; bs < uend; bs += kSplit, n0 += 8) {
       const int valid = min(kSplit, uend - bs);
-      if (tid <= (kSplit / kPage)) {
-        const int pi = bs / kPage + tid;
-        sm.page[tid] = (pi * kPage < uend) ? block_table[static_cast<size_t>(b) * max_pages + pi] : 0;
-      }
-      group_sync(0);
-      GlobalKV<HD> kv{kc, vc, sm.page, bs % kPage, hkv, g};
+      RingKV<HD> kv{&S.ring[0][0], full0, empty0, n0, kDecodeStages, abort_flag};
       float bo[OPT];
-      split_reduce<HD, G>(qr, kv, valid, scale_log2, sm, 0, bo);
+      split_reduce<HD, G>(qr, kv, valid, scale_log2, S.sm, 0, bo);
 #pragma unroll
       for (int j = 0; j < OPT; ++j) {
         const int k = tid + kGroupThreads * j;
@@ -386,22 +662,22 @@ __global__ void __launch_bounds__(kGroupThreads) decode_split_kernel(
             ro[j] = bo[j];
           } else {
             float mm = rm[hh], ll = rl[hh];
-            merge_state(mm, ll, ro[j], sm.m[hh], sm.l[hh], bo[j]);
+            merge_state(mm, ll, ro[j], S.sm.m[hh], S.sm.l[hh], bo[j]);
           }
         }
       }
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
         if (first) {
-          rm[hh] = sm.m[hh];
-          rl[hh] = sm.l[hh];
+          rm[hh] = S.sm.m[hh];
+          rl[hh] = S.sm.l[hh];
         } else {
           float oo = 0.f;
-          merge_state(rm[hh], rl[hh], oo, sm.m[hh], sm.l[hh], 0.f);
+          merge_state(rm[hh], rl[hh], oo, S.sm.m[hh], S.sm.l[hh], 0.f);
         }
       }
       first = false;
-      group_sync(0);  // smem reused by the next block / item
+      group_sync(0);  // the group scratch is reused by the next split
     }
     const size_t pidx = static_cast<size_t>(u) * hq + g * G;
 #pragma unroll
@@ -416,53 +692,12 @@ __global__ void __launch_bounds__(kGroupThreads) decode_split_kernel(
   }
 }
 
-// Merge of the split states of one row (a decode request or a prefill token)
-// for all heads of one kv group: thread (hh, d).  INVARIANT rows combine the
-// states in a pairwise tree over the split index (binary-counter form: the same
-// tree as the level-by-level tree over 2^BI_MERGE_DEPTH leaves padded with
-// empty states, since an empty state is an exact identity); FAST rows combine
-// left to right.
-__device__ __forceinline__ void merge_row(const Partials& part, size_t first_unit, int n, bool tree, int hq, int hd,
-                                          int h, int d, float& out_m, float& out_l, float& out_o) {
-  float m = -INFINITY, l = 0.f, o = 0.f;
-  if (!tree) {
-    for (int s = 0; s < n; ++s) {
-      const size_t pi = (first_unit + s) * hq + h;
-      merge_state(m, l, o, part.m[pi], part.l[pi], part.o[pi * hd + d]);
-    }
-  } else {
-    float sm_[BI_MERGE_DEPTH + 1], sl_[BI_MERGE_DEPTH + 1], so_[BI_MERGE_DEPTH + 1];
-    unsigned occ = 0;
-    for (int s = 0; s < n; ++s) {
-      const size_t pi = (first_unit + s) * hq + h;
-      float cm = part.m[pi], cl = part.l[pi], co = part.o[pi * hd + d];
-      int lvl = 0;
-      while (occ & (1u << lvl)) {
-        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
-        merge_state(am, al, ao, cm, cl, co);  // stack entry covers the lower indices
-        cm = am; cl = al; co = ao;
-        occ &= ~(1u << lvl);
-        ++lvl;
-      }
-      sm_[lvl] = cm; sl_[lvl] = cl; so_[lvl] = co;
-      occ |= (1u << lvl);
-    }
-    // fold what is left, smallest (rightmost) subtree first: merge(stack[lvl], acc)
-    for (int lvl = 0; lvl <= BI_MERGE_DEPTH; ++lvl) {
-      if (occ & (1u << lvl)) {
-        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
-        merge_state(am, al, ao, m, l, o);
-        m = am; l = al; o = ao;
-      }
-    }
-  }
-  out_m = m;
-  out_l = l;
-  out_o = o;
-}
 
+// Merge of the split states of each (request, query head) in a second kernel.
 __global__ void decode_merge_kernel(const Partials part, DecodePlan plan, __nv_bfloat16* __restrict__ out, int B,
                                     int hq, int hkv, int hd) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x / hkv;
   const int g = blockIdx.x % hkv;
   const int G = hq / hkv;
@@ -520,6 +755,8 @@ __device__ __forceinline__ void split_range(bool inv, int pos0, int s, int p, in
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int* __restrict__ q_start,
                                                             const int* __restrict__ q_pos0, int B, int T, int mode,
                                                             int target, PrefillPlan plan) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int part[1024];
 
   const int t = threadIdx.x;
@@ -605,7 +842,9 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vc,
     const int* __restrict__ block_table, const int* __restrict__ q_pos0, const int* __restrict__ q_start, int hq,
     int hkv, int max_pages, float scale_log2, PrefillPlan plan, Partials part) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   PrefillSmem<HD, G>& sm = *reinterpret_cast<PrefillSmem<HD, G>*>(smem_raw);
   constexpr int OPT = outputs_per_thread(HD, G);
   const int group = threadIdx.x / kGroupThreads;
@@ -670,6 +909,8 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
 __global__ void prefill_merge_kernel(const Partials part, PrefillPlan plan, const int* __restrict__ q_start,
                                      const int* __restrict__ q_pos0, int B, __nv_bfloat16* __restrict__ out, int hq,
                                      int hkv, int hd) {
+  pdl_wait();
+  pdl_trigger();
   const int tok = blockIdx.x / hkv;
   const int g = blockIdx.x % hkv;
   const int G = hq / hkv;
@@ -720,18 +961,30 @@ struct DecodeWs {
   size_t bytes;
 };
 
-DecodeWs carve_decode(void* ws, size_t cap, int B, const bi_attn_dims* dm) {
-  WsCarver cv(ws, cap);
+// Plan arrays of a decode batch (small; reusable by every layer of a step).
+size_t carve_decode_plan(void* base, int B, int hkv, DecodePlan* plan) {
+  WsCarver cv(base, 0);
+  plan->mode = cv.take<int>(B);
+  plan->ulen = cv.take<int>(B);
+  plan->nunits = cv.take<int>(B);
+  plan->prefix = cv.take<int>(B + 1);
+  return align_up(cv.used, 256);
+}
+
+size_t carve_decode_parts(void* base, size_t units, const bi_attn_dims* dm, Partials* part) {
+  WsCarver cv(base, 0);
+  part->m = cv.take<float>(units * dm->num_q_heads);
+  part->l = cv.take<float>(units * dm->num_q_heads);
+  part->o = cv.take<float>(units * dm->num_q_heads * dm->head_dim);
+  return align_up(cv.used, 256);
+}
+
+DecodeWs carve_decode(void* ws, size_t, int B, const bi_attn_dims* dm) {
   DecodeWs r;
-  r.plan.mode = cv.take<int>(B);
-  r.plan.ulen = cv.take<int>(B);
-  r.plan.nunits = cv.take<int>(B);
-  r.plan.prefix = cv.take<int>(B + 1);
+  const size_t pb = carve_decode_plan(ws, B, dm->num_kv_heads, &r.plan);
   const size_t units = static_cast<size_t>(B) * max_units_per_request(dm);
-  r.part.m = cv.take<float>(units * dm->num_q_heads);
-  r.part.l = cv.take<float>(units * dm->num_q_heads);
-  r.part.o = cv.take<float>(units * dm->num_q_heads * dm->head_dim);
-  r.bytes = cv.used;
+  const size_t qb = carve_decode_parts(ws ? static_cast<char*>(ws) + pb : nullptr, units, dm, &r.part);
+  r.bytes = pb + qb;
   return r;
 }
 
@@ -768,8 +1021,11 @@ template <int HD, int G>
 int decode_grid() {
   static int per_sm = 0;
   if (per_sm == 0) {
+    const size_t smem = sizeof(DecodeSmem<HD, G>);
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<HD, G>, kGroupThreads, 0) !=
+    if (cudaFuncSetAttribute(decode_split_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<HD, G>, kDecodeThreads, smem) !=
             cudaSuccess ||
         n < 1)
       n = 1;
@@ -781,18 +1037,27 @@ int decode_grid() {
 template <int HD, int G>
 bi_status decode_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* kv_lens,
                         int B, const bi_attn_dims* dm, void* out, bi_mode mode, int target, const DecodeWs& w,
-                        cudaStream_t s) {
-  const int fast_units = std::max(1, (4 * num_sms() + B * dm->num_kv_heads - 1) / (B * dm->num_kv_heads));
-  BI_TIMED(::bi::kTagAttnPlan, s, decode_plan_kernel<<<1, 1024, 0, s>>>(kv_lens, B, static_cast<int>(mode), target, fast_units, w.plan));
-  BI_LAUNCH_CHECK();
+                        cudaStream_t s, bool make_plan = true) {
+  if (make_plan) {
+    const int fast_units = std::max(1, (4 * num_sms() + B * dm->num_kv_heads - 1) / (B * dm->num_kv_heads));
+    BI_TIMED(::bi::kTagAttnPlan, s,
+             BI_PDL_CHECK(launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, kv_lens, B, dm->num_kv_heads, static_cast<int>(mode), target,
+                                                    fast_units, w.plan)));
+    BI_LAUNCH_CHECK();
+  }
   const float sl2 = dm->scale * kLog2e;
-  BI_TIMED(::bi::kTagAttnDecodeSplit, s, decode_split_kernel<HD, G><<<decode_grid<HD, G>(), kGroupThreads, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
-      static_cast<const __nv_bfloat16*>(vc), bt, kv_lens, B, dm->num_q_heads, dm->num_kv_heads, dm->max_pages, sl2,
-      w.plan, w.part));
+  const int grid = decode_grid<HD, G>();
+  const size_t dsmem = sizeof(DecodeSmem<HD, G>);
+  BI_TIMED(::bi::kTagAttnDecodeSplit, s,
+           BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G>, dim3(grid), dim3(kDecodeThreads), dsmem, s, 
+               static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
+               static_cast<const __nv_bfloat16*>(vc), bt, kv_lens, B, dm->num_q_heads, dm->num_kv_heads,
+               dm->max_pages, sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
-  BI_TIMED(::bi::kTagAttnDecodeMerge, s, decode_merge_kernel<<<B * dm->num_kv_heads, G * HD, 0, s>>>(w.part, w.plan, static_cast<__nv_bfloat16*>(out), B,
-                                                              dm->num_q_heads, dm->num_kv_heads, HD));
+  BI_TIMED(::bi::kTagAttnDecodeMerge, s,
+           BI_PDL_CHECK(launch_pdl(decode_merge_kernel, dim3(B * dm->num_kv_heads), dim3(G * HD), 0, s, w.part,
+                                   w.plan, static_cast<__nv_bfloat16*>(out), B, dm->num_q_heads, dm->num_kv_heads,
+                                   HD)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -801,7 +1066,7 @@ template <int HD, int G>
 bi_status prefill_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* q_start,
                          const int32_t* q_pos0, int B, int T, const bi_attn_dims* dm, void* out, bi_mode mode,
                          int target, const PrefillWs& w, cudaStream_t s) {
-  BI_TIMED(::bi::kTagAttnPlan, s, prefill_plan_kernel<<<1, 1024, 0, s>>>(q_start, q_pos0, B, T, static_cast<int>(mode), target, w.plan));
+  BI_TIMED(::bi::kTagAttnPlan, s, BI_PDL_CHECK(launch_pdl(prefill_plan_kernel, dim3(1), dim3(1024), 0, s, q_start, q_pos0, B, T, static_cast<int>(mode), target, w.plan)));
   BI_LAUNCH_CHECK();
   const size_t smem = sizeof(PrefillSmem<HD, G>);
   static bool attr_set = false;
@@ -811,14 +1076,14 @@ bi_status prefill_launch(const void* q, const void* kc, const void* vc, const in
     attr_set = true;
   }
   const float sl2 = dm->scale * kLog2e;
-  BI_TIMED(::bi::kTagAttnPrefillSplit, s, prefill_split_kernel<HD, G><<<num_sms(), kGroupThreads * kPrefillGroups, smem, s>>>(
+  BI_TIMED(::bi::kTagAttnPrefillSplit, s, BI_PDL_CHECK(launch_pdl(prefill_split_kernel<HD, G>, dim3(num_sms()), dim3(kGroupThreads * kPrefillGroups), smem, s, 
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
       static_cast<const __nv_bfloat16*>(vc), bt, q_pos0, q_start, dm->num_q_heads, dm->num_kv_heads, dm->max_pages,
-      sl2, w.plan, w.part));
+      sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
-  BI_TIMED(::bi::kTagAttnPrefillMerge, s, prefill_merge_kernel<<<T * dm->num_kv_heads, G * HD, 0, s>>>(w.part, w.plan, q_start, q_pos0, B,
+  BI_TIMED(::bi::kTagAttnPrefillMerge, s, BI_PDL_CHECK(launch_pdl(prefill_merge_kernel, dim3(T * dm->num_kv_heads), dim3(G * HD), 0, s, w.part, w.plan, q_start, q_pos0, B,
                                                                static_cast<__nv_bfloat16*>(out), dm->num_q_heads,
-                                                               dm->num_kv_heads, HD));
+                                                               dm->num_kv_heads, HD)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -914,18 +1179,12 @@ bi_status noalloc_scratch_address(void** out) {
 // workspace path, with the partial states sized for the units `mode` can plan
 // (INVARIANT: one per 256 tokens of the longest allowed request).
 DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode mode) {
-  WsCarver cv(base, kNoAllocScratchBytes);
   DecodeWs r;
-  r.plan.mode = cv.take<int>(B);
-  r.plan.ulen = cv.take<int>(B);
-  r.plan.nunits = cv.take<int>(B);
-  r.plan.prefix = cv.take<int>(B + 1);
+  const size_t pb = carve_decode_plan(base, B, dm->num_kv_heads, &r.plan);
   const int inv = (dm->max_pages * kPage + kSplit - 1) / kSplit;
   const size_t units = static_cast<size_t>(B) * (mode == BI_MODE_INVARIANT ? inv : std::max(inv, kMaxFastUnits));
-  r.part.m = cv.take<float>(units * dm->num_q_heads);
-  r.part.l = cv.take<float>(units * dm->num_q_heads);
-  r.part.o = cv.take<float>(units * dm->num_q_heads * dm->head_dim);
-  r.bytes = cv.used;
+  const size_t qb = carve_decode_parts(base ? static_cast<char*>(base) + pb : nullptr, units, dm, &r.part);
+  r.bytes = pb + qb;
   return r;
 }
 
@@ -956,6 +1215,33 @@ bi_status decode_attention_noalloc_impl(const void* q, const void* kc, const voi
                    mode == BI_MODE_PROTECTED ? target : -1, w, s);
 }
 
+// Decode attention for the layer loop: the plan lives in `plan_ws` (sized by
+// decode_plan_bytes) and is built only when make_plan is set, so the layers of
+// one step share it; the partial states live in `part_ws`.
+size_t decode_plan_bytes(int32_t B, int32_t hkv) {
+  attn::DecodePlan p;
+  return attn::carve_decode_plan(nullptr, B, hkv, &p);
+}
+
+size_t decode_parts_bytes(int32_t B, const bi_attn_dims* dims) {
+  attn::Partials p;
+  return attn::carve_decode_parts(nullptr, static_cast<size_t>(B) * attn::max_units_per_request(dims), dims, &p);
+}
+
+bi_status decode_attention_layer(const void* q, const void* kc, const void* vc, const int32_t* bt,
+                                 const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, void* out, bi_mode mode,
+                                 int32_t target, void* plan_ws, bool make_plan, void* part_ws, size_t part_bytes,
+                                 cudaStream_t s) {
+  BI_TRY(attn::check_dims(dims));
+  BI_REQUIRE(B >= 1 && plan_ws && part_ws && part_bytes >= decode_parts_bytes(B, dims), BI_ERR_WORKSPACE,
+             "decode attention: workspace");
+  attn::DecodeWs w;
+  attn::carve_decode_plan(plan_ws, B, dims->num_kv_heads, &w.plan);
+  attn::carve_decode_parts(part_ws, static_cast<size_t>(B) * attn::max_units_per_request(dims), dims, &w.part);
+  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, out, mode,
+                   mode == BI_MODE_PROTECTED ? target : -1, w, s, make_plan);
+}
+
 size_t decode_attention_ws(int32_t B, const bi_attn_dims* dims) {
   if (B <= 0 || attn::check_dims(dims) != BI_OK) return 0;
   return attn::carve_decode(nullptr, 0, B, dims).bytes;
@@ -964,6 +1250,22 @@ size_t decode_attention_ws(int32_t B, const bi_attn_dims* dims) {
 size_t prefill_attention_ws(int32_t B, int32_t T, const bi_attn_dims* dims) {
   if (B <= 0 || T <= 0 || attn::check_dims(dims) != BI_OK) return 0;
   return attn::carve_prefill(nullptr, 0, B, T, dims).bytes;
+}
+
+int take_attn_device_error(cudaStream_t s, int32_t* code) {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, attn::g_attn_err_word, sizeof(v), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return 1;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return 1;
+  if (v != 0) {
+    unsigned zero = 0;
+    if (cudaMemcpyToSymbolAsync(attn::g_attn_err_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return 1;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return 1;
+  }
+  *code = static_cast<int32_t>(v);
+  return 0;
 }
 
 }  // namespace bi

@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <string>
+#include <utility>
 
 #include "../../include/bi.h"
 
@@ -82,6 +83,34 @@ void prof_end(int slot, cudaStream_t s);
     __VA_ARGS__;                                                              \
     if (prof_slot_ >= 0) ::bi::prof_end(prof_slot_, (stream));                \
   } while (0)
+
+// Programmatic dependent launch: every library kernel is launched with
+// programmatic stream serialisation, so it may start while its predecessor in
+// the stream is still running.  Each kernel calls pdl_wait() before it reads
+// or writes memory that the predecessor touches (griddepcontrol.wait returns
+// once the predecessor grid has completed and its writes are visible), and
+// pdl_trigger() to let its own successor start launching early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Launch errors surface through cudaGetLastError (checked by BI_LAUNCH_CHECK).
+#define BI_PDL_CHECK(expr) (void)(expr)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -49,11 +49,14 @@ constexpr int kBM = 128;        // instruction / tile rows
 constexpr int kBN = 64;         // instruction columns
 constexpr int kBK = 64;         // k-tile (128 bytes of bf16: one swizzle row)
 constexpr int kUK = 16;         // instruction K
-constexpr int kThreads = 192;
+constexpr int kProducerWarps = 1;
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kBSubBytes = kBN * kBK * 2;   // 8 KiB per 64-column instruction tile
-constexpr int kSmemBudget = 200 * 1024;
-constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 227 * 1024;     // dynamic shared memory per CTA
+constexpr int kMaxStages = 16;
+constexpr int kOverreadSlack = kATileBytes;  // see the A-tile note below
 constexpr int kMaxSplitK = 16;
 
 __device__ unsigned int g_err_word = 0;
@@ -62,6 +65,11 @@ enum OutKind : int { kOutBF16 = 0, kOutF32 = 1 };
 
 struct Args {
   int M, N, K;
+  int a_rows;       // rows of A per TMA box (16, 32, 64 or 128)
+  int kbs;          // k-blocks per stage (one TMA box spans them when map3d)
+  int map3d;        // tensor maps are [kblock][rows][64] views (K % 64 == 0)
+  int stage_bytes;  // kbs x (A box + W instruction columns of B)
+  int stages;
   int m_tiles, n_tiles;  // n_tiles counts CTA-wide column tiles (64*W wide)
   int splits;            // K splits of unprotected tiles
   int tm0, tm1;          // m-tiles [tm0, tm1) are never split
@@ -151,6 +159,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -231,37 +247,52 @@ __device__ __forceinline__ void k_range(const Args& a, int s, int nsplit, int& k
   }
 }
 
-template <int W>
-struct Layout {
-  static constexpr int kStageBytes = kATileBytes + W * kBSubBytes;
-  static constexpr int kStages = (kSmemBudget / kStageBytes) < kMaxStages ? (kSmemBudget / kStageBytes) : kMaxStages;
-  static constexpr int kTmemCols = 2 * W * kBN;  // two accumulators (64, 128 or 256 columns each)
-  static constexpr int kBarBytes = 256;  // 2*kStages+5 mbarriers, tmem slot, abort flag
-  static constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + kBarBytes;
-};
+// Shared memory: [barrier block 1 KiB][stage 0]..[stage n-1][slack].  A stage
+// holds an A box of a_rows rows then the B box (W 64-row instruction tiles).
+//
+// A-tile note: the instruction always reads 128 rows of A (16 KiB) from the
+// stage start.  When M <= 64 only the first a_rows rows are loaded; the
+// instruction's rows a_rows..127 then read whatever follows in shared memory
+// (the B tile, the next stage, or the trailing slack, never outside the
+// allocation) and produce accumulator rows that are never stored.  Each output
+// row depends only on its own A row, so the rows that are stored are computed
+// exactly as with a full tile; the saved shared memory holds more weight bytes
+// in flight at decode sizes.
+constexpr int kBarBlock = 1024;
+
+__host__ __device__ constexpr size_t smem_bytes(int stages, int stage_bytes, int a_rows) {
+  return 1024 /* alignment slack */ + kBarBlock + static_cast<size_t>(stages) * stage_bytes +
+         (a_rows < kBM ? kOverreadSlack : 0);
+}
 
 template <int W>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                               const __grid_constant__ CUtensorMap tmW, const Args a) {
-  using L = Layout<W>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* tiles = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages * L::kStageBytes);
-  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  constexpr int kTmemCols = 2 * W * kBN;  // two accumulators (64, 128 or 256 columns each)
+  const int kStages = a.stages;
+  const int kStageBytes = a.stage_bytes;
+  const int kbs = a.kbs;
+  const int a_tile = a.a_rows * kBK * 2;      // one k-block of A
+  const int b_tile = W * kBSubBytes;          // one k-block of B
+  const int a_bytes = kbs * a_tile;           // A part of a stage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  unsigned char* tiles = smem + kBarBlock;
+  // bars: full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * L::kStages;
-  const uint32_t tfull0 = empty0 + 8 * L::kStages;
+  const uint32_t empty0 = full0 + 8 * kMaxStages;
+  const uint32_t tfull0 = empty0 + 8 * kMaxStages;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain_bar = tempty0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * L::kStages + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::kStages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, 1);
     }
@@ -275,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(L::kTmemCols)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -285,32 +316,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything below reads or writes memory shared with the previous kernel
+  pdl_wait();
+  pdl_trigger();
 
-  if (warp == 0) {
+  if (warp < kProducerWarps) {
     // ------------------------------------------------------------ TMA producer
+    // One thread issues A then B of every stage in consumption order.
     if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0;
-      uint32_t issued_mask = 0;  // stages holding a load issued by this thread
-      uint32_t issued_par = 0;   // parity of the phase that load completes
+      uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
+      int st = 0;        // stage slot and its phase parity, advanced in the same
+      uint32_t ph = 0;   // sequence as the MMA thread's
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         int mt, nt, s, ns, kb0, kb1;
         unit_coords(a, u, mt, nt, s, ns);
         k_range(a, s, ns, kb0, kb1);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += kbs) {
           if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * st;
-          const uint32_t sa = smem_u32(tiles + st * L::kStageBytes);
-          mbar_expect_tx(fb, L::kStageBytes);
-          tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
-          tma_load_2d(sa + kATileBytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+          const uint32_t sa = smem_u32(tiles + st * kStageBytes);
+          mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
+          if (a.map3d) {
+            tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
+            tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
+          } else {
+            tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
+            tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+          }
           issued_mask |= 1u << st;
           issued_par = (issued_par & ~(1u << st)) | (ph << st);
-          if (++st == L::kStages) {
+          if (++st == kStages) {
             st = 0;
             ph ^= 1u;
           }
@@ -318,13 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
       if (*abort_flag) {
         // let copies already in flight land before shared memory is released
-        for (int i = 0; i < L::kStages; ++i)
+        for (int i = 0; i < kStages; ++i)
           if (issued_mask & (1u << i)) wait_drain(full0 + 8 * i, (issued_par >> i) & 1u);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      const uint64_t desc0 = sw128_desc(smem_u32(tiles));
       int st = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -338,28 +378,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 2)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * W * kBN);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; kb += kbs) {
           if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(tiles + st * L::kStageBytes);
-          const uint64_t adesc = sw128_desc(sa);
+          // descriptors of this stage: start addresses advance in 16-byte units
+          const uint64_t sdesc = desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+          const int nkb = min(kbs, kb1 - kb);  // k-blocks of this stage inside the range
+          for (int j = 0; j < nkb; ++j) {
+            const uint64_t adesc = sdesc + static_cast<uint64_t>((j * a_tile) >> 4);
+            const uint64_t bdesc = sdesc + static_cast<uint64_t>((a_bytes + j * b_tile) >> 4);
+            const uint32_t first = (kb + j == kb0) ? 1u : 0u;
 #pragma unroll
-          for (int k = 0; k < kBK / kUK; ++k) {
-            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+            for (int k = 0; k < kBK / kUK; ++k) {
+              // the first instruction of a tile overwrites the accumulator, all others add
+              const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
 #pragma unroll
-            for (int n = 0; n < W; ++n) {
-              const uint64_t bdesc = sw128_desc(sa + kATileBytes + n * kBSubBytes);
-              // advance 32 bytes (16 bf16) along K inside the swizzled row
-              tc_mma(d0 + n * kBN, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc,
-                     accum);
+              for (int nn = 0; nn < W; ++nn)
+                tc_mma(d0 + nn * kBN, adesc + static_cast<uint64_t>(2 * k),
+                       bdesc + static_cast<uint64_t>(nn * (kBSubBytes >> 4) + 2 * k), kIdesc, accum);
             }
           }
           tc_commit(empty0 + 8 * st);  // stage free once these MMAs have read it
           any = true;
-          if (++st == L::kStages) {
+          if (++st == kStages) {
             st = 0;
             ph ^= 1u;
           }
@@ -378,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (4 warps)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quarter * 32 + lane;
     int acc = 0;
@@ -448,9 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(L::kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
   }
 }
@@ -459,6 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // left-to-right sum of its split partials (+ residual), rounded once.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, void* C, const __nv_bfloat16* __restrict__ R,
                                      int M, int N, int splits, int skip_r0, int skip_r1, int out_kind) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t chunks = static_cast<int64_t>(N) / 8;
   const int64_t n = static_cast<int64_t>(M) * chunks;
   for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
@@ -510,9 +556,10 @@ struct MapKey {
   const void* ptr;
   int64_t rows, K;
   int box_rows;
+  int kbs;  // 0: 2D map; >0: 3D [kblock][rows][64] view with boxes spanning kbs k-blocks
   int dev;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && dev == o.dev;
+    return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && kbs == o.kbs && dev == o.dev;
   }
 };
 struct MapKeyHash {
@@ -520,7 +567,7 @@ struct MapKeyHash {
     size_t h = reinterpret_cast<size_t>(k.ptr);
     h ^= static_cast<size_t>(k.rows) * 0x9E3779B97F4A7C15ull;
     h ^= static_cast<size_t>(k.K) * 0xC2B2AE3D27D4EB4Full;
-    h ^= static_cast<size_t>(k.box_rows * 131 + k.dev);
+    h ^= static_cast<size_t>(k.box_rows * 131 + k.dev + k.kbs * 7919);
     return h;
   }
 };
@@ -528,12 +575,15 @@ struct MapKeyHash {
 std::mutex g_map_mutex;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-// Tensor map of a [rows][K] bf16 row-major matrix, box 64 (K) x box_rows, 128-byte swizzle,
-// out-of-range elements read as zero.
-bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, CUtensorMap* out) {
+// Tensor map of a [rows][K] bf16 row-major matrix, 128-byte swizzle, out-of-range
+// elements read as zero.  2D (kbs == 0): box 64 (K) x box_rows.  3D (kbs > 0, K a
+// multiple of 64): the matrix viewed as [K/64][rows][64] (k-block stride 128
+// bytes), box 64 x box_rows x kbs, so one copy brings kbs consecutive k-blocks,
+// each landing as its own swizzled box_rows x 128-byte tile.
+bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, int kbs, CUtensorMap* out) {
   int dev = 0;
   cudaGetDevice(&dev);
-  MapKey key{ptr, rows, K, box_rows, dev};
+  MapKey key{ptr, rows, K, box_rows, kbs, dev};
   {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     auto it = g_maps.find(key);
@@ -544,13 +594,26 @@ bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, CUt
   }
   auto fn = encode_fn();
   BI_REQUIRE(fn != nullptr, BI_ERR_CUDA, "bi_gemm: cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (kbs == 0) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBK), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(K / kBK)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(kBK) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows),
+                         static_cast<cuuint32_t>(kbs)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   BI_REQUIRE(r == CUDA_SUCCESS, BI_ERR_CUDA, "bi_gemm: cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   std::lock_guard<std::mutex> lock(g_map_mutex);
   if (g_maps.size() > 4096) g_maps.clear();
@@ -560,6 +623,7 @@ bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, CUt
 
 struct Plan {
   int W;
+  int a_rows, kbs, map3d, stage_bytes, stages;
   int splits;
   int tm0, tm1;
   int m_tiles, n_tiles, units, kb_total, kb_per;
@@ -585,9 +649,29 @@ int choose_width(int64_t M, int64_t N) {
   return bw;
 }
 
+// Decode-sized M (one 128-row tile): the GEMM streams the weights, so take the
+// widest CTA tile that still gives every SM a tile (more weight bytes per stage).
+int choose_width_small_m(int64_t N) {
+  const int sms = num_sms();
+  const int widths[3] = {4, 2, 1};
+  for (int w : widths)
+    if ((N + w * kBN - 1) / (w * kBN) >= sms) return w;
+  return 1;
+}
+
 Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te) {
   Plan p;
-  p.W = choose_width(M, N);
+  p.W = M <= kBM ? choose_width_small_m(N) : choose_width(M, N);
+  p.a_rows = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : kBM;
+  // Each copy costs the copy engine a roughly fixed time, so at decode sizes a
+  // stage spans several k-blocks (one 3D box of >= 32 KiB of weights per copy).
+  // (A 3D copy costs more than a 2D box of the same bytes, so the 3D view is
+  // used only when a copy spans several k-blocks.)
+  p.kbs = (K % kBK == 0 && M <= kBM) ? std::max(1, 4 / p.W) : 1;
+  p.map3d = p.kbs > 1 ? 1 : 0;
+  p.stage_bytes = p.kbs * (p.a_rows * kBK * 2 + p.W * kBSubBytes);
+  const int budget = kSmemLimit - 1024 - kBarBlock - (p.a_rows < kBM ? kOverreadSlack : 0);
+  p.stages = std::min(kMaxStages, budget / p.stage_bytes);
   p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
   p.n_tiles = static_cast<int>((N + p.W * kBN - 1) / (p.W * kBN));
   p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
@@ -616,15 +700,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
 
 template <int W>
 bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
-  using L = Layout<W>;
   static bool attr = false;
   if (!attr) {
-    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(L::kSmemBytes)));
+    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
     attr = true;
   }
+  const size_t smem = smem_bytes(args.stages, args.stage_bytes, args.a_rows);
   const int grid = std::min(args.units, num_sms());
-  BI_TIMED(::bi::kTagGemm, s, gemm_tc_kernel<W><<<grid, kThreads, L::kSmemBytes, s>>>(ma, mw, args));
+  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<W>, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -682,6 +765,11 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te);
   gemm::Args args{};
   args.M = static_cast<int>(M);
+  args.a_rows = p.a_rows;
+  args.kbs = p.kbs;
+  args.map3d = p.map3d;
+  args.stage_bytes = p.stage_bytes;
+  args.stages = p.stages;
   args.N = static_cast<int>(N);
   args.K = static_cast<int>(K);
   args.m_tiles = p.m_tiles;
@@ -703,8 +791,8 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
     args.partial = static_cast<float*>(ws);
   }
   CUtensorMap ma, mw;
-  BI_TRY(gemm::tensor_map(A, M, K, gemm::kBM, &ma));
-  BI_TRY(gemm::tensor_map(Wt, N, K, p.W * gemm::kBN, &mw));
+  BI_TRY(gemm::tensor_map(A, M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
+  BI_TRY(gemm::tensor_map(Wt, N, K, p.W * gemm::kBN, p.map3d ? p.kbs : 0, &mw));
   bi_status st;
   if (p.W == 4) st = gemm::launch_w<4>(ma, mw, args, s);
   else if (p.W == 2) st = gemm::launch_w<2>(ma, mw, args, s);
@@ -714,8 +802,8 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
     const int64_t n = M * (N / 8);
     const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
     const int skip0 = p.tm0 * gemm::kBM, skip1 = static_cast<int>(std::min<int64_t>(M, int64_t(p.tm1) * gemm::kBM));
-    BI_TIMED(::bi::kTagSplitkReduce, s, gemm::splitk_reduce_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(args.partial, C, args.R, args.M, args.N,
-                                                                          p.splits, skip0, skip1, args.out_kind));
+    BI_TIMED(::bi::kTagSplitkReduce, s, BI_PDL_CHECK(launch_pdl(gemm::splitk_reduce_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, args.partial, C, args.R, args.M, args.N,
+                                                                          p.splits, skip0, skip1, args.out_kind)));
     BI_LAUNCH_CHECK();
   }
   return BI_OK;

@@ -21,6 +21,11 @@ bi_status prefill_attention_impl(const void*, const void*, const void*, const in
                                  const int32_t*, int32_t, int32_t, const bi_attn_dims*, void*, bi_mode, int32_t,
                                  void*, size_t, cudaStream_t);
 size_t decode_attention_ws(int32_t, const bi_attn_dims*);
+size_t decode_plan_bytes(int32_t, int32_t);
+size_t decode_parts_bytes(int32_t, const bi_attn_dims*);
+bi_status decode_attention_layer(const void*, const void*, const void*, const int32_t*, const int32_t*, int32_t,
+                                 const bi_attn_dims*, void*, bi_mode, int32_t, void*, bool, void*, size_t,
+                                 cudaStream_t);
 size_t prefill_attention_ws(int32_t, int32_t, const bi_attn_dims*);
 bi_status qkv_rope_store_impl(const void*, const float*, const float*, const int32_t*, const int32_t*,
                               const int32_t*, int32_t, const bi_attn_dims*, void*, void*, void*, cudaStream_t);
@@ -34,6 +39,8 @@ namespace {
 __global__ void batch_index_kernel(const int32_t* __restrict__ q_start, const int32_t* __restrict__ pos0, int B, int T,
                                    int32_t* __restrict__ token_req, int32_t* __restrict__ token_pos,
                                    int32_t* __restrict__ kv_len, int32_t* __restrict__ last_row) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < T) {
     int lo = 0, hi = B - 1;
@@ -53,6 +60,8 @@ __global__ void batch_index_kernel(const int32_t* __restrict__ q_start, const in
 // out[b] = in[rows[b]] (16-byte chunks)
 __global__ void gather_rows_kernel(const uint4* __restrict__ in, const int32_t* __restrict__ rows, uint4* __restrict__ out,
                                    int B, int64_t chunks) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   if (b >= B) return;
   const int64_t r = rows[b];
@@ -70,6 +79,7 @@ struct LayerBufs {
   void* att;  // [T][Hq*hd]
   void* gu;   // [T][2F]
   void* act;  // [T][F]
+  void* dplan;  // decode attention plan (shared by the layers of a step)
   void* sub;  // sub-op workspace
   size_t sub_bytes;
   // model-level extras
@@ -102,7 +112,7 @@ size_t sub_ws_bytes(const bi_model_dims* dm, const bi_batch* b, bi_mode mode, bo
   m = std::max(m, gemm_ws(T, d, F, mode));
   bi_attn_dims ad = attn_dims(dm, b);
   if (b->max_q_len == 1 && T == B)
-    m = std::max(m, decode_attention_ws(static_cast<int32_t>(B), &ad));
+    m = std::max(m, decode_parts_bytes(static_cast<int32_t>(B), &ad));
   else
     m = std::max(m, prefill_attention_ws(static_cast<int32_t>(B), static_cast<int32_t>(T), &ad));
   if (with_head) {
@@ -128,6 +138,7 @@ LayerBufs carve(void* ws, size_t cap, const bi_model_dims* dm, const bi_batch* b
   r.att = cv.take<__nv_bfloat16>(T * hq);
   r.gu = cv.take<__nv_bfloat16>(T * 2 * F);
   r.act = cv.take<__nv_bfloat16>(T * F);
+  r.dplan = cv.take<unsigned char>(decode_plan_bytes(static_cast<int32_t>(B), dm->num_kv_heads));
   if (model) {
     r.hidden = cv.take<__nv_bfloat16>(T * d);
     r.xl = cv.take<__nv_bfloat16>(B * d);
@@ -164,7 +175,7 @@ bi_status check_batch(const bi_batch* b) {
 // The layer body over precomputed batch indices.
 bi_status layer_body(const bi_model_dims* dm, const bi_layer_weights* w, const float* rc, const float* rs,
                      void* hidden, const bi_batch* b, void* kc, void* vc, bi_mode mode, const LayerBufs& L,
-                     cudaStream_t s) {
+                     bool plan_attention, cudaStream_t s) {
   const int64_t T = b->num_tokens, d = dm->d_model, F = dm->ffn_dim;
   const int64_t hq = static_cast<int64_t>(dm->num_q_heads) * dm->head_dim;
   const int64_t qkvw = static_cast<int64_t>(dm->num_q_heads + 2 * dm->num_kv_heads) * dm->head_dim;
@@ -180,8 +191,8 @@ bi_status layer_body(const bi_model_dims* dm, const bi_layer_weights* w, const f
   BI_TRY(qkv_rope_store_impl(L.qkv, rc, rs, L.token_pos, L.token_req, b->block_table, static_cast<int32_t>(T), &ad,
                              L.q, kc, vc, s));
   if (b->max_q_len == 1 && T == b->num_requests) {
-    BI_TRY(decode_attention_impl(L.q, kc, vc, b->block_table, L.kv_len, b->num_requests, &ad, L.att, mode, treq,
-                                 L.sub, L.sub_bytes, s));
+    BI_TRY(decode_attention_layer(L.q, kc, vc, b->block_table, L.kv_len, b->num_requests, &ad, L.att, mode, treq,
+                                  L.dplan, plan_attention, L.sub, L.sub_bytes, s));
   } else {
     BI_TRY(prefill_attention_impl(L.q, kc, vc, b->block_table, b->q_start, b->pos0, b->num_requests,
                                   static_cast<int32_t>(T), &ad, L.att, mode, treq, L.sub, L.sub_bytes, s));
@@ -196,8 +207,8 @@ bi_status layer_body(const bi_model_dims* dm, const bi_layer_weights* w, const f
 
 bi_status batch_index(const bi_batch* b, const LayerBufs& L, cudaStream_t s) {
   const int n = std::max(b->num_tokens, b->num_requests);
-  BI_TIMED(::bi::kTagBatchIndex, s, batch_index_kernel<<<(n + 255) / 256, 256, 0, s>>>(b->q_start, b->pos0, b->num_requests, b->num_tokens, L.token_req,
-                                                     L.token_pos, L.kv_len, L.last_row));
+  BI_TIMED(::bi::kTagBatchIndex, s, BI_PDL_CHECK(launch_pdl(batch_index_kernel, dim3((n + 255) / 256), dim3(256), 0, s, b->q_start, b->pos0, b->num_requests, b->num_tokens, L.token_req,
+                                                     L.token_pos, L.kv_len, L.last_row)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -227,7 +238,7 @@ bi_status layer_forward_impl(const bi_model_dims* dm, const bi_layer_weights* w,
   BI_REQUIRE(ws != nullptr && L.bytes <= ws_bytes, BI_ERR_WORKSPACE, "bi_layer_forward: workspace %zu < %zu",
              ws_bytes, L.bytes);
   BI_TRY(batch_index(b, L, s));
-  return layer_body(dm, w, rc, rs, hidden, b, kc, vc, mode, L, s);
+  return layer_body(dm, w, rc, rs, hidden, b, kc, vc, mode, L, true, s);
 }
 
 bi_status model_forward_impl(const bi_model_dims* dm, const bi_model_weights* mw, const float* rc, const float* rs,
@@ -252,12 +263,12 @@ bi_status model_forward_impl(const bi_model_dims* dm, const bi_model_weights* mw
   BI_TRY(embed_impl(ids, mw->embed, L.hidden, T, d, dm->vocab, s));
   for (int i = 0; i < mw->num_layers; ++i) {
     BI_REQUIRE(kcs[i] && vcs[i], BI_ERR_INVALID_ARG, "bi_model_forward: null cache of layer %d", i);
-    BI_TRY(layer_body(dm, &mw->layers[i], rc, rs, L.hidden, b, kcs[i], vcs[i], mode, L, s));
+    BI_TRY(layer_body(dm, &mw->layers[i], rc, rs, L.hidden, b, kcs[i], vcs[i], mode, L, i == 0, s));
   }
   const void* last = L.hidden;
   if (T != B) {
-    BI_TIMED(::bi::kTagGather, s, gather_rows_kernel<<<static_cast<unsigned>(B), 128, 0, s>>>(static_cast<const uint4*>(L.hidden), L.last_row,
-                                                                static_cast<uint4*>(L.xl), static_cast<int>(B), d / 8));
+    BI_TIMED(::bi::kTagGather, s, BI_PDL_CHECK(launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(B)), dim3(128), 0, s, static_cast<const uint4*>(L.hidden), L.last_row,
+                                                                static_cast<uint4*>(L.xl), static_cast<int>(B), d / 8)));
     BI_LAUNCH_CHECK();
     last = L.xl;
   }

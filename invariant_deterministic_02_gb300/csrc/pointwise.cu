@@ -12,6 +12,8 @@ namespace {
 
 __global__ void embed_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ table, uint4* __restrict__ out,
                              int64_t T, int64_t chunks_per_row, int64_t vocab) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = blockIdx.x;
   if (t >= T) return;
   const int64_t id = ids[t];
@@ -22,6 +24,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, const uint4* __res
 
 // cos/sin(p * theta^(-2i/hd)) in float64, rounded once to fp32.
 __global__ void rope_table_kernel(double theta, int hd, int max_pos, float* __restrict__ cs, float* __restrict__ sn) {
+  pdl_wait();
+  pdl_trigger();
   const int half = hd / 2;
   const int64_t n = static_cast<int64_t>(max_pos) * half;
   for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
@@ -43,6 +47,8 @@ __global__ void qkv_rope_store_kernel(const __nv_bfloat16* __restrict__ qkv, con
                                       const int32_t* __restrict__ token_req, const int32_t* __restrict__ block_table,
                                       int max_pages, int hq, int hkv, int hd, __nv_bfloat16* __restrict__ q_out,
                                       __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int pos = token_pos[t];
   const int req = token_req[t];
@@ -82,6 +88,8 @@ __global__ void qkv_rope_store_kernel(const __nv_bfloat16* __restrict__ qkv, con
 
 __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloat16* __restrict__ out, int64_t T,
                               int64_t F) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t chunks = F / 8;
   const int64_t n = T * chunks;
   for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
@@ -110,8 +118,8 @@ bi_status embed_impl(const int32_t* ids, const void* table, void* out, int64_t T
   if (T == 0) return BI_OK;
   BI_REQUIRE(ids && table && out && aligned16(table) && aligned16(out), BI_ERR_INVALID_ARG,
              "bi_embed: null or misaligned pointer");
-  BI_TIMED(::bi::kTagEmbed, s, embed_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(ids, static_cast<const uint4*>(table), static_cast<uint4*>(out),
-                                                        T, d / 8, vocab));
+  BI_TIMED(::bi::kTagEmbed, s, BI_PDL_CHECK(launch_pdl(embed_kernel, dim3(static_cast<unsigned>(T)), dim3(128), 0, s, ids, static_cast<const uint4*>(table), static_cast<uint4*>(out),
+                                                        T, d / 8, vocab)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -128,10 +136,10 @@ bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs,
              "bi_qkv_rope_store: null pointer");
   BI_REQUIRE(aligned16(qkv) && aligned16(q_out) && aligned16(kc) && aligned16(vc), BI_ERR_INVALID_ARG,
              "bi_qkv_rope_store: misaligned pointer");
-  BI_TIMED(::bi::kTagQkvRope, s, qkv_rope_store_kernel<<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
+  BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel, dim3(T), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
                                           block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
                                           static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(kc),
-                                          static_cast<__nv_bfloat16*>(vc)));
+                                          static_cast<__nv_bfloat16*>(vc))));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -143,8 +151,8 @@ bi_status swiglu_impl(const void* gu, void* out, int64_t T, int64_t F, cudaStrea
   BI_REQUIRE(gu && out && aligned16(gu) && aligned16(out), BI_ERR_INVALID_ARG, "bi_swiglu: null or misaligned");
   const int64_t n = T * (F / 8);
   const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 16);
-  BI_TIMED(::bi::kTagSwiglu, s, swiglu_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(gu),
-                                                            static_cast<__nv_bfloat16*>(out), T, F));
+  BI_TIMED(::bi::kTagSwiglu, s, BI_PDL_CHECK(launch_pdl(swiglu_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(gu),
+                                                            static_cast<__nv_bfloat16*>(out), T, F)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -156,7 +164,7 @@ bi_status rope_table_impl(double theta, int32_t hd, int32_t max_pos, float* cs, 
   BI_REQUIRE(cs && sn, BI_ERR_INVALID_ARG, "bi_rope_table: null pointer");
   const int64_t n = static_cast<int64_t>(max_pos) * (hd / 2);
   const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
-  BI_TIMED(::bi::kTagRopeTable, s, rope_table_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(theta, hd, max_pos, cs, sn));
+  BI_TIMED(::bi::kTagRopeTable, s, BI_PDL_CHECK(launch_pdl(rope_table_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, theta, hd, max_pos, cs, sn)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }

@@ -110,6 +110,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) rms_invariant_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
                                                                  T* y, int64_t row_begin, int64_t row_end, int d,
                                                                  float eps) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[kWarps];
   for (int64_t r = row_begin + blockIdx.x; r < row_end; r += gridDim.x)
     rms_row(x + r * d, gamma, y + r * d, d, eps, red);
@@ -120,6 +122,8 @@ template <typename T>
 __global__ void __launch_bounds__(kSplitThreads) rms_split_partial_kernel(const T* __restrict__ x, float* partial,
                                                                           int64_t rows, int d, int splits,
                                                                           int64_t skip_begin, int64_t skip_end) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int V = VecOf<T>::N;
   const int64_t r = blockIdx.x / splits;
   const int s = blockIdx.x % splits;
@@ -152,6 +156,8 @@ __global__ void __launch_bounds__(kThreads) rms_split_finish_kernel(const T* __r
                                                                     T* y, const float* partial, int64_t rows, int d,
                                                                     int splits, float eps, int64_t inv_begin,
                                                                     int64_t inv_end) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int V = VecOf<T>::N;
   __shared__ float red[kWarps];
   const int64_t r = blockIdx.x;
@@ -193,7 +199,7 @@ bi_status launch(const void* xv, const void* gv, void* yv, int64_t rows, int d, 
   if (splits == 1) {
     // Unsplit: the data-parallel schedule, identical to INVARIANT for every row.
     const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(num_sms()) * 8);
-    BI_TIMED(::bi::kTagRmsnorm, s, rms_invariant_kernel<T><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(x, g, y, 0, rows, d, eps));
+    BI_TIMED(::bi::kTagRmsnorm, s, BI_PDL_CHECK(launch_pdl(rms_invariant_kernel<T>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, x, g, y, 0, rows, d, eps)));
     BI_LAUNCH_CHECK();
     return BI_OK;
   }
@@ -201,11 +207,11 @@ bi_status launch(const void* xv, const void* gv, void* yv, int64_t rows, int d, 
   BI_REQUIRE(ws != nullptr && ws_bytes >= need, BI_ERR_WORKSPACE, "bi_rmsnorm: workspace %zu < %zu bytes", ws_bytes,
              need);
   float* partial = static_cast<float*>(ws);
-  BI_TIMED(::bi::kTagRmsnormSplit, s, rms_split_partial_kernel<T><<<static_cast<unsigned>(rows * splits), kSplitThreads, 0, s>>>(x, partial, rows, d,
-                                                                                             splits, tb, te));
+  BI_TIMED(::bi::kTagRmsnormSplit, s, BI_PDL_CHECK(launch_pdl(rms_split_partial_kernel<T>, dim3(static_cast<unsigned>(rows * splits)), dim3(kSplitThreads), 0, s, x, partial, rows, d,
+                                                                                             splits, tb, te)));
   BI_LAUNCH_CHECK();
-  BI_TIMED(::bi::kTagRmsnormSplit, s, rms_split_finish_kernel<T><<<static_cast<unsigned>(rows), kThreads, 0, s>>>(x, g, y, partial, rows, d, splits, eps,
-                                                                              tb, te));
+  BI_TIMED(::bi::kTagRmsnormSplit, s, BI_PDL_CHECK(launch_pdl(rms_split_finish_kernel<T>, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, s, x, g, y, partial, rows, d, splits, eps,
+                                                                              tb, te)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }

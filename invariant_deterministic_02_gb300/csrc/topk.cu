@@ -7,9 +7,12 @@
 // descending, index ascending): a total order, so the selected set and its
 // order are unique and do not depend on how the scan is parallelised.
 //
-// One CTA of 256 threads per row: thread t scans elements t, t+256, ... keeping
-// a sorted register list of the best KCAP, then the 256 lists are merged
-// pairwise in shared memory.
+// One CTA of 32 warps per row.  Each warp scans a contiguous segment of the row
+// (four consecutive elements per lane per step, 16-byte loads) and keeps its
+// best k in a sorted list spread over its lanes (lane j holds entry j); an
+// element enters only if it beats the list's last entry, so after the first few
+// steps almost every step is one compare and one ballot.  Warp 0 then folds the
+// 32 warp lists into one with the same insertion.
 #include <climits>
 
 #include "common.cuh"
@@ -17,92 +20,97 @@
 namespace bi {
 namespace {
 
-constexpr int kTopkThreads = 256;
-
-struct Cand {
-  float v;
-  int i;
-};
+constexpr int kTopkWarps = 32;
 
 __device__ __forceinline__ bool better(float av, int ai, float bv, int bi) { return av > bv || (av == bv && ai < bi); }
 
-template <int KCAP>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ logits, int64_t V, int k,
-                                                            float* __restrict__ top_v, int32_t* __restrict__ top_i,
-                                                            int32_t* __restrict__ greedy) {
-  extern __shared__ Cand lists[];  // [kTopkThreads][KCAP]
-  const int64_t row = blockIdx.x;
-  const float* x = logits + row * V;
-  float av[KCAP];
-  int ai[KCAP];
-#pragma unroll
-  for (int j = 0; j < KCAP; ++j) {
-    av[j] = -INFINITY;
-    ai[j] = INT_MAX;
-  }
-  for (int64_t e = threadIdx.x; e < V; e += kTopkThreads) {
-    const float v = x[e];
-    const int idx = static_cast<int>(e);
-    if (!better(v, idx, av[KCAP - 1], ai[KCAP - 1])) continue;
-#pragma unroll
-    for (int j = KCAP - 1; j >= 1; --j) {
-      if (better(v, idx, av[j - 1], ai[j - 1])) {
-        av[j] = av[j - 1];
-        ai[j] = ai[j - 1];
-      } else if (better(v, idx, av[j], ai[j])) {
-        av[j] = v;
-        ai[j] = idx;
-      }
-    }
-    if (better(v, idx, av[0], ai[0])) {
-      av[0] = v;
-      ai[0] = idx;
+// Insert (v, i) into the warp's sorted list (lanes < k hold entries, best first);
+// the caller has checked that it beats entry k-1.
+__device__ __forceinline__ void warp_insert(float& lv, int& li, float v, int i, int lane, int k) {
+  const unsigned m = __ballot_sync(0xffffffffu, lane < k && better(lv, li, v, i));
+  const int p = __popc(m);  // entries that stay ahead of the new one
+  const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+  const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+  if (lane < k) {
+    if (lane == p) {
+      lv = v;
+      li = i;
+    } else if (lane > p) {
+      lv = uv;
+      li = ui;
     }
   }
-  Cand* mine = lists + threadIdx.x * KCAP;
-#pragma unroll
-  for (int j = 0; j < KCAP; ++j) mine[j] = Cand{av[j], ai[j]};
-  __syncthreads();
-  // pairwise merges: list t takes the best KCAP of lists t and t + stride
-  for (int stride = 1; stride < kTopkThreads; stride <<= 1) {
-    if ((threadIdx.x % (2 * stride)) == 0) {
-      const Cand* a = lists + threadIdx.x * KCAP;
-      const Cand* b = lists + (threadIdx.x + stride) * KCAP;
-      Cand out[KCAP];
-      int ia = 0, ib = 0;
-#pragma unroll
-      for (int j = 0; j < KCAP; ++j) {
-        const bool take_a = better(a[ia].v, a[ia].i, b[ib].v, b[ib].i);
-        out[j] = take_a ? a[ia] : b[ib];
-        ia += take_a ? 1 : 0;
-        ib += take_a ? 0 : 1;
-      }
-      Cand* dst = lists + threadIdx.x * KCAP;
-#pragma unroll
-      for (int j = 0; j < KCAP; ++j) dst[j] = out[j];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x < k) {
-    top_v[row * k + threadIdx.x] = lists[threadIdx.x].v;
-    top_i[row * k + threadIdx.x] = lists[threadIdx.x].i;
-  }
-  if (greedy != nullptr && threadIdx.x == 0) greedy[row] = lists[0].i;
 }
 
-template <int KCAP>
-bi_status launch(const float* logits, int64_t rows, int64_t V, int k, float* tv, int32_t* ti, int32_t* greedy,
-                 cudaStream_t s) {
-  const size_t smem = sizeof(Cand) * KCAP * kTopkThreads;
-  static bool attr = false;
-  if (!attr) {
-    BI_CUDA_TRY(cudaFuncSetAttribute(topk_kernel<KCAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)));
-    attr = true;
+// Offer the 32 candidates held one per lane to the list.
+__device__ __forceinline__ void warp_offer(float& lv, int& li, float& tv, int& ti, float cv, int ci, int lane,
+                                           int k) {
+  unsigned mask = __ballot_sync(0xffffffffu, better(cv, ci, tv, ti));
+  while (mask) {
+    const int src = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const float v = __shfl_sync(0xffffffffu, cv, src);
+    const int i = __shfl_sync(0xffffffffu, ci, src);
+    if (better(v, i, tv, ti)) {
+      warp_insert(lv, li, v, i, lane, k);
+      tv = __shfl_sync(0xffffffffu, lv, k - 1);
+      ti = __shfl_sync(0xffffffffu, li, k - 1);
+    }
   }
-  BI_TIMED(::bi::kTagTopk, s, topk_kernel<KCAP><<<static_cast<unsigned>(rows), kTopkThreads, smem, s>>>(logits, V, k, tv, ti, greedy));
-  BI_LAUNCH_CHECK();
-  return BI_OK;
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits, int64_t V, int k,
+                                                               float* __restrict__ top_v, int32_t* __restrict__ top_i,
+                                                               int32_t* __restrict__ greedy) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float sv[kTopkWarps][32];
+  __shared__ int si[kTopkWarps][32];
+  const int64_t row = blockIdx.x;
+  const float* x = logits + row * V;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  float lv = -INFINITY, tv = -INFINITY;
+  int li = INT_MAX, ti = INT_MAX;
+  // segment of this warp: a multiple of 128 elements
+  const int64_t per = ((V + kTopkWarps - 1) / kTopkWarps + 127) / 128 * 128;
+  const int64_t s0 = warp * per, s1 = min(V, s0 + per);
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+  int64_t e = s0;
+  if (vec) {
+    for (; e + 128 <= s1; e += 128) {
+      const float4 f = *reinterpret_cast<const float4*>(x + e + 4 * lane);
+      const int base = static_cast<int>(e) + 4 * lane;
+      warp_offer(lv, li, tv, ti, f.x, base, lane, k);
+      warp_offer(lv, li, tv, ti, f.y, base + 1, lane, k);
+      warp_offer(lv, li, tv, ti, f.z, base + 2, lane, k);
+      warp_offer(lv, li, tv, ti, f.w, base + 3, lane, k);
+    }
+  }
+  for (; e < s1; e += 32) {
+    const int64_t idx = e + lane;
+    const float v = idx < s1 ? x[idx] : -INFINITY;
+    warp_offer(lv, li, tv, ti, v, idx < s1 ? static_cast<int>(idx) : INT_MAX, lane, k);
+  }
+  sv[warp][lane] = lv;
+  si[warp][lane] = li;
+  __syncthreads();
+  if (warp == 0) {
+    lv = sv[0][lane];
+    li = si[0][lane];
+    tv = __shfl_sync(0xffffffffu, lv, k - 1);
+    ti = __shfl_sync(0xffffffffu, li, k - 1);
+    for (int w = 1; w < kTopkWarps; ++w) {
+      const float cv = lane < k ? sv[w][lane] : -INFINITY;
+      const int ci = lane < k ? si[w][lane] : INT_MAX;
+      warp_offer(lv, li, tv, ti, cv, ci, lane, k);
+    }
+    if (lane < k) {
+      top_v[row * k + lane] = lv;
+      top_i[row * k + lane] = li;
+    }
+    if (greedy != nullptr && lane == 0) greedy[row] = li;
+  }
 }
 
 }  // namespace
@@ -114,9 +122,10 @@ bi_status topk_impl(const float* logits, int64_t rows, int64_t V, int32_t k, flo
   BI_REQUIRE(k >= 1 && k <= BI_TOPK_MAX && k <= V, BI_ERR_UNSUPPORTED, "bi_topk: k=%d (1..%d, <= V)", k, BI_TOPK_MAX);
   if (rows == 0) return BI_OK;
   BI_REQUIRE(logits && tv && ti, BI_ERR_INVALID_ARG, "bi_topk: null pointer");
-  if (k == 1) return launch<1>(logits, rows, V, k, tv, ti, greedy, s);
-  if (k <= 8) return launch<8>(logits, rows, V, k, tv, ti, greedy, s);
-  return launch<32>(logits, rows, V, k, tv, ti, greedy, s);
+  BI_TIMED(::bi::kTagTopk, s,
+           BI_PDL_CHECK(launch_pdl(topk_kernel, dim3(static_cast<unsigned>(rows)), dim3(kTopkWarps * 32), 0, s, logits, V, k, tv, ti, greedy)));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
 }
 
 }  // namespace bi
