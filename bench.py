@@ -245,7 +245,7 @@ def run_ours(args, rank, world, local_rank):
     if os.path.exists(tpath):
         tj = json.load(open(tpath))
         ent = tj.get(roof_name)
-        if ent and ent.get("source_sha") == _source_sha(ent.get("source")) and ent.get("workload") == "bench":
+        if ent and ent.get("source_sha") == _source_sha(ent.get("source")):
             traffic = ent.get("bytes_per_launch")
     launches_roof = kern[roof_name]["launches_per_step"]
     roofline = {"kernel": roof_name, "bound": bound, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
