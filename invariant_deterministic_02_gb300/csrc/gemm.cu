@@ -211,8 +211,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 }
 
 // Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N=64, M=128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);
+// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_for(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(kBM >> 4) << 24);
+}
 
 // unit -> (m tile, n tile, split index, split count)
 __device__ __forceinline__ void unit_coords(const Args& a, int u, int& mt, int& nt, int& s, int& nsplit) {
@@ -395,10 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             for (int k = 0; k < kBK / kUK; ++k) {
               // the first instruction of a tile overwrites the accumulator, all others add
               const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
-#pragma unroll
-              for (int nn = 0; nn < W; ++nn)
-                tc_mma(d0 + nn * kBN, adesc + static_cast<uint64_t>(2 * k),
-                       bdesc + static_cast<uint64_t>(nn * (kBSubBytes >> 4) + 2 * k), kIdesc, accum);
+              // one instruction spans the tile's W*64 columns: the B rows of a stage are
+              // contiguous 128-byte swizzle rows, 1024 bytes per 8-row group
+              tc_mma(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                     idesc_for(W * kBN), accum);
             }
           }
           tc_commit(empty0 + 8 * st);  // stage free once these MMAs have read it
