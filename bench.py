@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["invariant", "fast", "protected"], default="invariant")
+    ap.add_argument("--mode", choices=["invariant", "fast", "protected", "invariant_ksplit"], default="invariant")
     ap.add_argument("--batch", type=int, default=BATCH)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -34,6 +34,13 @@
  *     a negative control.  BI_MODE_PROTECTED gives the rows of one target the
  *     INVARIANT geometry and lets all other rows take the FAST one, in the same
  *     launches (BlockLock-Rows style [BlockLock]).
+ *     BI_MODE_INVARIANT_KSPLIT is INVARIANT with one change in the GEMM: the K
+ *     range of every output element is cut into a fixed number of parts that
+ *     depends on the weight shape (N, K) only, never on M, and the fp32 partials
+ *     are added in part order ("Batch-Invariant Kernel" notes, section GEMM: a K
+ *     split that depends on K alone keeps the matmul batch invariant).  Its bits
+ *     are batch invariant but differ from INVARIANT's; all other ops are as
+ *     INVARIANT.
  */
 #ifndef BI_H_
 #define BI_H_
@@ -56,7 +63,12 @@ typedef enum bi_status {
   BI_ERR_TIMEOUT = 5      /* a bounded in-kernel wait ran out (see bi_device_error) */
 } bi_status;
 
-typedef enum bi_mode { BI_MODE_INVARIANT = 0, BI_MODE_FAST = 1, BI_MODE_PROTECTED = 2 } bi_mode;
+typedef enum bi_mode {
+  BI_MODE_INVARIANT = 0,
+  BI_MODE_FAST = 1,
+  BI_MODE_PROTECTED = 2,
+  BI_MODE_INVARIANT_KSPLIT = 3
+} bi_mode;
 
 typedef enum bi_dtype { BI_F32 = 0, BI_BF16 = 1 } bi_dtype;
 
@@ -123,9 +135,20 @@ bi_status bi_rmsnorm(const void* x, const void* gamma, void* y, int64_t rows, in
  * the SM count (the non-invariant behaviour BI-notes "GEMM" describes).
  * PROTECTED: the 128-row tiles holding rows [target_row, target_row+target_count)
  * are never split; other tiles are as FAST.
+ * INVARIANT_KSPLIT: the k-tiles (64 wide) are cut into S = bi_gemm_ksplit(N, K)
+ * contiguous parts, part s holding k-tiles [floor(s*T/S), floor((s+1)*T/S)) of
+ * the T = ceil(K/64); each part is accumulated from zero as above and the
+ * result is ((0 + P_0) + P_1) + ... + P_{S-1} in fp32 (+ residual), rounded
+ * once.  For M <= 128 the parts run on separate CTAs and a second pass adds
+ * them (workspace S*M*N*4 bytes); for larger M one CTA computes the parts of a
+ * tile in turn and keeps the running sum in tensor memory.  Both give the same
+ * bits.  S = 1 gives exactly the INVARIANT result.
  * K must be a multiple of 8 and >= 8; M, N >= 0 (0 is a no-op); N multiple of 8.
  */
 size_t bi_gemm_workspace(int64_t M, int64_t N, int64_t K, bi_mode mode);
+/* The part count S of INVARIANT_KSPLIT for an N x K weight (1..16); a pure
+ * function of (N, K). */
+int32_t bi_gemm_ksplit(int64_t N, int64_t K);
 bi_status bi_gemm(const void* A, const void* W, void* C, const void* residual, int64_t M, int64_t N, int64_t K,
                   bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count, void* workspace,
                   size_t ws_bytes, bi_stream s);

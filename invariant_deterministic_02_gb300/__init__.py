@@ -26,7 +26,8 @@ BI_ERR_TIMEOUT = 5
 INVARIANT = 0
 FAST = 1
 PROTECTED = 2
-MODES = {"invariant": INVARIANT, "fast": FAST, "protected": PROTECTED}
+INVARIANT_KSPLIT = 3
+MODES = {"invariant": INVARIANT, "fast": FAST, "protected": PROTECTED, "invariant_ksplit": INVARIANT_KSPLIT}
 
 BI_F32 = 0
 BI_BF16 = 1
@@ -37,7 +38,7 @@ TOPK_MAX = 32
 
 EXPORTED = [
     "bi_status_string", "bi_last_error_message", "bi_version", "bi_num_sms", "bi_device_error",
-    "bi_rmsnorm_workspace", "bi_rmsnorm", "bi_gemm_workspace", "bi_gemm",
+    "bi_rmsnorm_workspace", "bi_rmsnorm", "bi_gemm_workspace", "bi_gemm_ksplit", "bi_gemm",
     "bi_decode_attention_workspace", "bi_decode_attention", "bi_decode_attention_noalloc",
     "bi_prefill_attention_workspace",
     "bi_prefill_attention", "bi_embed", "bi_rope_table", "bi_qkv_rope_store", "bi_swiglu", "bi_topk",
@@ -104,6 +105,7 @@ def _declare(lib):
         "bi_rmsnorm_workspace": (c_sz, [c_i64, c_i64, c_i32]),
         "bi_rmsnorm": (c_i32, [vp, vp, vp, c_i64, c_i64, c_i32, c_f, c_i32, c_i32, c_i32, vp, c_sz, vp]),
         "bi_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
+        "bi_gemm_ksplit": (c_i32, [c_i64, c_i64]),
         "bi_gemm": (c_i32, [vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i32, c_i32, c_i32, c_i32, vp, c_sz, vp]),
         "bi_decode_attention_workspace": (c_sz, [c_i32, P(AttnDims), c_i32]),
         "bi_decode_attention": (c_i32, [vp, vp, vp, vp, vp, c_i32, P(AttnDims), vp, c_i32, c_i32, vp, c_sz, vp]),
@@ -203,6 +205,11 @@ def bi_rmsnorm(x, gamma, y, eps: float, mode=INVARIANT, target_row=-1, target_co
     _check(lib().bi_rmsnorm(_p(x), _p(gamma), _p(y), rows, d, dt, eps, m, target_row, target_count, _p(ws), nb,
                             _stream(stream)), "bi_rmsnorm")
     return y
+
+
+def bi_gemm_ksplit(N: int, K: int) -> int:
+    """Part count of the INVARIANT_KSPLIT GEMM for an N x K weight."""
+    return int(lib().bi_gemm_ksplit(N, K))
 
 
 def bi_gemm(A, W, C, residual=None, mode=INVARIANT, target_row=-1, target_count=0, workspace=None, stream=None):

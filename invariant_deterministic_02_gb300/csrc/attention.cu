@@ -1038,6 +1038,7 @@ template <int HD, int G>
 bi_status decode_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* kv_lens,
                         int B, const bi_attn_dims* dm, void* out, bi_mode mode, int target, const DecodeWs& w,
                         cudaStream_t s, bool make_plan = true) {
+  if (mode == BI_MODE_INVARIANT_KSPLIT) mode = BI_MODE_INVARIANT;  // the split-K variant changes the GEMM only
   if (make_plan) {
     const int fast_units = std::max(1, (4 * num_sms() + B * dm->num_kv_heads - 1) / (B * dm->num_kv_heads));
     BI_TIMED(::bi::kTagAttnPlan, s,
@@ -1066,6 +1067,7 @@ template <int HD, int G>
 bi_status prefill_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* q_start,
                          const int32_t* q_pos0, int B, int T, const bi_attn_dims* dm, void* out, bi_mode mode,
                          int target, const PrefillWs& w, cudaStream_t s) {
+  if (mode == BI_MODE_INVARIANT_KSPLIT) mode = BI_MODE_INVARIANT;  // the split-K variant changes the GEMM only
   BI_TIMED(::bi::kTagAttnPlan, s, BI_PDL_CHECK(launch_pdl(prefill_plan_kernel, dim3(1), dim3(1024), 0, s, q_start, q_pos0, B, T, static_cast<int>(mode), target, w.plan)));
   BI_LAUNCH_CHECK();
   const size_t smem = sizeof(PrefillSmem<HD, G>);
@@ -1109,7 +1111,7 @@ bi_status decode_attention_impl(const void* q, const void* kc, const void* vc, c
   clear_error();
   BI_TRY(attn::check_dims(dims));
   BI_REQUIRE(B >= 0, BI_ERR_INVALID_ARG, "bi_decode_attention: B=%d", B);
-  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "mode %d",
              static_cast<int>(mode));
   BI_REQUIRE(mode != BI_MODE_PROTECTED || target < B, BI_ERR_INVALID_ARG, "target_request %d >= B %d", target, B);
   if (B == 0) return BI_OK;
@@ -1130,7 +1132,7 @@ bi_status prefill_attention_impl(const void* q, const void* kc, const void* vc, 
   clear_error();
   BI_TRY(attn::check_dims(dims));
   BI_REQUIRE(B >= 0 && T >= 0 && (B > 0 || T == 0), BI_ERR_INVALID_ARG, "bi_prefill_attention: B=%d T=%d", B, T);
-  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "mode %d",
              static_cast<int>(mode));
   BI_REQUIRE(mode != BI_MODE_PROTECTED || target < B, BI_ERR_INVALID_ARG, "target_request %d >= B %d", target, B);
   if (T == 0) return BI_OK;
@@ -1182,7 +1184,7 @@ DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode
   DecodeWs r;
   const size_t pb = carve_decode_plan(base, B, dm->num_kv_heads, &r.plan);
   const int inv = (dm->max_pages * kPage + kSplit - 1) / kSplit;
-  const size_t units = static_cast<size_t>(B) * (mode == BI_MODE_INVARIANT ? inv : std::max(inv, kMaxFastUnits));
+  const size_t units = static_cast<size_t>(B) * (mode_invariant(mode) ? inv : std::max(inv, kMaxFastUnits));
   const size_t qb = carve_decode_parts(base ? static_cast<char*>(base) + pb : nullptr, units, dm, &r.part);
   r.bytes = pb + qb;
   return r;
@@ -1196,7 +1198,7 @@ bi_status decode_attention_noalloc_impl(const void* q, const void* kc, const voi
   clear_error();
   BI_TRY(attn::check_dims(dims));
   BI_REQUIRE(B >= 0, BI_ERR_INVALID_ARG, "bi_decode_attention_noalloc: B=%d", B);
-  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "mode %d",
              static_cast<int>(mode));
   BI_REQUIRE(mode != BI_MODE_PROTECTED || target < B, BI_ERR_INVALID_ARG, "target_request %d >= B %d", target, B);
   if (B == 0) return BI_OK;

@@ -112,6 +112,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Launch errors surface through cudaGetLastError (checked by BI_LAUNCH_CHECK).
 #define BI_PDL_CHECK(expr) (void)(expr)
 
+// Modes whose reduction geometry never depends on the batch.
+inline bool mode_invariant(bi_mode m) { return m == BI_MODE_INVARIANT || m == BI_MODE_INVARIANT_KSPLIT; }
+inline bool mode_valid(bi_mode m) { return m >= BI_MODE_INVARIANT && m <= BI_MODE_INVARIANT_KSPLIT; }
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }

@@ -71,11 +71,11 @@ struct Args {
   int stage_bytes;  // kbs x (A box + W instruction columns of B)
   int stages;
   int m_tiles, n_tiles;  // n_tiles counts CTA-wide column tiles (64*W wide)
-  int splits;            // K splits of unprotected tiles
-  int tm0, tm1;          // m-tiles [tm0, tm1) are never split
+  int splits;            // K splits of the other tiles, one CTA unit each (partials summed by a second pass)
+  int tm0, tm1;          // m-tiles [tm0, tm1) are computed whole by one unit each
+  int seq;               // ... as `seq` K-split partials merged inside the CTA (1: one pass over K)
   int units;             // total work units
   int kb_total;          // k-tiles in K
-  int kb_per;            // k-tiles per split
   void* C;
   const __nv_bfloat16* R;  // residual or null
   float* partial;          // [splits][M][N] fp32 (split units only)
@@ -197,6 +197,18 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor
 // version 1, base offset 0 (tiles are 1024-byte aligned).
@@ -210,7 +222,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N=64, M=128.
 // Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_for(int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
@@ -218,11 +229,12 @@ __host__ __device__ constexpr uint32_t idesc_for(int n) {
 }
 
 // unit -> (m tile, n tile, split index, split count)
-__device__ __forceinline__ void unit_coords(const Args& a, int u, int& mt, int& nt, int& s, int& nsplit) {
+__device__ __forceinline__ void unit_coords(const Args& a, int u, int& mt, int& nt, int& s, int& nsplit, int& seq) {
   const int prot = a.tm1 - a.tm0;
   const int per_col = prot + (a.m_tiles - prot) * a.splits;
   nt = u / per_col;
   int r = u % per_col;
+  seq = 1;
   const int before = a.tm0 * a.splits;
   if (r < before) {
     mt = r / a.splits;
@@ -232,6 +244,7 @@ __device__ __forceinline__ void unit_coords(const Args& a, int u, int& mt, int& 
     mt = a.tm0 + (r - before);
     s = 0;
     nsplit = 1;
+    seq = a.seq;
   } else {
     r -= before + prot;
     mt = a.tm1 + r / a.splits;
@@ -240,14 +253,11 @@ __device__ __forceinline__ void unit_coords(const Args& a, int u, int& mt, int& 
   }
 }
 
-__device__ __forceinline__ void k_range(const Args& a, int s, int nsplit, int& kb0, int& kb1) {
-  if (nsplit == 1) {
-    kb0 = 0;
-    kb1 = a.kb_total;
-  } else {
-    kb0 = s * a.kb_per;
-    kb1 = min(a.kb_total, kb0 + a.kb_per);
-  }
+// K-split s of n: k-tiles [floor(s*T/n), floor((s+1)*T/n)), T = k-tiles in K.
+// The partition depends on (T, n) only; with n <= T every part is non-empty.
+__host__ __device__ __forceinline__ void k_range(int kb_total, int s, int nsplit, int& kb0, int& kb1) {
+  kb0 = static_cast<int>((static_cast<int64_t>(s) * kb_total) / nsplit);
+  kb1 = static_cast<int>((static_cast<int64_t>(s + 1) * kb_total) / nsplit);
 }
 
 // Shared memory: [barrier block 1 KiB][stage 0]..[stage n-1][slack].  A stage
@@ -273,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                                                               const __grid_constant__ CUtensorMap tmW, const Args a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kTmemCols = 2 * W * kBN;  // two accumulators (64, 128 or 256 columns each)
+  // two accumulators of W*64 columns, plus the running sum of merged units when
+  // it fits (W <= 2); allocations are powers of two
+  constexpr int kTmemCols = W == 1 ? 256 : 512;
   const int kStages = a.stages;
   const int kStageBytes = a.stage_bytes;
   const int kbs = a.kbs;
@@ -332,29 +344,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       int st = 0;        // stage slot and its phase parity, advanced in the same
       uint32_t ph = 0;   // sequence as the MMA thread's
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        int mt, nt, s, ns, kb0, kb1;
-        unit_coords(a, u, mt, nt, s, ns);
-        k_range(a, s, ns, kb0, kb1);
-        for (int kb = kb0; kb < kb1; kb += kbs) {
-          if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = full0 + 8 * st;
-          const uint32_t sa = smem_u32(tiles + st * kStageBytes);
-          mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
-          if (a.map3d) {
-            tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
-            tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
-          } else {
-            tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
-            tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
-          }
-          issued_mask |= 1u << st;
-          issued_par = (issued_par & ~(1u << st)) | (ph << st);
-          if (++st == kStages) {
-            st = 0;
-            ph ^= 1u;
+        int mt, nt, s, ns, seq;
+        unit_coords(a, u, mt, nt, s, ns, seq);
+        for (int q = 0; q < seq && ok; ++q) {
+          int kb0, kb1;
+          if (seq > 1) k_range(a.kb_total, q, seq, kb0, kb1);
+          else k_range(a.kb_total, s, ns, kb0, kb1);
+          for (int kb = kb0; kb < kb1; kb += kbs) {
+            if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + 8 * st;
+            const uint32_t sa = smem_u32(tiles + st * kStageBytes);
+            mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
+            if (a.map3d) {
+              tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
+              tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
+            } else {
+              tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
+              tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+            }
+            issued_mask |= 1u << st;
+            issued_par = (issued_par & ~(1u << st)) | (ph << st);
+            if (++st == kStages) {
+              st = 0;
+              ph ^= 1u;
+            }
           }
         }
       }
@@ -366,8 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // Every pass over a K range (a whole tile, one split unit, or one of the
+    // in-CTA partials of a merged unit) goes into the next of the two
+    // accumulators and is handed to the epilogue on its own.
     if (lane == 0) {
       const uint64_t desc0 = sw128_desc(smem_u32(tiles));
+      constexpr uint32_t kIdescW = idesc_for(W * kBN);
       int st = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -375,47 +395,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       bool ok = true;
       bool any = false;
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        int mt, nt, s, ns, kb0, kb1;
-        unit_coords(a, u, mt, nt, s, ns);
-        k_range(a, s, ns, kb0, kb1);
-        if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 2)) break;
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * W * kBN);
-        for (int kb = kb0; kb < kb1; kb += kbs) {
-          if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3)) {
+        int mt, nt, s, ns, seq;
+        unit_coords(a, u, mt, nt, s, ns, seq);
+        for (int q = 0; q < seq && ok; ++q) {
+          int kb0, kb1;
+          if (seq > 1) k_range(a.kb_total, q, seq, kb0, kb1);
+          else k_range(a.kb_total, s, ns, kb0, kb1);
+          if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 2)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // descriptors of this stage: start addresses advance in 16-byte units
-          const uint64_t sdesc = desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
-          const int nkb = min(kbs, kb1 - kb);  // k-blocks of this stage inside the range
-          for (int j = 0; j < nkb; ++j) {
-            const uint64_t adesc = sdesc + static_cast<uint64_t>((j * a_tile) >> 4);
-            const uint64_t bdesc = sdesc + static_cast<uint64_t>((a_bytes + j * b_tile) >> 4);
-            const uint32_t first = (kb + j == kb0) ? 1u : 0u;
+          const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * W * kBN);
+          for (int kb = kb0; kb < kb1; kb += kbs) {
+            if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // descriptors of this stage: start addresses advance in 16-byte units
+            const uint64_t sdesc = desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+            const int nkb = min(kbs, kb1 - kb);  // k-blocks of this stage inside the range
+            for (int j = 0; j < nkb; ++j) {
+              const uint64_t adesc = sdesc + static_cast<uint64_t>((j * a_tile) >> 4);
+              const uint64_t bdesc = sdesc + static_cast<uint64_t>((a_bytes + j * b_tile) >> 4);
+              const uint32_t first = (kb + j == kb0) ? 1u : 0u;
 #pragma unroll
-            for (int k = 0; k < kBK / kUK; ++k) {
-              // the first instruction of a tile overwrites the accumulator, all others add
-              const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
-              // one instruction spans the tile's W*64 columns: the B rows of a stage are
-              // contiguous 128-byte swizzle rows, 1024 bytes per 8-row group
-              tc_mma(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
-                     idesc_for(W * kBN), accum);
+              for (int k = 0; k < kBK / kUK; ++k) {
+                // the first instruction of a pass overwrites the accumulator, all others add;
+                // one instruction spans the tile's W*64 columns: the B rows of a stage are
+                // contiguous 128-byte swizzle rows, 1024 bytes per 8-row group
+                const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
+                tc_mma(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdescW,
+                       accum);
+              }
+            }
+            tc_commit(empty0 + 8 * st);  // stage free once these MMAs have read it
+            any = true;
+            if (++st == kStages) {
+              st = 0;
+              ph ^= 1u;
             }
           }
-          tc_commit(empty0 + 8 * st);  // stage free once these MMAs have read it
-          any = true;
-          if (++st == kStages) {
-            st = 0;
-            ph ^= 1u;
+          if (!ok) break;
+          tc_commit(tfull0 + 8 * acc);
+          if (++acc == 2) {
+            acc = 0;
+            acc_ph ^= 1u;
           }
-        }
-        if (!ok) break;
-        tc_commit(tfull0 + 8 * acc);
-        if (++acc == 2) {
-          acc = 0;
-          acc_ph ^= 1u;
         }
       }
       if (*abort_flag && any) {
@@ -426,65 +453,93 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
   } else {
     // ------------------------------------------------------------ epilogue (4 warps)
+    // Thread = one accumulator row (tensor-memory lane), 32 columns per load.
+    // Merged units: partial q is added into a running sum kept in a third
+    // tensor-memory buffer, sum = ((0 + P0) + P1) + ..., rounded once at the end;
+    // the second-pass reduction of split units adds the same partials in the
+    // same order, so both give the same bits.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t sum_base = lane_base + 2 * W * kBN;  // running-sum buffer (merged units only)
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-      int mt, nt, s, ns;
-      unit_coords(a, u, mt, nt, s, ns);
-      if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 4)) break;
-      tc_fence_after();
+    bool ok = true;
+    for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+      int mt, nt, s, ns, seq;
+      unit_coords(a, u, mt, nt, s, ns, seq);
       const int row = mt * kBM + row_in_tile;
       const bool row_ok = row < a.M;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * W * kBN;
+      for (int q = 0; q < seq; ++q) {
+        if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 4)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = lane_base + acc * W * kBN;
+        const bool last = q == seq - 1;
 #pragma unroll 1
-      for (int ch = 0; ch < 2 * W; ++ch) {
-        uint32_t r[32];
-        tc_ld32(tbase + ch * 32, r);
-        const int col0 = nt * W * kBN + ch * 32;
-        if (!row_ok || col0 >= a.N) continue;
-        if (ns > 1) {
-          float* dst = a.partial + (static_cast<size_t>(s) * a.M + row) * a.N + col0;
+        for (int ch = 0; ch < 2 * W; ++ch) {
+          uint32_t r[32];
+          tc_ld32(tbase + ch * 32, r);
+          if (seq > 1) {
+            if constexpr (W <= 2) {
+              uint32_t t[32];
+              if (q > 0) tc_ld32(sum_base + ch * 32, t);
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (col0 + 4 * g < a.N)
-              *reinterpret_cast<float4*>(dst + 4 * g) =
-                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
-                              __uint_as_float(r[4 * g + 3]));
-        } else if (a.out_kind == kOutF32) {
-          float* dst = static_cast<float*>(a.C) + static_cast<size_t>(row) * a.N + col0;
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (col0 + 4 * g < a.N)
-              *reinterpret_cast<float4*>(dst + 4 * g) =
-                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
-                              __uint_as_float(r[4 * g + 3]));
-        } else {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.C) + static_cast<size_t>(row) * a.N + col0;
-          const __nv_bfloat16* res = a.R ? a.R + static_cast<size_t>(row) * a.N + col0 : nullptr;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + 8 * g >= a.N) break;
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * g + e]);
-            if (res) {
-              float rv[8];
-              unpack8(*reinterpret_cast<const uint4*>(res + 8 * g), rv);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = __fadd_rn(f[e], rv[e]);
+              for (int e = 0; e < 32; ++e)
+                r[e] = __float_as_uint(__fadd_rn(q > 0 ? __uint_as_float(t[e]) : 0.f, __uint_as_float(r[e])));
+              if (!last) {
+                tc_st32(sum_base + ch * 32, r);
+                continue;
+              }
             }
-            *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(f);
+          }
+          const int col0 = nt * W * kBN + ch * 32;
+          if (!row_ok || col0 >= a.N) continue;
+          if (ns > 1) {
+            float* dst = a.partial + (static_cast<size_t>(s) * a.M + row) * a.N + col0;
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              if (col0 + 4 * g < a.N)
+                *reinterpret_cast<float4*>(dst + 4 * g) =
+                    make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+          } else if (a.out_kind == kOutF32) {
+            float* dst = static_cast<float*>(a.C) + static_cast<size_t>(row) * a.N + col0;
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              if (col0 + 4 * g < a.N)
+                *reinterpret_cast<float4*>(dst + 4 * g) =
+                    make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+          } else {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.C) + static_cast<size_t>(row) * a.N + col0;
+            const __nv_bfloat16* res = a.R ? a.R + static_cast<size_t>(row) * a.N + col0 : nullptr;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              if (col0 + 8 * g >= a.N) break;
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * g + e]);
+              if (res) {
+                float rv[8];
+                unpack8(*reinterpret_cast<const uint4*>(res + 8 * g), rv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = __fadd_rn(f[e], rv[e]);
+              }
+              *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(f);
+            }
           }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      if (++acc == 2) {
-        acc = 0;
-        acc_ph ^= 1u;
+        if (seq > 1 && !last) asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
       }
     }
   }
@@ -503,40 +558,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 }
 
 // Second pass of split-K: element (i, j) of an unprotected tile is the
-// left-to-right sum of its split partials (+ residual), rounded once.
+// left-to-right sum ((0 + P_0) + P_1) + ... of its split partials (+ residual),
+// rounded once.  A thread owns four columns of one row; the partials are
+// fetched four splits at a time so their loads are in flight together, and
+// added in split order.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, void* C, const __nv_bfloat16* __restrict__ R,
                                      int M, int N, int splits, int skip_r0, int skip_r1, int out_kind) {
   pdl_wait();
   pdl_trigger();
-  const int64_t chunks = static_cast<int64_t>(N) / 8;
+  const int64_t chunks = static_cast<int64_t>(N) / 4;
   const int64_t n = static_cast<int64_t>(M) * chunks;
+  const size_t plane = static_cast<size_t>(M) * N;
   for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
        k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int row = static_cast<int>(k / chunks);
-    const int col = static_cast<int>(k % chunks) * 8;
+    const int col = static_cast<int>(k % chunks) * 4;
     if (row >= skip_r0 && row < skip_r1) continue;
-    float f[8];
+    const float* p = partial + static_cast<size_t>(row) * N + col;
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= splits; s += 4) {
+      float4 v[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      const float* p = partial + (static_cast<size_t>(s) * M + row) * N + col;
-      const float4 a = *reinterpret_cast<const float4*>(p);
-      const float4 b = *reinterpret_cast<const float4*>(p + 4);
-      f[0] = __fadd_rn(f[0], a.x); f[1] = __fadd_rn(f[1], a.y); f[2] = __fadd_rn(f[2], a.z); f[3] = __fadd_rn(f[3], a.w);
-      f[4] = __fadd_rn(f[4], b.x); f[5] = __fadd_rn(f[5], b.y); f[6] = __fadd_rn(f[6], b.z); f[7] = __fadd_rn(f[7], b.w);
+      for (int j = 0; j < 4; ++j) v[j] = __ldcs(reinterpret_cast<const float4*>(p + (s + j) * plane));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f.x = __fadd_rn(f.x, v[j].x); f.y = __fadd_rn(f.y, v[j].y);
+        f.z = __fadd_rn(f.z, v[j].z); f.w = __fadd_rn(f.w, v[j].w);
+      }
     }
+    for (; s < splits; ++s) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(p + s * plane));
+      f.x = __fadd_rn(f.x, v.x); f.y = __fadd_rn(f.y, v.y); f.z = __fadd_rn(f.z, v.z); f.w = __fadd_rn(f.w, v.w);
+    }
+    const size_t o = static_cast<size_t>(row) * N + col;
     if (out_kind == kOutF32) {
-      float* dst = static_cast<float*>(C) + static_cast<size_t>(row) * N + col;
-      *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
+      *reinterpret_cast<float4*>(static_cast<float*>(C) + o) = f;
     } else {
       if (R) {
-        float rv[8];
-        unpack8(*reinterpret_cast<const uint4*>(R + static_cast<size_t>(row) * N + col), rv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __fadd_rn(f[e], rv[e]);
+        const uint2 rr = *reinterpret_cast<const uint2*>(R + o);
+        f.x = __fadd_rn(f.x, bf16_lo(rr.x)); f.y = __fadd_rn(f.y, bf16_hi(rr.x));
+        f.z = __fadd_rn(f.z, bf16_lo(rr.y)); f.w = __fadd_rn(f.w, bf16_hi(rr.y));
       }
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(C) + static_cast<size_t>(row) * N + col) = pack8(f);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(C) + o) =
+          make_uint2(pack_bf16x2(f.x, f.y), pack_bf16x2(f.z, f.w));
     }
   }
 }
@@ -624,23 +689,46 @@ bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, int
   return BI_OK;
 }
 
+// SM count used by the planner; with no device (workspace queries on a host
+// without a GPU) it assumes 152.
+int plan_sms() {
+  const int n = num_sms();
+  return n > 0 ? n : 152;
+}
+
 struct Plan {
   int W;
   int a_rows, kbs, map3d, stage_bytes, stages;
   int splits;
-  int tm0, tm1;
-  int m_tiles, n_tiles, units, kb_total, kb_per;
+  int tm0, tm1, seq;
+  int m_tiles, n_tiles, units, kb_total;
 };
 
-int choose_width(int64_t M, int64_t N) {
-  const int sms = num_sms();
+// Part count of the K-only split (INVARIANT_KSPLIT): enough parts that a
+// decode-sized GEMM (one 128-row tile, 256-column tiles) gives about one unit
+// per SM of a 152-SM part, at least 4 k-tiles per part, at most kMaxSplitK.
+// A constant target (not the device's SM count) keeps the bits the same on
+// every device.
+constexpr int kKsplitUnits = 152;
+int ksplit_count(int64_t N, int64_t K) {
+  const int64_t kb_total = (K + kBK - 1) / kBK;
+  const int64_t tiles = (N + 4 * kBN - 1) / (4 * kBN);
+  int64_t ks = std::max<int64_t>(1, kKsplitUnits / std::max<int64_t>(1, tiles));
+  ks = std::min<int64_t>(ks, kMaxSplitK);
+  ks = std::min<int64_t>(ks, std::max<int64_t>(1, kb_total / 4));
+  return static_cast<int>(ks);
+}
+
+int choose_width(int64_t M, int64_t N, int max_w) {
+  const int sms = plan_sms();
   const int64_t mt = (M + kBM - 1) / kBM;
   double best = -1.0;
   int bw = 1;
   const int widths[3] = {4, 2, 1};
-  const double penalty[3] = {1.0, 0.92, 0.80};  // shared-memory operand traffic per flop grows as W shrinks
+  const double penalty[3] = {1.0, 0.92, 0.80};  // operand bytes per flop grow as W shrinks
   for (int i = 0; i < 3; ++i) {
     const int w = widths[i];
+    if (w > max_w) continue;
     const int64_t tiles = mt * ((N + w * kBN - 1) / (w * kBN));
     const int64_t waves = (tiles + sms - 1) / sms;
     const double eff = static_cast<double>(tiles) / static_cast<double>(waves * sms) * penalty[i];
@@ -652,20 +740,60 @@ int choose_width(int64_t M, int64_t N) {
   return bw;
 }
 
-// Decode-sized M (one 128-row tile): the GEMM streams the weights, so take the
-// widest CTA tile that still gives every SM a tile (more weight bytes per stage).
-int choose_width_small_m(int64_t N) {
-  const int sms = num_sms();
-  const int widths[3] = {4, 2, 1};
-  for (int w : widths)
-    if ((N + w * kBN - 1) / (w * kBN) >= sms) return w;
-  return 1;
+// Decode-sized M (one 128-row tile): the GEMM streams the weights and every
+// CTA also reads the whole A block of its K range, so take the width that
+// minimises (waves of units) x (bytes a CTA reads per unit ~ W*64 + a_rows).
+int choose_width_small_m(int64_t N, int splits, int a_rows) {
+  const int sms = plan_sms();
+  int bw = 1;
+  int64_t best = INT64_MAX;
+  for (int w = 4; w >= 1; --w) {
+    const int64_t units = ((N + w * kBN - 1) / (w * kBN)) * splits;
+    const int64_t waves = (units + sms - 1) / sms;
+    const int64_t cost = waves * (w * kBN + a_rows);
+    if (cost < best) {
+      best = cost;
+      bw = w;
+    }
+  }
+  return bw;
 }
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te) {
   Plan p;
-  p.W = M <= kBM ? choose_width_small_m(N) : choose_width(M, N);
   p.a_rows = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : kBM;
+  p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
+  p.splits = 1;
+  p.tm0 = p.tm1 = 0;
+  p.seq = 1;
+  // A protected target in the only m-tile makes the whole launch INVARIANT.
+  if (mode == BI_MODE_PROTECTED && te > tb && p.m_tiles == 1) mode = BI_MODE_INVARIANT;
+  int max_w = 4;
+  if (mode == BI_MODE_INVARIANT_KSPLIT) {
+    const int ks = ksplit_count(N, K);
+    if (p.m_tiles == 1) {
+      p.splits = ks;  // parts on separate CTAs, added by the second pass
+    } else if (ks > 1) {
+      p.tm0 = 0;      // every tile merged in its CTA
+      p.tm1 = p.m_tiles;
+      p.seq = ks;
+      max_w = 2;      // the running sum needs a third accumulator-sized buffer
+    }
+  } else if (mode != BI_MODE_INVARIANT) {
+    // FAST: split K when there are fewer tiles than SMs (the split count
+    // follows M); PROTECTED: the target's tiles are not split.
+    const int w0 = M <= kBM ? choose_width_small_m(N, 1, p.a_rows) : choose_width(M, N, 4);
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * ((N + w0 * kBN - 1) / (w0 * kBN));
+    const int sms = plan_sms();
+    int sk = static_cast<int>(std::min<int64_t>(kMaxSplitK, std::max<int64_t>(1, sms / std::max<int64_t>(1, tiles))));
+    p.splits = std::max(1, std::min(sk, p.kb_total));
+    if (mode == BI_MODE_PROTECTED && te > tb) {
+      p.tm0 = static_cast<int>(tb / kBM);
+      p.tm1 = static_cast<int>((te - 1) / kBM) + 1;
+    }
+  }
+  p.W = M <= kBM ? choose_width_small_m(N, p.splits, p.a_rows) : choose_width(M, N, max_w);
   // Each copy costs the copy engine a roughly fixed time, so at decode sizes a
   // stage spans several k-blocks (one 3D box of >= 32 KiB of weights per copy).
   // (A 3D copy costs more than a 2D box of the same bytes, so the 3D view is
@@ -675,27 +803,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   p.stage_bytes = p.kbs * (p.a_rows * kBK * 2 + p.W * kBSubBytes);
   const int budget = kSmemLimit - 1024 - kBarBlock - (p.a_rows < kBM ? kOverreadSlack : 0);
   p.stages = std::min(kMaxStages, budget / p.stage_bytes);
-  p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
   p.n_tiles = static_cast<int>((N + p.W * kBN - 1) / (p.W * kBN));
-  p.kb_total = static_cast<int>((K + kBK - 1) / kBK);
-  p.splits = 1;
-  p.tm0 = p.tm1 = 0;
-  if (mode != BI_MODE_INVARIANT) {
-    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    const int sms = num_sms();
-    int s = static_cast<int>(std::min<int64_t>(kMaxSplitK, std::max<int64_t>(1, sms / std::max<int64_t>(1, tiles))));
-    s = std::min(s, p.kb_total);
-    if (s > 1) {
-      const int per = (p.kb_total + s - 1) / s;
-      s = (p.kb_total + per - 1) / per;
-    }
-    p.splits = std::max(1, s);
-    if (mode == BI_MODE_PROTECTED && te > tb) {
-      p.tm0 = static_cast<int>(tb / kBM);
-      p.tm1 = static_cast<int>((te - 1) / kBM) + 1;
-    }
-  }
-  p.kb_per = (p.kb_total + p.splits - 1) / p.splits;
   const int prot = p.tm1 - p.tm0;
   p.units = p.n_tiles * (prot + (p.m_tiles - prot) * p.splits);
   return p;
@@ -733,9 +841,11 @@ int take_gemm_device_error(cudaStream_t s, int32_t* code) {
 
 size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode) {
   if (mode == BI_MODE_INVARIANT || M <= 0 || N <= 0 || K <= 0) return 0;
-  gemm::Plan p = gemm::make_plan(M, N, K, mode, 0, 0);
-  if (p.splits <= 1) return 0;
-  return static_cast<size_t>(p.splits) * M * N * sizeof(float);
+  // PROTECTED: the largest need with or without a target
+  int splits = gemm::make_plan(M, N, K, mode, 0, 0).splits;
+  if (mode == BI_MODE_PROTECTED) splits = std::max(splits, gemm::make_plan(M, N, K, mode, 0, 1).splits);
+  if (splits <= 1) return 0;
+  return static_cast<size_t>(splits) * M * N * sizeof(float);
 }
 
 bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64_t M, int64_t N, int64_t K,
@@ -750,7 +860,7 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
              "bi_gemm: sizes beyond int32");
   BI_REQUIRE(out_dtype == BI_BF16 || out_dtype == BI_F32, BI_ERR_UNSUPPORTED, "bi_gemm: out dtype %d",
              static_cast<int>(out_dtype));
-  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "bi_gemm: mode %d",
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "bi_gemm: mode %d",
              static_cast<int>(mode));
   BI_REQUIRE(R == nullptr || out_dtype == BI_BF16, BI_ERR_UNSUPPORTED, "bi_gemm: residual needs bf16 output");
   int64_t tb = 0, te = 0;
@@ -766,6 +876,8 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   BI_REQUIRE(aligned16(A) && aligned16(Wt) && aligned16(C) && (R == nullptr || aligned16(R)), BI_ERR_INVALID_ARG,
              "bi_gemm: pointers must be 16-byte aligned");
   gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te);
+  BI_REQUIRE(p.seq == 1 || p.W <= 2, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (merged units at width %d)",
+             p.W);
   gemm::Args args{};
   args.M = static_cast<int>(M);
   args.a_rows = p.a_rows;
@@ -780,9 +892,9 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   args.splits = p.splits;
   args.tm0 = p.tm0;
   args.tm1 = p.tm1;
+  args.seq = p.seq;
   args.units = p.units;
   args.kb_total = p.kb_total;
-  args.kb_per = p.kb_per;
   args.C = C;
   args.R = static_cast<const __nv_bfloat16*>(R);
   args.out_kind = out_dtype == BI_F32 ? gemm::kOutF32 : gemm::kOutBF16;
@@ -798,11 +910,12 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   BI_TRY(gemm::tensor_map(Wt, N, K, p.W * gemm::kBN, p.map3d ? p.kbs : 0, &mw));
   bi_status st;
   if (p.W == 4) st = gemm::launch_w<4>(ma, mw, args, s);
+  else if (p.W == 3) st = gemm::launch_w<3>(ma, mw, args, s);
   else if (p.W == 2) st = gemm::launch_w<2>(ma, mw, args, s);
   else st = gemm::launch_w<1>(ma, mw, args, s);
   if (st != BI_OK) return st;
   if (p.splits > 1) {
-    const int64_t n = M * (N / 8);
+    const int64_t n = M * (N / 4);
     const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
     const int skip0 = p.tm0 * gemm::kBM, skip1 = static_cast<int>(std::min<int64_t>(M, int64_t(p.tm1) * gemm::kBM));
     BI_TIMED(::bi::kTagSplitkReduce, s, BI_PDL_CHECK(launch_pdl(gemm::splitk_reduce_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, args.partial, C, args.R, args.M, args.N,
@@ -816,6 +929,11 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
 
 extern "C" size_t bi_gemm_workspace(int64_t M, int64_t N, int64_t K, bi_mode mode) {
   return bi::gemm_ws(M, N, K, mode);
+}
+
+extern "C" int32_t bi_gemm_ksplit(int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0) return 1;
+  return bi::gemm::ksplit_count(N, K);
 }
 
 extern "C" bi_status bi_gemm(const void* A, const void* W, void* C, const void* residual, int64_t M, int64_t N,

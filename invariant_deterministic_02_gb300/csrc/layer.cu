@@ -231,7 +231,7 @@ bi_status layer_forward_impl(const bi_model_dims* dm, const bi_layer_weights* w,
   clear_error();
   BI_TRY(check_model_dims(dm));
   BI_TRY(check_batch(b));
-  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "mode %d",
              static_cast<int>(mode));
   BI_REQUIRE(hidden && kc && vc && rc && rs, BI_ERR_INVALID_ARG, "bi_layer_forward: null pointer");
   LayerBufs L = carve(ws, ws_bytes, dm, b, mode, false);
@@ -248,7 +248,7 @@ bi_status model_forward_impl(const bi_model_dims* dm, const bi_model_weights* mw
   clear_error();
   BI_TRY(check_model_dims(dm));
   BI_TRY(check_batch(b));
-  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "mode %d",
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "mode %d",
              static_cast<int>(mode));
   BI_REQUIRE(mw && mw->embed && mw->final_norm && mw->lm_head && mw->num_layers >= 0 &&
                  (mw->num_layers == 0 || (mw->layers && kcs && vcs)),

@@ -195,7 +195,7 @@ bi_status launch(const void* xv, const void* gv, void* yv, int64_t rows, int d, 
   const T* g = static_cast<const T*>(gv);
   T* y = static_cast<T*>(yv);
   constexpr int V = VecOf<T>::N;
-  const int splits = (mode == BI_MODE_INVARIANT) ? 1 : fast_splits(rows, d, V);
+  const int splits = mode_invariant(mode) ? 1 : fast_splits(rows, d, V);
   if (splits == 1) {
     // Unsplit: the data-parallel schedule, identical to INVARIANT for every row.
     const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(num_sms()) * 8);
@@ -238,7 +238,7 @@ bi_status rmsnorm_impl(const void* x, const void* gamma, void* y, int64_t rows, 
   BI_REQUIRE(rows >= 0 && d > 0, BI_ERR_INVALID_ARG, "bi_rmsnorm: rows=%lld d=%lld", static_cast<long long>(rows),
              static_cast<long long>(d));
   BI_REQUIRE(dtype == BI_F32 || dtype == BI_BF16, BI_ERR_UNSUPPORTED, "bi_rmsnorm: dtype %d", static_cast<int>(dtype));
-  BI_REQUIRE(mode >= BI_MODE_INVARIANT && mode <= BI_MODE_PROTECTED, BI_ERR_INVALID_ARG, "bi_rmsnorm: mode %d",
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "bi_rmsnorm: mode %d",
              static_cast<int>(mode));
   const int vec = dtype == BI_F32 ? 4 : 8;
   BI_REQUIRE(d % vec == 0 && d / vec <= kThreads * kMaxChunks, BI_ERR_UNSUPPORTED,
@@ -257,7 +257,7 @@ bi_status rmsnorm_impl(const void* x, const void* gamma, void* y, int64_t rows, 
 }
 
 size_t rmsnorm_ws(int64_t rows, int64_t d, bi_mode mode) {
-  if (mode == BI_MODE_INVARIANT || rows <= 0) return 0;
+  if (mode_invariant(mode) || rows <= 0) return 0;
   const int sms = num_sms();
   if (rows >= sms) return 0;
   return static_cast<size_t>(rows) * sms * sizeof(float);

@@ -66,3 +66,22 @@ def test_host_validation_rejects_bad_arguments_before_launch(libpath):
     # zero-size work is a no-op that succeeds without touching pointers
     assert l.bi_rmsnorm(None, None, None, 0, 16, bi.BI_BF16, 1e-5, 0, -1, 0, None, 0, None) == bi.BI_OK
     assert l.bi_gemm(None, None, None, None, 0, 8, 16, bi.BI_BF16, 0, -1, 0, None, 0, None) == bi.BI_OK
+
+
+def test_ksplit_part_count_depends_on_weight_shape_only(libpath):
+    # S = clamp(152 // ceil(N/256), 1, min(16, ceil(K/64) // 4)): a pure function of (N, K)
+    import invariant_deterministic_02_gb300 as bi
+    for (N, K), S in {(4096, 4096): 9, (6144, 4096): 6, (24576, 4096): 1, (151936, 4096): 1,
+                      (4096, 12288): 9, (4096, 14336): 9, (256, 512): 2, (256, 64): 1, (512, 2048): 8,
+                      (1032, 1000): 4, (40000, 512): 1}.items():
+        assert bi.bi_gemm_ksplit(N, K) == S, (N, K)
+    l = bi.lib()
+    f = 4
+    # decode-sized M: S partial planes of M x N fp32; larger M merges in the CTA and needs none
+    assert l.bi_gemm_workspace(64, 4096, 4096, bi.INVARIANT_KSPLIT) == 9 * 64 * 4096 * f
+    assert l.bi_gemm_workspace(128, 6144, 4096, bi.INVARIANT_KSPLIT) == 6 * 128 * 6144 * f
+    assert l.bi_gemm_workspace(129, 4096, 4096, bi.INVARIANT_KSPLIT) == 0
+    assert l.bi_gemm_workspace(64, 24576, 4096, bi.INVARIANT_KSPLIT) == 0
+    assert l.bi_gemm_workspace(64, 4096, 4096, bi.INVARIANT) == 0
+    # an out-of-range mode is rejected on the host
+    assert l.bi_gemm(None, None, None, None, 4, 8, 16, bi.BI_BF16, 4, -1, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG

@@ -113,6 +113,7 @@ def test_llama8b_layer_target_bitwise_across_batches_and_modes():
     rig.add_request("t", tlen - 1, 4321, tlen)
     ht = synth.normal((1, shape.d_model), 4322)
     ref = rig.run(cuda(ht), [("t", 1, tlen - 1)])
+    refk = rig.run(cuda(ht), [("t", 1, tlen - 1)], mode=bi.INVARIANT_KSPLIT)
     lens = synth.uniform_ints(63, 128, 4096, 50)
     for b in range(63):
         rig.add_request(b, int(lens[b]) - 1, 2000 + 2 * b, int(lens[b]))
@@ -131,9 +132,15 @@ def test_llama8b_layer_target_bitwise_across_batches_and_modes():
         refo = rig.oracle(h, items)
         assert max_rel_err(f64(outf), refo) <= TOL_BF16
         assert max_rel_err(f64(outp), refo) <= TOL_BF16
+        outk = rig.run(cuda(h), items, mode=bi.INVARIANT_KSPLIT)
+        assert bits_equal(outk[pos:pos + 1], refk), ("ksplit", B)
+        assert max_rel_err(f64(outk), refo) <= TOL_BF16
 
 
-def test_layer_chunked_prefill_equals_token_by_token_decode():
+@pytest.mark.parametrize("mode", [bi.INVARIANT, bi.INVARIANT_KSPLIT])
+def test_layer_chunked_prefill_equals_token_by_token_decode(mode):
+    # INVARIANT_KSPLIT: prefill chunks of > 128 tokens merge the K parts inside a CTA,
+    # decode runs them on separate CTAs; the bits must agree all the same
     shape = synth.LLAMA31_8B_LAYER
     L = 600
     h = synth.normal((L, shape.d_model), 70)
@@ -144,7 +151,7 @@ def test_layer_chunked_prefill_equals_token_by_token_decode():
         res = []
         p = 0
         for n in chunks:
-            res.append(rig.run(cuda(h[p:p + n]), [(0, n, p)]))
+            res.append(rig.run(cuda(h[p:p + n]), [(0, n, p)], mode=mode))
             p += n
         outs.append(torch.cat(res))
     for o in outs[1:]:
@@ -157,5 +164,5 @@ def test_layer_chunked_prefill_equals_token_by_token_decode():
     res = []
     for p in range(L):
         x = torch.cat([h[p:p + 1], hn[p:p + 1]])
-        res.append(rig.run(cuda(x), [(0, 1, p), (1, 1, p)])[0:1])
+        res.append(rig.run(cuda(x), [(0, 1, p), (1, 1, p)], mode=mode)[0:1])
     assert bits_equal(torch.cat(res), outs[0])

@@ -115,6 +115,9 @@ def test_tiny_model_greedy_bit_exact_across_compositions():
         assert_same(ref, got, "composition %d" % i)
     got = greedy_run(m, prompt, 30, [40, 24], 3, 1, 7, seed=50, mode=bi.PROTECTED)
     assert_same(ref, got, "protected")
+    refk = greedy_run(m, prompt, 30, [64], 0, 0, 0, seed=1, mode=bi.INVARIANT_KSPLIT)
+    got = greedy_run(m, prompt, 30, [7, 57], 2, 2, 63, seed=60, mode=bi.INVARIANT_KSPLIT)
+    assert_same(refk, got, "ksplit")
 
 
 @pytest.mark.slow
