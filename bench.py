@@ -129,7 +129,8 @@ def run_ours(args, rank, world, local_rank):
     K, W = args.steps, args.warmup
     shape = QWEN3_8B
     Ls = synth.uniform_ints(B, KV_LO, KV_HI, args.seed + 17 * rank)  # KV length at the first step
-    total_steps = W + 2 * K + K  # warm-up, timed, profiled, end-to-end
+    compare = [m for m in ("fast", "invariant_ksplit") if m != args.mode] if args.mode == "invariant" else []
+    total_steps = W + 2 * K + K + len(compare) * (K + 1)  # warm-up, timed, profiled, end-to-end, other modes
     pages = int(sum((int(L) + total_steps + 16) // 16 + 1 for L in Ls)) + 16
     model = BiModel(shape, BiModel.random_weights(shape, seed=args.seed + 1000 * rank), num_pages=pages,
                     page_seed=args.seed + 3)
@@ -156,17 +157,17 @@ def run_ours(args, rank, world, local_rank):
         return bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos[step].data_ptr(), d_bt.data_ptr(), max_pages, pages,
                         target, 0 if target >= 0 else -1, 1 if target >= 0 else 0)
 
-    ws_bytes = bi.bi_model_workspace(model.dims, batch_for(0), mode)
+    ws_bytes = max(bi.bi_model_workspace(model.dims, batch_for(0), bi.MODES[m]) for m in [args.mode] + compare)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     step = [0]
 
-    def one_step():
+    def one_step(m=mode):
         s = step[0]
         src, dst = ids[s % 2], ids[(s + 1) % 2]
         bi.bi_model_forward(model.dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s), model.k_ptrs,
-                            model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=dst, mode=mode, workspace=ws,
+                            model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=dst, mode=m, workspace=ws,
                             ws_bytes=ws_bytes, stream=sp)
         step[0] += 1
 
@@ -302,6 +303,26 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": round(B * world * K / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
+    # ---------------------------------------------------------------- the same steps in the other modes
+    # FAST: the non-invariant schedule (cost of invariance = FAST / INVARIANT throughput);
+    # INVARIANT_KSPLIT: the K-only split-K GEMM variant (also batch invariant)
+    modes = {}
+    for m in compare:
+        one_step(bi.MODES[m])
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(K):
+            one_step(bi.MODES[m])
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cms = c0.elapsed_time(c1)
+        modes[m] = {"value": round(B * world * K / (cms / 1000.0), 2), "unit": "tok/s",
+                    "ms_per_step": round(cms / K, 4)}
+    if "fast" in modes:
+        modes["invariant_over_fast_time"] = round(ms_per_step / modes["fast"]["ms_per_step"], 4)
+    assert bi.bi_device_error() == 0
+
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic: seeded random-init weights ~N(0,0.02), random token ids, "
@@ -313,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
             "clocks": ck, "e2e": e2e, "gpu_launches": int(round(launches_per_step * K)),
             "roofline": roofline, "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
                                                   for kk, vv in v.items()} for k, v in kern.items()},
-            "other_rooflines": others}
+            "other_rooflines": others, "modes": modes}
     return line
 
 

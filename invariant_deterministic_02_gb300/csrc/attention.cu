@@ -46,11 +46,17 @@ __device__ __forceinline__ void group_sync(int group) {
 }
 
 // Per-group shared scratch of the split function.
+// (o is written only after every warp has finished with z and e, so it shares
+// their storage: the smaller scratch lets three decode CTAs share an SM.)
 template <int HD, int G>
 struct SplitSmem {
-  float z[G][kSplit];               // scores (log2 domain), -inf where masked
-  __align__(16) float e[kSplit][4]; // exp2(z - m), position-major, heads padded to 4
-  __align__(16) float o[4][G][HD];  // per-warp partial weighted sums
+  union {
+    struct {
+      float z[G][kSplit];               // scores (log2 domain), -inf where masked
+      __align__(16) float e[kSplit][4]; // exp2(z - m), position-major, heads padded to 4
+    };
+    __align__(16) float o[4][G][HD];  // per-warp partial weighted sums
+  };
   float m[G];
   float l[G];
 };
@@ -375,6 +381,7 @@ __device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& k
     }
   }
   kv.after_v(w);
+  group_sync(group);  // every warp is done with e before o overwrites it
 #pragma unroll
   for (int hh = 0; hh < G; ++hh) {
     float* dst = &sm.o[w][hh][lane * DPO];
@@ -424,36 +431,63 @@ struct Partials {
 // states in a pairwise tree over the split index (binary-counter form: the same
 // tree as the level-by-level tree over 2^BI_MERGE_DEPTH leaves padded with
 // empty states, since an empty state is an exact identity); FAST rows combine
-// left to right.
+// left to right.  States are fetched 16 at a time (their loads in flight
+// together); an INVARIANT chunk of 16 consecutive splits is one complete
+// level-4 subtree, reduced level by level in registers, and the chunk results
+// go through the binary counter.
 // Partial states are read through L2 (__ldcg): in the decode kernel they were
 // written by other CTAs of the same launch.
+constexpr int kMergeChunk = 16;  // split states fetched together; a chunk is one level-4 subtree
+
 __device__ __forceinline__ void merge_row(const Partials& part, size_t first_unit, int n, bool tree, int hq, int hd,
                                           int h, int d, float& out_m, float& out_l, float& out_o) {
   float m = -INFINITY, l = 0.f, o = 0.f;
-  if (!tree) {
-    for (int s = 0; s < n; ++s) {
-      const size_t pi = (first_unit + s) * hq + h;
-      merge_state(m, l, o, __ldcg(part.m + pi), __ldcg(part.l + pi), __ldcg(part.o + pi * hd + d));
-    }
-  } else {
-    float sm_[BI_MERGE_DEPTH + 1], sl_[BI_MERGE_DEPTH + 1], so_[BI_MERGE_DEPTH + 1];
-    unsigned occ = 0;
-    for (int s = 0; s < n; ++s) {
-      const size_t pi = (first_unit + s) * hq + h;
-      float cm = __ldcg(part.m + pi), cl = __ldcg(part.l + pi), co = __ldcg(part.o + pi * hd + d);
-      int lvl = 0;
-      while (occ & (1u << lvl)) {
-        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
-        merge_state(am, al, ao, cm, cl, co);  // stack entry covers the lower indices
-        cm = am; cl = al; co = ao;
-        occ &= ~(1u << lvl);
-        ++lvl;
+  // stack of complete subtrees over chunk results (level 4 and up of the padded tree)
+  float sm_[BI_MERGE_DEPTH - 3], sl_[BI_MERGE_DEPTH - 3], so_[BI_MERGE_DEPTH - 3];
+  unsigned occ = 0;
+  for (int c0 = 0; c0 < n; c0 += kMergeChunk) {
+    // the chunk's states, loaded together (empty past n)
+    float cm[kMergeChunk], cl[kMergeChunk], co[kMergeChunk];
+#pragma unroll
+    for (int j = 0; j < kMergeChunk; ++j) {
+      if (c0 + j < n) {
+        const size_t pi = (first_unit + c0 + j) * hq + h;
+        cm[j] = __ldcg(part.m + pi);
+        cl[j] = __ldcg(part.l + pi);
+        co[j] = __ldcg(part.o + pi * hd + d);
+      } else {
+        cm[j] = -INFINITY;
+        cl[j] = 0.f;
+        co[j] = 0.f;
       }
-      sm_[lvl] = cm; sl_[lvl] = cl; so_[lvl] = co;
-      occ |= (1u << lvl);
     }
+    if (!tree) {
+      // FAST: left to right
+#pragma unroll
+      for (int j = 0; j < kMergeChunk; ++j) merge_state(m, l, o, cm[j], cl[j], co[j]);
+      continue;
+    }
+    // pairwise tree inside the chunk, level by level: (0,1), (2,3), ... then pairs of those
+#pragma unroll
+    for (int w = 1; w < kMergeChunk; w *= 2)
+#pragma unroll
+      for (int i = 0; i < kMergeChunk; i += 2 * w) merge_state(cm[i], cl[i], co[i], cm[i + w], cl[i + w], co[i + w]);
+    // push the chunk's subtree; equal-sized subtrees merge pairwise (binary counter)
+    float xm = cm[0], xl = cl[0], xo = co[0];
+    int lvl = 0;
+    while (occ & (1u << lvl)) {
+      float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
+      merge_state(am, al, ao, xm, xl, xo);  // stack entry covers the lower indices
+      xm = am; xl = al; xo = ao;
+      occ &= ~(1u << lvl);
+      ++lvl;
+    }
+    sm_[lvl] = xm; sl_[lvl] = xl; so_[lvl] = xo;
+    occ |= (1u << lvl);
+  }
+  if (tree) {
     // fold what is left, smallest (rightmost) subtree first: merge(stack[lvl], acc)
-    for (int lvl = 0; lvl <= BI_MERGE_DEPTH; ++lvl) {
+    for (int lvl = 0; lvl <= BI_MERGE_DEPTH - 4; ++lvl) {
       if (occ & (1u << lvl)) {
         float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
         merge_state(am, al, ao, m, l, o);
@@ -538,7 +572,13 @@ __device__ __forceinline__ int find_row(const int* prefix, int n, int u) {
 // its quarters land.  A unit (one request, one kv head, one planned range) is
 // one 256-position split under the invariant plan, or several consecutive
 // 256-position blocks combined left to right under the FAST plan.
-constexpr int kDecodeStages = 5;
+// Ring-size rule: the four consumer warps may wait on the four key quarters of
+// a split at once, so a stage's previous use must belong to an earlier phase
+// (stages >= 4); with fewer, a wait on the next use of a stage can be satisfied
+// by the completed parity of the use before it, and the ring's accounting
+// breaks.  (A 3-stage build did exactly that.)
+constexpr int kDecodeStages = 4;
+static_assert(kDecodeStages >= 4, "the four quarters of a phase may be waited on together");
 constexpr int kDecodeThreads = kGroupThreads + 32;
 
 template <int HD, int G>
@@ -551,7 +591,7 @@ struct DecodeSmem {
 };
 
 template <int HD, int G>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_split_kernel(
+__global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vc,
     const int* __restrict__ block_table, const int* __restrict__ kv_lens, int B, int hq, int hkv, int max_pages,
     float scale_log2, DecodePlan plan, Partials part) {

@@ -76,6 +76,8 @@ struct Args {
   int seq;               // ... as `seq` K-split partials merged inside the CTA (1: one pass over K)
   int units;             // total work units
   int kb_total;          // k-tiles in K
+  int prefetch_w;        // 1: W is constant while the previous kernel runs (weights of a forward pass), so
+                         // the first stages' W copies may be issued before waiting for that kernel
   void* C;
   const __nv_bfloat16* R;  // residual or null
   float* partial;          // [splits][M][N] fp32 (split units only)
@@ -331,7 +333,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // everything below reads or writes memory shared with the previous kernel
+  // Everything below reads or writes memory shared with the previous kernel,
+  // except the weight copies of the first stages when a.prefetch_w is set: the
+  // producer issues those first (their stages are fresh, so no empty-wait is
+  // needed) and only then waits, so weight latency overlaps the previous kernel.
+  int pre_stages = 0;  // stages whose W copy (and transaction count) was issued early
+  if (warp < kProducerWarps && lane == 0 && a.prefetch_w && blockIdx.x < a.units) {
+    int mt, nt, s, ns, seq, kb0, kb1;
+    unit_coords(a, blockIdx.x, mt, nt, s, ns, seq);
+    if (seq > 1) k_range(a.kb_total, 0, seq, kb0, kb1);
+    else k_range(a.kb_total, s, ns, kb0, kb1);
+    for (int kb = kb0; kb < kb1 && pre_stages < kStages; kb += kbs, ++pre_stages) {
+      const uint32_t fb = full0 + 8 * pre_stages;
+      const uint32_t sa = smem_u32(tiles + pre_stages * kStageBytes);
+      mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
+      if (a.map3d) tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
+      else tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+    }
+  }
   pdl_wait();
   pdl_trigger();
 
@@ -351,19 +370,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           if (seq > 1) k_range(a.kb_total, q, seq, kb0, kb1);
           else k_range(a.kb_total, s, ns, kb0, kb1);
           for (int kb = kb0; kb < kb1; kb += kbs) {
-            if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
-              ok = false;
-              break;
-            }
             const uint32_t fb = full0 + 8 * st;
             const uint32_t sa = smem_u32(tiles + st * kStageBytes);
-            mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
-            if (a.map3d) {
-              tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
-              tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
+            if (pre_stages > 0) {
+              // W of this stage is already on its way (issued before the wait): add A only
+              --pre_stages;
+              if (a.map3d) tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
+              else tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
             } else {
-              tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
-              tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+              if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
+              if (a.map3d) {
+                tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
+                tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
+              } else {
+                tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
+                tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+              }
             }
             issued_mask |= 1u << st;
             issued_par = (issued_par & ~(1u << st)) | (ph << st);
@@ -850,7 +876,7 @@ size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode) {
 
 bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64_t M, int64_t N, int64_t K,
                     bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count, void* ws,
-                    size_t ws_bytes, cudaStream_t s) {
+                    size_t ws_bytes, cudaStream_t s, bool weights_constant) {
   clear_error();
   BI_REQUIRE(M >= 0 && N >= 0 && K >= 8, BI_ERR_INVALID_ARG, "bi_gemm: M=%lld N=%lld K=%lld",
              static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
@@ -893,6 +919,7 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   args.tm0 = p.tm0;
   args.tm1 = p.tm1;
   args.seq = p.seq;
+  args.prefetch_w = weights_constant ? 1 : 0;
   args.units = p.units;
   args.kb_total = p.kb_total;
   args.C = C;
@@ -940,5 +967,5 @@ extern "C" bi_status bi_gemm(const void* A, const void* W, void* C, const void* 
                              int64_t K, bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count,
                              void* workspace, size_t ws_bytes, bi_stream s) {
   return bi::gemm_impl(A, W, C, residual, M, N, K, out_dtype, mode, target_row, target_count, workspace, ws_bytes,
-                       reinterpret_cast<cudaStream_t>(s));
+                       reinterpret_cast<cudaStream_t>(s), false);
 }

@@ -12,8 +12,10 @@ namespace bi {
 bi_status rmsnorm_impl(const void*, const void*, void*, int64_t, int64_t, bi_dtype, float, bi_mode, int32_t, int32_t,
                        void*, size_t, cudaStream_t);
 size_t rmsnorm_ws(int64_t, int64_t, bi_mode);
+// weights_constant: W is not written by the kernels of this forward pass, so the
+// GEMM may start fetching it before the previous kernel has finished
 bi_status gemm_impl(const void*, const void*, void*, const void*, int64_t, int64_t, int64_t, bi_dtype, bi_mode,
-                    int32_t, int32_t, void*, size_t, cudaStream_t);
+                    int32_t, int32_t, void*, size_t, cudaStream_t, bool weights_constant);
 size_t gemm_ws(int64_t, int64_t, int64_t, bi_mode);
 bi_status decode_attention_impl(const void*, const void*, const void*, const int32_t*, const int32_t*, int32_t,
                                 const bi_attn_dims*, void*, bi_mode, int32_t, void*, size_t, cudaStream_t);
@@ -187,7 +189,7 @@ bi_status layer_body(const bi_model_dims* dm, const bi_layer_weights* w, const f
              "layer: null weight pointer");
   bi_attn_dims ad = attn_dims(dm, b);
   BI_TRY(rmsnorm_impl(hidden, w->attn_norm, L.x, T, d, BI_BF16, dm->rms_eps, mode, trow, tcnt, L.sub, L.sub_bytes, s));
-  BI_TRY(gemm_impl(L.x, w->w_qkv, L.qkv, nullptr, T, qkvw, d, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s));
+  BI_TRY(gemm_impl(L.x, w->w_qkv, L.qkv, nullptr, T, qkvw, d, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s, true));
   BI_TRY(qkv_rope_store_impl(L.qkv, rc, rs, L.token_pos, L.token_req, b->block_table, static_cast<int32_t>(T), &ad,
                              L.q, kc, vc, s));
   if (b->max_q_len == 1 && T == b->num_requests) {
@@ -197,11 +199,11 @@ bi_status layer_body(const bi_model_dims* dm, const bi_layer_weights* w, const f
     BI_TRY(prefill_attention_impl(L.q, kc, vc, b->block_table, b->q_start, b->pos0, b->num_requests,
                                   static_cast<int32_t>(T), &ad, L.att, mode, treq, L.sub, L.sub_bytes, s));
   }
-  BI_TRY(gemm_impl(L.att, w->w_o, hidden, hidden, T, d, hq, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s));
+  BI_TRY(gemm_impl(L.att, w->w_o, hidden, hidden, T, d, hq, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s, true));
   BI_TRY(rmsnorm_impl(hidden, w->ffn_norm, L.x, T, d, BI_BF16, dm->rms_eps, mode, trow, tcnt, L.sub, L.sub_bytes, s));
-  BI_TRY(gemm_impl(L.x, w->w_gate_up, L.gu, nullptr, T, 2 * F, d, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s));
+  BI_TRY(gemm_impl(L.x, w->w_gate_up, L.gu, nullptr, T, 2 * F, d, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s, true));
   BI_TRY(swiglu_impl(L.gu, L.act, T, F, s));
-  BI_TRY(gemm_impl(L.act, w->w_down, hidden, hidden, T, d, F, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s));
+  BI_TRY(gemm_impl(L.act, w->w_down, hidden, hidden, T, d, F, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s, true));
   return BI_OK;
 }
 
@@ -277,7 +279,7 @@ bi_status model_forward_impl(const bi_model_dims* dm, const bi_model_weights* mw
   const int32_t tcnt = prot ? 1 : 0;
   BI_TRY(rmsnorm_impl(last, mw->final_norm, L.x, B, d, BI_BF16, dm->rms_eps, mode, trow, tcnt, L.sub, L.sub_bytes, s));
   BI_TRY(gemm_impl(L.x, mw->lm_head, logits, nullptr, B, dm->vocab, d, BI_F32, mode, trow, tcnt, L.sub, L.sub_bytes,
-                   s));
+                   s, true));
   BI_TRY(topk_impl(logits, B, dm->vocab, topk, top_v, top_i, greedy, s));
   return BI_OK;
 }
