@@ -581,12 +581,21 @@ constexpr int kDecodeStages = 4;
 static_assert(kDecodeStages >= 4, "the four quarters of a phase may be waited on together");
 constexpr int kDecodeThreads = kGroupThreads + 32;
 
+// Work items reach the consumers through a 2-slot ring filled by the producer
+// one item ahead: the item's descriptor and its G query rows (one bulk copy),
+// so the consumer warps never wait on global loads for their indexing or q.
+constexpr int kItemSlots = 2;
+
 template <int HD, int G>
 struct DecodeSmem {
   __nv_bfloat16 ring[kDecodeStages][64 * HD];
   SplitSmem<HD, G> sm;
+  __align__(16) __nv_bfloat16 qbuf[kItemSlots][G * HD];
+  int4 item[kItemSlots];  // {unit u, kv head g, first position, end position}
   unsigned long long full[kDecodeStages];
   unsigned long long empty[kDecodeStages];
+  unsigned long long item_full[kItemSlots];
+  unsigned long long item_empty[kItemSlots];
   int abort_flag;
 };
 
@@ -599,11 +608,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
   DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>(smem_raw);
   const uint32_t full0 = smem_u32(&S.full[0]);
   const uint32_t empty0 = smem_u32(&S.empty[0]);
+  const uint32_t ifull0 = smem_u32(&S.item_full[0]);
+  const uint32_t iempty0 = smem_u32(&S.item_empty[0]);
   volatile int* abort_flag = &S.abort_flag;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDecodeStages; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(ifull0 + 8 * i, 1);                 // producer's arrive + the q bytes
+      mbar_init(iempty0 + 8 * i, kGroupThreads / 32);  // one arrive per consumer warp
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -621,7 +636,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const int plane = threadIdx.x - kGroupThreads;
     int n = 0;
     uint32_t issued = 0, ipar = 0;
+    // item k's descriptor and q go to slot k % 2; an item is announced while
+    // the item before it is still being streamed
+    int ann = 0;
+    uint32_t ann_issued = 0;
+    auto announce = [&](int it) {
+      if (plane == 0) {
+        const int slot = ann % kItemSlots;
+        const uint32_t ph = static_cast<uint32_t>((ann / kItemSlots) & 1);
+        wait_bounded(iempty0 + 8 * slot, ph ^ 1u, abort_flag, 14);
+        const int u = it / hkv;
+        const int g = it % hkv;
+        const int b = find_row(plan.prefix, B, u);
+        const int ul = plan.ulen[b];
+        const int us = (u - plan.prefix[b]) * ul;
+        S.item[slot] = make_int4(u, g, us, min(kv_lens[b], us + ul));
+        mbar_expect_tx(ifull0 + 8 * slot, static_cast<uint32_t>(G * HD * 2));  // release: the descriptor store
+        bulk_g2s(smem_u32(&S.qbuf[slot][0]), q + (static_cast<size_t>(b) * hq + g * G) * HD, G * HD * 2,
+                 ifull0 + 8 * slot);
+        ann_issued |= 1u << slot;
+      }
+      ++ann;
+    };
+    if (static_cast<int>(blockIdx.x) < total) announce(blockIdx.x);
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
+      if (item + static_cast<int>(gridDim.x) < total) announce(item + gridDim.x);
       const int u = item / hkv;
       const int g = item % hkv;
       const int b = find_row(plan.prefix, B, u);
@@ -657,9 +696,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
       }
     }
     // keep the CTA resident until every copy it issued has landed
-    if (plane == 0)
+    if (plane == 0) {
       for (int i = 0; i < kDecodeStages; ++i)
         if (issued & (1u << i)) wait_drain(full0 + 8 * i, (ipar >> i) & 1u);
+      // the q copies of the last announced items
+      for (int k = max(0, ann - kItemSlots); k < ann; ++k)
+        if (ann_issued & (1u << (k % kItemSlots)))
+          wait_drain(ifull0 + 8 * (k % kItemSlots), static_cast<uint32_t>((k / kItemSlots) & 1));
+    }
     return;
   }
 
@@ -668,17 +712,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
   const int tid = threadIdx.x;
   const int c = (tid & 31) & 7;
   int n0 = 0;
-  for (int item = blockIdx.x; item < total; item += gridDim.x) {
-    const int u = item / hkv;
-    const int g = item % hkv;
-    const int b = find_row(plan.prefix, B, u);
-    const int s = u - plan.prefix[b];
-    const int L = kv_lens[b];
-    const int ul = plan.ulen[b];
-    const int ustart = s * ul;
-    const int uend = min(L, ustart + ul);
+  int icount = 0;
+  for (int item = blockIdx.x; item < total; item += gridDim.x, ++icount) {
+    const int islot = icount % kItemSlots;
+    wait_bounded(ifull0 + 8 * islot, static_cast<uint32_t>((icount / kItemSlots) & 1), abort_flag, 15);
+    const int4 desc = S.item[islot];
+    const int u = desc.x;
+    const int g = desc.y;
+    const int ustart = desc.z;
+    const int uend = desc.w;
     QRegs<HD, G> qr;
-    load_q<HD, G>(q + (static_cast<size_t>(b) * hq + g * G) * HD, c, qr);
+    load_q<HD, G>(&S.qbuf[islot][0], c, qr);
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(iempty0 + 8 * islot);  // descriptor and q are in registers
     float rm[G], rl[G], ro[OPT];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
