@@ -420,6 +420,27 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float& o, float 
   m = mx;
 }
 
+// merge_state applied to four outputs that share (m, l): each component gets
+// exactly the operations merge_state would give it.
+__device__ __forceinline__ void merge_state4(float& m, float& l, float4& o, float mb, float lb, const float4& ob) {
+  if (mb == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = mb;
+    l = lb;
+    o = ob;
+    return;
+  }
+  const float mx = fmaxf(m, mb);
+  const float ea = exp2f(__fsub_rn(m, mx));
+  const float eb = exp2f(__fsub_rn(mb, mx));
+  l = __fadd_rn(__fmul_rn(ea, l), __fmul_rn(eb, lb));
+  o.x = __fadd_rn(__fmul_rn(ea, o.x), __fmul_rn(eb, ob.x));
+  o.y = __fadd_rn(__fmul_rn(ea, o.y), __fmul_rn(eb, ob.y));
+  o.z = __fadd_rn(__fmul_rn(ea, o.z), __fmul_rn(eb, ob.z));
+  o.w = __fadd_rn(__fmul_rn(ea, o.w), __fmul_rn(eb, ob.w));
+  m = mx;
+}
+
 struct Partials {
   float* m;  // [units][Hq]
   float* l;  // [units][Hq]
@@ -427,7 +448,7 @@ struct Partials {
 };
 
 // Merge of the split states of one row (a decode request or a prefill token)
-// for all heads of one kv group: thread (hh, d).  INVARIANT rows combine the
+// for all heads of one kv group: thread (hh, d0) owns dims d0..d0+3.  INVARIANT rows combine the
 // states in a pairwise tree over the split index (binary-counter form: the same
 // tree as the level-by-level tree over 2^BI_MERGE_DEPTH leaves padded with
 // empty states, since an empty state is an exact identity); FAST rows combine
@@ -440,44 +461,49 @@ struct Partials {
 constexpr int kMergeChunk = 16;  // split states fetched together; a chunk is one level-4 subtree
 
 __device__ __forceinline__ void merge_row(const Partials& part, size_t first_unit, int n, bool tree, int hq, int hd,
-                                          int h, int d, float& out_m, float& out_l, float& out_o) {
-  float m = -INFINITY, l = 0.f, o = 0.f;
+                                          int h, int d0, float& out_m, float& out_l, float4& out_o) {
+  float m = -INFINITY, l = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   // stack of complete subtrees over chunk results (level 4 and up of the padded tree)
-  float sm_[BI_MERGE_DEPTH - 3], sl_[BI_MERGE_DEPTH - 3], so_[BI_MERGE_DEPTH - 3];
+  float sm_[BI_MERGE_DEPTH - 3], sl_[BI_MERGE_DEPTH - 3];
+  float4 so_[BI_MERGE_DEPTH - 3];
   unsigned occ = 0;
   for (int c0 = 0; c0 < n; c0 += kMergeChunk) {
     // the chunk's states, loaded together (empty past n)
-    float cm[kMergeChunk], cl[kMergeChunk], co[kMergeChunk];
+    float cm[kMergeChunk], cl[kMergeChunk];
+    float4 co[kMergeChunk];
 #pragma unroll
     for (int j = 0; j < kMergeChunk; ++j) {
       if (c0 + j < n) {
         const size_t pi = (first_unit + c0 + j) * hq + h;
         cm[j] = __ldcg(part.m + pi);
         cl[j] = __ldcg(part.l + pi);
-        co[j] = __ldcg(part.o + pi * hd + d);
+        co[j] = __ldcg(reinterpret_cast<const float4*>(part.o + pi * hd + d0));
       } else {
         cm[j] = -INFINITY;
         cl[j] = 0.f;
-        co[j] = 0.f;
+        co[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     if (!tree) {
       // FAST: left to right
 #pragma unroll
-      for (int j = 0; j < kMergeChunk; ++j) merge_state(m, l, o, cm[j], cl[j], co[j]);
+      for (int j = 0; j < kMergeChunk; ++j) merge_state4(m, l, o, cm[j], cl[j], co[j]);
       continue;
     }
     // pairwise tree inside the chunk, level by level: (0,1), (2,3), ... then pairs of those
 #pragma unroll
     for (int w = 1; w < kMergeChunk; w *= 2)
 #pragma unroll
-      for (int i = 0; i < kMergeChunk; i += 2 * w) merge_state(cm[i], cl[i], co[i], cm[i + w], cl[i + w], co[i + w]);
+      for (int i = 0; i < kMergeChunk; i += 2 * w) merge_state4(cm[i], cl[i], co[i], cm[i + w], cl[i + w], co[i + w]);
     // push the chunk's subtree; equal-sized subtrees merge pairwise (binary counter)
-    float xm = cm[0], xl = cl[0], xo = co[0];
+    float xm = cm[0], xl = cl[0];
+    float4 xo = co[0];
     int lvl = 0;
     while (occ & (1u << lvl)) {
-      float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
-      merge_state(am, al, ao, xm, xl, xo);  // stack entry covers the lower indices
+      float am = sm_[lvl], al = sl_[lvl];
+      float4 ao = so_[lvl];
+      merge_state4(am, al, ao, xm, xl, xo);  // stack entry covers the lower indices
       xm = am; xl = al; xo = ao;
       occ &= ~(1u << lvl);
       ++lvl;
@@ -489,8 +515,9 @@ __device__ __forceinline__ void merge_row(const Partials& part, size_t first_uni
     // fold what is left, smallest (rightmost) subtree first: merge(stack[lvl], acc)
     for (int lvl = 0; lvl <= BI_MERGE_DEPTH - 4; ++lvl) {
       if (occ & (1u << lvl)) {
-        float am = sm_[lvl], al = sl_[lvl], ao = so_[lvl];
-        merge_state(am, al, ao, m, l, o);
+        float am = sm_[lvl], al = sl_[lvl];
+        float4 ao = so_[lvl];
+        merge_state4(am, al, ao, m, l, o);
         m = am; l = al; o = ao;
       }
     }
@@ -498,6 +525,15 @@ __device__ __forceinline__ void merge_row(const Partials& part, size_t first_uni
   out_m = m;
   out_l = l;
   out_o = o;
+}
+
+// out[d0..d0+3] of one (row, head): o / l rounded to bf16 (0 where l == 0)
+__device__ __forceinline__ void store_out4(uint16_t* dst, float l, const float4& o) {
+  const float r0 = (l > 0.f) ? __fdiv_rn(o.x, l) : 0.f;
+  const float r1 = (l > 0.f) ? __fdiv_rn(o.y, l) : 0.f;
+  const float r2 = (l > 0.f) ? __fdiv_rn(o.z, l) : 0.f;
+  const float r3 = (l > 0.f) ? __fdiv_rn(o.w, l) : 0.f;
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
 }
 
 // ------------------------------------------------------------------ decode
@@ -787,14 +823,15 @@ __global__ void decode_merge_kernel(const Partials part, DecodePlan plan, __nv_b
   const int b = blockIdx.x / hkv;
   const int g = blockIdx.x % hkv;
   const int G = hq / hkv;
-  const int hh = threadIdx.x / hd;
-  const int d = threadIdx.x % hd;
+  const int q4 = hd / 4;  // threads per head: four dims each
+  const int hh = threadIdx.x / q4;
+  const int d0 = 4 * (threadIdx.x % q4);
   if (b >= B || hh >= G) return;
   const int h = g * G + hh;
-  float m, l, o;
-  merge_row(part, plan.prefix[b], plan.nunits[b], plan.mode[b] == kPlanInvariant, hq, hd, h, d, m, l, o);
-  const float r = (l > 0.f) ? __fdiv_rn(o, l) : 0.f;
-  reinterpret_cast<uint16_t*>(out)[(static_cast<size_t>(b) * hq + h) * hd + d] = to_bf16_bits(r);
+  float m, l;
+  float4 o;
+  merge_row(part, plan.prefix[b], plan.nunits[b], plan.mode[b] == kPlanInvariant, hq, hd, h, d0, m, l, o);
+  store_out4(reinterpret_cast<uint16_t*>(out) + (static_cast<size_t>(b) * hq + h) * hd + d0, l, o);
 }
 
 // ------------------------------------------------------------------ prefill
@@ -1000,8 +1037,9 @@ __global__ void prefill_merge_kernel(const Partials part, PrefillPlan plan, cons
   const int tok = blockIdx.x / hkv;
   const int g = blockIdx.x % hkv;
   const int G = hq / hkv;
-  const int hh = threadIdx.x / hd;
-  const int d = threadIdx.x % hd;
+  const int q4 = hd / 4;  // threads per head: four dims each
+  const int hh = threadIdx.x / q4;
+  const int d0 = 4 * (threadIdx.x % q4);
   if (hh >= G) return;
   int lo = 0, hi = B - 1;
   while (lo < hi) {
@@ -1011,10 +1049,10 @@ __global__ void prefill_merge_kernel(const Partials part, PrefillPlan plan, cons
   const int b = lo;
   const int h = g * G + hh;
   const int n = plan.tok_prefix[tok + 1] - plan.tok_prefix[tok];
-  float m, l, o;
-  merge_row(part, plan.tok_prefix[tok], n, plan.req_mode[b] == kPlanInvariant, hq, hd, h, d, m, l, o);
-  const float r = (l > 0.f) ? __fdiv_rn(o, l) : 0.f;
-  reinterpret_cast<uint16_t*>(out)[(static_cast<size_t>(tok) * hq + h) * hd + d] = to_bf16_bits(r);
+  float m, l;
+  float4 o;
+  merge_row(part, plan.tok_prefix[tok], n, plan.req_mode[b] == kPlanInvariant, hq, hd, h, d0, m, l, o);
+  store_out4(reinterpret_cast<uint16_t*>(out) + (static_cast<size_t>(tok) * hq + h) * hd + d0, l, o);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1142,7 +1180,7 @@ bi_status decode_launch(const void* q, const void* kc, const void* vc, const int
                dm->max_pages, sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
   BI_TIMED(::bi::kTagAttnDecodeMerge, s,
-           BI_PDL_CHECK(launch_pdl(decode_merge_kernel, dim3(B * dm->num_kv_heads), dim3(G * HD), 0, s, w.part,
+           BI_PDL_CHECK(launch_pdl(decode_merge_kernel, dim3(B * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part,
                                    w.plan, static_cast<__nv_bfloat16*>(out), B, dm->num_q_heads, dm->num_kv_heads,
                                    HD)));
   BI_LAUNCH_CHECK();
@@ -1169,7 +1207,7 @@ bi_status prefill_launch(const void* q, const void* kc, const void* vc, const in
       static_cast<const __nv_bfloat16*>(vc), bt, q_pos0, q_start, dm->num_q_heads, dm->num_kv_heads, dm->max_pages,
       sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
-  BI_TIMED(::bi::kTagAttnPrefillMerge, s, BI_PDL_CHECK(launch_pdl(prefill_merge_kernel, dim3(T * dm->num_kv_heads), dim3(G * HD), 0, s, w.part, w.plan, q_start, q_pos0, B,
+  BI_TIMED(::bi::kTagAttnPrefillMerge, s, BI_PDL_CHECK(launch_pdl(prefill_merge_kernel, dim3(T * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part, w.plan, q_start, q_pos0, B,
                                                                static_cast<__nv_bfloat16*>(out), dm->num_q_heads,
                                                                dm->num_kv_heads, HD)));
   BI_LAUNCH_CHECK();

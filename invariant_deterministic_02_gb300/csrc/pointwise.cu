@@ -40,49 +40,63 @@ __global__ void rope_table_kernel(double theta, int hd, int max_pos, float* __re
   }
 }
 
-// One CTA per token.  Work items: rotated pairs of q heads, rotated pairs of k
-// heads, v elements (8 at a time).
-__global__ void qkv_rope_store_kernel(const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ rc,
-                                      const float* __restrict__ rs, const int32_t* __restrict__ token_pos,
-                                      const int32_t* __restrict__ token_req, const int32_t* __restrict__ block_table,
-                                      int max_pages, int hq, int hkv, int hd, __nv_bfloat16* __restrict__ q_out,
-                                      __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc) {
+// One warp per (token, head row): task k < hq rotates q head k, then the kv
+// heads' k rows are rotated and stored in the paged cache, then their v rows
+// are copied there.  Lane j handles the rotation pairs (i, i + hd/2) for
+// i = 2j', 2j'+1 (j' = j, j+32, ...), so loads and stores move two elements.
+__global__ void __launch_bounds__(256) qkv_rope_store_kernel(
+    const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ rc, const float* __restrict__ rs,
+    const int32_t* __restrict__ token_pos, const int32_t* __restrict__ token_req,
+    const int32_t* __restrict__ block_table, int max_pages, int hq, int hkv, int hd, __nv_bfloat16* __restrict__ q_out,
+    __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
+  const int task = blockIdx.y * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (task >= hq + 2 * hkv) return;
   const int pos = token_pos[t];
-  const int req = token_req[t];
-  const int half = hd / 2;
   const int width = (hq + 2 * hkv) * hd;
   const uint16_t* row = reinterpret_cast<const uint16_t*>(qkv) + static_cast<size_t>(t) * width;
+  if (task >= hq + hkv) {
+    // v row of kv head h: copied unchanged
+    const int h = task - hq - hkv;
+    const int req = token_req[t];
+    const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
+    const uint4* src = reinterpret_cast<const uint4*>(row + (hq + hkv + h) * hd);
+    uint4* dst = reinterpret_cast<uint4*>(vc + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE +
+                                                pos % BI_PAGE_SIZE) * hd);
+    for (int k = lane; k < hd / 8; k += 32) dst[k] = src[k];
+    return;
+  }
+  const bool is_q = task < hq;
+  const int h = is_q ? task : task - hq;
+  const int half = hd / 2;
+  const uint16_t* src = row + (is_q ? 0 : hq * hd) + h * hd;
+  uint16_t* dst;
+  if (is_q) {
+    dst = reinterpret_cast<uint16_t*>(q_out) + (static_cast<size_t>(t) * hq + h) * hd;
+  } else {
+    const int req = token_req[t];
+    const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
+    dst = reinterpret_cast<uint16_t*>(kc) + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE +
+                                             pos % BI_PAGE_SIZE) * hd;
+  }
   const float* c_row = rc + static_cast<size_t>(pos) * half;
   const float* s_row = rs + static_cast<size_t>(pos) * half;
-  const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
-  const int slot = pos % BI_PAGE_SIZE;
-  uint16_t* qo = reinterpret_cast<uint16_t*>(q_out) + static_cast<size_t>(t) * hq * hd;
-  uint16_t* ko = reinterpret_cast<uint16_t*>(kc);
-  const int nq = hq * half, nk = hkv * half;
-  for (int it = threadIdx.x; it < nq + nk; it += blockDim.x) {
-    const bool is_q = it < nq;
-    const int k = is_q ? it : it - nq;
-    const int h = k / half, i = k % half;
-    const uint16_t* src = row + (is_q ? 0 : hq * hd) + h * hd;
-    const float a = __uint_as_float(static_cast<uint32_t>(src[i]) << 16);
-    const float b = __uint_as_float(static_cast<uint32_t>(src[i + half]) << 16);
-    const float c = c_row[i], s = s_row[i];
-    const float lo = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
-    const float hi = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
-    uint16_t* dst = is_q ? qo + h * hd
-                         : ko + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE + slot) * hd;
-    dst[i] = to_bf16_bits(lo);
-    dst[i + half] = to_bf16_bits(hi);
-  }
-  const int nv = hkv * hd / 8;
-  const uint4* vsrc = reinterpret_cast<const uint4*>(row + (hq + hkv) * hd);
-  for (int it = threadIdx.x; it < nv; it += blockDim.x) {
-    const int h = (it * 8) / hd, d = (it * 8) % hd;
-    uint4* dst = reinterpret_cast<uint4*>(vc + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE + slot) * hd + d);
-    *dst = vsrc[it];
+  for (int j = lane; j < half / 2; j += 32) {
+    const int i = 2 * j;
+    const uint32_t av = *reinterpret_cast<const uint32_t*>(src + i);
+    const uint32_t bv = *reinterpret_cast<const uint32_t*>(src + i + half);
+    const float2 c = *reinterpret_cast<const float2*>(c_row + i);
+    const float2 sn = *reinterpret_cast<const float2*>(s_row + i);
+    const float a0 = bf16_lo(av), a1 = bf16_hi(av), b0 = bf16_lo(bv), b1 = bf16_hi(bv);
+    const float lo0 = __fsub_rn(__fmul_rn(a0, c.x), __fmul_rn(b0, sn.x));
+    const float lo1 = __fsub_rn(__fmul_rn(a1, c.y), __fmul_rn(b1, sn.y));
+    const float hi0 = __fadd_rn(__fmul_rn(b0, c.x), __fmul_rn(a0, sn.x));
+    const float hi1 = __fadd_rn(__fmul_rn(b1, c.y), __fmul_rn(a1, sn.y));
+    *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(lo0, lo1);
+    *reinterpret_cast<uint32_t*>(dst + i + half) = pack_bf16x2(hi0, hi1);
   }
 }
 
@@ -136,7 +150,7 @@ bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs,
              "bi_qkv_rope_store: null pointer");
   BI_REQUIRE(aligned16(qkv) && aligned16(q_out) && aligned16(kc) && aligned16(vc), BI_ERR_INVALID_ARG,
              "bi_qkv_rope_store: misaligned pointer");
-  BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel, dim3(T), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
+  BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel, dim3(T, (dm->num_q_heads + 2 * dm->num_kv_heads + 7) / 8), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
                                           block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
                                           static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(kc),
                                           static_cast<__nv_bfloat16*>(vc))));
