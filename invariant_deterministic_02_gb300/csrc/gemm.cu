@@ -53,7 +53,6 @@ constexpr int kProducerWarps = 1;
 constexpr int kMmaWarp = kProducerWarps;
 constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KiB
-constexpr int kBSubBytes = kBN * kBK * 2;   // 8 KiB per 64-column instruction tile
 constexpr int kSmemLimit = 227 * 1024;     // dynamic shared memory per CTA
 constexpr int kMaxStages = 16;
 constexpr int kOverreadSlack = kATileBytes;  // see the A-tile note below
@@ -68,9 +67,9 @@ struct Args {
   int a_rows;       // rows of A per TMA box (16, 32, 64 or 128)
   int kbs;          // k-blocks per stage (one TMA box spans them when map3d)
   int map3d;        // tensor maps are [kblock][rows][64] views (K % 64 == 0)
-  int stage_bytes;  // kbs x (A box + W instruction columns of B)
+  int stage_bytes;  // kbs x (A box + TN rows of B)
   int stages;
-  int m_tiles, n_tiles;  // n_tiles counts CTA-wide column tiles (64*W wide)
+  int m_tiles, n_tiles;  // n_tiles counts CTA-wide column tiles (TN wide)
   int splits;            // K splits of the other tiles, one CTA unit each (partials summed by a second pass)
   int tm0, tm1;          // m-tiles [tm0, tm1) are computed whole by one unit each
   int seq;               // ... as `seq` K-split partials merged inside the CTA (1: one pass over K)
@@ -263,7 +262,7 @@ __host__ __device__ __forceinline__ void k_range(int kb_total, int s, int nsplit
 }
 
 // Shared memory: [barrier block 1 KiB][stage 0]..[stage n-1][slack].  A stage
-// holds an A box of a_rows rows then the B box (W 64-row instruction tiles).
+// holds kbs A boxes of a_rows rows then kbs B boxes of TN rows (one per k-block).
 //
 // A-tile note: the instruction always reads 128 rows of A (16 KiB) from the
 // stage start.  When M <= 64 only the first a_rows rows are loaded; the
@@ -280,19 +279,19 @@ __host__ __device__ constexpr size_t smem_bytes(int stages, int stage_bytes, int
          (a_rows < kBM ? kOverreadSlack : 0);
 }
 
-template <int W>
+template <int TN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                               const __grid_constant__ CUtensorMap tmW, const Args a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // two accumulators of W*64 columns, plus the running sum of merged units when
-  // it fits (W <= 2); allocations are powers of two
-  constexpr int kTmemCols = W == 1 ? 256 : 512;
+  // two accumulators of TN columns, plus the running sum of merged units when
+  // it fits (TN <= 128); allocations are powers of two
+  constexpr int kTmemCols = TN == 32 ? 128 : TN == 64 ? 256 : 512;
   const int kStages = a.stages;
   const int kStageBytes = a.stage_bytes;
   const int kbs = a.kbs;
   const int a_tile = a.a_rows * kBK * 2;      // one k-block of A
-  const int b_tile = W * kBSubBytes;          // one k-block of B
+  const int b_tile = TN * kBK * 2;            // one k-block of B
   const int a_bytes = kbs * a_tile;           // A part of a stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   unsigned char* tiles = smem + kBarBlock;
@@ -347,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       const uint32_t fb = full0 + 8 * pre_stages;
       const uint32_t sa = smem_u32(tiles + pre_stages * kStageBytes);
       mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
-      if (a.map3d) tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
-      else tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+      if (a.map3d) tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
+      else tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
     }
   }
   pdl_wait();
@@ -385,10 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
               mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
               if (a.map3d) {
                 tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
-                tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * (W * kBN), kb);
+                tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
               } else {
                 tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
-                tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * (W * kBN));
+                tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
               }
             }
             issued_mask |= 1u << st;
@@ -413,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // accumulators and is handed to the epilogue on its own.
     if (lane == 0) {
       const uint64_t desc0 = sw128_desc(smem_u32(tiles));
-      constexpr uint32_t kIdescW = idesc_for(W * kBN);
+      constexpr uint32_t kIdescW = idesc_for(TN);
       int st = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -432,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             break;
           }
           tc_fence_after();
-          const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * W * kBN);
+          const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * TN);
           for (int kb = kb0; kb < kb1; kb += kbs) {
             if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3)) {
               ok = false;
@@ -449,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
               for (int k = 0; k < kBK / kUK; ++k) {
                 // the first instruction of a pass overwrites the accumulator, all others add;
-                // one instruction spans the tile's W*64 columns: the B rows of a stage are
+                // one instruction spans the tile's TN columns: the B rows of a stage are
                 // contiguous 128-byte swizzle rows, 1024 bytes per 8-row group
                 const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
                 tc_mma(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdescW,
@@ -487,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t sum_base = lane_base + 2 * W * kBN;  // running-sum buffer (merged units only)
+    const uint32_t sum_base = lane_base + 2 * TN;  // running-sum buffer (merged units only)
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
@@ -502,14 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           break;
         }
         tc_fence_after();
-        const uint32_t tbase = lane_base + acc * W * kBN;
+        const uint32_t tbase = lane_base + acc * TN;
         const bool last = q == seq - 1;
 #pragma unroll 1
-        for (int ch = 0; ch < 2 * W; ++ch) {
+        for (int ch = 0; ch < TN / 32; ++ch) {
           uint32_t r[32];
           tc_ld32(tbase + ch * 32, r);
           if (seq > 1) {
-            if constexpr (W <= 2) {
+            if constexpr (TN <= 128) {
               uint32_t t[32];
               if (q > 0) tc_ld32(sum_base + ch * 32, t);
 #pragma unroll
@@ -521,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
               }
             }
           }
-          const int col0 = nt * W * kBN + ch * 32;
+          const int col0 = nt * TN + ch * 32;
           if (!row_ok || col0 >= a.N) continue;
           if (ns > 1) {
             float* dst = a.partial + (static_cast<size_t>(s) * a.M + row) * a.N + col0;
@@ -723,7 +722,7 @@ int plan_sms() {
 }
 
 struct Plan {
-  int W;
+  int TN;  // CTA tile width in columns: 32, 64, 128, 192 or 256
   int a_rows, kbs, map3d, stage_bytes, stages;
   int splits;
   int tm0, tm1, seq;
@@ -745,44 +744,44 @@ int ksplit_count(int64_t N, int64_t K) {
   return static_cast<int>(ks);
 }
 
-int choose_width(int64_t M, int64_t N, int max_w) {
+int choose_width(int64_t M, int64_t N, int max_tn) {
   const int sms = plan_sms();
   const int64_t mt = (M + kBM - 1) / kBM;
   double best = -1.0;
-  int bw = 1;
-  const int widths[3] = {4, 2, 1};
-  const double penalty[3] = {1.0, 0.92, 0.80};  // operand bytes per flop grow as W shrinks
+  int btn = 64;
+  const int widths[3] = {256, 128, 64};
+  const double penalty[3] = {1.0, 0.92, 0.80};  // operand bytes per flop grow as the tile narrows
   for (int i = 0; i < 3; ++i) {
-    const int w = widths[i];
-    if (w > max_w) continue;
-    const int64_t tiles = mt * ((N + w * kBN - 1) / (w * kBN));
+    const int tn = widths[i];
+    if (tn > max_tn) continue;
+    const int64_t tiles = mt * ((N + tn - 1) / tn);
     const int64_t waves = (tiles + sms - 1) / sms;
     const double eff = static_cast<double>(tiles) / static_cast<double>(waves * sms) * penalty[i];
     if (eff > best + 1e-9) {
       best = eff;
-      bw = w;
+      btn = tn;
     }
   }
-  return bw;
+  return btn;
 }
 
 // Decode-sized M (one 128-row tile): the GEMM streams the weights and every
 // CTA also reads the whole A block of its K range, so take the width that
-// minimises (waves of units) x (bytes a CTA reads per unit ~ W*64 + a_rows).
+// minimises (waves of units) x (bytes a CTA reads per unit ~ TN + a_rows).
 int choose_width_small_m(int64_t N, int splits, int a_rows) {
   const int sms = plan_sms();
-  int bw = 1;
+  int btn = 64;
   int64_t best = INT64_MAX;
-  for (int w = 4; w >= 1; --w) {
-    const int64_t units = ((N + w * kBN - 1) / (w * kBN)) * splits;
+  for (int tn : {256, 192, 128, 64, 32}) {
+    const int64_t units = ((N + tn - 1) / tn) * splits;
     const int64_t waves = (units + sms - 1) / sms;
-    const int64_t cost = waves * (w * kBN + a_rows);
+    const int64_t cost = waves * (tn + a_rows);
     if (cost < best) {
       best = cost;
-      bw = w;
+      btn = tn;
     }
   }
-  return bw;
+  return btn;
 }
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te) {
@@ -795,7 +794,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   p.seq = 1;
   // A protected target in the only m-tile makes the whole launch INVARIANT.
   if (mode == BI_MODE_PROTECTED && te > tb && p.m_tiles == 1) mode = BI_MODE_INVARIANT;
-  int max_w = 4;
+  int max_tn = 256;
   if (mode == BI_MODE_INVARIANT_KSPLIT) {
     const int ks = ksplit_count(N, K);
     if (p.m_tiles == 1) {
@@ -804,13 +803,26 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
       p.tm0 = 0;      // every tile merged in its CTA
       p.tm1 = p.m_tiles;
       p.seq = ks;
-      max_w = 2;      // the running sum needs a third accumulator-sized buffer
+      max_tn = 128;   // the running sum needs a third accumulator-sized buffer
     }
-  } else if (mode != BI_MODE_INVARIANT) {
+  }
+  int fast_tn = 0;
+  if (mode == BI_MODE_FAST || mode == BI_MODE_PROTECTED) {
     // FAST: split K when there are fewer tiles than SMs (the split count
-    // follows M); PROTECTED: the target's tiles are not split.
-    const int w0 = M <= kBM ? choose_width_small_m(N, 1, p.a_rows) : choose_width(M, N, 4);
-    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * ((N + w0 * kBN - 1) / (w0 * kBN));
+    // follows M); PROTECTED: the target's tiles are not split.  Its tile is
+    // the widest of 256/128/64 columns that still gives every SM a tile (else
+    // 64), as a conventional GEMM picks it.
+    fast_tn = 64;
+    if (M <= kBM) {
+      for (int tn : {256, 128, 64})
+        if ((N + tn - 1) / tn >= plan_sms()) {
+          fast_tn = tn;
+          break;
+        }
+    } else {
+      fast_tn = choose_width(M, N, 256);
+    }
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * ((N + fast_tn - 1) / fast_tn);
     const int sms = plan_sms();
     int sk = static_cast<int>(std::min<int64_t>(kMaxSplitK, std::max<int64_t>(1, sms / std::max<int64_t>(1, tiles))));
     p.splits = std::max(1, std::min(sk, p.kb_total));
@@ -819,32 +831,34 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
       p.tm1 = static_cast<int>((te - 1) / kBM) + 1;
     }
   }
-  p.W = M <= kBM ? choose_width_small_m(N, p.splits, p.a_rows) : choose_width(M, N, max_w);
+  if (fast_tn) p.TN = fast_tn;
+  else p.TN = M <= kBM ? choose_width_small_m(N, p.splits, p.a_rows) : choose_width(M, N, max_tn);
   // Each copy costs the copy engine a roughly fixed time, so at decode sizes a
-  // stage spans several k-blocks (one 3D box of >= 32 KiB of weights per copy).
-  // (A 3D copy costs more than a 2D box of the same bytes, so the 3D view is
-  // used only when a copy spans several k-blocks.)
-  p.kbs = (K % kBK == 0 && M <= kBM) ? std::max(1, 4 / p.W) : 1;
+  // stage spans several k-blocks (one 3D box of 16-32 KiB of weights per copy,
+  // at most 4 k-blocks so that several stages fit).  (A 3D copy costs more
+  // than a 2D box of the same bytes, so the 3D view is used only when a copy
+  // spans several k-blocks.)
+  p.kbs = (K % kBK == 0 && M <= kBM) ? std::min(4, std::max(1, 256 / p.TN)) : 1;
   p.map3d = p.kbs > 1 ? 1 : 0;
-  p.stage_bytes = p.kbs * (p.a_rows * kBK * 2 + p.W * kBSubBytes);
+  p.stage_bytes = p.kbs * (p.a_rows + p.TN) * kBK * 2;
   const int budget = kSmemLimit - 1024 - kBarBlock - (p.a_rows < kBM ? kOverreadSlack : 0);
   p.stages = std::min(kMaxStages, budget / p.stage_bytes);
-  p.n_tiles = static_cast<int>((N + p.W * kBN - 1) / (p.W * kBN));
+  p.n_tiles = static_cast<int>((N + p.TN - 1) / p.TN);
   const int prot = p.tm1 - p.tm0;
   p.units = p.n_tiles * (prot + (p.m_tiles - prot) * p.splits);
   return p;
 }
 
-template <int W>
+template <int TN>
 bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
+    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
     attr = true;
   }
   const size_t smem = smem_bytes(args.stages, args.stage_bytes, args.a_rows);
   const int grid = std::min(args.units, num_sms());
-  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<W>, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
+  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<TN>, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -902,8 +916,8 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   BI_REQUIRE(aligned16(A) && aligned16(Wt) && aligned16(C) && (R == nullptr || aligned16(R)), BI_ERR_INVALID_ARG,
              "bi_gemm: pointers must be 16-byte aligned");
   gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te);
-  BI_REQUIRE(p.seq == 1 || p.W <= 2, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (merged units at width %d)",
-             p.W);
+  BI_REQUIRE(p.seq == 1 || p.TN <= 128, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (merged units at width %d)",
+             p.TN);
   gemm::Args args{};
   args.M = static_cast<int>(M);
   args.a_rows = p.a_rows;
@@ -934,12 +948,13 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   }
   CUtensorMap ma, mw;
   BI_TRY(gemm::tensor_map(A, M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
-  BI_TRY(gemm::tensor_map(Wt, N, K, p.W * gemm::kBN, p.map3d ? p.kbs : 0, &mw));
+  BI_TRY(gemm::tensor_map(Wt, N, K, p.TN, p.map3d ? p.kbs : 0, &mw));
   bi_status st;
-  if (p.W == 4) st = gemm::launch_w<4>(ma, mw, args, s);
-  else if (p.W == 3) st = gemm::launch_w<3>(ma, mw, args, s);
-  else if (p.W == 2) st = gemm::launch_w<2>(ma, mw, args, s);
-  else st = gemm::launch_w<1>(ma, mw, args, s);
+  if (p.TN == 256) st = gemm::launch_w<256>(ma, mw, args, s);
+  else if (p.TN == 192) st = gemm::launch_w<192>(ma, mw, args, s);
+  else if (p.TN == 128) st = gemm::launch_w<128>(ma, mw, args, s);
+  else if (p.TN == 64) st = gemm::launch_w<64>(ma, mw, args, s);
+  else st = gemm::launch_w<32>(ma, mw, args, s);
   if (st != BI_OK) return st;
   if (p.splits > 1) {
     const int64_t n = M * (N / 4);
