@@ -8,32 +8,35 @@
 // Kernel" notes, section GEMM: the K split may depend on K only.)
 //
 // Reduction geometry, identical for every M, N and CTA shape:
-//   * one tensor-core instruction shape: tcgen05.mma.cta_group::1.kind::f16,
-//     M=128, N=64, K=16, bf16 operands from shared memory (128-byte swizzled,
-//     K-major), fp32 accumulator in tensor memory;
+//   * tcgen05.mma.kind::f16 with K=16, bf16 operands from shared memory
+//     (128-byte swizzled, K-major), fp32 accumulator in tensor memory;
 //   * the K range is consumed in 64-wide k-tiles in ascending order, four
 //     instructions of K=16 per k-tile in ascending order; the first
 //     instruction of an output tile overwrites the accumulator, all others add.
 // An output element therefore sees the same instruction sequence with the
-// same operands whatever M is, whichever CTA computes it and however many
-// 64-column instruction tiles a CTA covers.  The CTA column extent (64, 128 or
-// 256 columns = 1, 2 or 4 instructions per k-step) and the persistent
-// tile-to-CTA mapping are scheduling choices that never touch an element's
-// arithmetic.
+// same operands whatever M is and whichever CTA computes it.  The instruction's
+// M and N extents (M=128 on one SM, M=256 on an SM pair; N = the tile width,
+// 32-256 columns) and the persistent tile-to-CTA mapping are scheduling choices
+// that never touch an element's arithmetic; the row-0 M sweeps check this
+// bitwise across all of them.
+//
+// Two kernels:
+//   * gemm_tc_kernel<TN> (M <= 128, and every FAST / PROTECTED / KSPLIT launch):
+//     one CTA per 128 x TN tile.  Roles in a CTA of 192 threads: warp 0 issues
+//     TMA loads, warp 1 owns the tensor memory and issues the MMAs (one
+//     thread), warps 2-5 drain the accumulator (tcgen05.ld) and store.
+//   * gemm_tc2_kernel (INVARIANT, M > 128): a 2-CTA cluster per 256 x 256 tile
+//     with tcgen05.mma.cta_group::2 (see the comment above the kernel).
+// Shared-memory stages and two tensor-memory accumulators are handed between
+// roles with mbarriers.  Every wait is bounded: when one runs out the kernel
+// records a site code in a device error word, stops all roles, waits (bounded)
+// for its own copies and MMAs, frees its tensor memory and returns.
 //
 // FAST mode (the non-invariant schedule used to measure the cost of
 // invariance): when there are fewer tiles than SMs the K range is split over
 // several CTAs and the fp32 partials are added in a second pass, so an
 // element's rounding depends on M.  PROTECTED: tiles holding target rows are
-// never split.
-//
-// Roles in a CTA of 192 threads: warp 0 issues TMA loads, warp 1 owns the tensor
-// memory and issues the MMAs (one thread), warps 2-5 drain the accumulator
-// (tcgen05.ld) and store.  Shared-memory stages and two tensor-memory
-// accumulators are handed between roles with mbarriers.  Every wait is bounded:
-// when one runs out the kernel records a site code in a device error word,
-// stops all roles, waits (bounded) for its own copies and MMAs, frees its
-// tensor memory and returns.
+// never split.  INVARIANT_KSPLIT: a K split fixed by the weight shape (N, K).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
