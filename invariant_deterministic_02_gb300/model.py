@@ -181,6 +181,23 @@ class BiModel:
                 cache[idx] = vals.to(torch.bfloat16)
         self.lengths[req] = length
 
+    def copy_prefix(self, src: int, dst: int, tokens: int):
+        """Prefix-cache hit: give request `dst` (which must hold no tokens yet) the
+        first `tokens` cached positions of request `src`, by copying the K/V pages
+        that hold them (every layer).  Later tokens of `dst` continue at position
+        `tokens`; any part of a partly copied last page is overwritten then."""
+        if self.lengths.get(dst, 0) or self.pool.owned.get(dst):
+            raise ValueError("copy_prefix: destination request already holds tokens")
+        if tokens <= 0 or tokens > self.lengths.get(src, 0):
+            raise ValueError("copy_prefix: %d tokens of a %d-token request" % (tokens, self.lengths.get(src, 0)))
+        n = (tokens + PAGE_SIZE - 1) // PAGE_SIZE
+        s_idx = torch.tensor(self.pool.owned[src][:n], dtype=torch.int64, device=self.device)
+        d_idx = torch.tensor(self.pool.ensure(dst, tokens), dtype=torch.int64, device=self.device)
+        for caches in (self.k_caches, self.v_caches):
+            for c in caches:
+                c.index_copy_(0, d_idx, c.index_select(0, s_idx))
+        self.lengths[dst] = tokens
+
     def reset(self):
         for r in list(self.lengths.keys()) + list(self.pool.owned.keys()):
             self.release(r)

@@ -120,6 +120,49 @@ def test_tiny_model_greedy_bit_exact_across_compositions():
     assert_same(refk, got, "ksplit")
 
 
+def test_prefix_kv_reuse_across_batches_bitwise():
+    """A prompt's K/V computed inside one batch, reused by a new request in another
+    batch composition (a prefix-cache hit), continues with exactly the bits of a
+    request that computed everything alone."""
+    shape = tiny_shape()
+    m = BiModel.random(shape, seed=21, num_pages=4096, page_seed=9)
+    V = shape.vocab
+    prompt = synth.token_ids(64, V, 77)
+    suffix = synth.token_ids(20, V, 78)
+
+    def continue_decode(req, first_items, steps=12):
+        """Run `first_items` (req's suffix prefill, maybe with neighbours), then greedy
+        decode req for `steps` tokens, batched with the decoding neighbour "nb" if it exists."""
+        res = m.forward_batch(first_items)
+        slot = [r for r, _ in first_items].index(req)
+        toks, tops = [int(res.top_i[slot, 0])], [res.top_v[slot].cpu().numpy().view(np.uint32).copy()]
+        for _ in range(steps):
+            items = [(req, np.array([toks[-1]], dtype=np.int32))]
+            if "nb" in m.lengths:
+                items.append(("nb", np.array([7], dtype=np.int32)))
+            res = m.forward_batch(items)
+            toks.append(int(res.top_i[0, 0]))
+            tops.append(res.top_v[0].cpu().numpy().view(np.uint32).copy())
+        return toks, tops
+
+    # reference: prompt and suffix prefilled by the request alone, then decode alone
+    m.forward_batch([("ref", prompt)])
+    ref = continue_decode("ref", [("ref", suffix)])
+    m.reset()
+    # the prompt is prefilled by request "src" inside a batch of three
+    m.forward_batch([("a", synth.token_ids(300, V, 80)), ("src", prompt), ("b", synth.token_ids(17, V, 81))])
+    m.release("a")
+    m.release("b")
+    # a new request reuses the prompt's 64 cached positions (4 pages) and prefills only the suffix,
+    # in a batch with a decoding neighbour that has a long history
+    m.install_history("nb", 1500, 82)
+    m.copy_prefix("src", "dst", 64)
+    got = continue_decode("dst", [("nb", np.array([5], dtype=np.int32)), ("dst", suffix)])
+    assert got[0] == ref[0]
+    for a, b in zip(got[1], ref[1]):
+        assert np.array_equal(a, b)
+
+
 @pytest.mark.slow
 def test_qwen3_8b_greedy_200_tokens_bit_exact_across_compositions():
     """Full Qwen3-8B-shaped random-init model: a 512-token seeded prompt, greedy 200 tokens."""
