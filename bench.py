@@ -35,7 +35,7 @@ METRIC = "invariant decode tok/s (8B-shape, B=1..64); GEMM TFLOP/s & attn GB/s v
 BATCH = 64
 KV_LO, KV_HI = 128, 4096
 TOPK = 20
-WORKLOAD = ("Qwen3-8B-shaped decode step (36 layers, d4096, 32/8 heads, hd128, FFN 12288, vocab 151936), "
+WORKLOAD = ("Qwen3-8B-shaped decode step (36 layers, d4096, 32/8 heads, hd128, q/k head RMSNorm, FFN 12288, vocab 151936), "
             "B=64 requests, cached KV lengths U{128..4096}, greedy top-20")
 
 

@@ -267,6 +267,12 @@ typedef struct bi_layer_weights {
   const void* ffn_norm;  /* [d] bf16 */
   const void* w_gate_up; /* [2F][d] bf16: gate rows 0..F-1, up rows F..2F-1 */
   const void* w_down;    /* [d][F] bf16 */
+  /* Optional per-head RMSNorm of q and k before RoPE (Qwen3; NULL = none):
+   * [head_dim] bf16 weights; each head row x of head_dim values becomes
+   * bf16((x / sqrt(sum(x^2)/head_dim + rms_eps)) * g) in fp32, the sum of squares
+   * taken in one fixed order that depends on head_dim only.  Both or neither. */
+  const void* q_norm;
+  const void* k_norm;
 } bi_layer_weights;
 
 typedef struct bi_model_dims {

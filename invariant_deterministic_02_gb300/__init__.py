@@ -67,7 +67,8 @@ class AttnDims(ctypes.Structure):
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [("attn_norm", ctypes.c_void_p), ("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p),
-                ("ffn_norm", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+                ("ffn_norm", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p)]
 
 
 class ModelDims(ctypes.Structure):

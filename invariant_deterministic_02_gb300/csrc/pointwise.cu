@@ -40,15 +40,22 @@ __global__ void rope_table_kernel(double theta, int hd, int max_pos, float* __re
   }
 }
 
+__device__ __forceinline__ float round_bf16f(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
 // One warp per (token, head row): task k < hq rotates q head k, then the kv
 // heads' k rows are rotated and stored in the paged cache, then their v rows
 // are copied there.  Lane j handles the rotation pairs (i, i + hd/2) for
 // i = 2j', 2j'+1 (j' = j, j+32, ...), so loads and stores move two elements.
+// With qn / kn (Qwen3's per-head norms) a q or k row is first RMS-normalised
+// over its hd values: lane sums of squares in the order (i, i+1, i+hd/2,
+// i+hd/2+1) per pair, a xor butterfly over the warp (every lane gets the same
+// bits), r = 1/sqrt(sum/hd + eps), x -> bf16((x*r)*g), then rotated.
 __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
     const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ rc, const float* __restrict__ rs,
     const int32_t* __restrict__ token_pos, const int32_t* __restrict__ token_req,
     const int32_t* __restrict__ block_table, int max_pages, int hq, int hkv, int hd, __nv_bfloat16* __restrict__ q_out,
-    __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc) {
+    __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc, const __nv_bfloat16* __restrict__ qn,
+    const __nv_bfloat16* __restrict__ kn, float eps) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
@@ -84,13 +91,37 @@ __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
   }
   const float* c_row = rc + static_cast<size_t>(pos) * half;
   const float* s_row = rs + static_cast<size_t>(pos) * half;
+  const __nv_bfloat16* g = is_q ? qn : kn;
+  float r = 0.f;
+  if (g != nullptr) {
+    float ss = 0.f;
+    for (int j = lane; j < half / 2; j += 32) {
+      const int i = 2 * j;
+      const uint32_t av = *reinterpret_cast<const uint32_t*>(src + i);
+      const uint32_t bv = *reinterpret_cast<const uint32_t*>(src + i + half);
+      const float x[4] = {bf16_lo(av), bf16_hi(av), bf16_lo(bv), bf16_hi(bv)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss = __fadd_rn(ss, __fmul_rn(x[e], x[e]));
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+    r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(hd)), eps)));
+  }
   for (int j = lane; j < half / 2; j += 32) {
     const int i = 2 * j;
     const uint32_t av = *reinterpret_cast<const uint32_t*>(src + i);
     const uint32_t bv = *reinterpret_cast<const uint32_t*>(src + i + half);
     const float2 c = *reinterpret_cast<const float2*>(c_row + i);
     const float2 sn = *reinterpret_cast<const float2*>(s_row + i);
-    const float a0 = bf16_lo(av), a1 = bf16_hi(av), b0 = bf16_lo(bv), b1 = bf16_hi(bv);
+    float a0 = bf16_lo(av), a1 = bf16_hi(av), b0 = bf16_lo(bv), b1 = bf16_hi(bv);
+    if (g != nullptr) {
+      const uint32_t ga = *reinterpret_cast<const uint32_t*>(g + i);
+      const uint32_t gb = *reinterpret_cast<const uint32_t*>(g + i + half);
+      a0 = round_bf16f(__fmul_rn(__fmul_rn(a0, r), bf16_lo(ga)));
+      a1 = round_bf16f(__fmul_rn(__fmul_rn(a1, r), bf16_hi(ga)));
+      b0 = round_bf16f(__fmul_rn(__fmul_rn(b0, r), bf16_lo(gb)));
+      b1 = round_bf16f(__fmul_rn(__fmul_rn(b1, r), bf16_hi(gb)));
+    }
     const float lo0 = __fsub_rn(__fmul_rn(a0, c.x), __fmul_rn(b0, sn.x));
     const float lo1 = __fsub_rn(__fmul_rn(a1, c.y), __fmul_rn(b1, sn.y));
     const float hi0 = __fadd_rn(__fmul_rn(b0, c.x), __fmul_rn(a0, sn.x));
@@ -140,7 +171,8 @@ bi_status embed_impl(const int32_t* ids, const void* table, void* out, int64_t T
 
 bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs, const int32_t* token_pos,
                               const int32_t* token_req, const int32_t* block_table, int32_t T,
-                              const bi_attn_dims* dm, void* q_out, void* kc, void* vc, cudaStream_t s) {
+                              const bi_attn_dims* dm, void* q_out, void* kc, void* vc, cudaStream_t s,
+                              const void* q_norm, const void* k_norm, float eps) {
   BI_REQUIRE(dm && T >= 0, BI_ERR_INVALID_ARG, "bi_qkv_rope_store: dims/T");
   BI_REQUIRE(dm->head_dim % 16 == 0 && dm->head_dim >= 16 && dm->num_kv_heads >= 1 && dm->num_q_heads >= 1,
              BI_ERR_UNSUPPORTED, "bi_qkv_rope_store: head_dim %d", dm->head_dim);
@@ -150,10 +182,13 @@ bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs,
              "bi_qkv_rope_store: null pointer");
   BI_REQUIRE(aligned16(qkv) && aligned16(q_out) && aligned16(kc) && aligned16(vc), BI_ERR_INVALID_ARG,
              "bi_qkv_rope_store: misaligned pointer");
+  BI_REQUIRE((q_norm == nullptr) == (k_norm == nullptr) && (q_norm == nullptr || (aligned16(q_norm) && aligned16(k_norm))),
+             BI_ERR_INVALID_ARG, "layer: q_norm and k_norm must be both null or both 16-byte aligned");
   BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel, dim3(T, (dm->num_q_heads + 2 * dm->num_kv_heads + 7) / 8), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
                                           block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
                                           static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(kc),
-                                          static_cast<__nv_bfloat16*>(vc))));
+                                          static_cast<__nv_bfloat16*>(vc), static_cast<const __nv_bfloat16*>(q_norm),
+                                          static_cast<const __nv_bfloat16*>(k_norm), eps)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -203,7 +238,7 @@ extern "C" bi_status bi_qkv_rope_store(const void* qkv, const float* rope_cos, c
                                        bi_stream s) {
   bi::clear_error();
   return bi::qkv_rope_store_impl(qkv, rope_cos, rope_sin, token_pos, token_req, block_table, T, dims, q_out, k_cache,
-                                 v_cache, reinterpret_cast<cudaStream_t>(s));
+                                 v_cache, reinterpret_cast<cudaStream_t>(s), nullptr, nullptr, 0.f);
 }
 
 extern "C" bi_status bi_swiglu(const void* gu, void* out, int64_t T, int64_t F, bi_stream s) {

@@ -79,7 +79,9 @@ class BiModel:
         self.v_ptrs = (ctypes.c_void_p * max(1, shape.n_layers))(*[v.data_ptr() for v in self.v_caches])
         self._layer_structs = (LayerWeights * max(1, shape.n_layers))(*[
             LayerWeights(lw["attn_norm"].data_ptr(), lw["w_qkv"].data_ptr(), lw["w_o"].data_ptr(),
-                         lw["ffn_norm"].data_ptr(), lw["w_gate_up"].data_ptr(), lw["w_down"].data_ptr())
+                         lw["ffn_norm"].data_ptr(), lw["w_gate_up"].data_ptr(), lw["w_down"].data_ptr(),
+                         lw["q_norm"].data_ptr() if "q_norm" in lw else None,
+                         lw["k_norm"].data_ptr() if "k_norm" in lw else None)
             for lw in weights["layers"]])
         self.mw = ModelWeights(weights["embed"].data_ptr(), self._layer_structs, shape.n_layers,
                                weights["final_norm"].data_ptr(), weights["lm_head"].data_ptr())
@@ -112,6 +114,9 @@ class BiModel:
                     "w_gate_up": synth.normal_device((2 * L.ffn_dim, L.d_model), s + 5, std=std, device=device),
                     "w_down": synth.normal_device((L.d_model, L.ffn_dim), s + 6, std=std, device=device),
                 })
+                if L.qk_norm:
+                    layers[-1]["q_norm"] = synth.normal_device((L.head_dim,), s + 7, std=0.1, mean=1.0, device=device)
+                    layers[-1]["k_norm"] = synth.normal_device((L.head_dim,), s + 8, std=0.1, mean=1.0, device=device)
             embed = synth.normal_device((shape.vocab, L.d_model), seed + 1, std=std, device=device)
             head = synth.normal_device((shape.vocab, L.d_model), seed + 2, std=std, device=device)
         return {"embed": embed, "layers": layers, "final_norm": torch.ones(L.d_model, dtype=torch.bfloat16,

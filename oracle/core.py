@@ -253,6 +253,8 @@ def layer_forward(h, w, shape, kv: OracleKV, layer: int, requests, pos0) -> np.n
     to the cache before attention, so cached and new tokens are one sequence).
 
       x1 = bf16(rms(h, g1));      qkv = bf16(x1 Wqkv^T)
+      [Qwen3 only, w has q_norm/k_norm: q, k = bf16(rms_head(q, gq)), bf16(rms_head(k, gk)),
+       the RMSNorm of every head row of head_dim values]
       q, k = bf16(rope(q)), bf16(rope(k));  append k, v to the cache
       att = bf16(attention(q, K, V));       h1 = bf16(h + att Wo^T)
       x2 = bf16(rms(h1, g2));     gu = bf16(x2 Wgu^T)
@@ -267,6 +269,9 @@ def layer_forward(h, w, shape, kv: OracleKV, layer: int, requests, pos0) -> np.n
     q = qkv[:, :Hq * hd].reshape(T, Hq, hd)
     k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(T, Hkv, hd)
     v = qkv[:, (Hq + Hkv) * hd:].reshape(T, Hkv, hd)
+    if "q_norm" in w:
+        q = round_bf16(rmsnorm(q, w["q_norm"], shape.rms_eps))  # per head row (last axis = head_dim)
+        k = round_bf16(rmsnorm(k, w["k_norm"], shape.rms_eps))
     att = np.zeros((T, Hq, hd), dtype=F64)
     t0 = 0
     scale = 1.0 / math.sqrt(hd)

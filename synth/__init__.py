@@ -116,6 +116,7 @@ class LayerShape:
     rms_eps: float = 1e-5
     rope_theta: float = 500000.0
     page_size: int = 16
+    qk_norm: bool = False  # per-head RMSNorm of q and k before RoPE (Qwen3)
 
     @property
     def qkv_dim(self) -> int:
@@ -123,8 +124,9 @@ class LayerShape:
 
 
 LLAMA31_8B_LAYER = LayerShape(4096, 32, 8, 128, 14336, 1e-5, 500000.0)
-QWEN3_8B_LAYER = LayerShape(4096, 32, 8, 128, 12288, 1e-6, 1000000.0)
+QWEN3_8B_LAYER = LayerShape(4096, 32, 8, 128, 12288, 1e-6, 1000000.0, qk_norm=True)
 TINY_LAYER = LayerShape(256, 4, 2, 64, 512, 1e-5, 10000.0)
+TINY_QK_LAYER = LayerShape(256, 4, 2, 64, 512, 1e-5, 10000.0, qk_norm=True)
 
 
 def layer_weights(shape: LayerShape, seed: int, std: float = 0.02, gamma_std: float = 0.0):
@@ -136,12 +138,12 @@ def layer_weights(shape: LayerShape, seed: int, std: float = 0.02, gamma_std: fl
     d, F, hd = shape.d_model, shape.ffn_dim, shape.head_dim
     qo = shape.n_q_heads * hd
 
-    def gamma(s):
+    def gamma(s, n=d):
         if gamma_std == 0.0:
-            return torch.ones(d, dtype=BF16)
-        return normal((d,), s, std=gamma_std, mean=1.0)
+            return torch.ones(n, dtype=BF16)
+        return normal((n,), s, std=gamma_std, mean=1.0)
 
-    return {
+    w = {
         "attn_norm": gamma(seed + 1),
         "w_qkv": normal((shape.qkv_dim, d), seed + 2, std=std),
         "w_o": normal((d, qo), seed + 3, std=std),
@@ -149,6 +151,10 @@ def layer_weights(shape: LayerShape, seed: int, std: float = 0.02, gamma_std: fl
         "w_gate_up": normal((2 * F, d), seed + 5, std=std),
         "w_down": normal((d, F), seed + 6, std=std),
     }
+    if shape.qk_norm:
+        w["q_norm"] = gamma(seed + 7, hd)
+        w["k_norm"] = gamma(seed + 8, hd)
+    return w
 
 
 def normal_device(shape, seed: int, std: float = 1.0, mean: float = 0.0, dtype=BF16, device="cuda") -> torch.Tensor:

@@ -22,7 +22,8 @@ class LayerRig:
         self.w_host = synth.layer_weights(shape, seed, std=0.02, gamma_std=gamma_std)
         self.w = {k: cuda(v) for k, v in self.w_host.items()}
         self.lw = bi.LayerWeights(*[self.w[k].data_ptr() for k in
-                                    ("attn_norm", "w_qkv", "w_o", "ffn_norm", "w_gate_up", "w_down")])
+                                    ("attn_norm", "w_qkv", "w_o", "ffn_norm", "w_gate_up", "w_down")],
+                                  *[self.w[k].data_ptr() if k in self.w else None for k in ("q_norm", "k_norm")])
         self.dims = bi.ModelDims(shape.d_model, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn_dim, 8,
                                  PS, max_pos, shape.rms_eps)
         half = shape.head_dim // 2
@@ -74,8 +75,9 @@ class LayerRig:
                                     [p for _, _, p in items])
 
 
-def test_tiny_layer_prefill_then_decode_parity():
-    rig = LayerRig(synth.TINY_LAYER, 3)
+@pytest.mark.parametrize("shape", [synth.TINY_LAYER, synth.TINY_QK_LAYER], ids=["plain", "qk_norm"])
+def test_tiny_layer_prefill_then_decode_parity(shape):
+    rig = LayerRig(shape, 3)
     rig.add_request(0, 0, 10, 64)
     rig.add_request(1, 0, 12, 64)
     h = synth.normal((42, 256), 5)
@@ -137,11 +139,13 @@ def test_llama8b_layer_target_bitwise_across_batches_and_modes():
         assert max_rel_err(f64(outk), refo) <= TOL_BF16
 
 
-@pytest.mark.parametrize("mode", [bi.INVARIANT, bi.INVARIANT_KSPLIT])
-def test_layer_chunked_prefill_equals_token_by_token_decode(mode):
+@pytest.mark.parametrize("mode,shape", [(bi.INVARIANT, synth.LLAMA31_8B_LAYER),
+                                        (bi.INVARIANT_KSPLIT, synth.LLAMA31_8B_LAYER),
+                                        (bi.INVARIANT, synth.QWEN3_8B_LAYER)], ids=["llama", "llama-ksplit", "qwen3-qknorm"])
+def test_layer_chunked_prefill_equals_token_by_token_decode(mode, shape):
     # INVARIANT_KSPLIT: prefill chunks of > 128 tokens merge the K parts inside a CTA,
-    # decode runs them on separate CTAs; the bits must agree all the same
-    shape = synth.LLAMA31_8B_LAYER
+    # decode runs them on separate CTAs; the bits must agree all the same.  The Qwen3
+    # layer adds the per-head q/k RMSNorm before RoPE.
     L = 600
     h = synth.normal((L, shape.d_model), 70)
     outs = []

@@ -14,12 +14,13 @@ bi = pytest.importorskip("invariant_deterministic_02_gb300")
 from invariant_deterministic_02_gb300.model import QWEN3_8B, BiModel, ModelShape  # noqa: E402
 
 
-def tiny_shape():
-    return ModelShape(layer=synth.TINY_LAYER, n_layers=2, vocab=512, max_pos=2048)
+def tiny_shape(layer=synth.TINY_LAYER):
+    return ModelShape(layer=layer, n_layers=2, vocab=512, max_pos=2048)
 
 
-def test_tiny_model_prefill_and_decode_parity():
-    shape = tiny_shape()
+@pytest.mark.parametrize("layer", [synth.TINY_LAYER, synth.TINY_QK_LAYER], ids=["plain", "qk_norm"])
+def test_tiny_model_prefill_and_decode_parity(layer):
+    shape = tiny_shape(layer)
     m = BiModel.random(shape, seed=11, num_pages=256)
     prompts = [synth.token_ids(n, shape.vocab, 90 + n) for n in (37, 5, 120)]
     out = m.forward_batch([(i, p) for i, p in enumerate(prompts)])
