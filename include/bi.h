@@ -128,10 +128,10 @@ bi_status bi_rmsnorm(const void* x, const void* gamma, void* y, int64_t rows, in
  * layout, K contiguous).  C: device [M][N] of `out_dtype` (bf16 or f32).
  * residual: NULL or device [M][N] bf16, added to the fp32 accumulator before the
  * single rounding to out_dtype (C may alias residual).
- * INVARIANT: tcgen05 tensor cores (K=16 instructions, bf16 in, fp32 accumulate
- * in tensor memory), k-tiles of 64 consumed in ascending order, the whole K
- * range of an output element reduced by one instruction stream (one CTA, or an
- * SM pair for M > 128); nothing in that order depends on M or N.  FAST: split-K chosen from the tile count and
+ * INVARIANT: tcgen05 tensor cores (M=128, K=16 instructions, bf16 in, fp32
+ * accumulate in tensor memory), k-tiles of 64 consumed in ascending order, the
+ * whole K range of an output element reduced by one CTA; nothing in that order
+ * depends on M or N.  FAST: split-K chosen from the tile count and
  * the SM count (the non-invariant behaviour BI-notes "GEMM" describes).
  * PROTECTED: the 128-row tiles holding rows [target_row, target_row+target_count)
  * are never split; other tiles are as FAST.

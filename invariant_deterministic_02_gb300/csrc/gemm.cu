@@ -8,29 +8,24 @@
 // Kernel" notes, section GEMM: the K split may depend on K only.)
 //
 // Reduction geometry, identical for every M, N and CTA shape:
-//   * tcgen05.mma.kind::f16 with K=16, bf16 operands from shared memory
-//     (128-byte swizzled, K-major), fp32 accumulator in tensor memory;
+//   * tcgen05.mma.cta_group::1.kind::f16 with M=128, K=16, bf16 operands from
+//     shared memory (128-byte swizzled, K-major), fp32 accumulator in tensor memory;
 //   * the K range is consumed in 64-wide k-tiles in ascending order, four
 //     instructions of K=16 per k-tile in ascending order; the first
 //     instruction of an output tile overwrites the accumulator, all others add.
 // An output element therefore sees the same instruction sequence with the
-// same operands whatever M is and whichever CTA computes it.  The instruction's
-// M and N extents (M=128 on one SM, M=256 on an SM pair; N = the tile width,
-// 32-256 columns) and the persistent tile-to-CTA mapping are scheduling choices
-// that never touch an element's arithmetic; the row-0 M sweeps check this
-// bitwise across all of them.
+// same operands whatever M is and whichever CTA computes it.  The
+// instruction's N extent (the CTA tile width, 32-256 columns) and the
+// persistent tile-to-CTA mapping are scheduling choices that never touch an
+// element's arithmetic; the row-0 M sweeps check this bitwise across widths.
 //
-// Two kernels:
-//   * gemm_tc_kernel<TN> (M <= 128, and every FAST / PROTECTED / KSPLIT launch):
-//     one CTA per 128 x TN tile.  Roles in a CTA of 192 threads: warp 0 issues
-//     TMA loads, warp 1 owns the tensor memory and issues the MMAs (one
-//     thread), warps 2-5 drain the accumulator (tcgen05.ld) and store.
-//   * gemm_tc2_kernel (INVARIANT, M > 128): a 2-CTA cluster per 256 x 256 tile
-//     with tcgen05.mma.cta_group::2 (see the comment above the kernel).
-// Shared-memory stages and two tensor-memory accumulators are handed between
-// roles with mbarriers.  Every wait is bounded: when one runs out the kernel
-// records a site code in a device error word, stops all roles, waits (bounded)
-// for its own copies and MMAs, frees its tensor memory and returns.
+// Roles in a CTA of 192 threads: warp 0 issues TMA loads, warp 1 owns the
+// tensor memory and issues the MMAs (one thread), warps 2-5 drain the
+// accumulator (tcgen05.ld) and store.  Shared-memory stages and two
+// tensor-memory accumulators are handed between roles with mbarriers.  Every
+// wait is bounded: when one runs out the kernel records a site code in a
+// device error word, stops all roles, waits (bounded) for its own copies and
+// MMAs, frees its tensor memory and returns.
 //
 // FAST mode (the non-invariant schedule used to measure the cost of
 // invariance): when there are fewer tiles than SMs the K range is split over
@@ -503,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           ok = false;
           break;
         }
+        __syncwarp();  // lanes leave the wait at different times; tcgen05.ld needs the whole warp
         tc_fence_after();
         const uint32_t tbase = lane_base + acc * TN;
         const bool last = q == seq - 1;
@@ -581,297 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
-                 : "memory");
-  }
-}
-
-// ------------------------------------------------------------------ two-SM tiles (M > 128)
-// A cluster of two CTAs computes 256x256 output tiles with tcgen05.mma.cta_group::2
-// (instruction M=256, N=256, K=16).  CTA rank r loads A rows [256i + 128r, +128)
-// and B rows [256j + 128r, +128) of every k-tile into its own shared memory; the
-// even CTA issues the MMAs, which read both CTAs' operands and accumulate rows
-// 128r.. of the tile into each CTA's own tensor memory.  Per SM this moves
-// 32 KiB of operands per 4.2 MFLOP (a 1-CTA 128x256 tile moves 48 KiB), which is
-// what lets the copy engines keep the tensor cores fed.  Per element the
-// instruction sequence (ascending k-tiles, K=16 steps, the first overwriting
-// the accumulator) is the one of the single-CTA kernel.
-//
-// Synchronisation: full[s] lives in the even CTA and counts both CTAs' copy
-// bytes (armed once by the even CTA's producer); the MMA commits arrive on
-// empty[s] and tfull[a] of both CTAs (multicast); both CTAs' epilogue warps
-// arrive on the even CTA's tempty[a].  Before leaving, the two CTAs exchange an
-// arrival on each other's exit barrier, so neither frees its shared or tensor
-// memory while the other may still address it.  Every wait is bounded.
-constexpr int kTN2 = 256;
-constexpr int kAccs2 = 2;                  // accumulators of 256 columns in tensor memory
-constexpr int kTmemCols2 = 256 * kAccs2;  // allocated by the pair collectively
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// address of the same shared variable in CTA `cta` of this cluster
-__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t cta) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(cta));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
-                                                 int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
-      "[%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
-      : "memory");
-}
-__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// arrive on the barrier at this shared offset in the CTAs of `mask` (bit r = rank r)
-// once the MMAs issued so far have completed
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask = 3) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
-__host__ __device__ constexpr uint32_t idesc_pair() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kTN2 >> 3) << 17) |
-         (static_cast<uint32_t>(256 >> 4) << 24);
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const Args a) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kTmemCols = kTmemCols2;
-  const int kStages = a.stages;
-  const int kStageBytes = a.stage_bytes;  // 16 KiB of A + 16 KiB of B (this CTA's halves)
-  constexpr int a_tile = kBM * kBK * 2;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  unsigned char* tiles = smem + kBarBlock;
-  // bars: full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain, exit, tmem slot + abort word
-  const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = full0 + 8 * kMaxStages;
-  const uint32_t tfull0 = empty0 + 8 * kMaxStages;
-  const uint32_t tempty0 = tfull0 + 16;
-  const uint32_t drain_bar = tempty0 + 16;
-  const uint32_t exit_bar = drain_bar + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 6);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
-  const bool leader = rank == 0;
-  const int cid = blockIdx.x >> 1;
-  const int nclusters = gridDim.x >> 1;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(full0 + 8 * i, 1);  // the even CTA's producer; bytes of both CTAs
-      mbar_init(empty0 + 8 * i, 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(tfull0 + 8 * i, 1);
-      mbar_init(tempty0 + 8 * i, 8);  // four epilogue warps in each CTA
-    }
-    mbar_init(drain_bar, 1);
-    mbar_init(exit_bar, 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
-  }
-  if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  // both CTAs' barriers are initialised before either addresses the other's
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // the pair's allocation must give both CTAs the same columns; if not, do no work
-  uint32_t peer_base;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_base) : "r"(peer_addr(smem_u32(tmem_slot), rank ^ 1u))
-               : "memory");
-  const bool alloc_ok = peer_base == tmem_base;
-  if (!alloc_ok && threadIdx.x == 0) atomicCAS(&g_err_word, 0u, 30u);
-  pdl_wait();
-  pdl_trigger();
-  const int m_tiles2 = (a.M + 255) / 256;
-  const int units = alloc_ok ? m_tiles2 * a.n_tiles : 0;
-
-  if (warp < kProducerWarps) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0) {
-      uint32_t issued_mask = 0, issued_par = 0;
-      const uint32_t full_leader0 = peer_addr(full0, 0);
-      int st = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int u = cid; u < units && ok; u += nclusters) {
-        const int nt = u / m_tiles2, mt2 = u % m_tiles2;
-        const int arow = mt2 * 256 + static_cast<int>(rank) * kBM;
-        const int brow = nt * kTN2 + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < a.kb_total; ++kb) {
-          if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 21)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sa = smem_u32(tiles + st * kStageBytes);
-          if (leader) mbar_expect_tx(full0 + 8 * st, static_cast<uint32_t>(2 * kStageBytes));
-          tma_load_2d_pair(sa, &tmA, full_leader0 + 8 * st, kb * kBK, arow);
-          tma_load_2d_pair(sa + a_tile, &tmW, full_leader0 + 8 * st, kb * kBK, brow);
-          issued_mask |= 1u << st;
-          issued_par = (issued_par & ~(1u << st)) | (ph << st);
-          if (++st == kStages) {
-            st = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-      if (*abort_flag && leader) {
-        for (int i = 0; i < kStages; ++i)
-          if (issued_mask & (1u << i)) wait_drain(full0 + 8 * i, (issued_par >> i) & 1u);
-      }
-      // the even CTA's commits for the last use of each stage arrive in this
-      // CTA's shared memory: let them land before the CTA may leave
-      for (int i = 0; i < kStages; ++i)
-        if (issued_mask & (1u << i)) wait_drain(empty0 + 8 * i, (issued_par >> i) & 1u);
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (lane == 0 && leader) {
-      const uint64_t desc0 = sw128_desc(smem_u32(tiles));
-      constexpr uint32_t kIdesc2 = idesc_pair();
-      int st = 0;
-      uint32_t ph = 0;
-      int acc = 0;
-      uint32_t acc_ph = 0;
-      bool ok = true;
-      bool any = false;
-      for (int u = cid; u < units && ok; u += nclusters) {
-        if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 22)) break;
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * kTN2);
-        for (int kb = 0; kb < a.kb_total; ++kb) {
-          if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 23)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t adesc = desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
-          const uint64_t bdesc = adesc + static_cast<uint64_t>(a_tile >> 4);
-#pragma unroll
-          for (int k = 0; k < kBK / kUK; ++k)
-            tc_mma_pair(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc2,
-                        (k > 0 || kb > 0) ? 1u : 0u);
-          tc_commit_pair(empty0 + 8 * st);
-          any = true;
-          if (++st == kStages) {
-            st = 0;
-            ph ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit_pair(tfull0 + 8 * acc);
-        if (++acc == kAccs2) {
-          acc = 0;
-          acc_ph ^= 1u;
-        }
-      }
-      if (*abort_flag && any) {
-        tc_commit_pair(drain_bar, 1);
-        wait_drain(drain_bar, 0);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue (4 warps, both CTAs)
-    const int quarter = warp & 3;
-    const int row_in_tile = quarter * 32 + lane;
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t tempty_leader0 = peer_addr(tempty0, 0);
-    int acc = 0;
-    uint32_t acc_ph = 0;
-    for (int u = cid; u < units; u += nclusters) {
-      const int nt = u / m_tiles2, mt2 = u % m_tiles2;
-      if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 24)) break;
-      tc_fence_after();
-      const int row = mt2 * 256 + static_cast<int>(rank) * kBM + row_in_tile;
-      const bool row_ok = row < a.M;
-      const uint32_t tbase = lane_base + acc * kTN2;
-#pragma unroll 1
-      for (int ch = 0; ch < kTN2 / 32; ++ch) {
-        uint32_t r[32];
-        tc_ld32(tbase + ch * 32, r);
-        const int col0 = nt * kTN2 + ch * 32;
-        if (!row_ok || col0 >= a.N) continue;
-        if (a.out_kind == kOutF32) {
-          float* dst = static_cast<float*>(a.C) + static_cast<size_t>(row) * a.N + col0;
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (col0 + 4 * g < a.N)
-              *reinterpret_cast<float4*>(dst + 4 * g) =
-                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                              __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
-        } else {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.C) + static_cast<size_t>(row) * a.N + col0;
-          const __nv_bfloat16* res = a.R ? a.R + static_cast<size_t>(row) * a.N + col0 : nullptr;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + 8 * g >= a.N) break;
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * g + e]);
-            if (res) {
-              float rv[8];
-              unpack8(*reinterpret_cast<const uint4*>(res + 8 * g), rv);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = __fadd_rn(f[e], rv[e]);
-            }
-            *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(f);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8 * acc);
-      if (++acc == kAccs2) {
-        acc = 0;
-        acc_ph ^= 1u;
-      }
-    }
-  }
-
-  // Teardown: every MMA has completed once this CTA's epilogue consumed the
-  // last accumulator; the handshake keeps the pair's shared and tensor memory
-  // alive until the peer is done with them.
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    mbar_arrive_cluster(peer_addr(exit_bar, rank ^ 1u));
-    wait_drain(exit_bar, 0);
-  }
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
   }
 }
@@ -1143,20 +848,6 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   return p;
 }
 
-bi_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
-    attr = true;
-  }
-  const size_t smem = 1024 + kBarBlock + static_cast<size_t>(args.stages) * args.stage_bytes + kOverreadSlack;
-  const int units = ((args.M + 255) / 256) * args.n_tiles;
-  const int grid = 2 * std::min(units, plan_sms() / 2);
-  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc2_kernel, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
-  BI_LAUNCH_CHECK();
-  return BI_OK;
-}
-
 template <int TN>
 bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
   static bool attr = false;
@@ -1223,31 +914,6 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   BI_REQUIRE(A && Wt && C, BI_ERR_INVALID_ARG, "bi_gemm: null pointer");
   BI_REQUIRE(aligned16(A) && aligned16(Wt) && aligned16(C) && (R == nullptr || aligned16(R)), BI_ERR_INVALID_ARG,
              "bi_gemm: pointers must be 16-byte aligned");
-  if (mode == BI_MODE_INVARIANT && M > gemm::kBM) {
-    // two-SM 256x256 tiles: the same per-element arithmetic as the one-CTA kernel
-    gemm::Args args{};
-    args.M = static_cast<int>(M);
-    args.N = static_cast<int>(N);
-    args.K = static_cast<int>(K);
-    args.a_rows = gemm::kBM;
-    args.kbs = 1;
-    args.map3d = 0;
-    args.stage_bytes = 2 * gemm::kBM * gemm::kBK * 2;  // this CTA's 128 A rows + 128 B rows of a k-tile
-    args.stages = std::min(gemm::kMaxStages, (gemm::kSmemLimit - 1024 - gemm::kBarBlock - gemm::kOverreadSlack) /
-                                                 args.stage_bytes);
-    args.m_tiles = static_cast<int>((M + gemm::kBM - 1) / gemm::kBM);
-    args.n_tiles = static_cast<int>((N + gemm::kTN2 - 1) / gemm::kTN2);
-    args.splits = 1;
-    args.seq = 1;
-    args.kb_total = static_cast<int>((K + gemm::kBK - 1) / gemm::kBK);
-    args.C = C;
-    args.R = static_cast<const __nv_bfloat16*>(R);
-    args.out_kind = out_dtype == BI_F32 ? gemm::kOutF32 : gemm::kOutBF16;
-    CUtensorMap ma, mw;
-    BI_TRY(gemm::tensor_map(A, M, K, gemm::kBM, 0, &ma));
-    BI_TRY(gemm::tensor_map(Wt, N, K, 128, 0, &mw));
-    return gemm::launch_pair(ma, mw, args, s);
-  }
   gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te);
   BI_REQUIRE(p.seq == 1 || p.TN <= 128, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (merged units at width %d)",
              p.TN);

@@ -13,7 +13,7 @@ import numpy as np
 import torch
 
 import synth
-from . import (Batch, LayerWeights, ModelDims, ModelWeights, PAGE_SIZE, bi_model_forward, bi_model_workspace,
+from . import (PROTECTED, Batch, LayerWeights, ModelDims, ModelWeights, PAGE_SIZE, bi_model_forward, bi_model_workspace,
                bi_rope_table, INVARIANT)
 
 
@@ -185,6 +185,34 @@ class BiModel:
                 vals = torch.randn((n, L.n_kv_heads, PAGE_SIZE, L.head_dim), generator=g, device=self.device)
                 cache[idx] = vals.to(torch.bfloat16)
         self.lengths[req] = length
+
+    def pack_prefill(self, items, target, k: int = 20, tile_rows: int = 128, dummy="__pack_dummy__"):
+        """BlockLock-Pack-style shared prefill of a protected request (zhaixingw.cn
+        post on BlockLock, section on the two modes: terminal-anchored packing with
+        an isolated dummy segment, then the protected request's KV state is taken
+        out and it decodes alone).
+
+        items: (request id, tokens) pairs, one of them `target`.  The target is
+        packed last; a dummy request of filler tokens is inserted just before it
+        so that the target's first token starts on a `tile_rows` boundary of the
+        packed batch (its GEMM row tiles then hold no other request); the batch
+        runs in PROTECTED mode with the target protected (the others take the
+        FAST schedule); the dummy's pages are released afterwards.  The target's
+        K/V stay in its own pages, ready for target-only decode.
+        Returns (ForwardOut of the packed batch, the target's row)."""
+        others = [(r, t) for r, t in items if r != target]
+        tgt = [t for r, t in items if r == target]
+        if len(tgt) != 1:
+            raise ValueError("pack_prefill: target must appear once among the items")
+        pad = (-sum(len(t) for _, t in others)) % tile_rows
+        packed = list(others)
+        if pad:
+            packed.append((dummy, np.zeros(pad, dtype=np.int32)))
+        packed.append((target, tgt[0]))
+        out = self.forward_batch(packed, k=k, mode=PROTECTED, target_request=len(packed) - 1)
+        if pad:
+            self.release(dummy)
+        return out, len(packed) - 1
 
     def copy_prefix(self, src: int, dst: int, tokens: int):
         """Prefix-cache hit: give request `dst` (which must hold no tokens yet) the

@@ -121,6 +121,45 @@ def test_tiny_model_greedy_bit_exact_across_compositions():
     assert_same(refk, got, "ksplit")
 
 
+def test_blocklock_pack_target_bits_equal_invariant_alone():
+    """BlockLock-Pack reading: the protected request is packed last behind a dummy
+    segment that aligns it to a 128-row tile, the shared prefill runs PROTECTED
+    (the neighbours FAST), then the target decodes alone.  Its tokens and top-20
+    bits equal those of the target computed alone in INVARIANT mode, whatever the
+    neighbours are."""
+    shape = tiny_shape()
+    m = BiModel.random(shape, seed=31, num_pages=4096, page_seed=11)
+    V = shape.vocab
+    prompt = synth.token_ids(90, V, 300)
+
+    def decode_alone(req, first_tok, steps=12):
+        toks, tops = [first_tok], []
+        for _ in range(steps):
+            res = m.forward_batch([(req, np.array([toks[-1]], dtype=np.int32))], mode=bi.INVARIANT)
+            toks.append(int(res.top_i[0, 0]))
+            tops.append(res.top_v[0].cpu().numpy().view(np.uint32).copy())
+        return toks, tops
+
+    res = m.forward_batch([("t", prompt)], mode=bi.INVARIANT)
+    ref_first = (int(res.top_i[0, 0]), res.top_v[0].cpu().numpy().view(np.uint32).copy())
+    ref = decode_alone("t", ref_first[0])
+    m.reset()
+    for trial, lens in enumerate([(37, 200), (5,), (130, 64, 300)]):
+        items = [("n%d" % j, synth.token_ids(n, V, 400 + 10 * trial + j)) for j, n in enumerate(lens)]
+        items.insert(trial % (len(items) + 1), ("t", prompt))
+        out, row = m.pack_prefill(items, "t")
+        assert out.top_i[row, 0].item() == ref_first[0]
+        assert np.array_equal(out.top_v[row].cpu().numpy().view(np.uint32), ref_first[1])
+        for r, _ in items:
+            if r != "t":
+                m.release(r)
+        got = decode_alone("t", ref_first[0])
+        assert got[0] == ref[0], trial
+        for a, b in zip(got[1], ref[1]):
+            assert np.array_equal(a, b), trial
+        m.reset()
+
+
 def test_prefix_kv_reuse_across_batches_bitwise():
     """A prompt's K/V computed inside one batch, reused by a new request in another
     batch composition (a prefix-cache hit), continues with exactly the bits of a
