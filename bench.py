@@ -501,12 +501,15 @@ def main():
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
+            # sample steps until about 10 s of CPU work (at most 16 steps)
             smp = OracleSample(args)
-            runs = [smp.step_seconds() for _ in range(2)]
+            runs = []
+            while len(runs) < 16 and (len(runs) < 2 or sum(c for _, c in runs) < 10.0):
+                runs.append(smp.step_seconds())
             v = args.batch / statistics.mean(t for t, _ in runs)
             line["cpu_baseline"] = {"value": round(v, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
-                                    "kind": "oracle", "sample": smp.text + "; 2 steps, %.1f s of CPU work" %
-                                    sum(c for _, c in runs)}
+                                    "kind": "oracle", "sample": smp.text + "; %d steps, %.1f s of CPU work" %
+                                    (len(runs), sum(c for _, c in runs))}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
