@@ -5,10 +5,9 @@ One step = one greedy decode step of a Qwen3-8B-shaped random-init model (36
 layers, d 4096, 32/8 heads, head_dim 128, FFN 12288, vocab 151936) for a batch
 of 64 requests whose cached KV lengths are drawn uniform on [128, 4096]:
 embedding, per layer RMSNorm -> QKV GEMM -> q/k head RMSNorm + RoPE + paged KV
-store -> split-KV
-attention + merge tree -> O GEMM (+residual) -> RMSNorm -> gate|up GEMM ->
-SwiGLU -> down GEMM (+residual), then final RMSNorm, lm-head (fp32 logits) and
-top-20.  All of it runs in libbi's kernels through bi_model_forward.
+store -> split-KV attention + merge tree -> O GEMM (+residual) -> RMSNorm ->
+gate|up GEMM -> SwiGLU -> down GEMM (+residual), then final RMSNorm, lm-head
+(fp32 logits) and top-20.  All of it runs in libbi's kernels through bi_model_forward.
 
 Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
 on a bounded sample of the same workload instead.
