@@ -243,35 +243,49 @@ class OracleKV:
         self.v[(layer, req)] = np.concatenate([self.v.get((layer, req), empty), v_new], axis=0)
 
 
-def layer_forward(h, w, shape, kv: OracleKV, layer: int, requests, pos0) -> np.ndarray:
+def _keep(x):
+    """No rounding: the value is carried at (more than) fp32 precision."""
+    return np.asarray(x, dtype=F64)
+
+
+def layer_forward(h, w, shape, kv: OracleKV, layer: int, requests, pos0, act32: bool = False) -> np.ndarray:
     """One pre-norm decoder layer over a batch of requests.
 
-    h: [T][d] (bf16 values); w: dict of float64 weights (see synth.layer_weights);
+    h: [T][d]; w: dict of float64 weights (see synth.layer_weights);
     requests: list of (request id, number of query tokens) in token order;
     pos0[i]: absolute position of request i's first query token, which must
     equal the request's current cache length (K/V of new tokens are appended
     to the cache before attention, so cached and new tokens are one sequence).
 
-      x1 = bf16(rms(h, g1));      qkv = bf16(x1 Wqkv^T)
-      [Qwen3 only, w has q_norm/k_norm: q, k = bf16(rms_head(q, gq)), bf16(rms_head(k, gk)),
+      x1 = R(rms(h, g1));      qkv = R(x1 Wqkv^T)
+      [Qwen3 only, w has q_norm/k_norm: q, k = R(rms_head(q, gq)), R(rms_head(k, gk)),
        the RMSNorm of every head row of head_dim values]
-      q, k = bf16(rope(q)), bf16(rope(k));  append k, v to the cache
-      att = bf16(attention(q, K, V));       h1 = bf16(h + att Wo^T)
-      x2 = bf16(rms(h1, g2));     gu = bf16(x2 Wgu^T)
-      a = bf16(silu(g) * u);      h2 = bf16(h1 + a Wd^T)
+      q = R(rope(q));  k = bf16(rope(k));  v = bf16(v);  append k, v to the cache
+      att = R(attention(q, K, V));       h1 = R(h + att Wo^T)
+      x2 = R(rms(h1, g2));     gu = R(x2 Wgu^T)
+      a = R(silu(g) * u);      h2 = R(h1 + a Wd^T)
+
+    R is the rounding of the activations between steps: bf16 by default.  With
+    act32 -- the mixed-precision mitigation that the TML-digest names in section 2
+    and again in section 6 (weights stay stored in 16 bits, activations are fp32)
+    -- R is the identity: the oracle carries every activation exactly and the
+    CUDA path carries it in fp32.  The KV cache holds bf16 in both cases (k and
+    v are rounded when they are stored; reading: the cache is stored state, like
+    the weights).
     """
+    R = _keep if act32 else round_bf16
     h = np.asarray(h, dtype=F64)
     Hq, Hkv, hd = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
     F = shape.ffn_dim
-    x1 = round_bf16(rmsnorm(h, w["attn_norm"], shape.rms_eps))
-    qkv = round_bf16(gemm(x1, w["w_qkv"]))
+    x1 = R(rmsnorm(h, w["attn_norm"], shape.rms_eps))
+    qkv = R(gemm(x1, w["w_qkv"]))
     T = h.shape[0]
     q = qkv[:, :Hq * hd].reshape(T, Hq, hd)
     k = qkv[:, Hq * hd:(Hq + Hkv) * hd].reshape(T, Hkv, hd)
     v = qkv[:, (Hq + Hkv) * hd:].reshape(T, Hkv, hd)
     if "q_norm" in w:
-        q = round_bf16(rmsnorm(q, w["q_norm"], shape.rms_eps))  # per head row (last axis = head_dim)
-        k = round_bf16(rmsnorm(k, w["k_norm"], shape.rms_eps))
+        q = R(rmsnorm(q, w["q_norm"], shape.rms_eps))  # per head row (last axis = head_dim)
+        k = R(rmsnorm(k, w["k_norm"], shape.rms_eps))
     att = np.zeros((T, Hq, hd), dtype=F64)
     t0 = 0
     scale = 1.0 / math.sqrt(hd)
@@ -280,26 +294,27 @@ def layer_forward(h, w, shape, kv: OracleKV, layer: int, requests, pos0) -> np.n
             raise ValueError("request %r: cache holds %d tokens, first query at %d"
                              % (req, kv.length(layer, req), p0))
         pos = np.arange(p0, p0 + nq)
-        qr = round_bf16(rope(q[t0:t0 + nq], pos, shape.rope_theta))
+        qr = R(rope(q[t0:t0 + nq], pos, shape.rope_theta))
         kr = round_bf16(rope(k[t0:t0 + nq], pos, shape.rope_theta))
-        kv.append(layer, req, kr, v[t0:t0 + nq])
+        kv.append(layer, req, kr, round_bf16(v[t0:t0 + nq]))
         att[t0:t0 + nq] = attention(qr, kv.k[(layer, req)], kv.v[(layer, req)], pos, scale)
         t0 += nq
-    att = round_bf16(att).reshape(T, Hq * hd)
-    h1 = round_bf16(h + gemm(att, w["w_o"]))
-    x2 = round_bf16(rmsnorm(h1, w["ffn_norm"], shape.rms_eps))
-    gu = round_bf16(gemm(x2, w["w_gate_up"]))
-    a = round_bf16(swiglu(gu[:, :F], gu[:, F:]))
-    return round_bf16(h1 + gemm(a, w["w_down"]))
+    att = R(att).reshape(T, Hq * hd)
+    h1 = R(h + gemm(att, w["w_o"]))
+    x2 = R(rmsnorm(h1, w["ffn_norm"], shape.rms_eps))
+    gu = R(gemm(x2, w["w_gate_up"]))
+    a = R(swiglu(gu[:, :F], gu[:, F:]))
+    return R(h1 + gemm(a, w["w_down"]))
 
 
-def model_forward(ids, emb, layers, final_norm, lm_head, shape, kv: OracleKV, requests, pos0):
+def model_forward(ids, emb, layers, final_norm, lm_head, shape, kv: OracleKV, requests, pos0, act32: bool = False):
     """Embedding gather -> decoder layers -> final RMSNorm -> lm-head logits.
 
     Returns float32-rounded logits [T][V] (the lm-head output is kept in fp32).
+    act32: activations carried without rounding (see layer_forward).
     """
     h = np.asarray(emb, dtype=F64)[np.asarray(ids, dtype=np.int64)]
     for i, w in enumerate(layers):
-        h = layer_forward(h, w, shape, kv, i, requests, pos0)
-    xf = round_bf16(rmsnorm(h, final_norm, shape.rms_eps))
+        h = layer_forward(h, w, shape, kv, i, requests, pos0, act32=act32)
+    xf = (_keep if act32 else round_bf16)(rmsnorm(h, final_norm, shape.rms_eps))
     return round_f32(gemm(xf, lm_head))

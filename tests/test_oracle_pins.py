@@ -343,30 +343,65 @@ def _tiny_weights(shape, seed, zero=()):
     return w
 
 
-def test_layer_zero_projections_is_identity():
+@pytest.mark.parametrize("act32", [False, True])
+def test_layer_zero_projections_is_identity(act32):
     shape = synth.TINY_LAYER
     w = _tiny_weights(shape, 1, zero=("w_o", "w_down"))
     h = synth.normal((5, shape.d_model), 3).double().numpy()
+    if act32:
+        h = h * (1 + 2.0 ** -12)  # not bf16-representable: an activation rounding would show
     kv = oracle.OracleKV(1, shape.n_kv_heads, shape.head_dim)
-    out = oracle.layer_forward(h, w, shape, kv, 0, [(0, 5)], [0])
+    out = oracle.layer_forward(h, w, shape, kv, 0, [(0, 5)], [0], act32=act32)
     assert np.array_equal(out, h)
     assert kv.length(0, 0) == 5
+    # the cache holds bf16 values in both variants
+    assert np.array_equal(oracle.round_bf16(kv.k[(0, 0)]), kv.k[(0, 0)])
+    assert np.array_equal(oracle.round_bf16(kv.v[(0, 0)]), kv.v[(0, 0)])
 
 
-def test_layer_prefill_equals_token_by_token_and_requests_independent():
+@pytest.mark.parametrize("act32", [False, True])
+def test_layer_prefill_equals_token_by_token_and_requests_independent(act32):
     shape = synth.TINY_LAYER
     w = _tiny_weights(shape, 2)
     h = synth.normal((7, shape.d_model), 4).double().numpy()
     kv1 = oracle.OracleKV(1, shape.n_kv_heads, shape.head_dim)
-    full = oracle.layer_forward(h, w, shape, kv1, 0, [(0, 7)], [0])
+    full = oracle.layer_forward(h, w, shape, kv1, 0, [(0, 7)], [0], act32=act32)
     kv2 = oracle.OracleKV(1, shape.n_kv_heads, shape.head_dim)
-    rows = [oracle.layer_forward(h[t:t + 1], w, shape, kv2, 0, [(0, 1)], [t]) for t in range(7)]
-    assert np.allclose(np.concatenate(rows), full, rtol=0, atol=0)
+    rows = [oracle.layer_forward(h[t:t + 1], w, shape, kv2, 0, [(0, 1)], [t], act32=act32) for t in range(7)]
+    # With bf16 activations the roundings absorb the float64 matmul's own
+    # batch-dependent summation order, so the rows agree exactly; with act32 they
+    # agree to float64 rounding.
+    tol = 1e-12 if act32 else 0
+    assert np.allclose(np.concatenate(rows), full, rtol=tol, atol=tol)
     # a second request in the same batch does not change the first one's rows
     kv3 = oracle.OracleKV(1, shape.n_kv_heads, shape.head_dim)
     h2 = np.concatenate([h, synth.normal((3, shape.d_model), 5).double().numpy()])
-    both = oracle.layer_forward(h2, w, shape, kv3, 0, [(0, 7), (1, 3)], [0, 0])
-    assert np.array_equal(both[:7], full)
+    both = oracle.layer_forward(h2, w, shape, kv3, 0, [(0, 7), (1, 3)], [0, 0], act32=act32)
+    assert np.allclose(both[:7], full, rtol=tol, atol=tol)
+
+
+def test_layer_act32_single_token_by_hand():
+    # fp32-activation variant: nothing is rounded between the steps except the
+    # cached k and v (bf16).  One token at position 0 attends only to itself, so
+    # its attention output is its own bf16-rounded v.
+    shape = synth.TINY_LAYER
+    w = _tiny_weights(shape, 3)
+    d, hd, Hq, Hkv, F = shape.d_model, shape.head_dim, shape.n_q_heads, shape.n_kv_heads, shape.ffn_dim
+    h = synth.normal((1, d), 6).double().numpy()
+    kv = oracle.OracleKV(1, Hkv, hd)
+    out = oracle.layer_forward(h, w, shape, kv, 0, [(0, 1)], [0], act32=True)
+    x1 = h / np.sqrt(np.mean(h * h) + shape.rms_eps) * w["attn_norm"]
+    v = oracle.round_bf16(x1 @ w["w_qkv"][(Hq + Hkv) * hd:].T).reshape(Hkv, hd)
+    att = np.concatenate([v[hh // (Hq // Hkv)] for hh in range(Hq)])
+    h1 = h[0] + att @ w["w_o"].T
+    x2 = h1 / np.sqrt(np.mean(h1 * h1) + shape.rms_eps) * w["ffn_norm"]
+    g, u = x2 @ w["w_gate_up"][:F].T, x2 @ w["w_gate_up"][F:].T
+    h2 = h1 + (g / (1 + np.exp(-g)) * u) @ w["w_down"].T
+    assert np.allclose(out[0], h2, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(kv.v[(0, 0)][0], v)
+    # the bf16 variant differs (it rounds between the steps)
+    kv2 = oracle.OracleKV(1, Hkv, hd)
+    assert not np.array_equal(oracle.layer_forward(h, w, shape, kv2, 0, [(0, 1)], [0]), out)
 
 
 def test_layer_attention_branch_single_token():
@@ -395,3 +430,36 @@ def test_model_without_layers_is_norm_then_head():
     assert np.array_equal(logits[0], logits[2])
     x = emb[49] / np.sqrt(np.mean(emb[49] ** 2) + shape.rms_eps)
     assert np.allclose(logits[1], oracle.round_bf16(x) @ head.T, rtol=1e-6)
+    # fp32 activations: the normalised row is not rounded before the head
+    l32 = oracle.model_forward(ids, emb, [], g, head, shape, kv, [(0, 3)], [0], act32=True)
+    assert np.allclose(l32[1], x @ head.T, rtol=1e-6)
+    assert not np.allclose(l32[1], oracle.round_bf16(x) @ head.T, rtol=1e-6, atol=0)
+
+
+def test_three_bf16_terms_hold_an_fp32_value_exactly():
+    # The reading behind the fp32-activation GEMM: an fp32 value a is the exact
+    # sum of three bf16 values, hi = bf16(a), mid = bf16(a - hi),
+    # lo = bf16(a - hi - mid), the differences taken in fp32 (exact there);
+    # each bf16 x bf16 product is exact in fp32.  Checked over random values and
+    # the binade edges of the range the activations use.
+    rng = np.random.default_rng(0)
+    a = np.concatenate([rng.standard_normal(200000) * 10.0 ** rng.integers(-30, 30, 200000),
+                        np.float32(2.0) ** np.arange(-100, 100),
+                        np.nextafter(np.float32(2.0) ** np.arange(-100, 100), np.float32(0)).astype(np.float64)])
+    a = a.astype(np.float32)
+    hi = oracle.round_bf16(a.astype(np.float64)).astype(np.float32)
+    r1 = a - hi
+    mid = oracle.round_bf16(r1.astype(np.float64)).astype(np.float32)
+    r2 = r1 - mid
+    lo = oracle.round_bf16(r2.astype(np.float64)).astype(np.float32)
+    total = hi.astype(np.float64) + mid.astype(np.float64) + lo.astype(np.float64)
+    # exact wherever the third term stays in bf16's normal range (|a| >= 2**-110);
+    # below that the remainder is rounded to bf16's subnormal spacing 2**-133
+    big = np.abs(a) >= 2.0 ** -110
+    assert big.sum() > 0.99 * a.size
+    assert np.array_equal(r2[big], lo[big])  # the third term is already a bf16 value
+    assert np.array_equal(total[big], a[big].astype(np.float64))
+    assert np.all(np.abs(total - a.astype(np.float64)) <= 2.0 ** -134)
+    w = oracle.round_bf16(rng.standard_normal(hi.size)).astype(np.float32)
+    for t in (hi, mid, lo):
+        assert np.array_equal((t * w).astype(np.float64), t.astype(np.float64) * w.astype(np.float64))
