@@ -130,7 +130,9 @@ def run_ours(args, rank, world, local_rank):
     shape = QWEN3_8B
     Ls = synth.uniform_ints(B, KV_LO, KV_HI, args.seed + 17 * rank)  # KV length at the first step
     compare = [m for m in ("fast", "invariant_ksplit") if m != args.mode] if args.mode == "invariant" else []
-    total_steps = W + 2 * K + K + len(compare) * (K + 1)  # warm-up, timed, profiled, end-to-end, other modes
+    act32 = args.mode == "invariant"  # also time the fp32-activation variant of the same step
+    # warm-up, timed, profiled, end-to-end, other modes, fp32 activations
+    total_steps = W + 2 * K + K + len(compare) * (K + 1) + (K + 1 if act32 else 0)
     pages = int(sum((int(L) + total_steps + 16) // 16 + 1 for L in Ls)) + 16
     model = BiModel(shape, BiModel.random_weights(shape, seed=args.seed + 1000 * rank), num_pages=pages,
                     page_seed=args.seed + 3)
@@ -157,16 +159,20 @@ def run_ours(args, rank, world, local_rank):
         return bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos[step].data_ptr(), d_bt.data_ptr(), max_pages, pages,
                         target, 0 if target >= 0 else -1, 1 if target >= 0 else 0)
 
+    dims32 = bi.ModelDims.from_buffer_copy(model.dims)  # same model, fp32 activations
+    dims32.act_f32 = 1
     ws_bytes = max(bi.bi_model_workspace(model.dims, batch_for(0), bi.MODES[m]) for m in [args.mode] + compare)
+    if act32:
+        ws_bytes = max(ws_bytes, bi.bi_model_workspace(dims32, batch_for(0), mode))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
     step = [0]
 
-    def one_step(m=mode):
+    def one_step(m=mode, dims=model.dims):
         s = step[0]
         src, dst = ids[s % 2], ids[(s + 1) % 2]
-        bi.bi_model_forward(model.dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s), model.k_ptrs,
+        bi.bi_model_forward(dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s), model.k_ptrs,
                             model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=dst, mode=m, workspace=ws,
                             ws_bytes=ws_bytes, stream=sp)
         step[0] += 1
@@ -305,20 +311,22 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------------------------------------------------------- the same steps in the other modes
     # FAST: the non-invariant schedule (cost of invariance = FAST / INVARIANT throughput);
-    # INVARIANT_KSPLIT: the K-only split-K GEMM variant (also batch invariant)
+    # INVARIANT_KSPLIT: the K-only split-K GEMM variant (also batch invariant);
+    # invariant_act_f32: INVARIANT with fp32 activations (bf16 weights and KV cache)
     modes = {}
-    for m in compare:
-        one_step(bi.MODES[m])
+    runs = [(m, bi.MODES[m], model.dims) for m in compare] + ([("invariant_act_f32", mode, dims32)] if act32 else [])
+    for name, m, dims in runs:
+        one_step(m, dims)
         torch.cuda.synchronize()
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         c0.record(stream)
         for _ in range(K):
-            one_step(bi.MODES[m])
+            one_step(m, dims)
         c1.record(stream)
         torch.cuda.synchronize()
         cms = c0.elapsed_time(c1)
-        modes[m] = {"value": round(B * world * K / (cms / 1000.0), 2), "unit": "tok/s",
-                    "ms_per_step": round(cms / K, 4)}
+        modes[name] = {"value": round(B * world * K / (cms / 1000.0), 2), "unit": "tok/s",
+                       "ms_per_step": round(cms / K, 4)}
     if "fast" in modes:
         modes["invariant_over_fast_time"] = round(ms_per_step / modes["fast"]["ms_per_step"], 4)
     assert bi.bi_device_error() == 0

@@ -153,13 +153,31 @@ bi_status bi_gemm(const void* A, const void* W, void* C, const void* residual, i
                   bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count, void* workspace,
                   size_t ws_bytes, bi_stream s);
 
+/* fp32 activations times bf16 weights (the mixed-precision mitigation the
+ * TML-digest names in §2 and §6: weights stay 16-bit, activations fp32).
+ * A: device [M][K] fp32.  W: device [N][K] bf16.  C: device [M][N] fp32.
+ * residual: NULL or device [M][N] fp32 added before C is written (C may alias it).
+ * Each fp32 A value is split into three bf16 values hi + mid + lo whose sum is
+ * the value (exact for |a| >= 2^-110; below that the error is < 2^-133), and the
+ * tensor cores reduce, per k16 step, hi*W, mid*W, lo*W in that order with exact
+ * products and fp32 accumulation; otherwise the schedule and every mode are as
+ * bi_gemm (same k order, same K-split rules).  The workspace holds the three
+ * planes (3*M*K bf16) plus what the mode needs; size from
+ * bi_gemm_f32a_workspace.  K, N multiples of 8; A, C, residual 16-byte aligned. */
+size_t bi_gemm_f32a_workspace(int64_t M, int64_t N, int64_t K, bi_mode mode);
+bi_status bi_gemm_f32a(const float* A, const void* W, float* C, const float* residual, int64_t M, int64_t N,
+                       int64_t K, bi_mode mode, int32_t target_row, int32_t target_count, void* workspace,
+                       size_t ws_bytes, bi_stream s);
+
 /* ------------------------------------------------------------------ attention
  * Paged KV cache: k_cache and v_cache are device [num_pages][num_kv_heads][page_size][head_dim]
  * bf16 (page_size must be 16).  block_table: device int32 [B][max_pages];
  * entry i of row b names the physical page of tokens [16i, 16i+16) of request b.
  * Entries past a request's length are never read.
  * Query head h reads kv head h / (num_q_heads / num_kv_heads).  head_dim 64 or
- * 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ * 128; num_q_heads / num_kv_heads in {1, 2, 4}.
+ * act_f32 (dims): 0 = q and out bf16; 1 = q and out fp32 (fp32-activation
+ * layers; the cache stays bf16 and the arithmetic is the same).
  *
  * INVARIANT [TML-digest §3.3 fixed split size; BI-notes "Flash Attention"]: the
  * keys of a query at absolute position p are cut into fixed splits
@@ -181,6 +199,7 @@ typedef struct bi_attn_dims {
   int32_t max_pages; /* row stride of block_table */
   int32_t num_pages; /* pages in each cache (for validation of the cache extent) */
   float scale;       /* score scale, normally 1/sqrt(head_dim) */
+  int32_t act_f32;   /* 0: q and out bf16; 1: q and out fp32 */
 } bi_attn_dims;
 
 /* Decode: one query token per request.  q: device [B][num_q_heads][head_dim] bf16;
@@ -285,6 +304,12 @@ typedef struct bi_model_dims {
   int32_t page_size; /* BI_PAGE_SIZE */
   int32_t max_pos;   /* rows of the RoPE tables */
   float rms_eps;
+  /* 0: bf16 activations (hidden state and every tensor between the steps);
+   * 1: fp32 activations with bf16 weights and a bf16 KV cache (the mixed-precision
+   * mitigation, TML-digest §2/§6): hidden is fp32, nothing is rounded between the
+   * steps except the k and v stored in the cache, and every GEMM multiplies the
+   * fp32 activations exactly (bi_gemm_f32a).  Same schedules, same invariance. */
+  int32_t act_f32;
 } bi_model_dims;
 
 /* A batch of requests.  Request b owns tokens q_start[b] .. q_start[b+1]-1 at
@@ -304,10 +329,10 @@ typedef struct bi_batch {
   int32_t target_count;   /* its token count */
 } bi_batch;
 
-/* Pre-norm decoder layer, in place on hidden [T][d] bf16:
+/* Pre-norm decoder layer, in place on hidden [T][d] (bf16, or fp32 when dims->act_f32):
  *   x = rms(h)*g1; qkv = x Wqkv^T; rope(q,k); store k,v in the cache; a = attn(q, cache);
  *   h = h + a Wo^T; x = rms(h)*g2; gu = x Wgu^T; h = h + (silu(g)*u) Wd^T
- * with bf16 tensors between the steps and the residual adds fused into the GEMMs
+ * with bf16 tensors (fp32 when dims->act_f32) between the steps and the residual adds fused into the GEMMs
  * (reading: the pages fix the three reductions but not the layer, so the
  * standard Llama/Qwen-shaped layer is taken).  The K/V of the batch's tokens are
  * written to the cache before attention, so cached and new tokens are reduced

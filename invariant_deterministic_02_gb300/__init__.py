@@ -39,6 +39,7 @@ TOPK_MAX = 32
 EXPORTED = [
     "bi_status_string", "bi_last_error_message", "bi_version", "bi_num_sms", "bi_device_error",
     "bi_rmsnorm_workspace", "bi_rmsnorm", "bi_gemm_workspace", "bi_gemm_ksplit", "bi_gemm",
+    "bi_gemm_f32a_workspace", "bi_gemm_f32a",
     "bi_decode_attention_workspace", "bi_decode_attention", "bi_decode_attention_noalloc",
     "bi_prefill_attention_workspace",
     "bi_prefill_attention", "bi_embed", "bi_rope_table", "bi_qkv_rope_store", "bi_swiglu", "bi_topk",
@@ -62,7 +63,7 @@ def _status_name(st):
 class AttnDims(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32), ("num_pages", ctypes.c_int32),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("act_f32", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -74,7 +75,8 @@ class LayerWeights(ctypes.Structure):
 class ModelDims(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32), ("vocab", ctypes.c_int32),
-                ("page_size", ctypes.c_int32), ("max_pos", ctypes.c_int32), ("rms_eps", ctypes.c_float)]
+                ("page_size", ctypes.c_int32), ("max_pos", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+                ("act_f32", ctypes.c_int32)]
 
 
 class Batch(ctypes.Structure):
@@ -108,6 +110,8 @@ def _declare(lib):
         "bi_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
         "bi_gemm_ksplit": (c_i32, [c_i64, c_i64]),
         "bi_gemm": (c_i32, [vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i32, c_i32, c_i32, c_i32, vp, c_sz, vp]),
+        "bi_gemm_f32a_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
+        "bi_gemm_f32a": (c_i32, [vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i32, c_i32, c_i32, vp, c_sz, vp]),
         "bi_decode_attention_workspace": (c_sz, [c_i32, P(AttnDims), c_i32]),
         "bi_decode_attention": (c_i32, [vp, vp, vp, vp, vp, c_i32, P(AttnDims), vp, c_i32, c_i32, vp, c_sz, vp]),
         "bi_decode_attention_noalloc": (c_i32, [vp, vp, vp, vp, vp, c_i32, P(AttnDims), vp, c_i32, c_i32, vp]),
@@ -225,15 +229,36 @@ def bi_gemm(A, W, C, residual=None, mode=INVARIANT, target_row=-1, target_count=
     return C
 
 
+def bi_gemm_f32a(A, W, C, residual=None, mode=INVARIANT, target_row=-1, target_count=0, workspace=None,
+                 stream=None):
+    """fp32 A [M][K] times bf16 W [N][K] into fp32 C (+ fp32 residual)."""
+    M, K = A.shape
+    N = W.shape[0]
+    m = _mode(mode)
+    need = lib().bi_gemm_f32a_workspace(M, N, K, m)
+    ws, nb = _ws(need, A.device, workspace)
+    _check(lib().bi_gemm_f32a(_p(A), _p(W), _p(C), _p(residual), M, N, K, m, target_row, target_count, _p(ws), nb,
+                              _stream(stream)), "bi_gemm_f32a")
+    return C
+
+
 def attn_dims(num_q_heads, num_kv_heads, head_dim, max_pages, num_pages, scale=None) -> AttnDims:
     return AttnDims(num_q_heads, num_kv_heads, head_dim, PAGE_SIZE, max_pages, num_pages,
-                    (1.0 / head_dim ** 0.5) if scale is None else scale)
+                    (1.0 / head_dim ** 0.5) if scale is None else scale, 0)
+
+
+def _dims_for(dims: AttnDims, q) -> AttnDims:
+    """A copy of dims whose act_f32 follows the dtype of q (fp32 q and out, or bf16)."""
+    d = AttnDims.from_buffer_copy(dims)
+    d.act_f32 = 1 if q.dtype == torch.float32 else 0
+    return d
 
 
 def bi_decode_attention(q, k_cache, v_cache, block_table, kv_lens, dims: AttnDims, out, mode=INVARIANT,
                         target_request=-1, workspace=None, stream=None):
     B = q.shape[0]
     m = _mode(mode)
+    dims = _dims_for(dims, q)
     need = lib().bi_decode_attention_workspace(B, ctypes.byref(dims), m)
     ws, nb = _ws(need, q.device, workspace)
     _check(lib().bi_decode_attention(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(kv_lens), B,
@@ -246,6 +271,7 @@ def bi_decode_attention_noalloc(q, k_cache, v_cache, block_table, kv_lens, dims:
                                 target_request=-1, stream=None):
     """bi_decode_attention without a workspace: the library serves the scratch from a
     fixed 16 MiB device array of its own (for callers that cannot allocate)."""
+    dims = _dims_for(dims, q)
     _check(lib().bi_decode_attention_noalloc(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(kv_lens),
                                              q.shape[0], ctypes.byref(dims), _p(out), _mode(mode), target_request,
                                              _stream(stream)), "bi_decode_attention_noalloc")
@@ -257,6 +283,7 @@ def bi_prefill_attention(q, k_cache, v_cache, block_table, q_start, q_pos0, dims
     T = q.shape[0]
     B = q_pos0.shape[0]
     m = _mode(mode)
+    dims = _dims_for(dims, q)
     need = lib().bi_prefill_attention_workspace(B, T, ctypes.byref(dims), m)
     ws, nb = _ws(need, q.device, workspace)
     _check(lib().bi_prefill_attention(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(q_start), _p(q_pos0), B,

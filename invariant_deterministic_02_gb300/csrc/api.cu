@@ -47,7 +47,8 @@ namespace {
 const char* const kTagNames[kTagCount] = {
     "rmsnorm",          "rmsnorm_split",       "gemm",        "splitk_reduce", "attn_plan",   "attn_decode_split",
     "attn_decode_merge", "attn_prefill_split", "attn_prefill_merge", "qkv_rope_store", "swiglu", "embed",
-    "topk",             "batch_index",         "gather_rows", "rope_table"};
+    "topk",             "batch_index",         "gather_rows", "rope_table",
+    "split_planes"};
 
 struct ProfState {
   std::mutex mu;

@@ -229,6 +229,23 @@ __device__ __forceinline__ void load_q(const __nv_bfloat16* qrow /* [Hq][HD] at 
   }
 }
 
+// The same registers from fp32 query rows (fp32-activation layers).
+template <int HD, int G>
+__device__ __forceinline__ void load_q(const float* qrow /* [Hq][HD] at head g*G */, int c, QRegs<HD, G>& qr) {
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+    for (int i = 0; i < HD / 64; ++i) {
+      const float4 a = *reinterpret_cast<const float4*>(qrow + hh * HD + 64 * i + 8 * c);
+      const float4 b = *reinterpret_cast<const float4*>(qrow + hh * HD + 64 * i + 8 * c + 4);
+      qr.q[hh][4 * i + 0] = make_float2(a.x, a.y);
+      qr.q[hh][4 * i + 1] = make_float2(a.z, a.w);
+      qr.q[hh][4 * i + 2] = make_float2(b.x, b.y);
+      qr.q[hh][4 * i + 3] = make_float2(b.z, b.w);
+    }
+  }
+}
+
 // Sum of the 8 partial dot products of one position held by lanes 8s..8s+7
 // (one per head in dot[]), reduced with halving exchanges: lane c ends with the
 // full sum of head head_of_lane(c).  The additions are those of a xor-butterfly
@@ -527,13 +544,14 @@ __device__ __forceinline__ void merge_row(const Partials& part, size_t first_uni
   out_o = o;
 }
 
-// out[d0..d0+3] of one (row, head): o / l rounded to bf16 (0 where l == 0)
-__device__ __forceinline__ void store_out4(uint16_t* dst, float l, const float4& o) {
+// out[d0..d0+3] of one (row, head) at element offset off: o / l (0 where
+// l == 0), rounded to bf16, kept in fp32, or split into three bf16 planes.
+__device__ __forceinline__ void store_out4(const ActDst& out, size_t off, float l, const float4& o) {
   const float r0 = (l > 0.f) ? __fdiv_rn(o.x, l) : 0.f;
   const float r1 = (l > 0.f) ? __fdiv_rn(o.y, l) : 0.f;
   const float r2 = (l > 0.f) ? __fdiv_rn(o.z, l) : 0.f;
   const float r3 = (l > 0.f) ? __fdiv_rn(o.w, l) : 0.f;
-  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(r0, r1), pack_bf16x2(r2, r3));
+  act_store4(out, off, r0, r1, r2, r3);
 }
 
 // ------------------------------------------------------------------ decode
@@ -637,9 +655,11 @@ struct DecodeSmem {
 
 template <int HD, int G>
 __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vc,
-    const int* __restrict__ block_table, const int* __restrict__ kv_lens, int B, int hq, int hkv, int max_pages,
-    float scale_log2, DecodePlan plan, Partials part) {
+    const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const __nv_bfloat16* __restrict__ kc,
+    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, const int* __restrict__ kv_lens, int B,
+    int hq, int hkv, int max_pages, float scale_log2, DecodePlan plan, Partials part) {
+  // qf: fp32 queries (fp32-activation layers; q unused).  The consumers then
+  // read q from global memory and the item ring carries the descriptor only.
   extern __shared__ __align__(128) unsigned char smem_raw[];
   DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>(smem_raw);
   const uint32_t full0 = smem_u32(&S.full[0]);
@@ -687,10 +707,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
         const int ul = plan.ulen[b];
         const int us = (u - plan.prefix[b]) * ul;
         S.item[slot] = make_int4(u, g, us, min(kv_lens[b], us + ul));
-        mbar_expect_tx(ifull0 + 8 * slot, static_cast<uint32_t>(G * HD * 2));  // release: the descriptor store
-        bulk_g2s(smem_u32(&S.qbuf[slot][0]), q + (static_cast<size_t>(b) * hq + g * G) * HD, G * HD * 2,
-                 ifull0 + 8 * slot);
-        ann_issued |= 1u << slot;
+        if (qf != nullptr) {
+          mbar_arrive(ifull0 + 8 * slot);  // release: the descriptor store
+        } else {
+          mbar_expect_tx(ifull0 + 8 * slot, static_cast<uint32_t>(G * HD * 2));  // release: the descriptor store
+          bulk_g2s(smem_u32(&S.qbuf[slot][0]), q + (static_cast<size_t>(b) * hq + g * G) * HD, G * HD * 2,
+                   ifull0 + 8 * slot);
+          ann_issued |= 1u << slot;
+        }
       }
       ++ann;
     };
@@ -758,7 +782,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const int ustart = desc.z;
     const int uend = desc.w;
     QRegs<HD, G> qr;
-    load_q<HD, G>(&S.qbuf[islot][0], c, qr);
+    if (qf != nullptr) {
+      const int b = find_row(plan.prefix, B, u);
+      load_q<HD, G>(qf + (static_cast<size_t>(b) * hq + g * G) * HD, c, qr);
+    } else {
+      load_q<HD, G>(&S.qbuf[islot][0], c, qr);
+    }
     __syncwarp();
     if ((tid & 31) == 0) mbar_arrive(iempty0 + 8 * islot);  // descriptor and q are in registers
     float rm[G], rl[G], ro[OPT];
@@ -816,8 +845,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
 
 
 // Merge of the split states of each (request, query head) in a second kernel.
-__global__ void decode_merge_kernel(const Partials part, DecodePlan plan, __nv_bfloat16* __restrict__ out, int B,
-                                    int hq, int hkv, int hd) {
+__global__ void decode_merge_kernel(const Partials part, DecodePlan plan, ActDst out, int B, int hq, int hkv,
+                                    int hd) {
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x / hkv;
@@ -831,7 +860,7 @@ __global__ void decode_merge_kernel(const Partials part, DecodePlan plan, __nv_b
   float m, l;
   float4 o;
   merge_row(part, plan.prefix[b], plan.nunits[b], plan.mode[b] == kPlanInvariant, hq, hd, h, d0, m, l, o);
-  store_out4(reinterpret_cast<uint16_t*>(out) + (static_cast<size_t>(b) * hq + h) * hd + d0, l, o);
+  store_out4(out, (static_cast<size_t>(b) * hq + h) * hd + d0, l, o);
 }
 
 // ------------------------------------------------------------------ prefill
@@ -962,9 +991,10 @@ struct PrefillSmem {
 
 template <int HD, int G>
 __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc, const __nv_bfloat16* __restrict__ vc,
-    const int* __restrict__ block_table, const int* __restrict__ q_pos0, const int* __restrict__ q_start, int hq,
-    int hkv, int max_pages, float scale_log2, PrefillPlan plan, Partials part) {
+    const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const __nv_bfloat16* __restrict__ kc,
+    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, const int* __restrict__ q_pos0,
+    const int* __restrict__ q_start, int hq, int hkv, int max_pages, float scale_log2, PrefillPlan plan,
+    Partials part) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -1011,7 +1041,8 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
       split_range(inv, pos0, s, p, st_t, en_t);
       const int valid = en_t - st_t;  // >= 1; same origin st as the staged rows
       QRegs<HD, G> qr;
-      load_q<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
+      if (qf != nullptr) load_q<HD, G>(qf + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
+      else load_q<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
       float bo[OPT];
       split_reduce<HD, G>(qr, kv, valid, scale_log2, sm.grp[group], group, bo);
       const size_t pidx = (static_cast<size_t>(plan.tok_prefix[tok]) + s) * hq + g * G;
@@ -1030,8 +1061,7 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
 }
 
 __global__ void prefill_merge_kernel(const Partials part, PrefillPlan plan, const int* __restrict__ q_start,
-                                     const int* __restrict__ q_pos0, int B, __nv_bfloat16* __restrict__ out, int hq,
-                                     int hkv, int hd) {
+                                     const int* __restrict__ q_pos0, int B, ActDst out, int hq, int hkv, int hd) {
   pdl_wait();
   pdl_trigger();
   const int tok = blockIdx.x / hkv;
@@ -1052,7 +1082,7 @@ __global__ void prefill_merge_kernel(const Partials part, PrefillPlan plan, cons
   float m, l;
   float4 o;
   merge_row(part, plan.tok_prefix[tok], n, plan.req_mode[b] == kPlanInvariant, hq, hd, h, d0, m, l, o);
-  store_out4(reinterpret_cast<uint16_t*>(out) + (static_cast<size_t>(tok) * hq + h) * hd + d0, l, o);
+  store_out4(out, (static_cast<size_t>(tok) * hq + h) * hd + d0, l, o);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1160,8 +1190,10 @@ int decode_grid() {
 
 template <int HD, int G>
 bi_status decode_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* kv_lens,
-                        int B, const bi_attn_dims* dm, void* out, bi_mode mode, int target, const DecodeWs& w,
+                        int B, const bi_attn_dims* dm, const ActDst& out, bi_mode mode, int target, const DecodeWs& w,
                         cudaStream_t s, bool make_plan = true) {
+  // fp32-activation layers: fp32 queries (the consumers read them from global memory)
+  const bool qf = dm->act_f32 != 0;
   if (mode == BI_MODE_INVARIANT_KSPLIT) mode = BI_MODE_INVARIANT;  // the split-K variant changes the GEMM only
   if (make_plan) {
     const int fast_units = std::max(1, (4 * num_sms() + B * dm->num_kv_heads - 1) / (B * dm->num_kv_heads));
@@ -1175,22 +1207,22 @@ bi_status decode_launch(const void* q, const void* kc, const void* vc, const int
   const size_t dsmem = sizeof(DecodeSmem<HD, G>);
   BI_TIMED(::bi::kTagAttnDecodeSplit, s,
            BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G>, dim3(grid), dim3(kDecodeThreads), dsmem, s, 
-               static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
-               static_cast<const __nv_bfloat16*>(vc), bt, kv_lens, B, dm->num_q_heads, dm->num_kv_heads,
-               dm->max_pages, sl2, w.plan, w.part)));
+               qf ? nullptr : static_cast<const __nv_bfloat16*>(q), qf ? static_cast<const float*>(q) : nullptr,
+               static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt, kv_lens, B,
+               dm->num_q_heads, dm->num_kv_heads, dm->max_pages, sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
   BI_TIMED(::bi::kTagAttnDecodeMerge, s,
            BI_PDL_CHECK(launch_pdl(decode_merge_kernel, dim3(B * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part,
-                                   w.plan, static_cast<__nv_bfloat16*>(out), B, dm->num_q_heads, dm->num_kv_heads,
-                                   HD)));
+                                   w.plan, out, B, dm->num_q_heads, dm->num_kv_heads, HD)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
 
 template <int HD, int G>
 bi_status prefill_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* q_start,
-                         const int32_t* q_pos0, int B, int T, const bi_attn_dims* dm, void* out, bi_mode mode,
-                         int target, const PrefillWs& w, cudaStream_t s) {
+                         const int32_t* q_pos0, int B, int T, const bi_attn_dims* dm, const ActDst& out,
+                         bi_mode mode, int target, const PrefillWs& w, cudaStream_t s) {
+  const bool qf = dm->act_f32 != 0;  // fp32 queries
   if (mode == BI_MODE_INVARIANT_KSPLIT) mode = BI_MODE_INVARIANT;  // the split-K variant changes the GEMM only
   BI_TIMED(::bi::kTagAttnPlan, s, BI_PDL_CHECK(launch_pdl(prefill_plan_kernel, dim3(1), dim3(1024), 0, s, q_start, q_pos0, B, T, static_cast<int>(mode), target, w.plan)));
   BI_LAUNCH_CHECK();
@@ -1203,13 +1235,12 @@ bi_status prefill_launch(const void* q, const void* kc, const void* vc, const in
   }
   const float sl2 = dm->scale * kLog2e;
   BI_TIMED(::bi::kTagAttnPrefillSplit, s, BI_PDL_CHECK(launch_pdl(prefill_split_kernel<HD, G>, dim3(num_sms()), dim3(kGroupThreads * kPrefillGroups), smem, s, 
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kc),
-      static_cast<const __nv_bfloat16*>(vc), bt, q_pos0, q_start, dm->num_q_heads, dm->num_kv_heads, dm->max_pages,
-      sl2, w.plan, w.part)));
+      qf ? nullptr : static_cast<const __nv_bfloat16*>(q), qf ? static_cast<const float*>(q) : nullptr,
+      static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt, q_pos0, q_start,
+      dm->num_q_heads, dm->num_kv_heads, dm->max_pages, sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
   BI_TIMED(::bi::kTagAttnPrefillMerge, s, BI_PDL_CHECK(launch_pdl(prefill_merge_kernel, dim3(T * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part, w.plan, q_start, q_pos0, B,
-                                                               static_cast<__nv_bfloat16*>(out), dm->num_q_heads,
-                                                               dm->num_kv_heads, HD)));
+                                                               out, dm->num_q_heads, dm->num_kv_heads, HD)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -1245,7 +1276,8 @@ bi_status decode_attention_impl(const void* q, const void* kc, const void* vc, c
   attn::DecodeWs w = attn::carve_decode(ws, ws_bytes, B, dims);
   BI_REQUIRE(ws != nullptr && w.bytes <= ws_bytes, BI_ERR_WORKSPACE, "bi_decode_attention: workspace %zu < %zu",
              ws_bytes, w.bytes);
-  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, out, mode,
+  const ActDst od{out, 0, dims->act_f32 ? kActF32 : kActBF16};
+  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, od, mode,
                    mode == BI_MODE_PROTECTED ? target : -1, w, s);
 }
 
@@ -1265,6 +1297,22 @@ bi_status prefill_attention_impl(const void* q, const void* kc, const void* vc, 
              "bi_prefill_attention: q/caches/out must be 16-byte aligned");
   attn::PrefillWs w = attn::carve_prefill(ws, ws_bytes, B, T, dims);
   BI_REQUIRE(ws != nullptr && w.bytes <= ws_bytes, BI_ERR_WORKSPACE, "bi_prefill_attention: workspace %zu < %zu",
+             ws_bytes, w.bytes);
+  const ActDst od{out, 0, dims->act_f32 ? kActF32 : kActBF16};
+  BI_ATTN_DISPATCH(attn::prefill_launch, q, kc, vc, bt, q_start, q_pos0, B, T, dims, od, mode,
+                   mode == BI_MODE_PROTECTED ? target : -1, w, s);
+}
+
+// Prefill attention inside the layer: output written as `out` says (three
+// bf16 planes for fp32-activation layers).
+bi_status prefill_attention_layer(const void* q, const void* kc, const void* vc, const int32_t* bt,
+                                  const int32_t* q_start, const int32_t* q_pos0, int32_t B, int32_t T,
+                                  const bi_attn_dims* dims, const ActDst& out, bi_mode mode, int32_t target, void* ws,
+                                  size_t ws_bytes, cudaStream_t s) {
+  BI_TRY(attn::check_dims(dims));
+  if (T == 0) return BI_OK;
+  attn::PrefillWs w = attn::carve_prefill(ws, ws_bytes, B, T, dims);
+  BI_REQUIRE(ws != nullptr && w.bytes <= ws_bytes, BI_ERR_WORKSPACE, "prefill attention: workspace %zu < %zu",
              ws_bytes, w.bytes);
   BI_ATTN_DISPATCH(attn::prefill_launch, q, kc, vc, bt, q_start, q_pos0, B, T, dims, out, mode,
                    mode == BI_MODE_PROTECTED ? target : -1, w, s);
@@ -1337,7 +1385,8 @@ bi_status decode_attention_noalloc_impl(const void* q, const void* kc, const voi
   void* base = nullptr;
   BI_TRY(attn::noalloc_scratch_address(&base));
   attn::DecodeWs w = attn::carve_decode_noalloc(base, B, dims, mode);
-  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, out, mode,
+  const ActDst od{out, 0, dims->act_f32 ? kActF32 : kActBF16};
+  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, od, mode,
                    mode == BI_MODE_PROTECTED ? target : -1, w, s);
 }
 
@@ -1355,9 +1404,9 @@ size_t decode_parts_bytes(int32_t B, const bi_attn_dims* dims) {
 }
 
 bi_status decode_attention_layer(const void* q, const void* kc, const void* vc, const int32_t* bt,
-                                 const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, void* out, bi_mode mode,
-                                 int32_t target, void* plan_ws, bool make_plan, void* part_ws, size_t part_bytes,
-                                 cudaStream_t s) {
+                                 const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, const ActDst& out,
+                                 bi_mode mode, int32_t target, void* plan_ws, bool make_plan, void* part_ws,
+                                 size_t part_bytes, cudaStream_t s) {
   BI_TRY(attn::check_dims(dims));
   BI_REQUIRE(B >= 1 && plan_ws && part_ws && part_bytes >= decode_parts_bytes(B, dims), BI_ERR_WORKSPACE,
              "decode attention: workspace");

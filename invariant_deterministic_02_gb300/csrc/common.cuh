@@ -70,6 +70,7 @@ enum KernelTag : int {
   kTagBatchIndex,
   kTagGather,
   kTagRopeTable,
+  kTagSplitPlanes,
   kTagCount
 };
 extern volatile int g_profiling;
@@ -161,6 +162,56 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                     pack_bf16x2(f[6], f[7]));
+}
+
+// ------------------------------------------------------------------ fp32 activations as three bf16 planes
+// An fp32 value a is the sum hi + mid + lo of three bf16 values, hi = bf16(a),
+// mid = bf16(a - hi), lo = a - hi - mid: each fp32 difference is exact (it only
+// removes leading significant bits), and the last remainder has at most 8
+// significant bits, so it is a bf16 value itself whenever it stays in bf16's
+// normal range (|a| >= 2^-110; below that it is rounded to 2^-133).  An fp32
+// activation tensor [rows][cols] that feeds a GEMM is stored as three bf16
+// planes [3][rows][cols]; a bf16 x bf16 product is exact in fp32, so the GEMM
+// over the planes with fp32 accumulation multiplies the fp32 activations by
+// the bf16 weights without rounding the activations.
+__device__ __forceinline__ void split3(float a, float& hi, float& mid, float& lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(a));
+  const float r = __fsub_rn(a, hi);
+  mid = __bfloat162float(__float2bfloat16_rn(r));
+  lo = __fsub_rn(r, mid);
+}
+
+// Four consecutive values into the three planes at p, p + plane, p + 2 plane
+// (p 8-byte aligned).
+__device__ __forceinline__ void store_planes4(uint16_t* p, size_t plane, float a, float b, float c, float d) {
+  float h[4], m[4], l[4];
+  split3(a, h[0], m[0], l[0]);
+  split3(b, h[1], m[1], l[1]);
+  split3(c, h[2], m[2], l[2]);
+  split3(d, h[3], m[3], l[3]);
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+  *reinterpret_cast<uint2*>(p + plane) = make_uint2(pack_bf16x2(m[0], m[1]), pack_bf16x2(m[2], m[3]));
+  *reinterpret_cast<uint2*>(p + 2 * plane) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+}
+
+// Where a producing kernel writes activations: bf16, fp32, or fp32 as three
+// bf16 planes (`plane` elements apart) for a GEMM that consumes them.
+enum ActKind : int { kActBF16 = 0, kActF32 = 1, kActPlanes = 2 };
+struct ActDst {
+  void* p;
+  size_t plane;  // elements between planes (kActPlanes)
+  int kind;
+};
+
+// Four consecutive values at element offset off (a multiple of 4).
+__device__ __forceinline__ void act_store4(const ActDst& d, size_t off, float a, float b, float c, float e) {
+  if (d.kind == kActF32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(d.p) + off) = make_float4(a, b, c, e);
+  } else if (d.kind == kActPlanes) {
+    store_planes4(static_cast<uint16_t*>(d.p) + off, d.plane, a, b, c, e);
+  } else {
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(d.p) + off) = make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, e));
+  }
 }
 
 // Loads that bypass L1 allocation for streamed-once data.

@@ -32,6 +32,13 @@
 // several CTAs and the fp32 partials are added in a second pass, so an
 // element's rounding depends on M.  PROTECTED: tiles holding target rows are
 // never split.  INVARIANT_KSPLIT: a K split fixed by the weight shape (N, K).
+//
+// fp32 activations (planes = 3): A holds fp32 activations as three bf16 planes
+// hi, mid, lo whose sum is the fp32 value (common.cuh); every k16 step issues
+// the instruction once per plane, in plane order, on the same B operand, so
+// C = sum_k (hi + mid + lo)[i][k] * W[j][k] with exact products and fp32
+// accumulation.  The order is fixed per element, so this is as batch invariant
+// as the one-plane GEMM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -79,6 +86,9 @@ struct Args {
   const __nv_bfloat16* R;  // residual or null
   float* partial;          // [splits][M][N] fp32 (split units only)
   int out_kind;
+  int planes;              // 1: bf16 A; 3: fp32 A as three bf16 planes of plane_rows rows each
+  int plane_rows;
+  const float* Rf;         // fp32 residual (fp32 output) or null
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -290,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const int kbs = a.kbs;
   const int a_tile = a.a_rows * kBK * 2;      // one k-block of A
   const int b_tile = TN * kBK * 2;            // one k-block of B
-  const int a_bytes = kbs * a_tile;           // A part of a stage
+  const int a_plane = kbs * a_tile;           // one plane of A in a stage
+  const int a_bytes = a.planes * a_plane;     // A part of a stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   unsigned char* tiles = smem + kBarBlock;
   // bars: full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain
@@ -369,24 +380,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           for (int kb = kb0; kb < kb1; kb += kbs) {
             const uint32_t fb = full0 + 8 * st;
             const uint32_t sa = smem_u32(tiles + st * kStageBytes);
-            if (pre_stages > 0) {
-              // W of this stage is already on its way (issued before the wait): add A only
+            // W of a prefetched stage is already on its way (issued before the wait): add A only
+            const bool fresh = pre_stages == 0;
+            if (!fresh) {
               --pre_stages;
-              if (a.map3d) tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
-              else tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
             } else {
               if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
                 ok = false;
                 break;
               }
               mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
-              if (a.map3d) {
-                tma_load_3d(sa, &tmA, fb, 0, mt * kBM, kb);
-                tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
-              } else {
-                tma_load_2d(sa, &tmA, fb, kb * kBK, mt * kBM);
-                tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
-              }
+            }
+            for (int pl = 0; pl < a.planes; ++pl) {
+              const int arow = pl * a.plane_rows + mt * kBM;
+              if (a.map3d) tma_load_3d(sa + pl * a_plane, &tmA, fb, 0, arow, kb);
+              else tma_load_2d(sa + pl * a_plane, &tmA, fb, kb * kBK, arow);
+            }
+            if (fresh) {
+              if (a.map3d) tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
+              else tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
             }
             issued_mask |= 1u << st;
             issued_par = (issued_par & ~(1u << st)) | (ph << st);
@@ -443,14 +455,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
               const uint64_t adesc = sdesc + static_cast<uint64_t>((j * a_tile) >> 4);
               const uint64_t bdesc = sdesc + static_cast<uint64_t>((a_bytes + j * b_tile) >> 4);
               const uint32_t first = (kb + j == kb0) ? 1u : 0u;
+              if (a.planes == 1) {
 #pragma unroll
-              for (int k = 0; k < kBK / kUK; ++k) {
-                // the first instruction of a pass overwrites the accumulator, all others add;
-                // one instruction spans the tile's TN columns: the B rows of a stage are
-                // contiguous 128-byte swizzle rows, 1024 bytes per 8-row group
-                const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
-                tc_mma(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdescW,
-                       accum);
+                for (int k = 0; k < kBK / kUK; ++k) {
+                  // the first instruction of a pass overwrites the accumulator, all others add;
+                  // one instruction spans the tile's TN columns: the B rows of a stage are
+                  // contiguous 128-byte swizzle rows, 1024 bytes per 8-row group
+                  const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
+                  tc_mma(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdescW,
+                         accum);
+                }
+              } else {
+                // fp32 A: per k16 step the planes hi, mid, lo in order, same B operand
+#pragma unroll
+                for (int k = 0; k < kBK / kUK; ++k) {
+                  for (int pl = 0; pl < a.planes; ++pl) {
+                    const uint32_t accum = (k > 0 || pl > 0 || !first) ? 1u : 0u;
+                    tc_mma(d0, adesc + static_cast<uint64_t>(((pl * a_plane) >> 4) + 2 * k),
+                           bdesc + static_cast<uint64_t>(2 * k), kIdescW, accum);
+                  }
+                }
               }
             }
             tc_commit(empty0 + 8 * st);  // stage free once these MMAs have read it
@@ -531,12 +555,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                                 __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
           } else if (a.out_kind == kOutF32) {
             float* dst = static_cast<float*>(a.C) + static_cast<size_t>(row) * a.N + col0;
+            const float* res = a.Rf ? a.Rf + static_cast<size_t>(row) * a.N + col0 : nullptr;
 #pragma unroll
             for (int g = 0; g < 8; ++g)
-              if (col0 + 4 * g < a.N)
-                *reinterpret_cast<float4*>(dst + 4 * g) =
-                    make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+              if (col0 + 4 * g < a.N) {
+                float4 v = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                       __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+                if (res) {
+                  const float4 rv = *reinterpret_cast<const float4*>(res + 4 * g);
+                  v.x = __fadd_rn(v.x, rv.x); v.y = __fadd_rn(v.y, rv.y);
+                  v.z = __fadd_rn(v.z, rv.z); v.w = __fadd_rn(v.w, rv.w);
+                }
+                *reinterpret_cast<float4*>(dst + 4 * g) = v;
+              }
           } else {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.C) + static_cast<size_t>(row) * a.N + col0;
             const __nv_bfloat16* res = a.R ? a.R + static_cast<size_t>(row) * a.N + col0 : nullptr;
@@ -587,7 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 // fetched four splits at a time so their loads are in flight together, and
 // added in split order.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, void* C, const __nv_bfloat16* __restrict__ R,
-                                     int M, int N, int splits, int skip_r0, int skip_r1, int out_kind) {
+                                     const float* __restrict__ Rf, int M, int N, int splits, int skip_r0, int skip_r1,
+                                     int out_kind) {
   pdl_wait();
   pdl_trigger();
   const int64_t chunks = static_cast<int64_t>(N) / 4;
@@ -617,6 +649,10 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, void* C,
     }
     const size_t o = static_cast<size_t>(row) * N + col;
     if (out_kind == kOutF32) {
+      if (Rf) {
+        const float4 rv = *reinterpret_cast<const float4*>(Rf + o);
+        f.x = __fadd_rn(f.x, rv.x); f.y = __fadd_rn(f.y, rv.y); f.z = __fadd_rn(f.z, rv.z); f.w = __fadd_rn(f.w, rv.w);
+      }
       *reinterpret_cast<float4*>(static_cast<float*>(C) + o) = f;
     } else {
       if (R) {
@@ -783,7 +819,9 @@ int choose_width_small_m(int64_t N, int splits, int a_rows) {
   return btn;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te) {
+// planes: 1 for bf16 A, 3 for fp32 A held as three bf16 planes (each plane
+// adds an A box to every stage).
+Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te, int planes = 1) {
   Plan p;
   p.a_rows = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : kBM;
   p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
@@ -831,16 +869,20 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
     }
   }
   if (fast_tn) p.TN = fast_tn;
-  else p.TN = M <= kBM ? choose_width_small_m(N, p.splits, p.a_rows) : choose_width(M, N, max_tn);
+  else p.TN = M <= kBM ? choose_width_small_m(N, p.splits, planes * p.a_rows) : choose_width(M, N, max_tn);
   // Each copy costs the copy engine a roughly fixed time, so at decode sizes a
   // stage spans several k-blocks (one 3D box of 16-32 KiB of weights per copy,
   // at most 4 k-blocks so that several stages fit).  (A 3D copy costs more
   // than a 2D box of the same bytes, so the 3D view is used only when a copy
   // spans several k-blocks.)
   p.kbs = (K % kBK == 0 && M <= kBM) ? std::min(4, std::max(1, 256 / p.TN)) : 1;
-  p.map3d = p.kbs > 1 ? 1 : 0;
-  p.stage_bytes = p.kbs * (p.a_rows + p.TN) * kBK * 2;
   const int budget = kSmemLimit - 1024 - kBarBlock - (p.a_rows < kBM ? kOverreadSlack : 0);
+  // fp32 A triples the A part of a stage: keep at least three stages in flight
+  const int kblock_bytes = (planes * p.a_rows + p.TN) * kBK * 2;
+  if (planes > 1)
+    while (p.kbs > 1 && budget / (p.kbs * kblock_bytes) < 3) p.kbs /= 2;
+  p.map3d = p.kbs > 1 ? 1 : 0;
+  p.stage_bytes = p.kbs * kblock_bytes;
   p.stages = std::min(kMaxStages, budget / p.stage_bytes);
   p.n_tiles = static_cast<int>((N + p.TN - 1) / p.TN);
   const int prot = p.tm1 - p.tm0;
@@ -878,30 +920,37 @@ int take_gemm_device_error(cudaStream_t s, int32_t* code) {
   return 0;
 }
 
-size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode) {
+size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode, int planes) {
   if (mode == BI_MODE_INVARIANT || M <= 0 || N <= 0 || K <= 0) return 0;
   // PROTECTED: the largest need with or without a target
-  int splits = gemm::make_plan(M, N, K, mode, 0, 0).splits;
-  if (mode == BI_MODE_PROTECTED) splits = std::max(splits, gemm::make_plan(M, N, K, mode, 0, 1).splits);
+  int splits = gemm::make_plan(M, N, K, mode, 0, 0, planes).splits;
+  if (mode == BI_MODE_PROTECTED) splits = std::max(splits, gemm::make_plan(M, N, K, mode, 0, 1, planes).splits);
   if (splits <= 1) return 0;
   return static_cast<size_t>(splits) * M * N * sizeof(float);
 }
 
-bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64_t M, int64_t N, int64_t K,
-                    bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count, void* ws,
-                    size_t ws_bytes, cudaStream_t s, bool weights_constant) {
-  clear_error();
+size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode) { return gemm_ws(M, N, K, mode, 1); }
+
+namespace {
+
+// Shared body of the bf16-A and fp32-A (planes) GEMMs.  A: [M][K] bf16, or
+// three bf16 planes [3][M][K] when planes == 3.  R: bf16 residual (bf16 out);
+// Rf: fp32 residual (fp32 out).
+bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const void* R, const float* Rf, int64_t M,
+                    int64_t N, int64_t K, bi_dtype out_dtype, bi_mode mode, int32_t target_row,
+                    int32_t target_count, void* ws, size_t ws_bytes, cudaStream_t s, bool weights_constant) {
   BI_REQUIRE(M >= 0 && N >= 0 && K >= 8, BI_ERR_INVALID_ARG, "bi_gemm: M=%lld N=%lld K=%lld",
              static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
   BI_REQUIRE(K % 8 == 0 && N % 8 == 0, BI_ERR_UNSUPPORTED, "bi_gemm: K (%lld) and N (%lld) must be multiples of 8",
              static_cast<long long>(K), static_cast<long long>(N));
-  BI_REQUIRE(M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), BI_ERR_UNSUPPORTED,
+  BI_REQUIRE(planes * M < (int64_t(1) << 31) && N < (int64_t(1) << 31) && K < (int64_t(1) << 31), BI_ERR_UNSUPPORTED,
              "bi_gemm: sizes beyond int32");
   BI_REQUIRE(out_dtype == BI_BF16 || out_dtype == BI_F32, BI_ERR_UNSUPPORTED, "bi_gemm: out dtype %d",
              static_cast<int>(out_dtype));
   BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "bi_gemm: mode %d",
              static_cast<int>(mode));
   BI_REQUIRE(R == nullptr || out_dtype == BI_BF16, BI_ERR_UNSUPPORTED, "bi_gemm: residual needs bf16 output");
+  BI_REQUIRE(Rf == nullptr || out_dtype == BI_F32, BI_ERR_UNSUPPORTED, "bi_gemm: fp32 residual needs fp32 output");
   int64_t tb = 0, te = 0;
   if (mode == BI_MODE_PROTECTED && target_row >= 0) {
     BI_REQUIRE(target_count >= 1 && target_row + static_cast<int64_t>(target_count) <= M, BI_ERR_INVALID_ARG,
@@ -912,11 +961,13 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   }
   if (M == 0 || N == 0) return BI_OK;
   BI_REQUIRE(A && Wt && C, BI_ERR_INVALID_ARG, "bi_gemm: null pointer");
-  BI_REQUIRE(aligned16(A) && aligned16(Wt) && aligned16(C) && (R == nullptr || aligned16(R)), BI_ERR_INVALID_ARG,
-             "bi_gemm: pointers must be 16-byte aligned");
-  gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te);
+  BI_REQUIRE(aligned16(A) && aligned16(Wt) && aligned16(C) && (R == nullptr || aligned16(R)) &&
+                 (Rf == nullptr || aligned16(Rf)),
+             BI_ERR_INVALID_ARG, "bi_gemm: pointers must be 16-byte aligned");
+  gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te, planes);
   BI_REQUIRE(p.seq == 1 || p.TN <= 128, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (merged units at width %d)",
              p.TN);
+  BI_REQUIRE(p.stages >= 2, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (%d stages)", p.stages);
   gemm::Args args{};
   args.M = static_cast<int>(M);
   args.a_rows = p.a_rows;
@@ -937,6 +988,9 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   args.kb_total = p.kb_total;
   args.C = C;
   args.R = static_cast<const __nv_bfloat16*>(R);
+  args.Rf = Rf;
+  args.planes = planes;
+  args.plane_rows = static_cast<int>(M);
   args.out_kind = out_dtype == BI_F32 ? gemm::kOutF32 : gemm::kOutBF16;
   args.partial = nullptr;
   if (p.splits > 1) {
@@ -946,7 +1000,8 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
     args.partial = static_cast<float*>(ws);
   }
   CUtensorMap ma, mw;
-  BI_TRY(gemm::tensor_map(A, M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
+  // the planes form one [planes*M][K] matrix; plane p's rows start at p*M
+  BI_TRY(gemm::tensor_map(A, planes * M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
   BI_TRY(gemm::tensor_map(Wt, N, K, p.TN, p.map3d ? p.kbs : 0, &mw));
   bi_status st;
   if (p.TN == 256) st = gemm::launch_w<256>(ma, mw, args, s);
@@ -959,17 +1014,86 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
     const int64_t n = M * (N / 4);
     const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
     const int skip0 = p.tm0 * gemm::kBM, skip1 = static_cast<int>(std::min<int64_t>(M, int64_t(p.tm1) * gemm::kBM));
-    BI_TIMED(::bi::kTagSplitkReduce, s, BI_PDL_CHECK(launch_pdl(gemm::splitk_reduce_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, args.partial, C, args.R, args.M, args.N,
+    BI_TIMED(::bi::kTagSplitkReduce, s, BI_PDL_CHECK(launch_pdl(gemm::splitk_reduce_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, args.partial, C, args.R, args.Rf, args.M, args.N,
                                                                           p.splits, skip0, skip1, args.out_kind)));
     BI_LAUNCH_CHECK();
   }
   return BI_OK;
 }
 
+// fp32 [rows][cols] -> three bf16 planes [3][rows][cols] (cols % 4 == 0).
+__global__ void split_planes_kernel(const float* __restrict__ x, uint16_t* __restrict__ y, int64_t n4, size_t plane) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n4;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = *reinterpret_cast<const float4*>(x + 4 * k);
+    store_planes4(y + 4 * k, plane, v.x, v.y, v.z, v.w);
+  }
+}
+
+size_t planes_bytes(int64_t M, int64_t K) { return align_up(static_cast<size_t>(3) * M * K * 2, 256); }
+
+}  // namespace
+
+bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64_t M, int64_t N, int64_t K,
+                    bi_dtype out_dtype, bi_mode mode, int32_t target_row, int32_t target_count, void* ws,
+                    size_t ws_bytes, cudaStream_t s, bool weights_constant) {
+  clear_error();
+  return gemm_core(A, 1, Wt, C, R, nullptr, M, N, K, out_dtype, mode, target_row, target_count, ws, ws_bytes, s,
+                   weights_constant);
+}
+
+// fp32-activation layers: A already split into three bf16 planes [3][M][K] by
+// the kernel that produced it; fp32 output, optional fp32 residual.
+bi_status gemm_planes_impl(const void* A_planes, const void* Wt, float* C, const float* Rf, int64_t M, int64_t N,
+                           int64_t K, bi_mode mode, int32_t target_row, int32_t target_count, void* ws,
+                           size_t ws_bytes, cudaStream_t s, bool weights_constant) {
+  return gemm_core(A_planes, 3, Wt, C, nullptr, Rf, M, N, K, BI_F32, mode, target_row, target_count, ws, ws_bytes, s,
+                   weights_constant);
+}
+
+size_t gemm_f32a_ws(int64_t M, int64_t N, int64_t K, bi_mode mode) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return planes_bytes(M, K) + gemm_ws(M, N, K, mode, 3);
+}
+
+bi_status gemm_f32a_impl(const float* A, const void* Wt, float* C, const float* Rf, int64_t M, int64_t N, int64_t K,
+                         bi_mode mode, int32_t target_row, int32_t target_count, void* ws, size_t ws_bytes,
+                         cudaStream_t s) {
+  clear_error();
+  BI_REQUIRE(M >= 0 && N >= 0 && K >= 8 && K % 8 == 0, BI_ERR_INVALID_ARG, "bi_gemm_f32a: M=%lld N=%lld K=%lld",
+             static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "bi_gemm_f32a: mode %d", static_cast<int>(mode));
+  if (M == 0 || N == 0) return BI_OK;
+  BI_REQUIRE(A && aligned16(A), BI_ERR_INVALID_ARG, "bi_gemm_f32a: null or misaligned A");
+  const size_t pb = planes_bytes(M, K);
+  BI_REQUIRE(ws != nullptr && aligned16(ws) && ws_bytes >= gemm_f32a_ws(M, N, K, mode), BI_ERR_WORKSPACE,
+             "bi_gemm_f32a: workspace %zu < %zu bytes", ws_bytes, gemm_f32a_ws(M, N, K, mode));
+  uint16_t* planes = static_cast<uint16_t*>(ws);
+  const int64_t n4 = M * K / 4;
+  const int64_t grid = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(num_sms()) * 8);
+  BI_TIMED(::bi::kTagSplitPlanes, s, BI_PDL_CHECK(launch_pdl(split_planes_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, A, planes, n4, static_cast<size_t>(M * K))));
+  BI_LAUNCH_CHECK();
+  return gemm_core(planes, 3, Wt, C, nullptr, Rf, M, N, K, BI_F32, mode, target_row, target_count,
+                   static_cast<char*>(ws) + pb, ws_bytes - pb, s, false);
+}
+
 }  // namespace bi
 
 extern "C" size_t bi_gemm_workspace(int64_t M, int64_t N, int64_t K, bi_mode mode) {
   return bi::gemm_ws(M, N, K, mode);
+}
+
+extern "C" size_t bi_gemm_f32a_workspace(int64_t M, int64_t N, int64_t K, bi_mode mode) {
+  return bi::gemm_f32a_ws(M, N, K, mode);
+}
+
+extern "C" bi_status bi_gemm_f32a(const float* A, const void* W, float* C, const float* residual, int64_t M,
+                                  int64_t N, int64_t K, bi_mode mode, int32_t target_row, int32_t target_count,
+                                  void* workspace, size_t ws_bytes, bi_stream s) {
+  return bi::gemm_f32a_impl(A, W, C, residual, M, N, K, mode, target_row, target_count, workspace, ws_bytes,
+                            reinterpret_cast<cudaStream_t>(s));
 }
 
 extern "C" int32_t bi_gemm_ksplit(int64_t N, int64_t K) {

@@ -4,6 +4,7 @@
 // invariant as they stand (devpress digest of "Defeating Nondeterminism in LLM
 // Inference", section 3: pointwise operations need no change).
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -49,13 +50,32 @@ __device__ __forceinline__ float round_bf16f(float v) { return __bfloat162float(
 // With qn / kn (Qwen3's per-head norms) a q or k row is first RMS-normalised
 // over its hd values: lane sums of squares in the order (i, i+1, i+hd/2,
 // i+hd/2+1) per pair, a xor butterfly over the warp (every lane gets the same
-// bits), r = 1/sqrt(sum/hd + eps), x -> bf16((x*r)*g), then rotated.
+// bits), r = 1/sqrt(sum/hd + eps), x -> (x*r)*g (rounded to bf16 with bf16
+// activations), then rotated.
+// F32 (fp32 activations): qkv and q_out are fp32 and nothing is rounded except
+// the k and v rows stored in the bf16 cache.
+template <bool F32>
+struct QkvIo {
+  using T = typename std::conditional<F32, float, __nv_bfloat16>::type;
+  // elements (i, i+1) of a row as floats
+  static __device__ __forceinline__ float2 ld2(const T* p) {
+    if constexpr (F32) {
+      return *reinterpret_cast<const float2*>(p);
+    } else {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+      return make_float2(bf16_lo(v), bf16_hi(v));
+    }
+  }
+};
+
+template <bool F32>
 __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
-    const __nv_bfloat16* __restrict__ qkv, const float* __restrict__ rc, const float* __restrict__ rs,
+    const typename QkvIo<F32>::T* __restrict__ qkv, const float* __restrict__ rc, const float* __restrict__ rs,
     const int32_t* __restrict__ token_pos, const int32_t* __restrict__ token_req,
-    const int32_t* __restrict__ block_table, int max_pages, int hq, int hkv, int hd, __nv_bfloat16* __restrict__ q_out,
-    __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc, const __nv_bfloat16* __restrict__ qn,
-    const __nv_bfloat16* __restrict__ kn, float eps) {
+    const int32_t* __restrict__ block_table, int max_pages, int hq, int hkv, int hd,
+    typename QkvIo<F32>::T* __restrict__ q_out, __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
+    const __nv_bfloat16* __restrict__ qn, const __nv_bfloat16* __restrict__ kn, float eps) {
+  using T = typename QkvIo<F32>::T;
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
@@ -64,30 +84,40 @@ __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
   if (task >= hq + 2 * hkv) return;
   const int pos = token_pos[t];
   const int width = (hq + 2 * hkv) * hd;
-  const uint16_t* row = reinterpret_cast<const uint16_t*>(qkv) + static_cast<size_t>(t) * width;
+  const T* row = qkv + static_cast<size_t>(t) * width;
   if (task >= hq + hkv) {
-    // v row of kv head h: copied unchanged
+    // v row of kv head h: stored in the cache (rounded to bf16 from fp32 activations)
     const int h = task - hq - hkv;
     const int req = token_req[t];
     const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
-    const uint4* src = reinterpret_cast<const uint4*>(row + (hq + hkv + h) * hd);
+    const T* src = row + (hq + hkv + h) * hd;
     uint4* dst = reinterpret_cast<uint4*>(vc + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE +
                                                 pos % BI_PAGE_SIZE) * hd);
-    for (int k = lane; k < hd / 8; k += 32) dst[k] = src[k];
+    for (int k = lane; k < hd / 8; k += 32) {
+      if constexpr (F32) {
+        const float4 a = reinterpret_cast<const float4*>(src)[2 * k];
+        const float4 b = reinterpret_cast<const float4*>(src)[2 * k + 1];
+        dst[k] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                            pack_bf16x2(b.z, b.w));
+      } else {
+        dst[k] = reinterpret_cast<const uint4*>(src)[k];
+      }
+    }
     return;
   }
   const bool is_q = task < hq;
   const int h = is_q ? task : task - hq;
   const int half = hd / 2;
-  const uint16_t* src = row + (is_q ? 0 : hq * hd) + h * hd;
-  uint16_t* dst;
+  const T* src = row + (is_q ? 0 : hq * hd) + h * hd;
+  T* qdst = nullptr;
+  uint16_t* kdst = nullptr;
   if (is_q) {
-    dst = reinterpret_cast<uint16_t*>(q_out) + (static_cast<size_t>(t) * hq + h) * hd;
+    qdst = q_out + (static_cast<size_t>(t) * hq + h) * hd;
   } else {
     const int req = token_req[t];
     const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
-    dst = reinterpret_cast<uint16_t*>(kc) + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE +
-                                             pos % BI_PAGE_SIZE) * hd;
+    kdst = reinterpret_cast<uint16_t*>(kc) + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE +
+                                              pos % BI_PAGE_SIZE) * hd;
   }
   const float* c_row = rc + static_cast<size_t>(pos) * half;
   const float* s_row = rs + static_cast<size_t>(pos) * half;
@@ -97,9 +127,9 @@ __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
     float ss = 0.f;
     for (int j = lane; j < half / 2; j += 32) {
       const int i = 2 * j;
-      const uint32_t av = *reinterpret_cast<const uint32_t*>(src + i);
-      const uint32_t bv = *reinterpret_cast<const uint32_t*>(src + i + half);
-      const float x[4] = {bf16_lo(av), bf16_hi(av), bf16_lo(bv), bf16_hi(bv)};
+      const float2 av = QkvIo<F32>::ld2(src + i);
+      const float2 bv = QkvIo<F32>::ld2(src + i + half);
+      const float x[4] = {av.x, av.y, bv.x, bv.y};
 #pragma unroll
       for (int e = 0; e < 4; ++e) ss = __fadd_rn(ss, __fmul_rn(x[e], x[e]));
     }
@@ -109,25 +139,38 @@ __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
   }
   for (int j = lane; j < half / 2; j += 32) {
     const int i = 2 * j;
-    const uint32_t av = *reinterpret_cast<const uint32_t*>(src + i);
-    const uint32_t bv = *reinterpret_cast<const uint32_t*>(src + i + half);
+    const float2 av = QkvIo<F32>::ld2(src + i);
+    const float2 bv = QkvIo<F32>::ld2(src + i + half);
     const float2 c = *reinterpret_cast<const float2*>(c_row + i);
     const float2 sn = *reinterpret_cast<const float2*>(s_row + i);
-    float a0 = bf16_lo(av), a1 = bf16_hi(av), b0 = bf16_lo(bv), b1 = bf16_hi(bv);
+    float a0 = av.x, a1 = av.y, b0 = bv.x, b1 = bv.y;
     if (g != nullptr) {
       const uint32_t ga = *reinterpret_cast<const uint32_t*>(g + i);
       const uint32_t gb = *reinterpret_cast<const uint32_t*>(g + i + half);
-      a0 = round_bf16f(__fmul_rn(__fmul_rn(a0, r), bf16_lo(ga)));
-      a1 = round_bf16f(__fmul_rn(__fmul_rn(a1, r), bf16_hi(ga)));
-      b0 = round_bf16f(__fmul_rn(__fmul_rn(b0, r), bf16_lo(gb)));
-      b1 = round_bf16f(__fmul_rn(__fmul_rn(b1, r), bf16_hi(gb)));
+      a0 = __fmul_rn(__fmul_rn(a0, r), bf16_lo(ga));
+      a1 = __fmul_rn(__fmul_rn(a1, r), bf16_hi(ga));
+      b0 = __fmul_rn(__fmul_rn(b0, r), bf16_lo(gb));
+      b1 = __fmul_rn(__fmul_rn(b1, r), bf16_hi(gb));
+      if constexpr (!F32) {
+        a0 = round_bf16f(a0);
+        a1 = round_bf16f(a1);
+        b0 = round_bf16f(b0);
+        b1 = round_bf16f(b1);
+      }
     }
     const float lo0 = __fsub_rn(__fmul_rn(a0, c.x), __fmul_rn(b0, sn.x));
     const float lo1 = __fsub_rn(__fmul_rn(a1, c.y), __fmul_rn(b1, sn.y));
     const float hi0 = __fadd_rn(__fmul_rn(b0, c.x), __fmul_rn(a0, sn.x));
     const float hi1 = __fadd_rn(__fmul_rn(b1, c.y), __fmul_rn(a1, sn.y));
-    *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16x2(lo0, lo1);
-    *reinterpret_cast<uint32_t*>(dst + i + half) = pack_bf16x2(hi0, hi1);
+    if (kdst != nullptr || !F32) {
+      uint16_t* d = kdst != nullptr ? kdst : reinterpret_cast<uint16_t*>(qdst);
+      *reinterpret_cast<uint32_t*>(d + i) = pack_bf16x2(lo0, lo1);
+      *reinterpret_cast<uint32_t*>(d + i + half) = pack_bf16x2(hi0, hi1);
+    } else {
+      float* d = reinterpret_cast<float*>(qdst);
+      *reinterpret_cast<float2*>(d + i) = make_float2(lo0, lo1);
+      *reinterpret_cast<float2*>(d + i + half) = make_float2(hi0, hi1);
+    }
   }
 }
 
@@ -154,6 +197,47 @@ __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloat1
   }
 }
 
+// fp32 activations: gu fp32 [T][2F], out three bf16 planes [3][T][F]; the same
+// per-element arithmetic as the bf16 kernel.
+__global__ void swiglu_planes_kernel(const float* __restrict__ gu, uint16_t* __restrict__ out, int64_t T, int64_t F) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t chunks = F / 4;
+  const int64_t n = T * chunks;
+  const size_t plane = static_cast<size_t>(T) * F;
+  for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = k / chunks, c = k % chunks;
+    const float4 gv = *reinterpret_cast<const float4*>(gu + t * 2 * F + c * 4);
+    const float4 uv = *reinterpret_cast<const float4*>(gu + t * 2 * F + F + c * 4);
+    const float g[4] = {gv.x, gv.y, gv.z, gv.w};
+    const float u[4] = {uv.x, uv.y, uv.z, uv.w};
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float sg = __fdiv_rn(g[e], __fadd_rn(1.0f, expf(-g[e])));
+      o[e] = __fmul_rn(sg, u[e]);
+    }
+    store_planes4(out + t * F + c * 4, plane, o[0], o[1], o[2], o[3]);
+  }
+}
+
+// fp32 activations: the bf16 embedding row widened to fp32.
+__global__ void embed_f32_kernel(const int32_t* __restrict__ ids, const uint4* __restrict__ table,
+                                 float4* __restrict__ out, int64_t T, int64_t chunks_per_row, int64_t vocab) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t t = blockIdx.x;
+  if (t >= T) return;
+  const int64_t id = ids[t];
+  const bool ok = id >= 0 && id < vocab;
+  for (int64_t c = threadIdx.x; c < chunks_per_row; c += blockDim.x) {
+    const uint4 u = ok ? table[id * chunks_per_row + c] : make_uint4(0, 0, 0, 0);
+    out[(t * chunks_per_row + c) * 2] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    out[(t * chunks_per_row + c) * 2 + 1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+  }
+}
+
 }  // namespace
 
 bi_status embed_impl(const int32_t* ids, const void* table, void* out, int64_t T, int64_t d, int64_t vocab,
@@ -172,7 +256,7 @@ bi_status embed_impl(const int32_t* ids, const void* table, void* out, int64_t T
 bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs, const int32_t* token_pos,
                               const int32_t* token_req, const int32_t* block_table, int32_t T,
                               const bi_attn_dims* dm, void* q_out, void* kc, void* vc, cudaStream_t s,
-                              const void* q_norm, const void* k_norm, float eps) {
+                              const void* q_norm, const void* k_norm, float eps, bool act_f32) {
   BI_REQUIRE(dm && T >= 0, BI_ERR_INVALID_ARG, "bi_qkv_rope_store: dims/T");
   BI_REQUIRE(dm->head_dim % 16 == 0 && dm->head_dim >= 16 && dm->num_kv_heads >= 1 && dm->num_q_heads >= 1,
              BI_ERR_UNSUPPORTED, "bi_qkv_rope_store: head_dim %d", dm->head_dim);
@@ -184,11 +268,20 @@ bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs,
              "bi_qkv_rope_store: misaligned pointer");
   BI_REQUIRE((q_norm == nullptr) == (k_norm == nullptr) && (q_norm == nullptr || (aligned16(q_norm) && aligned16(k_norm))),
              BI_ERR_INVALID_ARG, "layer: q_norm and k_norm must be both null or both 16-byte aligned");
-  BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel, dim3(T, (dm->num_q_heads + 2 * dm->num_kv_heads + 7) / 8), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
-                                          block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
-                                          static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(kc),
-                                          static_cast<__nv_bfloat16*>(vc), static_cast<const __nv_bfloat16*>(q_norm),
-                                          static_cast<const __nv_bfloat16*>(k_norm), eps)));
+  const dim3 grid(T, (dm->num_q_heads + 2 * dm->num_kv_heads + 7) / 8);
+  if (act_f32) {
+    BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel<true>, grid, dim3(256), 0, s, static_cast<const float*>(qkv), rc, rs, token_pos, token_req,
+                                            block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
+                                            static_cast<float*>(q_out), static_cast<__nv_bfloat16*>(kc),
+                                            static_cast<__nv_bfloat16*>(vc), static_cast<const __nv_bfloat16*>(q_norm),
+                                            static_cast<const __nv_bfloat16*>(k_norm), eps)));
+  } else {
+    BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel<false>, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
+                                            block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
+                                            static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(kc),
+                                            static_cast<__nv_bfloat16*>(vc), static_cast<const __nv_bfloat16*>(q_norm),
+                                            static_cast<const __nv_bfloat16*>(k_norm), eps)));
+  }
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -202,6 +295,34 @@ bi_status swiglu_impl(const void* gu, void* out, int64_t T, int64_t F, cudaStrea
   const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 16);
   BI_TIMED(::bi::kTagSwiglu, s, BI_PDL_CHECK(launch_pdl(swiglu_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(gu),
                                                             static_cast<__nv_bfloat16*>(out), T, F)));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+// fp32 activations: gu fp32 [T][2F] -> three bf16 planes [3][T][F].
+bi_status swiglu_planes_impl(const void* gu, void* out, int64_t T, int64_t F, cudaStream_t s) {
+  BI_REQUIRE(T >= 0 && F > 0 && F % 8 == 0, BI_ERR_INVALID_ARG, "swiglu: T=%lld F=%lld", static_cast<long long>(T),
+             static_cast<long long>(F));
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(gu && out && aligned16(gu) && aligned16(out), BI_ERR_INVALID_ARG, "swiglu: null or misaligned");
+  const int64_t n = T * (F / 4);
+  const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(num_sms()) * 16);
+  BI_TIMED(::bi::kTagSwiglu, s, BI_PDL_CHECK(launch_pdl(swiglu_planes_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, static_cast<const float*>(gu),
+                                                            static_cast<uint16_t*>(out), T, F)));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
+}
+
+// fp32 activations: embedding rows (bf16 table) widened to fp32 [T][d].
+bi_status embed_f32_impl(const int32_t* ids, const void* table, void* out, int64_t T, int64_t d, int64_t vocab,
+                         cudaStream_t s) {
+  BI_REQUIRE(T >= 0 && d > 0 && d % 8 == 0 && vocab > 0, BI_ERR_INVALID_ARG, "embed: T=%lld d=%lld vocab=%lld",
+             static_cast<long long>(T), static_cast<long long>(d), static_cast<long long>(vocab));
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(ids && table && out && aligned16(table) && aligned16(out), BI_ERR_INVALID_ARG,
+             "embed: null or misaligned pointer");
+  BI_TIMED(::bi::kTagEmbed, s, BI_PDL_CHECK(launch_pdl(embed_f32_kernel, dim3(static_cast<unsigned>(T)), dim3(128), 0, s, ids, static_cast<const uint4*>(table), static_cast<float4*>(out),
+                                                        T, d / 8, vocab)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -238,7 +359,7 @@ extern "C" bi_status bi_qkv_rope_store(const void* qkv, const float* rope_cos, c
                                        bi_stream s) {
   bi::clear_error();
   return bi::qkv_rope_store_impl(qkv, rope_cos, rope_sin, token_pos, token_req, block_table, T, dims, q_out, k_cache,
-                                 v_cache, reinterpret_cast<cudaStream_t>(s), nullptr, nullptr, 0.f);
+                                 v_cache, reinterpret_cast<cudaStream_t>(s), nullptr, nullptr, 0.f, false);
 }
 
 extern "C" bi_status bi_swiglu(const void* gu, void* out, int64_t T, int64_t F, bi_stream s) {

@@ -15,6 +15,9 @@
 // FAST (the non-invariant schedule the pages describe): when there are fewer
 // rows than SMs, each row is split over several CTAs whose partial sums are
 // combined in a second pass, so a row's reduction order depends on the batch.
+//
+// fp32-activation layers: x fp32, gamma bf16 (weights stay 16-bit), y written
+// as three bf16 planes for the GEMM that consumes it (common.cuh).
 #include "common.cuh"
 
 namespace bi {
@@ -44,11 +47,27 @@ __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&f)[8]) 
   uint4 u = *reinterpret_cast<const uint4*>(p);
   unpack8(u, f);
 }
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&f)[4]) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+}
 __device__ __forceinline__ void store_vec(float* p, const float (&f)[4]) {
   *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
 }
 __device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&f)[8]) {
   *reinterpret_cast<uint4*>(p) = pack8(f);
+}
+
+// Output of V values at element offset off of row y: the input type, or
+// (PL, fp32 input) three bf16 planes `plane` elements apart.
+template <typename TX, bool PL, int V>
+__device__ __forceinline__ void store_out(void* y, size_t plane, size_t off, const float (&o)[V]) {
+  if constexpr (PL) {
+    static_assert(V == 4, "planes are written from fp32 rows");
+    store_planes4(static_cast<uint16_t*>(y) + off, plane, o[0], o[1], o[2], o[3]);
+  } else {
+    store_vec(static_cast<TX*>(y) + off, o);
+  }
 }
 
 // Fixed xor-butterfly: every lane ends with the same bits (fp add commutes).
@@ -70,11 +89,12 @@ __device__ __forceinline__ float inv_rms(float sumsq, int d, float eps) {
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 }
 
-// The invariant computation of one row by one CTA of kThreads threads.
-template <typename T>
-__device__ __forceinline__ void rms_row(const T* __restrict__ x, const T* __restrict__ gamma, T* y, int d, float eps,
-                                        float* red) {
-  constexpr int V = VecOf<T>::N;
+// The invariant computation of one row by one CTA of kThreads threads; y and
+// plane: the row's output (element offsets within it as for x).
+template <typename TX, typename TG, bool PL>
+__device__ __forceinline__ void rms_row(const TX* __restrict__ x, const TG* __restrict__ gamma, void* y, size_t plane,
+                                        int d, float eps, float* red) {
+  constexpr int V = VecOf<TX>::N;
   const int nchunks = d / V;
   const int t = threadIdx.x;
   float xs[kMaxChunks][V];
@@ -101,30 +121,37 @@ __device__ __forceinline__ void rms_row(const T* __restrict__ x, const T* __rest
       load_vec(gamma + static_cast<size_t>(c) * V, g);
 #pragma unroll
       for (int e = 0; e < V; ++e) o[e] = __fmul_rn(__fmul_rn(xs[i][e], r), g[e]);
-      store_vec(y + static_cast<size_t>(c) * V, o);
+      store_out<TX, PL, V>(y, plane, static_cast<size_t>(c) * V, o);
     }
   }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) rms_invariant_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
-                                                                 T* y, int64_t row_begin, int64_t row_end, int d,
-                                                                 float eps) {
+// Output row r of y (the row's first element; planes share the row offset).
+template <typename TX, bool PL>
+__device__ __forceinline__ void* out_row(void* y, int64_t r, int d) {
+  if constexpr (PL) return static_cast<uint16_t*>(y) + r * d;
+  else return static_cast<TX*>(y) + r * d;
+}
+
+template <typename TX, typename TG, bool PL>
+__global__ void __launch_bounds__(kThreads) rms_invariant_kernel(const TX* __restrict__ x, const TG* __restrict__ gamma,
+                                                                 void* y, size_t plane, int64_t row_begin,
+                                                                 int64_t row_end, int d, float eps) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[kWarps];
   for (int64_t r = row_begin + blockIdx.x; r < row_end; r += gridDim.x)
-    rms_row(x + r * d, gamma, y + r * d, d, eps, red);
+    rms_row<TX, TG, PL>(x + r * d, gamma, out_row<TX, PL>(y, r, d), plane, d, eps, red);
 }
 
 // FAST pass 1: CTA (row, s) sums the squares of chunk range s of its row.
-template <typename T>
-__global__ void __launch_bounds__(kSplitThreads) rms_split_partial_kernel(const T* __restrict__ x, float* partial,
+template <typename TX>
+__global__ void __launch_bounds__(kSplitThreads) rms_split_partial_kernel(const TX* __restrict__ x, float* partial,
                                                                           int64_t rows, int d, int splits,
                                                                           int64_t skip_begin, int64_t skip_end) {
   pdl_wait();
   pdl_trigger();
-  constexpr int V = VecOf<T>::N;
+  constexpr int V = VecOf<TX>::N;
   const int64_t r = blockIdx.x / splits;
   const int s = blockIdx.x % splits;
   if (r >= rows || (r >= skip_begin && r < skip_end)) return;
@@ -151,19 +178,21 @@ __global__ void __launch_bounds__(kSplitThreads) rms_split_partial_kernel(const 
 
 // FAST pass 2: one CTA per row; split rows add their partials left to right,
 // rows in [inv_begin, inv_end) run the invariant row function instead.
-template <typename T>
-__global__ void __launch_bounds__(kThreads) rms_split_finish_kernel(const T* __restrict__ x, const T* __restrict__ gamma,
-                                                                    T* y, const float* partial, int64_t rows, int d,
+template <typename TX, typename TG, bool PL>
+__global__ void __launch_bounds__(kThreads) rms_split_finish_kernel(const TX* __restrict__ x,
+                                                                    const TG* __restrict__ gamma, void* y, size_t plane,
+                                                                    const float* partial, int64_t rows, int d,
                                                                     int splits, float eps, int64_t inv_begin,
                                                                     int64_t inv_end) {
   pdl_wait();
   pdl_trigger();
-  constexpr int V = VecOf<T>::N;
+  constexpr int V = VecOf<TX>::N;
   __shared__ float red[kWarps];
   const int64_t r = blockIdx.x;
   if (r >= rows) return;
+  void* yr = out_row<TX, PL>(y, r, d);
   if (r >= inv_begin && r < inv_end) {
-    rms_row(x + r * d, gamma, y + r * d, d, eps, red);
+    rms_row<TX, TG, PL>(x + r * d, gamma, yr, plane, d, eps, red);
     return;
   }
   float tot = 0.f;
@@ -176,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) rms_split_finish_kernel(const T* __r
     load_vec(gamma + static_cast<int64_t>(c) * V, g);
 #pragma unroll
     for (int e = 0; e < V; ++e) o[e] = __fmul_rn(__fmul_rn(f[e], rr), g[e]);
-    store_vec(y + r * d + static_cast<int64_t>(c) * V, o);
+    store_out<TX, PL, V>(yr, plane, static_cast<size_t>(c) * V, o);
   }
 }
 
@@ -188,18 +217,18 @@ int fast_splits(int64_t rows, int d, int vec) {
   return max(1, min(by_sms, by_work));
 }
 
-template <typename T>
-bi_status launch(const void* xv, const void* gv, void* yv, int64_t rows, int d, float eps, bi_mode mode,
+template <typename TX, typename TG, bool PL>
+bi_status launch(const void* xv, const void* gv, void* y, int64_t rows, int d, float eps, bi_mode mode,
                  int64_t tb, int64_t te, void* ws, size_t ws_bytes, cudaStream_t s) {
-  const T* x = static_cast<const T*>(xv);
-  const T* g = static_cast<const T*>(gv);
-  T* y = static_cast<T*>(yv);
-  constexpr int V = VecOf<T>::N;
+  const TX* x = static_cast<const TX*>(xv);
+  const TG* g = static_cast<const TG*>(gv);
+  const size_t plane = static_cast<size_t>(rows) * d;
+  constexpr int V = VecOf<TX>::N;
   const int splits = mode_invariant(mode) ? 1 : fast_splits(rows, d, V);
   if (splits == 1) {
     // Unsplit: the data-parallel schedule, identical to INVARIANT for every row.
     const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(num_sms()) * 8);
-    BI_TIMED(::bi::kTagRmsnorm, s, BI_PDL_CHECK(launch_pdl(rms_invariant_kernel<T>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, x, g, y, 0, rows, d, eps)));
+    BI_TIMED(::bi::kTagRmsnorm, s, BI_PDL_CHECK(launch_pdl(rms_invariant_kernel<TX, TG, PL>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, x, g, y, plane, int64_t(0), rows, d, eps)));
     BI_LAUNCH_CHECK();
     return BI_OK;
   }
@@ -207,10 +236,10 @@ bi_status launch(const void* xv, const void* gv, void* yv, int64_t rows, int d, 
   BI_REQUIRE(ws != nullptr && ws_bytes >= need, BI_ERR_WORKSPACE, "bi_rmsnorm: workspace %zu < %zu bytes", ws_bytes,
              need);
   float* partial = static_cast<float*>(ws);
-  BI_TIMED(::bi::kTagRmsnormSplit, s, BI_PDL_CHECK(launch_pdl(rms_split_partial_kernel<T>, dim3(static_cast<unsigned>(rows * splits)), dim3(kSplitThreads), 0, s, x, partial, rows, d,
+  BI_TIMED(::bi::kTagRmsnormSplit, s, BI_PDL_CHECK(launch_pdl(rms_split_partial_kernel<TX>, dim3(static_cast<unsigned>(rows * splits)), dim3(kSplitThreads), 0, s, x, partial, rows, d,
                                                                                              splits, tb, te)));
   BI_LAUNCH_CHECK();
-  BI_TIMED(::bi::kTagRmsnormSplit, s, BI_PDL_CHECK(launch_pdl(rms_split_finish_kernel<T>, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, s, x, g, y, partial, rows, d, splits, eps,
+  BI_TIMED(::bi::kTagRmsnormSplit, s, BI_PDL_CHECK(launch_pdl(rms_split_finish_kernel<TX, TG, PL>, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, s, x, g, y, plane, partial, rows, d, splits, eps,
                                                                               tb, te)));
   BI_LAUNCH_CHECK();
   return BI_OK;
@@ -252,8 +281,26 @@ bi_status rmsnorm_impl(const void* x, const void* gamma, void* y, int64_t rows, 
   BI_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(y), BI_ERR_INVALID_ARG,
              "bi_rmsnorm: pointers must be 16-byte aligned");
   if (dtype == BI_F32)
-    return launch<float>(x, gamma, y, rows, static_cast<int>(d), eps, mode, tb, te, ws, ws_bytes, s);
-  return launch<__nv_bfloat16>(x, gamma, y, rows, static_cast<int>(d), eps, mode, tb, te, ws, ws_bytes, s);
+    return launch<float, float, false>(x, gamma, y, rows, static_cast<int>(d), eps, mode, tb, te, ws, ws_bytes, s);
+  return launch<__nv_bfloat16, __nv_bfloat16, false>(x, gamma, y, rows, static_cast<int>(d), eps, mode, tb, te, ws,
+                                                     ws_bytes, s);
+}
+
+// fp32-activation layers: x fp32 [rows][d], gamma bf16 [d], y three bf16 planes
+// [3][rows][d] (rows*d elements apart).  Same reduction order as bi_rmsnorm on
+// fp32 rows.
+bi_status rmsnorm_planes_impl(const void* x, const void* gamma, void* y, int64_t rows, int64_t d, float eps,
+                              bi_mode mode, int32_t target_row, int32_t target_count, void* ws, size_t ws_bytes,
+                              cudaStream_t s) {
+  BI_REQUIRE(rows >= 0 && d > 0 && d % 4 == 0 && d / 4 <= kThreads * kMaxChunks, BI_ERR_UNSUPPORTED,
+             "rmsnorm (fp32 activations): rows=%lld d=%lld", static_cast<long long>(rows), static_cast<long long>(d));
+  BI_REQUIRE(mode_valid(mode), BI_ERR_INVALID_ARG, "rmsnorm: mode %d", static_cast<int>(mode));
+  int64_t tb, te;
+  BI_TRY(check_target(mode, rows, target_row, target_count, &tb, &te));
+  if (rows == 0) return BI_OK;
+  BI_REQUIRE(x && gamma && y && aligned16(x) && aligned16(gamma) && aligned16(y), BI_ERR_INVALID_ARG,
+             "rmsnorm (fp32 activations): null or misaligned pointer");
+  return launch<float, __nv_bfloat16, true>(x, gamma, y, rows, static_cast<int>(d), eps, mode, tb, te, ws, ws_bytes, s);
 }
 
 size_t rmsnorm_ws(int64_t rows, int64_t d, bi_mode mode) {

@@ -61,13 +61,15 @@ class PagePool:
 
 
 class BiModel:
-    def __init__(self, shape: ModelShape, weights: dict, num_pages: int, device="cuda", page_seed: int | None = None):
+    def __init__(self, shape: ModelShape, weights: dict, num_pages: int, device="cuda", page_seed: int | None = None,
+                 act_f32: bool = False):
+        """act_f32: fp32 activations with the same bf16 weights and bf16 KV cache."""
         self.shape = shape
         self.device = device
         L = shape.layer
         self.w = weights
         self.dims = ModelDims(L.d_model, L.n_q_heads, L.n_kv_heads, L.head_dim, L.ffn_dim, shape.vocab, PAGE_SIZE,
-                              shape.max_pos, L.rms_eps)
+                              shape.max_pos, L.rms_eps, 1 if act_f32 else 0)
         self.rope_cos = torch.empty((shape.max_pos, L.head_dim // 2), dtype=torch.float32, device=device)
         self.rope_sin = torch.empty_like(self.rope_cos)
         bi_rope_table(L.rope_theta, L.head_dim, shape.max_pos, self.rope_cos, self.rope_sin)
@@ -123,8 +125,9 @@ class BiModel:
                                                                             device=device), "lm_head": head}
 
     @classmethod
-    def random(cls, shape: ModelShape, seed: int, device="cuda", num_pages: int = 512, page_seed: int | None = 3):
-        return cls(shape, cls.random_weights(shape, seed, device), num_pages, device, page_seed)
+    def random(cls, shape: ModelShape, seed: int, device="cuda", num_pages: int = 512, page_seed: int | None = 3,
+               act_f32: bool = False):
+        return cls(shape, cls.random_weights(shape, seed, device), num_pages, device, page_seed, act_f32)
 
     def host_weights(self):
         """float64 numpy copies of the weights (for the oracle on small models)."""

@@ -85,3 +85,23 @@ def test_ksplit_part_count_depends_on_weight_shape_only(libpath):
     assert l.bi_gemm_workspace(64, 4096, 4096, bi.INVARIANT) == 0
     # an out-of-range mode is rejected on the host
     assert l.bi_gemm(None, None, None, None, 4, 8, 16, bi.BI_BF16, 4, -1, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+
+
+def test_fp32_activation_entry_points_validate_and_size_on_the_host(libpath):
+    import invariant_deterministic_02_gb300 as bi
+    l = bi.lib()
+    planes = lambda M, K: (3 * M * K * 2 + 255) // 256 * 256  # noqa: E731  three bf16 planes of A, 256-byte aligned
+    assert l.bi_gemm_f32a_workspace(64, 4096, 4096, bi.INVARIANT) == planes(64, 4096)
+    assert l.bi_gemm_f32a_workspace(64, 4096, 4096, bi.INVARIANT_KSPLIT) == planes(64, 4096) + 9 * 64 * 4096 * 4
+    assert l.bi_gemm_f32a_workspace(0, 4096, 4096, bi.INVARIANT) == 0
+    assert l.bi_gemm_f32a(None, None, None, None, 0, 8, 16, 0, -1, 0, None, 0, None) == bi.BI_OK
+    assert l.bi_gemm_f32a(None, None, None, None, 4, 8, 7, 0, -1, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert l.bi_gemm_f32a(None, None, None, None, 4, 8, 16, 9, -1, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert l.bi_gemm_f32a(None, None, None, None, 4, 8, 16, 0, -1, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    # act_f32 is a trailing field of both dims structs; zero keeps bf16 activations
+    assert ctypes.sizeof(bi.AttnDims) == 8 * 4 and ctypes.sizeof(bi.ModelDims) == 10 * 4
+    dims = [bi.ModelDims(256, 4, 2, 64, 512, 512, 16, 2048, 1e-5, a) for a in (0, 1, 2)]
+    qs = (ctypes.c_int32 * 2)(0, 4)
+    batch = bi.Batch(1, 4, 4, ctypes.addressof(qs), ctypes.addressof(qs), ctypes.addressof(qs), 1, 1, -1, 0, 0)
+    w16, w32, bad = [l.bi_layer_workspace(ctypes.byref(d), ctypes.byref(batch), 0) for d in dims]
+    assert w32 > w16 > 0 and bad == 0

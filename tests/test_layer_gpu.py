@@ -17,15 +17,16 @@ PS = 16
 class LayerRig:
     """One layer's weights, RoPE tables and a paged cache holding per-request histories."""
 
-    def __init__(self, shape, seed, max_pos=8192, num_pages=4096, gamma_std=0.1):
+    def __init__(self, shape, seed, max_pos=8192, num_pages=4096, gamma_std=0.1, act_f32=False):
         self.shape = shape
+        self.act_f32 = act_f32  # hidden states fp32 (fp32-activation layer) instead of bf16
         self.w_host = synth.layer_weights(shape, seed, std=0.02, gamma_std=gamma_std)
         self.w = {k: cuda(v) for k, v in self.w_host.items()}
         self.lw = bi.LayerWeights(*[self.w[k].data_ptr() for k in
                                     ("attn_norm", "w_qkv", "w_o", "ffn_norm", "w_gate_up", "w_down")],
                                   *[self.w[k].data_ptr() if k in self.w else None for k in ("q_norm", "k_norm")])
         self.dims = bi.ModelDims(shape.d_model, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn_dim, 8,
-                                 PS, max_pos, shape.rms_eps)
+                                 PS, max_pos, shape.rms_eps, 1 if act_f32 else 0)
         half = shape.head_dim // 2
         self.cos = torch.empty((max_pos, half), dtype=torch.float32, device="cuda")
         self.sin = torch.empty_like(self.cos)
@@ -47,7 +48,7 @@ class LayerRig:
         self.hist[req] = (f64(K), f64(V))
 
     def run(self, h, items, mode=bi.INVARIANT, target=-1):
-        """items: list of (request, n_tokens, pos0).  h: [T][d] bf16 (cuda), updated in place."""
+        """items: list of (request, n_tokens, pos0).  h: [T][d] bf16, or fp32 with act_f32 (cuda), updated in place."""
         B = len(items)
         counts = [n for _, n, _ in items]
         qs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
@@ -72,7 +73,7 @@ class LayerRig:
             kv.set(0, r, K[:p0], V[:p0])
         w = {k: f64(v) for k, v in self.w_host.items()}
         return oracle.layer_forward(f64(h_in), w, self.shape, kv, 0, [(r, n) for r, n, _ in items],
-                                    [p for _, _, p in items])
+                                    [p for _, _, p in items], act32=self.act_f32)
 
 
 @pytest.mark.parametrize("shape", [synth.TINY_LAYER, synth.TINY_QK_LAYER], ids=["plain", "qk_norm"])
