@@ -25,8 +25,10 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
-    a = a.detach().contiguous().cpu()
-    b = b.detach().contiguous().cpu()
+    # a fresh dense copy: .contiguous() keeps the stride of a size-1 dimension,
+    # which a byte view does not accept
+    a = torch.empty_like(a, device="cpu", memory_format=torch.contiguous_format).copy_(a.detach())
+    b = torch.empty_like(b, device="cpu", memory_format=torch.contiguous_format).copy_(b.detach())
     if a.shape != b.shape or a.dtype != b.dtype:
         return False
     return bool(torch.equal(a.view(torch.uint8), b.view(torch.uint8)))

@@ -19,11 +19,19 @@ from invariant_deterministic_02_gb300.model import BiModel, ModelShape  # noqa: 
 F32 = torch.float32
 
 # Tolerances of the fp32-activation path, against the float64 oracle:
-# GEMM: the three plane products are exact and accumulate in fp32; the running
-#   sum is rounded about once per K=16 instruction (<= 2^-24 of its size), so
-#   over K <= 12288 the error is ~1e-6 of rms(C); 4e-5 covers the maximum over
-#   millions of elements.
-TOL_GEMM32 = 4e-5
+# GEMM: the three plane products are exact; the tensor cores add each
+#   instruction's products into the fp32 accumulator with an error of up to one
+#   unit in the last place of the running sum (the measured maximum error grows
+#   linearly with K, as truncation does), so after n = 3*ceil(K/16) instructions
+#   the error is below n * 2^-23 of the sums' size: 9.2e-5 at K = 4096, 2.7e-4
+#   at K = 12288 (measured maxima: 4.1e-5 and 1.2e-4).  Activations rounded to
+#   bf16 first are off by ~2^-9 per element, several 1e-3 on C.
+
+
+def tol_gemm32(K):
+    return 3 * -(-K // 16) * 2.0 ** -23
+
+
 # Attention: a score is an fp32 dot product of head_dim terms of size ~1 (sums
 #   ~10), rounded to ~1e-5 absolute, which enters the softmax weights as a
 #   relative error of that order.
@@ -77,7 +85,7 @@ def test_random_parity_and_gain_over_bf16_activations(M, N, K):
     exact = oracle.gemm(f64(A), f64(W))
     C = gemm32(cuda(A), cuda(W))
     err32 = max_rel_err(f64(C), exact)
-    assert err32 <= TOL_GEMM32
+    assert err32 <= tol_gemm32(K)
     # the same product with the activations rounded to bf16 first is far off
     Cb = torch.empty((M, N), dtype=F32, device="cuda")
     bi.bi_gemm(cuda(A).to(torch.bfloat16), cuda(W), Cb)
@@ -91,7 +99,7 @@ def test_fp32_residual_in_place():
     W = synth.normal((N, K), 52, std=0.02)
     R = synth.normal((M, N), 53, dtype=F32)
     C = gemm32(cuda(A), cuda(W), R=cuda(R))
-    assert max_rel_err(f64(C), oracle.gemm(f64(A), f64(W)) + f64(R)) <= TOL_GEMM32
+    assert max_rel_err(f64(C), oracle.gemm(f64(A), f64(W)) + f64(R)) <= tol_gemm32(K)
     Rc = cuda(R)
     bi.bi_gemm_f32a(cuda(A), cuda(W), Rc, residual=Rc)
     torch.cuda.synchronize()
@@ -117,9 +125,9 @@ def test_row0_bitwise_across_M_and_modes():
             rowp = gemm32(A, W, mode=bi.PROTECTED, tr=0, tc=1)[0:1]
             assert bits_equal(rowp, ref), M
             Cf = gemm32(A, W, mode=bi.FAST)
-            assert max_rel_err(f64(Cf[:4]), oracle.gemm(f64(A[:4]), f64(W))) <= TOL_GEMM32
-    assert max_rel_err(f64(ref), oracle.gemm(f64(target), f64(W))) <= TOL_GEMM32
-    assert max_rel_err(f64(refk), oracle.gemm(f64(target), f64(W))) <= TOL_GEMM32
+            assert max_rel_err(f64(Cf[:4]), oracle.gemm(f64(A[:4]), f64(W))) <= tol_gemm32(K)
+    assert max_rel_err(f64(ref), oracle.gemm(f64(target), f64(W))) <= tol_gemm32(K)
+    assert max_rel_err(f64(refk), oracle.gemm(f64(target), f64(W))) <= tol_gemm32(K)
 
 
 # ---------------------------------------------------------------- attention with fp32 q
@@ -284,7 +292,7 @@ def test_tiny_model_parity():
 def test_tiny_model_greedy_bit_exact_across_compositions():
     from tests.test_model_gpu import assert_same, greedy_run
     shape = tiny_shape()
-    m = BiModel.random(shape, seed=14, num_pages=16384, page_seed=6, act_f32=True)
+    m = BiModel.random(shape, seed=14, num_pages=40000, page_seed=6, act_f32=True)
     prompt = synth.token_ids(64, shape.vocab, 4321)
     ref = greedy_run(m, prompt, 20, [64], 0, 0, 0, seed=2)
     for i, (chunks, nb, slot, dnb) in enumerate([([64], 3, 1, 5), ([7, 57], 2, 2, 63)]):
