@@ -86,8 +86,7 @@ struct Args {
   const __nv_bfloat16* R;  // residual or null
   float* partial;          // [splits][M][N] fp32 (split units only)
   int out_kind;
-  int planes;              // 1: bf16 A; 3: fp32 A as three bf16 planes of plane_rows rows each
-  int plane_rows;
+  int plane_rows;          // rows of each A plane (three planes for fp32 A; the kernel's PL)
   const float* Rf;         // fp32 residual (fp32 output) or null
 };
 
@@ -287,7 +286,9 @@ __host__ __device__ constexpr size_t smem_bytes(int stages, int stage_bytes, int
          (a_rows < kBM ? kOverreadSlack : 0);
 }
 
-template <int TN>
+// PL: planes of A (1: bf16 A; 3: fp32 A as three bf16 planes).  A compile-time
+// count keeps the one-plane kernel free of the plane loops on its latency path.
+template <int TN, int PL>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                               const __grid_constant__ CUtensorMap tmW, const Args a) {
   extern __shared__ unsigned char smem_raw[];
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const int a_tile = a.a_rows * kBK * 2;      // one k-block of A
   const int b_tile = TN * kBK * 2;            // one k-block of B
   const int a_plane = kbs * a_tile;           // one plane of A in a stage
-  const int a_bytes = a.planes * a_plane;     // A part of a stage
+  const int a_bytes = PL * a_plane;           // A part of a stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   unsigned char* tiles = smem + kBarBlock;
   // bars: full[kMaxStages], empty[kMaxStages], tfull[2], tempty[2], drain
@@ -380,25 +381,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           for (int kb = kb0; kb < kb1; kb += kbs) {
             const uint32_t fb = full0 + 8 * st;
             const uint32_t sa = smem_u32(tiles + st * kStageBytes);
-            // W of a prefetched stage is already on its way (issued before the wait): add A only
-            const bool fresh = pre_stages == 0;
-            if (!fresh) {
+            if (pre_stages > 0) {
+              // W of this stage is already on its way (issued before the wait): add A only
               --pre_stages;
+#pragma unroll
+              for (int pl = 0; pl < PL; ++pl) {
+                if (a.map3d) tma_load_3d(sa + pl * a_plane, &tmA, fb, 0, pl * a.plane_rows + mt * kBM, kb);
+                else tma_load_2d(sa + pl * a_plane, &tmA, fb, kb * kBK, pl * a.plane_rows + mt * kBM);
+              }
             } else {
               if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
                 ok = false;
                 break;
               }
               mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
-            }
-            for (int pl = 0; pl < a.planes; ++pl) {
-              const int arow = pl * a.plane_rows + mt * kBM;
-              if (a.map3d) tma_load_3d(sa + pl * a_plane, &tmA, fb, 0, arow, kb);
-              else tma_load_2d(sa + pl * a_plane, &tmA, fb, kb * kBK, arow);
-            }
-            if (fresh) {
-              if (a.map3d) tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
-              else tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
+              if (a.map3d) {
+#pragma unroll
+                for (int pl = 0; pl < PL; ++pl)
+                  tma_load_3d(sa + pl * a_plane, &tmA, fb, 0, pl * a.plane_rows + mt * kBM, kb);
+                tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
+              } else {
+#pragma unroll
+                for (int pl = 0; pl < PL; ++pl)
+                  tma_load_2d(sa + pl * a_plane, &tmA, fb, kb * kBK, pl * a.plane_rows + mt * kBM);
+                tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
+              }
             }
             issued_mask |= 1u << st;
             issued_par = (issued_par & ~(1u << st)) | (ph << st);
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
               const uint64_t adesc = sdesc + static_cast<uint64_t>((j * a_tile) >> 4);
               const uint64_t bdesc = sdesc + static_cast<uint64_t>((a_bytes + j * b_tile) >> 4);
               const uint32_t first = (kb + j == kb0) ? 1u : 0u;
-              if (a.planes == 1) {
+              if constexpr (PL == 1) {
 #pragma unroll
                 for (int k = 0; k < kBK / kUK; ++k) {
                   // the first instruction of a pass overwrites the accumulator, all others add;
@@ -469,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 // fp32 A: per k16 step the planes hi, mid, lo in order, same B operand
 #pragma unroll
                 for (int k = 0; k < kBK / kUK; ++k) {
-                  for (int pl = 0; pl < a.planes; ++pl) {
+#pragma unroll
+                  for (int pl = 0; pl < PL; ++pl) {
                     const uint32_t accum = (k > 0 || pl > 0 || !first) ? 1u : 0u;
                     tc_mma(d0, adesc + static_cast<uint64_t>(((pl * a_plane) >> 4) + 2 * k),
                            bdesc + static_cast<uint64_t>(2 * k), kIdescW, accum);
@@ -555,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                                 __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
           } else if (a.out_kind == kOutF32) {
             float* dst = static_cast<float*>(a.C) + static_cast<size_t>(row) * a.N + col0;
-            const float* res = a.Rf ? a.Rf + static_cast<size_t>(row) * a.N + col0 : nullptr;
+            // fp32 residual: fp32-activation layers only
+            const float* res = (PL > 1 && a.Rf) ? a.Rf + static_cast<size_t>(row) * a.N + col0 : nullptr;
 #pragma unroll
             for (int g = 0; g < 8; ++g)
               if (col0 + 4 * g < a.N) {
@@ -890,16 +899,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   return p;
 }
 
-template <int TN>
+template <int TN, int PL>
 bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
+    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<TN, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
     attr = true;
   }
   const size_t smem = smem_bytes(args.stages, args.stage_bytes, args.a_rows);
   const int grid = std::min(args.units, num_sms());
-  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<TN>, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
+  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<TN, PL>, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
@@ -989,7 +998,6 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   args.C = C;
   args.R = static_cast<const __nv_bfloat16*>(R);
   args.Rf = Rf;
-  args.planes = planes;
   args.plane_rows = static_cast<int>(M);
   args.out_kind = out_dtype == BI_F32 ? gemm::kOutF32 : gemm::kOutBF16;
   args.partial = nullptr;
@@ -1004,11 +1012,19 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   BI_TRY(gemm::tensor_map(A, planes * M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
   BI_TRY(gemm::tensor_map(Wt, N, K, p.TN, p.map3d ? p.kbs : 0, &mw));
   bi_status st;
-  if (p.TN == 256) st = gemm::launch_w<256>(ma, mw, args, s);
-  else if (p.TN == 192) st = gemm::launch_w<192>(ma, mw, args, s);
-  else if (p.TN == 128) st = gemm::launch_w<128>(ma, mw, args, s);
-  else if (p.TN == 64) st = gemm::launch_w<64>(ma, mw, args, s);
-  else st = gemm::launch_w<32>(ma, mw, args, s);
+  if (planes == 1) {
+    if (p.TN == 256) st = gemm::launch_w<256, 1>(ma, mw, args, s);
+    else if (p.TN == 192) st = gemm::launch_w<192, 1>(ma, mw, args, s);
+    else if (p.TN == 128) st = gemm::launch_w<128, 1>(ma, mw, args, s);
+    else if (p.TN == 64) st = gemm::launch_w<64, 1>(ma, mw, args, s);
+    else st = gemm::launch_w<32, 1>(ma, mw, args, s);
+  } else {
+    if (p.TN == 256) st = gemm::launch_w<256, 3>(ma, mw, args, s);
+    else if (p.TN == 192) st = gemm::launch_w<192, 3>(ma, mw, args, s);
+    else if (p.TN == 128) st = gemm::launch_w<128, 3>(ma, mw, args, s);
+    else if (p.TN == 64) st = gemm::launch_w<64, 3>(ma, mw, args, s);
+    else st = gemm::launch_w<32, 3>(ma, mw, args, s);
+  }
   if (st != BI_OK) return st;
   if (p.splits > 1) {
     const int64_t n = M * (N / 4);
