@@ -114,6 +114,28 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------------- replicas (N > 1)
+def replica_seeds(seed: int, rank: int) -> dict:
+    """Seeds of one rank's replica: its own weights, KV lengths and cached
+    histories, so every rank decodes a different batch (no data is shared)."""
+    return {"weights": seed + 1000 * rank, "kv_lens": seed + 17 * rank, "history": seed * 7919 + rank}
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of the ranks' values: the job takes as long as its slowest rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(batch: int, world: int, steps: int, seconds: float) -> float:
+    """Tokens per second of the whole job: every rank decodes `batch` tokens per step."""
+    return batch * world * steps / seconds
+
+
 # ---------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -128,16 +150,17 @@ def run_ours(args, rank, world, local_rank):
     B = args.batch
     K, W = args.steps, args.warmup
     shape = QWEN3_8B
-    Ls = synth.uniform_ints(B, KV_LO, KV_HI, args.seed + 17 * rank)  # KV length at the first step
+    seeds = replica_seeds(args.seed, rank)
+    Ls = synth.uniform_ints(B, KV_LO, KV_HI, seeds["kv_lens"])  # KV length at the first step
     compare = [m for m in ("fast", "invariant_ksplit") if m != args.mode] if args.mode == "invariant" else []
     act32 = args.mode == "invariant"  # also time the fp32-activation variant of the same step
     # warm-up, timed, profiled, end-to-end, other modes, fp32 activations
     total_steps = W + 2 * K + K + len(compare) * (K + 1) + (K + 1 if act32 else 0)
     pages = int(sum((int(L) + total_steps + 16) // 16 + 1 for L in Ls)) + 16
-    model = BiModel(shape, BiModel.random_weights(shape, seed=args.seed + 1000 * rank), num_pages=pages,
+    model = BiModel(shape, BiModel.random_weights(shape, seed=seeds["weights"]), num_pages=pages,
                     page_seed=args.seed + 3)
     for b in range(B):
-        model.install_history(b, int(Ls[b]) - 1, args.seed * 7919 + 131 * b + rank)
+        model.install_history(b, int(Ls[b]) - 1, seeds["history"] + 131 * b)
     # block table covering every step; pos0 of step s is L_b - 1 + s
     rows = [model.pool.ensure(b, int(Ls[b]) + total_steps) for b in range(B)]
     max_pages = max(len(r) for r in rows)
@@ -201,13 +224,9 @@ def run_ours(args, rank, world, local_rank):
     if dist:
         dist.barrier()
     ck = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     ms_per_step = ms / K
-    value = B * world * K / (ms / 1000.0)
+    value = job_throughput(B, world, K, ms / 1000.0)
     assert bi.bi_device_error() == 0
 
     # ---------------------------------------------------------------- profiled pass: per-kernel event timing
@@ -301,12 +320,8 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
         h_ids[:] = h_out_i[:, 0]
         step[0] += 1
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": round(B * world * K / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    e2e = {"value": round(job_throughput(B, world, K, e2e_s), 2), "unit": "tok/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
     # ---------------------------------------------------------------- the same steps in the other modes
@@ -325,7 +340,8 @@ def run_ours(args, rank, world, local_rank):
         c1.record(stream)
         torch.cuda.synchronize()
         cms = c0.elapsed_time(c1)
-        modes[name] = {"value": round(B * world * K / (cms / 1000.0), 2), "unit": "tok/s",
+        cms = max_over_ranks(cms, dist, dev)
+        modes[name] = {"value": round(job_throughput(B, world, K, cms / 1000.0), 2), "unit": "tok/s",
                        "ms_per_step": round(cms / K, 4)}
     if "fast" in modes:
         modes["invariant_over_fast_time"] = round(ms_per_step / modes["fast"]["ms_per_step"], 4)
