@@ -205,18 +205,6 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// The first 16 of r from 16 consecutive columns (the 16-column remainder of a
-// tile whose width is not a multiple of 32).
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -307,9 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // two accumulators of TN columns, plus the running sum of merged units when
   // it fits (TN <= 128); allocations are powers of two
-  constexpr int kTmemNeed = TN <= 128 ? 3 * TN : 2 * TN;
-  constexpr int kTmemCols = kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static_assert(kTmemNeed <= 512 && TN % 16 == 0, "tile width");
+  constexpr int kTmemCols = TN == 32 ? 128 : TN == 64 ? 256 : 512;
   const int kStages = a.stages;
   const int kStageBytes = a.stage_bytes;
   const int kbs = a.kbs;
@@ -549,16 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const uint32_t tbase = lane_base + acc * TN;
         const bool last = q == seq - 1;
 #pragma unroll 1
-        for (int ch = 0; ch < (TN + 31) / 32; ++ch) {
+        for (int ch = 0; ch < TN / 32; ++ch) {
           uint32_t r[32];
-          // a width that is not a multiple of 32 ends in a 16-column chunk
-          const bool part = (TN % 32 != 0) && ch == TN / 32;
-          const int ncol = part ? 16 : 32;
-          if (part) tc_ld16(tbase + ch * 32, r);
-          else tc_ld32(tbase + ch * 32, r);
+          tc_ld32(tbase + ch * 32, r);
           if (seq > 1) {
-            // merged units (K parts summed in tensor memory) use widths that are multiples of 32
-            if constexpr (TN <= 128 && TN % 32 == 0) {
+            if constexpr (TN <= 128) {
               uint32_t t[32];
               if (q > 0) tc_ld32(sum_base + ch * 32, t);
 #pragma unroll
@@ -576,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             float* dst = a.partial + (static_cast<size_t>(s) * a.M + row) * a.N + col0;
 #pragma unroll
             for (int g = 0; g < 8; ++g)
-              if (4 * g < ncol && col0 + 4 * g < a.N)
+              if (col0 + 4 * g < a.N)
                 *reinterpret_cast<float4*>(dst + 4 * g) =
                     make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
                                 __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
@@ -586,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const float* res = (PL > 1 && a.Rf) ? a.Rf + static_cast<size_t>(row) * a.N + col0 : nullptr;
 #pragma unroll
             for (int g = 0; g < 8; ++g)
-              if (4 * g < ncol && col0 + 4 * g < a.N) {
+              if (col0 + 4 * g < a.N) {
                 float4 v = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
                                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
                 if (res) {
@@ -601,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const __nv_bfloat16* res = a.R ? a.R + static_cast<size_t>(row) * a.N + col0 : nullptr;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-              if (8 * g >= ncol || col0 + 8 * g >= a.N) break;
+              if (col0 + 8 * g >= a.N) break;
               float f[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * g + e]);
@@ -835,7 +816,7 @@ int choose_width_small_m(int64_t N, int splits, int a_rows) {
   const int sms = plan_sms();
   int btn = 64;
   int64_t best = INT64_MAX;
-  for (int tn : {256, 192, 176, 128, 96, 64, 48, 32}) {
+  for (int tn : {256, 192, 128, 64, 32}) {
     const int64_t units = ((N + tn - 1) / tn) * splits;
     const int64_t waves = (units + sms - 1) / sms;
     const int64_t cost = waves * (tn + a_rows);
@@ -932,22 +913,6 @@ bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& arg
   return BI_OK;
 }
 
-// Launch at tile width tn (one of the widths the planners choose).
-template <int PL>
-bi_status launch_tn(int tn, const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
-  switch (tn) {
-    case 256: return launch_w<256, PL>(ma, mw, args, s);
-    case 192: return launch_w<192, PL>(ma, mw, args, s);
-    case 176: return launch_w<176, PL>(ma, mw, args, s);
-    case 128: return launch_w<128, PL>(ma, mw, args, s);
-    case 96: return launch_w<96, PL>(ma, mw, args, s);
-    case 64: return launch_w<64, PL>(ma, mw, args, s);
-    case 48: return launch_w<48, PL>(ma, mw, args, s);
-    case 32: return launch_w<32, PL>(ma, mw, args, s);
-    default: set_error("bi_gemm: internal plan error (width %d)", tn); return BI_ERR_UNSUPPORTED;
-  }
-}
-
 }  // namespace gemm
 
 int take_gemm_device_error(cudaStream_t s, int32_t* code) {
@@ -1009,8 +974,8 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
                  (Rf == nullptr || aligned16(Rf)),
              BI_ERR_INVALID_ARG, "bi_gemm: pointers must be 16-byte aligned");
   gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te, planes);
-  BI_REQUIRE(p.seq == 1 || (p.TN <= 128 && p.TN % 32 == 0), BI_ERR_UNSUPPORTED,
-             "bi_gemm: internal plan error (merged units at width %d)", p.TN);
+  BI_REQUIRE(p.seq == 1 || p.TN <= 128, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (merged units at width %d)",
+             p.TN);
   BI_REQUIRE(p.stages >= 2, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (%d stages)", p.stages);
   gemm::Args args{};
   args.M = static_cast<int>(M);
@@ -1047,8 +1012,19 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   BI_TRY(gemm::tensor_map(A, planes * M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
   BI_TRY(gemm::tensor_map(Wt, N, K, p.TN, p.map3d ? p.kbs : 0, &mw));
   bi_status st;
-  if (planes == 1) st = gemm::launch_tn<1>(p.TN, ma, mw, args, s);
-  else st = gemm::launch_tn<3>(p.TN, ma, mw, args, s);
+  if (planes == 1) {
+    if (p.TN == 256) st = gemm::launch_w<256, 1>(ma, mw, args, s);
+    else if (p.TN == 192) st = gemm::launch_w<192, 1>(ma, mw, args, s);
+    else if (p.TN == 128) st = gemm::launch_w<128, 1>(ma, mw, args, s);
+    else if (p.TN == 64) st = gemm::launch_w<64, 1>(ma, mw, args, s);
+    else st = gemm::launch_w<32, 1>(ma, mw, args, s);
+  } else {
+    if (p.TN == 256) st = gemm::launch_w<256, 3>(ma, mw, args, s);
+    else if (p.TN == 192) st = gemm::launch_w<192, 3>(ma, mw, args, s);
+    else if (p.TN == 128) st = gemm::launch_w<128, 3>(ma, mw, args, s);
+    else if (p.TN == 64) st = gemm::launch_w<64, 3>(ma, mw, args, s);
+    else st = gemm::launch_w<32, 3>(ma, mw, args, s);
+  }
   if (st != BI_OK) return st;
   if (p.splits > 1) {
     const int64_t n = M * (N / 4);
