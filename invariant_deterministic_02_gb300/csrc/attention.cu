@@ -45,6 +45,21 @@ __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(group + 1), "r"(kGroupThreads) : "memory");
 }
 
+// Barrier of one group that also returns whether any of its threads passed `p`:
+// every thread of the group leaves with the same answer.
+__device__ __forceinline__ bool group_any(int group, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred ip, op;\n\t"
+      "setp.ne.u32 ip, %1, 0;\n\t"
+      "barrier.red.or.pred op, %2, %3, ip;\n\t"
+      "selp.u32 %0, 1, 0, op;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(group + 1), "r"(kGroupThreads)
+      : "memory");
+  return r != 0;
+}
+
 // Per-group shared scratch of the split function.
 // (o is written only after every warp has finished with z and e, so it shares
 // their storage: the smaller scratch lets three decode CTAs share an SM.)
@@ -562,6 +577,7 @@ struct DecodePlan {
   int* ulen;     // [B] positions per unit
   int* nunits;   // [B]
   int* prefix;   // [B+1]
+  int* counter;  // [1] next unclaimed work item of the split kernel (0 between launches)
 };
 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict__ kv_lens, int B, int hkv, int mode,
@@ -570,6 +586,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict
   pdl_trigger();
   __shared__ int part[1024];
   const int t = threadIdx.x;
+  if (t == 0) *plan.counter = 0;
   const int per = (B + 1023) / 1024;
   const int b0 = min(B, t * per), b1 = min(B, b0 + per);
   int local = 0;
@@ -692,8 +709,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const int plane = threadIdx.x - kGroupThreads;
     int n = 0;
     uint32_t issued = 0, ipar = 0;
+    // Work items are claimed from a counter shared by the launch's CTAs, one
+    // item ahead, so a CTA that finishes early takes more; which CTA reduces
+    // an item changes nothing in its arithmetic.
+    auto claim = [&]() -> int {
+      int it = 0;
+      if (plane == 0) it = atomicAdd(plan.counter, 1);
+      return __shfl_sync(0xffffffffu, it, 0);
+    };
     // item k's descriptor and q go to slot k % 2; an item is announced while
-    // the item before it is still being streamed
+    // the item before it is still being streamed; a claim past the last item
+    // is announced as an end marker (u = -1)
     int ann = 0;
     uint32_t ann_issued = 0;
     auto announce = [&](int it) {
@@ -701,6 +727,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
         const int slot = ann % kItemSlots;
         const uint32_t ph = static_cast<uint32_t>((ann / kItemSlots) & 1);
         wait_bounded(iempty0 + 8 * slot, ph ^ 1u, abort_flag, 14);
+        if (it >= total) {
+          S.item[slot] = make_int4(-1, 0, 0, 0);
+          mbar_arrive(ifull0 + 8 * slot);  // release: the descriptor store
+          ann_issued &= ~(1u << slot);
+          ++ann;
+          return;
+        }
         const int u = it / hkv;
         const int g = it % hkv;
         const int b = find_row(plan.prefix, B, u);
@@ -718,9 +751,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
       }
       ++ann;
     };
-    if (static_cast<int>(blockIdx.x) < total) announce(blockIdx.x);
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      if (item + static_cast<int>(gridDim.x) < total) announce(item + gridDim.x);
+    int item = claim();
+    announce(item);
+    while (item < total) {
+      const int next = claim();
+      announce(next);
       const int u = item / hkv;
       const int g = item % hkv;
       const int b = find_row(plan.prefix, B, u);
@@ -754,6 +789,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
           ipar = (ipar & ~(1u << st)) | (ph << st);
         }
       }
+      item = next;
     }
     // keep the CTA resident until every copy it issued has landed
     if (plane == 0) {
@@ -772,11 +808,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
   const int tid = threadIdx.x;
   const int c = (tid & 31) & 7;
   int n0 = 0;
-  int icount = 0;
-  for (int item = blockIdx.x; item < total; item += gridDim.x, ++icount) {
+  // items in the order the producer announces them, up to its end marker (a
+  // CTA never gets more than `total`; a wait that gave up ends the loop too)
+  for (int icount = 0; icount <= total; ++icount) {
     const int islot = icount % kItemSlots;
-    wait_bounded(ifull0 + 8 * islot, static_cast<uint32_t>((icount / kItemSlots) & 1), abort_flag, 15);
+    const bool ok = wait_bounded(ifull0 + 8 * islot, static_cast<uint32_t>((icount / kItemSlots) & 1), abort_flag, 15);
     const int4 desc = S.item[islot];
+    // one decision for the whole group (its warps meet at named barriers below)
+    if (group_any(0, !ok || desc.x < 0)) break;
     const int u = desc.x;
     const int g = desc.y;
     const int ustart = desc.z;
@@ -849,6 +888,8 @@ __global__ void decode_merge_kernel(const Partials part, DecodePlan plan, ActDst
                                     int hd) {
   pdl_wait();
   pdl_trigger();
+  // the split kernel has finished: its work counter starts from zero for the next launch
+  if (blockIdx.x == 0 && threadIdx.x == 0) *plan.counter = 0;
   const int b = blockIdx.x / hkv;
   const int g = blockIdx.x % hkv;
   const int G = hq / hkv;
@@ -1122,6 +1163,7 @@ size_t carve_decode_plan(void* base, int B, int hkv, DecodePlan* plan) {
   plan->ulen = cv.take<int>(B);
   plan->nunits = cv.take<int>(B);
   plan->prefix = cv.take<int>(B + 1);
+  plan->counter = cv.take<int>(1);
   return align_up(cv.used, 256);
 }
 
