@@ -232,6 +232,9 @@ def bi_gemm(A, W, C, residual=None, mode=INVARIANT, target_row=-1, target_count=
 def bi_gemm_f32a(A, W, C, residual=None, mode=INVARIANT, target_row=-1, target_count=0, workspace=None,
                  stream=None):
     """fp32 A [M][K] times bf16 W [N][K] into fp32 C (+ fp32 residual)."""
+    if A.dtype != torch.float32 or C.dtype != torch.float32 or W.dtype != torch.bfloat16 or \
+            (residual is not None and residual.dtype != torch.float32):
+        raise TypeError("bi_gemm_f32a: A, C (and residual) must be float32 and W bfloat16")
     M, K = A.shape
     N = W.shape[0]
     m = _mode(mode)
