@@ -202,10 +202,10 @@ typedef struct bi_attn_dims {
   int32_t act_f32;   /* 0: q and out bf16; 1: q and out fp32 */
 } bi_attn_dims;
 
-/* Decode: one query token per request.  q: device [B][num_q_heads][head_dim] bf16;
- * the query of request b sits at position kv_lens[b]-1 and its own K/V must
- * already be in the cache.  kv_lens: device int32 [B], 1 <= kv_len <= max_pages*16.
- * out: device [B][num_q_heads][head_dim] bf16. */
+/* Decode: one query token per request.  q: device [B][num_q_heads][head_dim] bf16
+ * (fp32 when dims->act_f32); the query of request b sits at position kv_lens[b]-1
+ * and its own K/V must already be in the cache.  kv_lens: device int32 [B],
+ * 1 <= kv_len <= max_pages*16.  out: device [B][num_q_heads][head_dim], as q. */
 size_t bi_decode_attention_workspace(int32_t B, const bi_attn_dims* dims, bi_mode mode);
 bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                               const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, void* out, bi_mode mode,
@@ -236,7 +236,7 @@ bi_status bi_decode_attention_noalloc(const void* q, const void* k_cache, const 
                                       bi_stream s);
 
 /* Prefill (any number of query tokens per request, causal by absolute position).
- * q: device [T][num_q_heads][head_dim] bf16, tokens of request b at rows
+ * q: device [T][num_q_heads][head_dim] bf16 (fp32 when dims->act_f32), tokens of request b at rows
  * q_start[b] .. q_start[b+1]-1 (q_start device int32 [B+1], q_start[0] = 0,
  * q_start[B] = T), at absolute positions q_pos0[b] + i (q_pos0 device int32 [B]).
  * K/V of every query token must already be in the cache.  out: as q. */
@@ -288,8 +288,9 @@ typedef struct bi_layer_weights {
   const void* w_down;    /* [d][F] bf16 */
   /* Optional per-head RMSNorm of q and k before RoPE (Qwen3; NULL = none):
    * [head_dim] bf16 weights; each head row x of head_dim values becomes
-   * bf16((x / sqrt(sum(x^2)/head_dim + rms_eps)) * g) in fp32, the sum of squares
-   * taken in one fixed order that depends on head_dim only.  Both or neither. */
+   * (x / sqrt(sum(x^2)/head_dim + rms_eps)) * g in fp32, rounded to bf16 unless the
+   * activations are fp32, the sum of squares taken in one fixed order that depends
+   * on head_dim only.  Both or neither. */
   const void* q_norm;
   const void* k_norm;
 } bi_layer_weights;
