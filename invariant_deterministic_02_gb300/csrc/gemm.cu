@@ -62,7 +62,6 @@ constexpr int kSmemLimit = 227 * 1024;     // dynamic shared memory per CTA
 constexpr int kMaxStages = 16;
 constexpr int kOverreadSlack = kATileBytes;  // see the A-tile note below
 constexpr int kMaxSplitK = 16;
-constexpr int kL2Ahead = 8;  // stages of W prefetched into L2 beyond the ring at decode sizes
 
 __device__ unsigned int g_err_word = 0;
 
@@ -83,7 +82,6 @@ struct Args {
   int kb_total;          // k-tiles in K
   int prefetch_w;        // 1: W is constant while the previous kernel runs (weights of a forward pass), so
                          // the first stages' W copies may be issued before waiting for that kernel
-  int l2_ahead;          // >0: W boxes are prefetched into L2 this many stages beyond the ring (decode sizes)
   void* C;
   const __nv_bfloat16* R;  // residual or null
   float* partial;          // [splits][M][N] fp32 (split units only)
@@ -175,21 +173,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
           "r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
-}
-
-// Pull a box into L2 only (no shared memory, no barrier): a hint that the
-// demand copy of the same box, issued later, will find it there.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -395,15 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           int kb0, kb1;
           if (seq > 1) k_range(a.kb_total, q, seq, kb0, kb1);
           else k_range(a.kb_total, s, ns, kb0, kb1);
-          // W boxes this far ahead of the copy being issued are pulled into L2 first, so the
-          // ring's copies find them there; the stages the ring holds at the start are skipped
-          const int pf_dist = (kStages + a.l2_ahead) * kbs;
-          if (a.l2_ahead > 0) {
-            for (int kbp = kb0 + kStages * kbs; kbp < kb1 && kbp < kb0 + pf_dist; kbp += kbs) {
-              if (a.map3d) tma_prefetch_3d(&tmW, 0, nt * TN, kbp);
-              else tma_prefetch_2d(&tmW, kbp * kBK, nt * TN);
-            }
-          }
           for (int kb = kb0; kb < kb1; kb += kbs) {
             const uint32_t fb = full0 + 8 * st;
             const uint32_t sa = smem_u32(tiles + st * kStageBytes);
@@ -432,10 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                   tma_load_2d(sa + pl * a_plane, &tmA, fb, kb * kBK, pl * a.plane_rows + mt * kBM);
                 tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
               }
-            }
-            if (a.l2_ahead > 0 && kb + pf_dist < kb1) {
-              if (a.map3d) tma_prefetch_3d(&tmW, 0, nt * TN, kb + pf_dist);
-              else tma_prefetch_2d(&tmW, (kb + pf_dist) * kBK, nt * TN);
             }
             issued_mask |= 1u << st;
             issued_par = (issued_par & ~(1u << st)) | (ph << st);
@@ -1023,8 +993,6 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   args.tm1 = p.tm1;
   args.seq = p.seq;
   args.prefetch_w = weights_constant ? 1 : 0;
-  // decode sizes (one 128-row tile): every weight byte is read by one CTA, straight from HBM
-  args.l2_ahead = p.m_tiles == 1 ? gemm::kL2Ahead : 0;
   args.units = p.units;
   args.kb_total = p.kb_total;
   args.C = C;
