@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--batch", type=int, default=BATCH)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None, help="keep the raw SM clock samples of the timed region here")
     ap.add_argument("--case", choices=["model", "attn", "gemm", "topk"], default="model",
                     help="model: the decode-step workload; attn/gemm/topk: one kernel on a small single-layer "
                          "case (for profiler captures), printing that kernel's timing")
@@ -71,14 +72,20 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path: str | None = None):
+        """path: where the raw nvidia-smi samples go (a temporary file when not given)."""
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        self.tmp = path is None
+        if path is None:
+            import tempfile
+            fd, path = tempfile.mkstemp(prefix="bi_clocks_", suffix=".csv")
+            os.close(fd)
+        self.path = path
         self.gpu = gpu_index
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
@@ -97,7 +104,11 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        if self.tmp:
+            os.remove(self.path)
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -209,7 +220,8 @@ def run_ours(args, rank, world, local_rank):
 
     # ---------------------------------------------------------------- timed region (device-resident inputs)
     clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]),
+                          args.clocks_csv if world == 1 else None)
     clocks.start()
     time.sleep(0.3)
     if dist:
