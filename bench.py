@@ -95,6 +95,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            if self.tmp and os.path.exists(self.path):
+                os.remove(self.path)
             return None
         self.proc.terminate()
         try:
