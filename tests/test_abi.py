@@ -105,3 +105,45 @@ def test_fp32_activation_entry_points_validate_and_size_on_the_host(libpath):
     batch = bi.Batch(1, 4, 4, ctypes.addressof(qs), ctypes.addressof(qs), ctypes.addressof(qs), 1, 1, -1, 0, 0)
     w16, w32, bad = [l.bi_layer_workspace(ctypes.byref(d), ctypes.byref(batch), 0) for d in dims]
     assert w32 > w16 > 0 and bad == 0
+
+
+def test_layer_and_model_entry_points_reject_bad_arguments_before_launch(libpath):
+    # every failure below is found on the host before anything is launched, so no GPU is needed
+    import invariant_deterministic_02_gb300 as bi
+    l = bi.lib()
+    qs = (ctypes.c_int32 * 2)(0, 4)
+    batch = bi.Batch(1, 4, 4, ctypes.addressof(qs), ctypes.addressof(qs), ctypes.addressof(qs), 1, 1, -1, 0, 0)
+    good = bi.ModelDims(256, 4, 2, 64, 512, 512, 16, 2048, 1e-5, 0)
+    lw = bi.LayerWeights(*([None] * 8))
+    dummy = ctypes.c_void_p(16)
+    # act_f32 must be 0 or 1
+    bad = bi.ModelDims(256, 4, 2, 64, 512, 512, 16, 2048, 1e-5, 3)
+    assert l.bi_layer_forward(ctypes.byref(bad), ctypes.byref(lw), dummy, dummy, dummy, ctypes.byref(batch), dummy,
+                              dummy, 0, dummy, 1 << 30, None) == bi.BI_ERR_INVALID_ARG
+    assert b"act_f32" in l.bi_last_error_message()
+    # page size other than 16, d_model not a multiple of 8
+    for dims in (bi.ModelDims(256, 4, 2, 64, 512, 512, 8, 2048, 1e-5, 0),
+                 bi.ModelDims(260, 4, 2, 64, 512, 512, 16, 2048, 1e-5, 0)):
+        assert l.bi_layer_forward(ctypes.byref(dims), ctypes.byref(lw), dummy, dummy, dummy, ctypes.byref(batch),
+                                  dummy, dummy, 0, dummy, 1 << 30, None) == bi.BI_ERR_UNSUPPORTED
+    # a mode outside the enum, a null hidden state, a workspace smaller than the query
+    assert l.bi_layer_forward(ctypes.byref(good), ctypes.byref(lw), dummy, dummy, dummy, ctypes.byref(batch), dummy,
+                              dummy, 9, dummy, 1 << 30, None) == bi.BI_ERR_INVALID_ARG
+    assert l.bi_layer_forward(ctypes.byref(good), ctypes.byref(lw), dummy, dummy, None, ctypes.byref(batch), dummy,
+                              dummy, 0, dummy, 1 << 30, None) == bi.BI_ERR_INVALID_ARG
+    need = l.bi_layer_workspace(ctypes.byref(good), ctypes.byref(batch), 0)
+    assert need > 0
+    assert l.bi_layer_forward(ctypes.byref(good), ctypes.byref(lw), dummy, dummy, dummy, ctypes.byref(batch), dummy,
+                              dummy, 0, dummy, need - 1, None) == bi.BI_ERR_WORKSPACE
+    # a batch whose protected request lies outside it
+    bad_batch = bi.Batch(1, 4, 4, ctypes.addressof(qs), ctypes.addressof(qs), ctypes.addressof(qs), 1, 1, 3, 0, 1)
+    assert l.bi_layer_workspace(ctypes.byref(good), ctypes.byref(bad_batch), 0) == 0
+    # the model entry point: null model pointers, then a vocabulary that is not a multiple of 8
+    args = (dummy, dummy, dummy, ctypes.byref(batch), None, None, dummy, 20, dummy, dummy, None, 0, dummy, 1 << 30,
+            None)
+    mw = bi.ModelWeights(None, None, 0, None, None)
+    assert l.bi_model_forward(ctypes.byref(good), ctypes.byref(mw), *args) == bi.BI_ERR_INVALID_ARG
+    mw = bi.ModelWeights(16, None, 0, 16, 16)  # no layers: only the embedding, final norm and head are named
+    odd = bi.ModelDims(256, 4, 2, 64, 512, 500, 16, 2048, 1e-5, 0)
+    assert l.bi_model_forward(ctypes.byref(odd), ctypes.byref(mw), *args) == bi.BI_ERR_UNSUPPORTED
+    assert b"vocab" in l.bi_last_error_message()
