@@ -210,3 +210,40 @@ def test_empty_batch_and_bad_workspace():
         bi.bi_decode_attention(q, req.kc, req.vc, req.bt, cuda(torch.tensor([20], dtype=torch.int32)), req.dims,
                                torch.empty_like(q), workspace=small)
     assert ei.value.status == bi.BI_ERR_WORKSPACE
+
+
+def test_full_config_256_requests_up_to_32768_tokens():
+    """Decode at the full size of the attention config: 256 requests whose KV lengths
+    are log-uniform in [64, 32768], one of them forced to 32768 (128 splits: the whole
+    merge tree), K/V drawn on the device.  Oracle parity on sampled requests, and the
+    longest request's bits equal to decoding it alone."""
+    hq, hkv, hd, B = 32, 8, 128, 256
+    lens = synth.loguniform_ints(B, 64, 32768, 501).tolist()
+    lens[17] = 32768
+    layout = synth.paged_layout(lens, PS, 502)
+    kc = torch.empty((layout.num_pages, hkv, PS, hd), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    kc.view(torch.int16).fill_(-1)  # NaN patterns in unused slots: a masked-lane read would show
+    vc.view(torch.int16).fill_(-1)
+
+    def kv(b):
+        return (synth.normal_device((lens[b], hkv, hd), 10000 + 2 * b),
+                synth.normal_device((lens[b], hkv, hd), 10001 + 2 * b))
+
+    for b in range(B):
+        synth.fill_paged(kc, vc, layout.block_table[b], *kv(b))
+    bt = cuda(torch.from_numpy(layout.block_table))
+    dims = bi.attn_dims(hq, hkv, hd, layout.max_pages, layout.num_pages)
+    q = synth.normal_device((B, hq, hd), 503)
+    kl = cuda(torch.tensor(lens, dtype=torch.int32))
+    out = torch.empty_like(q)
+    bi.bi_decode_attention(q, kc, vc, bt, kl, dims, out)
+    torch.cuda.synchronize()
+    for b in sorted({17, int(np.argmin(lens)), 0, 100, 255}):
+        K, V = kv(b)
+        ref = oracle.attention(f64(q[b:b + 1]), f64(K), f64(V), [lens[b] - 1], dims.scale)[0]
+        assert max_rel_err(f64(out[b]), oracle.round_bf16(ref)) <= TOL_BF16, (b, lens[b])
+    one = torch.empty_like(q[17:18])
+    bi.bi_decode_attention(q[17:18].contiguous(), kc, vc, bt[17:18].contiguous(), kl[17:18].contiguous(), dims, one)
+    torch.cuda.synchronize()
+    assert bits_equal(one, out[17:18])
