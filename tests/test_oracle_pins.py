@@ -463,3 +463,29 @@ def test_three_bf16_terms_hold_an_fp32_value_exactly():
     w = oracle.round_bf16(rng.standard_normal(hi.size)).astype(np.float32)
     for t in (hi, mid, lo):
         assert np.array_equal((t * w).astype(np.float64), t.astype(np.float64) * w.astype(np.float64))
+
+
+def test_reduction_order_changes_fp32_sums_but_not_the_float64_oracle():
+    # The mechanism behind the method (zhaixingw.cn BlockLock post, its numpy reproduction of the tiling effect):
+    # the same 4096-term dot products summed tile by tile with different tile widths round differently in fp32.
+    # In float64 the orders agree to float64 rounding, which is why the oracle's sums can stand for the exact
+    # ones at the tolerances the GPU tests use.
+    rng = np.random.default_rng(11)
+    K, N = 4096, 64
+    x = rng.standard_normal((8, K)).astype(np.float32)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+
+    def tiled(dtype, tile):
+        acc = np.zeros((8, N), dtype=dtype)
+        for k0 in range(0, K, tile):  # tiles in ascending k, each summed on its own, then added in order
+            part = np.einsum("ik,jk->ij", x[:, k0:k0 + tile].astype(dtype), W[:, k0:k0 + tile].astype(dtype))
+            acc = (acc + part).astype(dtype)
+        return acc.astype(np.float64)
+
+    exact = oracle.gemm(x.astype(np.float64), W.astype(np.float64))
+    scale = np.max(np.abs(exact))
+    d32 = np.max(np.abs(tiled(np.float32, 4096) - tiled(np.float32, 32)))
+    d64 = np.max(np.abs(tiled(np.float64, 4096) - tiled(np.float64, 32)))
+    assert 0 < d32 <= 1e-4 * scale  # fp32: a real, small difference
+    assert d64 <= 1e-12 * scale  # float64: order does not matter at any tolerance used
+    assert np.max(np.abs(tiled(np.float64, 32) - exact)) <= 1e-12 * scale
