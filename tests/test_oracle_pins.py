@@ -418,6 +418,80 @@ def test_layer_attention_branch_single_token():
     assert np.allclose(out[0], oracle.round_bf16(h[0] + att @ w["w_o"].T), rtol=0, atol=0)
 
 
+def test_layer_qk_norm_branch_by_hand():
+    # Qwen3-shaped layers normalise every q head row and every k head row (head_dim values each) with their
+    # own RMSNorm weights before RoPE (reading: the pages never describe the layer; the standard Qwen3 block
+    # is taken).  A new token at position P attends to P cached keys and to itself; with w_down = 0 the layer
+    # output is R(h + att Wo^T).  The computation below is written element by element from that reading.
+    # Each plausible slip in the oracle's branch -- the norm after RoPE, q_norm and k_norm swapped, one norm
+    # over all heads of a token -- moves the result by more than 5% of the attention term.
+    shape = synth.TINY_QK_LAYER
+    w = _tiny_weights(shape, 4, zero=("w_down",))
+    d, hd, Hq, Hkv = shape.d_model, shape.head_dim, shape.n_q_heads, shape.n_kv_heads
+    G, eps, P = Hq // Hkv, shape.rms_eps, 5
+    # widely spread head-norm weights, so that mixing dims i and i + hd/2 (RoPE) before or after them shows
+    w["q_norm"] = synth.normal((hd,), 12, std=0.5, mean=1.0).double().numpy()
+    w["k_norm"] = synth.normal((hd,), 13, std=0.5, mean=1.0).double().numpy()
+    h = synth.normal((1, d), 9).double().numpy()
+    K0 = synth.normal((P, Hkv, hd), 10).double().numpy()
+    V0 = synth.normal((P, Hkv, hd), 11).double().numpy()
+    kv = oracle.OracleKV(1, Hkv, hd)
+    kv.set(0, 0, K0, V0)
+    out = oracle.layer_forward(h, w, shape, kv, 0, [(0, 1)], [P])[0]
+    R = oracle.round_bf16  # pinned on its own above
+
+    def norm_row(row, g):
+        ms = sum(float(v) * float(v) for v in row) / len(row)
+        r = 1.0 / math.sqrt(ms + eps)
+        return np.array([float(v) * r * float(gi) for v, gi in zip(row, g)])
+
+    def rot(vec, pos):
+        half = hd // 2
+        o = np.empty(hd)
+        for i in range(half):
+            ang = pos * shape.rope_theta ** (-2.0 * i / hd)
+            c, s = math.cos(ang), math.sin(ang)
+            o[i] = vec[i] * c - vec[i + half] * s
+            o[i + half] = vec[i + half] * c + vec[i] * s
+        return o
+
+    def by_hand(variant):
+        x1 = R(norm_row(h[0], w["attn_norm"]))
+        qkv = R(x1 @ w["w_qkv"].T)
+        q = qkv[:Hq * hd].reshape(Hq, hd)
+        k = qkv[Hq * hd:(Hq + Hkv) * hd].reshape(Hkv, hd)
+        v = R(qkv[(Hq + Hkv) * hd:].reshape(Hkv, hd))
+        gq, gk = (w["k_norm"], w["q_norm"]) if variant == "swapped" else (w["q_norm"], w["k_norm"])
+        if variant == "after_rope":
+            qr = R(np.array([norm_row(rot(r, P), gq) for r in q]))
+            kr = R(np.array([norm_row(rot(r, P), gk) for r in k]))
+        else:
+            if variant == "across_heads":
+                qn = R(norm_row(q.ravel(), np.tile(gq, Hq))).reshape(Hq, hd)
+                kn = R(norm_row(k.ravel(), np.tile(gk, Hkv))).reshape(Hkv, hd)
+            else:
+                qn = R(np.array([norm_row(r, gq) for r in q]))
+                kn = R(np.array([norm_row(r, gk) for r in k]))
+            qr = R(np.array([rot(r, P) for r in qn]))
+            kr = R(np.array([rot(r, P) for r in kn]))
+        att = np.empty((Hq, hd))
+        for hh in range(Hq):
+            g = hh // G
+            keys = [K0[j, g] for j in range(P)] + [kr[g]]
+            vals = [V0[j, g] for j in range(P)] + [v[g]]
+            z = [sum(float(x) * float(y) for x, y in zip(qr[hh], key)) / math.sqrt(hd) for key in keys]
+            e = [math.exp(t - max(z)) for t in z]
+            att[hh] = sum(ej * vj for ej, vj in zip(e, vals)) / sum(e)
+        return R(h[0] + R(att).ravel() @ w["w_o"].T)
+
+    ref = by_hand("reading")
+    term = np.max(np.abs(ref - h[0]))  # size of the attention term
+    assert np.max(np.abs(out - ref)) <= 1e-3 * term
+    assert np.array_equal(oracle.round_bf16(kv.k[(0, 0)][P]), kv.k[(0, 0)][P])  # the new key is cached as bf16
+    for slip in ("after_rope", "swapped", "across_heads"):
+        assert np.max(np.abs(by_hand(slip) - ref)) >= 2e-2 * term, slip
+
+
 def test_model_without_layers_is_norm_then_head():
     shape = synth.TINY_LAYER
     V = 50
@@ -465,27 +539,50 @@ def test_three_bf16_terms_hold_an_fp32_value_exactly():
         assert np.array_equal((t * w).astype(np.float64), t.astype(np.float64) * w.astype(np.float64))
 
 
+def _sum_in_order(terms, dtype, order):
+    """Sum terms [rows][K] along K in dtype, in one of three orders: "serial"
+    (one running sum, k ascending), "pairwise" (a balanced tree: neighbours
+    added level by level), or an int w (blocks of w consecutive terms summed
+    serially, then the block sums added serially)."""
+    t = np.asarray(terms, dtype=dtype)
+    if order == "serial":
+        acc = np.zeros(t.shape[0], dtype=dtype)
+        for k in range(t.shape[1]):
+            acc = (acc + t[:, k]).astype(dtype)
+        return acc
+    if order == "pairwise":
+        while t.shape[1] > 1:
+            if t.shape[1] % 2:
+                t = np.concatenate([t, np.zeros((t.shape[0], 1), dtype=dtype)], axis=1)
+            t = (t[:, 0::2] + t[:, 1::2]).astype(dtype)
+        return t[:, 0]
+    blocks = np.stack([_sum_in_order(t[:, k0:k0 + order], dtype, "serial")
+                       for k0 in range(0, t.shape[1], order)], axis=1)
+    return _sum_in_order(blocks, dtype, "serial")
+
+
 def test_reduction_order_changes_fp32_sums_but_not_the_float64_oracle():
-    # The mechanism behind the method (zhaixingw.cn BlockLock post, its numpy reproduction of the tiling effect):
-    # the same 4096-term dot products summed tile by tile with different tile widths round differently in fp32.
-    # In float64 the orders agree to float64 rounding, which is why the oracle's sums can stand for the exact
-    # ones at the tolerances the GPU tests use.
+    # The mechanism behind the method (zhaixingw.cn BlockLock post, its float32 reproduction of the tiling
+    # effect; devpress digest, section 2.1 on non-associative floating-point addition): one dot product
+    # summed in different orders -- a running sum, a pairwise tree, blocks of the tile widths the GEMM uses
+    # (32 .. 256 columns, 16-term instruction steps) -- rounds differently in fp32.  In float64 all the
+    # orders agree to float64 rounding, which is why the oracle's sums can stand for the exact ones.
     rng = np.random.default_rng(11)
-    K, N = 4096, 64
-    x = rng.standard_normal((8, K)).astype(np.float32)
-    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
-
-    def tiled(dtype, tile):
-        acc = np.zeros((8, N), dtype=dtype)
-        for k0 in range(0, K, tile):  # tiles in ascending k, each summed on its own, then added in order
-            part = np.einsum("ik,jk->ij", x[:, k0:k0 + tile].astype(dtype), W[:, k0:k0 + tile].astype(dtype))
-            acc = (acc + part).astype(dtype)
-        return acc.astype(np.float64)
-
-    exact = oracle.gemm(x.astype(np.float64), W.astype(np.float64))
+    K = 4096
+    a = rng.standard_normal((16, K)).astype(np.float32)
+    b = (rng.standard_normal((16, K)) * 0.02).astype(np.float32)
+    terms = a.astype(np.float64) * b.astype(np.float64)  # every fp32 x fp32 product is exact in float64
+    exact = np.array([oracle.gemm(a[r:r + 1].astype(np.float64), b[r:r + 1].astype(np.float64))[0, 0]
+                      for r in range(a.shape[0])])
     scale = np.max(np.abs(exact))
-    d32 = np.max(np.abs(tiled(np.float32, 4096) - tiled(np.float32, 32)))
-    d64 = np.max(np.abs(tiled(np.float64, 4096) - tiled(np.float64, 32)))
-    assert 0 < d32 <= 1e-4 * scale  # fp32: a real, small difference
-    assert d64 <= 1e-12 * scale  # float64: order does not matter at any tolerance used
-    assert np.max(np.abs(tiled(np.float64, 32) - exact)) <= 1e-12 * scale
+    orders = ["serial", "pairwise", 16, 32, 64, 256]
+    s32 = [_sum_in_order(terms.astype(np.float32), np.float32, o).astype(np.float64) for o in orders]
+    s64 = [_sum_in_order(terms, np.float64, o) for o in orders]
+    spread32 = max(np.max(np.abs(x - s32[0])) for x in s32[1:])
+    spread64 = max(np.max(np.abs(x - s64[0])) for x in s64[1:])
+    assert 0 < spread32 <= 1e-4 * scale  # fp32: a real, small difference between orders
+    assert spread64 <= 1e-12 * scale  # float64: the order does not matter at any tolerance used
+    for x in s64:
+        assert np.max(np.abs(x - exact)) <= 1e-12 * scale
+    # the orders really are different ones: a running sum and a tree disagree on some rows in fp32
+    assert np.any(s32[0] != s32[1])
