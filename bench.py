@@ -35,6 +35,10 @@ METRIC = "invariant decode tok/s (8B-shape, B=1..64); GEMM TFLOP/s & attn GB/s v
 BATCH = 64
 KV_LO, KV_HI = 128, 4096
 TOPK = 20
+SWEEP_BATCHES = (1, 8)
+GEMM_SWEEP_M = (256, 1024, 4096)
+GEMM_SWEEP_N = (4096, 14336, 151936)
+GEMM_SWEEP_K = 4096
 WORKLOAD = ("Qwen3-8B-shaped decode step (36 layers, d4096, 32/8 heads, hd128, q/k head RMSNorm, FFN 12288, vocab 151936), "
             "B=64 requests, cached KV lengths U{128..4096}, greedy top-20")
 
@@ -54,6 +58,8 @@ def parse():
                     help="model: the decode-step workload; attn/gemm/topk: one kernel on a small single-layer "
                          "case (for profiler captures), printing that kernel's timing")
     ap.add_argument("--gemm-shape", default="64,24576,4096", help="M,N,K of --case gemm")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the GEMM sweep, RMSNorm roofline and smaller decode batches")
     return ap.parse_args()
 
 
@@ -165,10 +171,13 @@ def run_ours(args, rank, world, local_rank):
     shape = QWEN3_8B
     seeds = replica_seeds(args.seed, rank)
     Ls = synth.uniform_ints(B, KV_LO, KV_HI, seeds["kv_lens"])  # KV length at the first step
-    compare = [m for m in ("fast", "invariant_ksplit") if m != args.mode] if args.mode == "invariant" else []
+    compare = ([m for m in ("fast", "invariant_ksplit", "protected") if m != args.mode]
+               if args.mode == "invariant" else [])
     act32 = args.mode == "invariant"  # also time the fp32-activation variant of the same step
-    # warm-up, timed, profiled, end-to-end, other modes, fp32 activations
-    total_steps = W + 2 * K + K + len(compare) * (K + 1) + (K + 1 if act32 else 0)
+    sweep_b = [b for b in SWEEP_BATCHES if b < B] if args.mode == "invariant" and not args.no_extras else []
+    # warm-up, timed, profiled, end-to-end, other modes, fp32 activations, smaller decode batches
+    total_steps = (W + 2 * K + K + len(compare) * (K + 1) + (K + 1 if act32 else 0) +
+                   len(sweep_b) * (W + K))
     pages = int(sum((int(L) + total_steps + 16) // 16 + 1 for L in Ls)) + 16
     model = BiModel(shape, BiModel.random_weights(shape, seed=seeds["weights"]), num_pages=pages,
                     page_seed=args.seed + 3)
@@ -191,13 +200,16 @@ def run_ours(args, rank, world, local_rank):
     ti = torch.empty((B, TOPK), dtype=torch.int32, device=dev)
     target = 0 if args.mode == "protected" else -1
 
-    def batch_for(step):
-        return bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos[step].data_ptr(), d_bt.data_ptr(), max_pages, pages,
-                        target, 0 if target >= 0 else -1, 1 if target >= 0 else 0)
+    def batch_for(step, m=None, nb=B):
+        # PROTECTED protects request 0 (its one token row); nb < B: the first nb requests
+        t = 0 if (m if m is not None else mode) == bi.PROTECTED else -1
+        return bi.Batch(nb, nb, 1, d_qs.data_ptr(), d_pos[step].data_ptr(), d_bt.data_ptr(), max_pages, pages,
+                        t, 0 if t >= 0 else -1, 1 if t >= 0 else 0)
 
     dims32 = bi.ModelDims.from_buffer_copy(model.dims)  # same model, fp32 activations
     dims32.act_f32 = 1
-    ws_bytes = max(bi.bi_model_workspace(model.dims, batch_for(0), bi.MODES[m]) for m in [args.mode] + compare)
+    ws_bytes = max(bi.bi_model_workspace(model.dims, batch_for(0, bi.MODES[m]), bi.MODES[m])
+                   for m in [args.mode] + compare)
     if act32:
         ws_bytes = max(ws_bytes, bi.bi_model_workspace(dims32, batch_for(0), mode))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -205,10 +217,10 @@ def run_ours(args, rank, world, local_rank):
     sp = stream.cuda_stream
     step = [0]
 
-    def one_step(m=mode, dims=model.dims):
+    def one_step(m=mode, dims=model.dims, nb=B):
         s = step[0]
         src, dst = ids[s % 2], ids[(s + 1) % 2]
-        bi.bi_model_forward(dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s), model.k_ptrs,
+        bi.bi_model_forward(dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s, m, nb), model.k_ptrs,
                             model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=dst, mode=m, workspace=ws,
                             ws_bytes=ws_bytes, stream=sp)
         step[0] += 1
@@ -359,6 +371,36 @@ def run_ours(args, rank, world, local_rank):
                        "ms_per_step": round(cms / K, 4)}
     if "fast" in modes:
         modes["invariant_over_fast_time"] = round(ms_per_step / modes["fast"]["ms_per_step"], 4)
+    if "protected" in modes:
+        modes["protected"]["target_request"] = 0
+
+    # ---------------------------------------------------------------- smaller decode batches (B = 1, 8)
+    # the first nb requests of the same model and caches; roofline: the weights every step streams
+    # (all layers + lm-head) plus the KV of those requests, against the measured HBM copy bandwidth
+    w_bytes = weight_bytes_per_step(shape)
+    decode_sweep = {}
+    for nb in sweep_b:
+        for _ in range(W):
+            one_step(mode, model.dims, nb)
+        torch.cuda.synchronize()
+        s0 = step[0]
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(K):
+            one_step(mode, model.dims, nb)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cms = max_over_ranks(c0.elapsed_time(c1), dist, dev) / K
+        kvb = float((pos_all[s0:s0 + K, :nb] + 1).sum(axis=1).mean()) * L.n_kv_heads * L.head_dim * 4 * shape.n_layers
+        gbs = (w_bytes + kvb) / (cms / 1000.0) / 1e9
+        decode_sweep["B%d" % nb] = {"value": round(nb * world / (cms / 1000.0), 2), "unit": "tok/s",
+                                    "ms_per_step": round(cms, 4), "bytes_per_step": round(w_bytes + kvb),
+                                    "achieved_GBs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+    kvb64 = kv_bytes_step
+    gbs64 = (w_bytes + kvb64) / (ms_per_step / 1000.0) / 1e9
+    decode_sweep["B%d" % B] = {"value": round(value, 2), "unit": "tok/s", "ms_per_step": round(ms_per_step, 4),
+                               "bytes_per_step": round(w_bytes + kvb64), "achieved_GBs": round(gbs64, 1),
+                               "frac_hbm": round(gbs64 / pk["hbm_gbs"], 4), "note": "the headline run"}
     assert bi.bi_device_error() == 0
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -373,6 +415,8 @@ def run_ours(args, rank, world, local_rank):
             "roofline": roofline, "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
                                                   for kk, vv in v.items()} for k, v in kern.items()},
             "other_rooflines": others, "modes": modes}
+    if decode_sweep:
+        line["decode_batch_sweep"] = decode_sweep
     return line
 
 
@@ -384,6 +428,96 @@ def _source_sha(rel):
     if not os.path.exists(p):
         return None
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def weight_bytes_per_step(shape) -> float:
+    """Bytes of weights one decode step streams: every layer's projections and
+    norms, the final norm and the lm-head (the embedding rows gathered are B rows)."""
+    L = shape.layer
+    per_layer = (L.qkv_dim * L.d_model + L.d_model * L.n_q_heads * L.head_dim + 2 * L.ffn_dim * L.d_model +
+                 L.d_model * L.ffn_dim + 2 * L.d_model + (2 * L.head_dim if L.qk_norm else 0))
+    return 2.0 * (shape.n_layers * per_layer + L.d_model + shape.vocab * L.d_model)
+
+
+class L2Flush:
+    """Writes a buffer larger than L2 (129 MB) between timed launches."""
+
+    def __init__(self, torch):
+        self.buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_launches(torch, fn, reps: int, flush) -> float:
+    """Median milliseconds of `fn` over `reps` launches, each bracketed by CUDA events on
+    the current (launching) stream, L2 flushed before each."""
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        fn()
+        e1.record(st)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def gemm_sweep(torch, bi, synth, pk, warmup: int, reps: int) -> dict:
+    """INVARIANT bi_gemm over the GEMM-sweep shapes at M >= 256 (K = 4096; bf16 out, fp32 out for the
+    lm-head width N = 151936), timed alone with L2 flushed: TFLOP/s against the burst bf16 peak and
+    against the roofline min(peak, AI * HBM); cuBLAS (torch.matmul, bf16 out) on the same operands for
+    context."""
+    flush = L2Flush(torch)
+    out = {}
+    Kd = GEMM_SWEEP_K
+    peak_t = pk["bf16_tflops"]
+    for N in GEMM_SWEEP_N:
+        W = synth.normal_device((N, Kd), 900 + N, std=0.02)
+        for M in GEMM_SWEEP_M:
+            A = synth.normal_device((M, Kd), 800 + M)
+            f32 = N == 151936
+            C = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
+            fn = lambda: bi.bi_gemm(A, W, C)
+            for _ in range(warmup):
+                fn()
+            ms = time_launches(torch, fn, reps, flush)
+            flops = 2.0 * M * N * Kd
+            byts = 2.0 * (M * Kd + N * Kd) + (4 if f32 else 2) * M * N
+            tf = flops / (ms / 1000.0) / 1e12
+            roof = min(peak_t, flops / byts * pk["hbm_gbs"] * 1e9 / 1e12)
+            cb = lambda: torch.matmul(A, W.t())
+            for _ in range(2):
+                cb()
+            cms = time_launches(torch, cb, reps, flush)
+            out["M%d_N%d" % (M, N)] = {"ms": round(ms, 4), "TFLOPs": round(tf, 1), "frac_peak": round(tf / peak_t, 4),
+                                       "roofline_TFLOPs": round(roof, 1), "frac_roofline": round(tf / roof, 4),
+                                       "out": "f32" if f32 else "bf16",
+                                       "cublas_TFLOPs": round(flops / (cms / 1000.0) / 1e12, 1)}
+            del A, C
+        del W
+    torch.cuda.synchronize()
+    return {"K": Kd, "peak_TFLOPs": peak_t, "peak_src": pk["src"] + " bf16_tflops (burst, kernel timed alone)",
+            "l2": "flushed before each launch (256 MB write)", "shapes": out}
+
+
+def rmsnorm_roofline(torch, bi, synth, pk, warmup: int, reps: int) -> dict:
+    """INVARIANT bi_rmsnorm on 16384 rows x 4096 bf16 (one CTA per row): GB/s of the algorithmic bytes
+    (each row read once and written once, gamma once) against the measured HBM copy bandwidth."""
+    rows, d = 16384, 4096
+    x = synth.normal_device((rows, d), 501)
+    g = synth.normal_device((d,), 502, std=0.1, mean=1.0)
+    y = torch.empty_like(x)
+    fn = lambda: bi.bi_rmsnorm(x, g, y, 1e-5)
+    for _ in range(warmup):
+        fn()
+    ms = time_launches(torch, fn, reps, L2Flush(torch))
+    byts = 2.0 * rows * d * 2 + 2 * d
+    gbs = byts / (ms / 1000.0) / 1e9
+    return {"rows": rows, "d": d, "dtype": "bf16", "ms": round(ms, 4), "achieved_GBs": round(gbs, 1),
+            "peak": pk["hbm_gbs"], "frac": round(gbs / pk["hbm_gbs"], 4), "bytes_per_launch": byts}
 
 
 # ---------------------------------------------------------------------------- oracle (CPU) arm
@@ -537,6 +671,15 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     line = run_ours(args, rank, world, local_rank)
+    if args.mode == "invariant" and not args.no_extras:
+        import torch
+
+        import synth
+        import invariant_deterministic_02_gb300 as bi
+        pk = peaks()
+        line["gemm_sweep"] = gemm_sweep(torch, bi, synth, pk, max(3, args.warmup), 10)
+        line["rmsnorm"] = rmsnorm_roofline(torch, bi, synth, pk, max(3, args.warmup), 20)
+        assert bi.bi_device_error() == 0
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             # sample steps until about 10 s of CPU work (at most 16 steps)

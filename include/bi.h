@@ -86,9 +86,32 @@ int32_t bi_version(void);
 /* Streaming-multiprocessor count of the current device (0 if none). */
 int32_t bi_num_sms(void);
 /* Reads and clears the device error words of all kernels (after synchronising
- * `s`).  *code = 0 when no in-kernel wait ran out, else a nonzero site code.
- * Returns BI_ERR_TIMEOUT when *code != 0. */
+ * `s`).  *code = 0 when nothing was recorded, else the site code of the first
+ * event recorded:
+ *   1-4   GEMM: a bounded wait ran out (1 copy slot free, 2 accumulator free,
+ *         3 copies landed, 4 accumulator ready)          -> BI_ERR_TIMEOUT
+ *   11-15 attention: a bounded wait ran out              -> BI_ERR_TIMEOUT
+ *   16    decode attention: a kv_len outside [0, max_pages*16]; it was clamped
+ *   17    attention: a block-table entry outside [0, num_pages), or a position
+ *         past the request's block-table row; page 0 was read instead
+ *   21    K/V store: a position past the block-table row or a page outside the
+ *         cache; that token's K/V were not stored
+ *   22    K/V store: a position outside the RoPE tables; the last row was used
+ *                                                        -> BI_ERR_INVALID_ARG
+ * (16-22: the kernels check these device-side inputs so that no access leaves
+ * the caller's buffers; the outputs of the affected rows are undefined.) */
 bi_status bi_device_error(int32_t* code, bi_stream s);
+
+/* Test hook for the failure path of the bounded in-kernel waits (the pages have
+ * no counterpart).  Arms the next GEMM launch made by this host thread (bi_gemm,
+ * bi_gemm_f32a, or a GEMM inside a layer or model call) so that CTA 0 issues no
+ * copies for its first stage and every wait of that launch gives up after
+ * wait_ns nanoseconds instead of 2 s.  The launch still ends on its own: the
+ * wait for the missing stage runs out, all roles stop, copies in flight are
+ * drained and tensor memory is freed; bi_device_error() then returns
+ * BI_ERR_TIMEOUT with a GEMM site code.  That launch's output is undefined; the
+ * next launch is unaffected.  wait_ns in [1e6, 2e9], else BI_ERR_INVALID_ARG. */
+bi_status bi_debug_arm_gemm_stall(int64_t wait_ns);
 
 /* Kernel timing (off by default).  bi_profile_start creates 2*max_launches CUDA
  * events up front; while it is on, every kernel launch of the library is
@@ -205,7 +228,10 @@ typedef struct bi_attn_dims {
 /* Decode: one query token per request.  q: device [B][num_q_heads][head_dim] bf16
  * (fp32 when dims->act_f32); the query of request b sits at position kv_lens[b]-1
  * and its own K/V must already be in the cache.  kv_lens: device int32 [B],
- * 1 <= kv_len <= max_pages*16.  out: device [B][num_q_heads][head_dim], as q. */
+ * 1 <= kv_len <= max_pages*16 (a length outside [0, max_pages*16] is clamped and
+ * reported by bi_device_error as site 16; block-table entries outside
+ * [0, num_pages) are reported as site 17 and read as page 0).
+ * out: device [B][num_q_heads][head_dim], as q. */
 size_t bi_decode_attention_workspace(int32_t B, const bi_attn_dims* dims, bi_mode mode);
 bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
                               const int32_t* kv_lens, int32_t B, const bi_attn_dims* dims, void* out, bi_mode mode,
@@ -219,13 +245,16 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
  * the library's own device data, which every GPU that loads the library holds
  * until the process exits.  The pages have no counterpart of this call.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up the scratch array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make that
- *     first call before any stream capture.
+ *   - The first call on a device (and again in a new CUDA context of that
+ *     device, e.g. after cudaDeviceReset) looks up the scratch array's device
+ *     address (cudaGetSymbolAddress, with that device current) and caches it;
+ *     make that first call before any stream capture.
  *   - Batches whose scratch need exceeds 16 MiB are rejected with
- *     BI_ERR_UNSUPPORTED and a message naming the need (INVARIANT needs
- *     B * ceil(max_pages*16/256) * num_q_heads * (head_dim+2) * 4 bytes plus a
- *     few int32 per request; FAST/PROTECTED plan up to 64 splits per request).
+ *     BI_ERR_UNSUPPORTED and a message naming the need: U * num_q_heads *
+ *     (head_dim+2) * 4 bytes plus a few int32 per request, for U split units:
+ *     INVARIANT U = B * ceil(max_pages*16/256); FAST U = B * f with
+ *     f = min(64, ceil(4 * SMs / (B * num_kv_heads))); PROTECTED
+ *     U = (B-1) * f + max(f, ceil(max_pages*16/256)).
  *   - All calls share the one array and each call writes every scratch byte it
  *     reads, so nothing needs clearing between calls; calls whose kernels
  *     overlap on the GPU (e.g. on two streams) race on the array and must be

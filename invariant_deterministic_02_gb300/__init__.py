@@ -38,6 +38,7 @@ TOPK_MAX = 32
 
 EXPORTED = [
     "bi_status_string", "bi_last_error_message", "bi_version", "bi_num_sms", "bi_device_error",
+    "bi_debug_arm_gemm_stall",
     "bi_rmsnorm_workspace", "bi_rmsnorm", "bi_gemm_workspace", "bi_gemm_ksplit", "bi_gemm",
     "bi_gemm_f32a_workspace", "bi_gemm_f32a",
     "bi_decode_attention_workspace", "bi_decode_attention", "bi_decode_attention_noalloc",
@@ -105,6 +106,7 @@ def _declare(lib):
         "bi_version": (c_i32, []),
         "bi_num_sms": (c_i32, []),
         "bi_device_error": (c_i32, [P(c_i32), vp]),
+        "bi_debug_arm_gemm_stall": (c_i32, [c_i64]),
         "bi_rmsnorm_workspace": (c_sz, [c_i64, c_i64, c_i32]),
         "bi_rmsnorm": (c_i32, [vp, vp, vp, c_i64, c_i64, c_i32, c_f, c_i32, c_i32, c_i32, vp, c_sz, vp]),
         "bi_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
@@ -193,11 +195,20 @@ def bi_num_sms() -> int:
 
 
 def bi_device_error(stream=None) -> int:
+    """Synchronises, reads and clears the kernels' device error words: 0, or the
+    site code of the first in-kernel wait that ran out (1-15) or of the first
+    out-of-range KV length, block-table entry or position a kernel met (>= 16)."""
     code = ctypes.c_int32(0)
     st = lib().bi_device_error(ctypes.byref(code), _stream(stream))
-    if st not in (BI_OK, BI_ERR_TIMEOUT):
+    if st not in (BI_OK, BI_ERR_TIMEOUT, BI_ERR_INVALID_ARG) or (st != BI_OK and code.value == 0):
         _check(st, "bi_device_error")
     return int(code.value)
+
+
+def bi_debug_arm_gemm_stall(wait_ns: int):
+    """Test hook: the next bi_gemm of this thread drops one stage's copies and its
+    waits give up after wait_ns (see include/bi.h)."""
+    _check(lib().bi_debug_arm_gemm_stall(int(wait_ns)), "bi_debug_arm_gemm_stall")
 
 
 def bi_rmsnorm(x, gamma, y, eps: float, mode=INVARIANT, target_row=-1, target_count=0, workspace=None,

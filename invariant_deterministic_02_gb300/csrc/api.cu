@@ -1,5 +1,8 @@
 // Library-wide C entry points: status strings, error detail, device facts.
+#include <map>
 #include <mutex>
+#include <set>
+#include <tuple>
 #include <vector>
 
 #include "common.cuh"
@@ -36,9 +39,41 @@ int num_sms() {
   return g_sm_count[dev];
 }
 
+namespace {
+std::mutex g_attr_mutex;
+std::set<std::tuple<const void*, int, int>> g_smem_set;          // (kernel, device, bytes) already raised
+std::map<std::tuple<const void*, int, int, size_t>, int> g_occ;  // (kernel, device, threads, smem) -> CTAs/SM
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  const auto key = std::make_tuple(kernel, dev, bytes);
+  if (g_smem_set.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_smem_set.insert(key);
+  return e;
+}
+
+int occupancy_per_sm(const void* kernel, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  const auto key = std::make_tuple(kernel, dev, threads, smem);
+  auto it = g_occ.find(key);
+  if (it != g_occ.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+  g_occ[key] = n;
+  return n;
+}
+
 // Defined next to the kernels that own a device error word.
 int take_gemm_device_error(cudaStream_t s, int32_t* code);
 int take_attn_device_error(cudaStream_t s, int32_t* code);
+int take_pointwise_device_error(cudaStream_t s, int32_t* code);
 
 // ------------------------------------------------------------------ launch timer
 volatile int g_profiling = 0;
@@ -150,16 +185,19 @@ extern "C" bi_status bi_device_error(int32_t* code, bi_stream s) {
   *code = 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   BI_CUDA_TRY(cudaStreamSynchronize(st));
-  int32_t c = 0, ca = 0;
-  if (bi::take_gemm_device_error(st, &c) != 0 || bi::take_attn_device_error(st, &ca) != 0) {
-    bi::set_error("bi_device_error: reading the device error word failed");
+  int32_t cg = 0, ca = 0, cp = 0;
+  if (bi::take_gemm_device_error(st, &cg) != 0 || bi::take_attn_device_error(st, &ca) != 0 ||
+      bi::take_pointwise_device_error(st, &cp) != 0) {
+    bi::set_error("bi_device_error: reading the device error words failed");
     return BI_ERR_CUDA;
   }
-  if (c == 0) c = ca;
+  const int32_t c = cg != 0 ? cg : ca != 0 ? ca : cp;
   *code = c;
-  if (c != 0) {
-    bi::set_error("an in-kernel wait ran out (site code %d)", c);
-    return BI_ERR_TIMEOUT;
+  if (c == 0) return BI_OK;
+  if (c >= 16) {
+    bi::set_error("a kernel met an out-of-range KV length, block-table entry or position (site code %d)", c);
+    return BI_ERR_INVALID_ARG;
   }
-  return BI_OK;
+  bi::set_error("an in-kernel wait ran out (site code %d)", c);
+  return BI_ERR_TIMEOUT;
 }

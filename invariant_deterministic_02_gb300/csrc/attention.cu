@@ -573,6 +573,7 @@ __device__ __forceinline__ void store_out4(const ActDst& out, size_t off, float 
 // Plan per request b: geometry (invariant or fast), unit length, unit count,
 // exclusive prefix of unit counts.  One CTA; B may be large.
 struct DecodePlan {
+  int* len;      // [B] KV length, clamped to [0, max_pages*16] (an out-of-range length is reported)
   int* mode;     // [B]
   int* ulen;     // [B] positions per unit
   int* nunits;   // [B]
@@ -580,8 +581,27 @@ struct DecodePlan {
   int* counter;  // [1] next unclaimed work item of the split kernel (0 between launches)
 };
 
+// Error-word site codes of this file: 11-15 a bounded wait ran out; 16 a KV
+// length outside [0, max_pages*16] (clamped); 17 a block-table entry outside
+// [0, num_pages) or a position past the block-table row (page 0 read instead).
+constexpr unsigned kSiteBadLength = 16;
+constexpr unsigned kSiteBadPage = 17;
+
+// Page of position-block `pi` of a request's block-table row, checked: an entry
+// past the row or outside the cache is reported and replaced by page 0, so no
+// access leaves the caller's buffers.
+__device__ __forceinline__ int checked_page(const int* __restrict__ brow, int pi, int max_pages, int num_pages) {
+  const int pg = (pi >= 0 && pi < max_pages) ? brow[pi] : -1;
+  if (pg < 0 || pg >= num_pages) {
+    atomicCAS(&g_attn_err_word, 0u, kSiteBadPage);
+    return 0;
+  }
+  return pg;
+}
+
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict__ kv_lens, int B, int hkv, int mode,
-                                                           int target, int fast_units_wanted, DecodePlan plan) {
+                                                           int target, int fast_units_wanted, int max_tokens,
+                                                           DecodePlan plan) {
   pdl_wait();
   pdl_trigger();
   __shared__ int part[1024];
@@ -591,7 +611,12 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict
   const int b0 = min(B, t * per), b1 = min(B, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b) {
-    const int L = kv_lens[b];
+    int L = kv_lens[b];
+    if (L < 0 || L > max_tokens) {
+      atomicCAS(&g_attn_err_word, 0u, kSiteBadLength);
+      L = L < 0 ? 0 : max_tokens;
+    }
+    plan.len[b] = L;
     const bool inv = (mode == BI_MODE_INVARIANT) || (mode == BI_MODE_PROTECTED && b == target);
     int ul, n;
     if (inv) {
@@ -673,8 +698,8 @@ struct DecodeSmem {
 template <int HD, int G>
 __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const __nv_bfloat16* __restrict__ kc,
-    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, const int* __restrict__ kv_lens, int B,
-    int hq, int hkv, int max_pages, float scale_log2, DecodePlan plan, Partials part) {
+    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, int B, int hq, int hkv, int max_pages,
+    int num_pages, float scale_log2, DecodePlan plan, Partials part) {
   // qf: fp32 queries (fp32-activation layers; q unused).  The consumers then
   // read q from global memory and the item ring carries the descriptor only.
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -739,7 +764,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
         const int b = find_row(plan.prefix, B, u);
         const int ul = plan.ulen[b];
         const int us = (u - plan.prefix[b]) * ul;
-        S.item[slot] = make_int4(u, g, us, min(kv_lens[b], us + ul));
+        S.item[slot] = make_int4(u, g, us, min(plan.len[b], us + ul));
         if (qf != nullptr) {
           mbar_arrive(ifull0 + 8 * slot);  // release: the descriptor store
         } else {
@@ -760,7 +785,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
       const int g = item % hkv;
       const int b = find_row(plan.prefix, B, u);
       const int s = u - plan.prefix[b];
-      const int L = kv_lens[b];
+      const int L = plan.len[b];
       const int ul = plan.ulen[b];
       const int ustart = s * ul;
       const int uend = min(L, ustart + ul);
@@ -781,7 +806,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
           __syncwarp();
           if (plane < npg) {
             const __nv_bfloat16* cache = (j < 4) ? kc : vc;
-            const int page = brow[(bs + q0) / kPage + plane];
+            const int page = checked_page(brow, (bs + q0) / kPage + plane, max_pages, num_pages);
             const __nv_bfloat16* src = cache + (static_cast<size_t>(page) * hkv + g) * kPage * HD;
             bulk_g2s(smem_u32(&S.ring[st][plane * kPage * HD]), src, kPage * HD * 2, fb);
           }
@@ -1034,8 +1059,8 @@ template <int HD, int G>
 __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_kernel(
     const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, const int* __restrict__ q_pos0,
-    const int* __restrict__ q_start, int hq, int hkv, int max_pages, float scale_log2, PrefillPlan plan,
-    Partials part) {
+    const int* __restrict__ q_start, int hq, int hkv, int max_pages, int num_pages, float scale_log2,
+    PrefillPlan plan, Partials part) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -1067,7 +1092,7 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
     for (int idx = threadIdx.x; idx < rows * CH; idx += blockDim.x) {
       const int r = idx / CH, ch = idx % CH;
       const int pos = st + r;
-      const int pg = block_table[static_cast<size_t>(b) * max_pages + pos / kPage];
+      const int pg = checked_page(block_table + static_cast<size_t>(b) * max_pages, pos / kPage, max_pages, num_pages);
       const size_t off = ((static_cast<size_t>(pg) * hkv + g) * kPage + (pos % kPage)) * HD + ch * 8;
       *reinterpret_cast<uint4*>(&sm.k[r][ch * 8]) = *reinterpret_cast<const uint4*>(kc + off);
       *reinterpret_cast<uint4*>(&sm.v[r][ch * 8]) = *reinterpret_cast<const uint4*>(vc + off);
@@ -1159,6 +1184,7 @@ struct DecodeWs {
 // Plan arrays of a decode batch (small; reusable by every layer of a step).
 size_t carve_decode_plan(void* base, int B, int hkv, DecodePlan* plan) {
   WsCarver cv(base, 0);
+  plan->len = cv.take<int>(B);
   plan->mode = cv.take<int>(B);
   plan->ulen = cv.take<int>(B);
   plan->nunits = cv.take<int>(B);
@@ -1214,21 +1240,17 @@ PrefillWs carve_prefill(void* ws, size_t cap, int B, int T, const bi_attn_dims* 
 }
 
 template <int HD, int G>
-int decode_grid() {
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    const size_t smem = sizeof(DecodeSmem<HD, G>);
-    int n = 0;
-    if (cudaFuncSetAttribute(decode_split_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<HD, G>, kDecodeThreads, smem) !=
-            cudaSuccess ||
-        n < 1)
-      n = 1;
-    per_sm = n;
-  }
-  return per_sm * num_sms();
+bi_status decode_grid(int* grid) {
+  const size_t smem = sizeof(DecodeSmem<HD, G>);
+  const void* fn = reinterpret_cast<const void*>(decode_split_kernel<HD, G>);
+  BI_CUDA_TRY(ensure_smem_limit(fn, static_cast<int>(smem)));
+  *grid = occupancy_per_sm(fn, kDecodeThreads, smem) * num_sms();
+  return BI_OK;
 }
+
+// Units per request the FAST plan asks for (the plan kernel caps it at 64 and
+// at the request's page count): about four work items per SM over the batch.
+int fast_units_wanted(int B, int hkv) { return std::max(1, (4 * num_sms() + B * hkv - 1) / (B * hkv)); }
 
 template <int HD, int G>
 bi_status decode_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* kv_lens,
@@ -1238,20 +1260,21 @@ bi_status decode_launch(const void* q, const void* kc, const void* vc, const int
   const bool qf = dm->act_f32 != 0;
   if (mode == BI_MODE_INVARIANT_KSPLIT) mode = BI_MODE_INVARIANT;  // the split-K variant changes the GEMM only
   if (make_plan) {
-    const int fast_units = std::max(1, (4 * num_sms() + B * dm->num_kv_heads - 1) / (B * dm->num_kv_heads));
+    const int fast_units = fast_units_wanted(B, dm->num_kv_heads);
     BI_TIMED(::bi::kTagAttnPlan, s,
-             BI_PDL_CHECK(launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, kv_lens, B, dm->num_kv_heads, static_cast<int>(mode), target,
-                                                    fast_units, w.plan)));
+             BI_PDL_CHECK(launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, kv_lens, B, dm->num_kv_heads,
+                                     static_cast<int>(mode), target, fast_units, dm->max_pages * kPage, w.plan)));
     BI_LAUNCH_CHECK();
   }
   const float sl2 = dm->scale * kLog2e;
-  const int grid = decode_grid<HD, G>();
+  int grid = 0;
+  BI_TRY((decode_grid<HD, G>(&grid)));
   const size_t dsmem = sizeof(DecodeSmem<HD, G>);
   BI_TIMED(::bi::kTagAttnDecodeSplit, s,
            BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G>, dim3(grid), dim3(kDecodeThreads), dsmem, s, 
                qf ? nullptr : static_cast<const __nv_bfloat16*>(q), qf ? static_cast<const float*>(q) : nullptr,
-               static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt, kv_lens, B,
-               dm->num_q_heads, dm->num_kv_heads, dm->max_pages, sl2, w.plan, w.part)));
+               static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt, B,
+               dm->num_q_heads, dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
   BI_TIMED(::bi::kTagAttnDecodeMerge, s,
            BI_PDL_CHECK(launch_pdl(decode_merge_kernel, dim3(B * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part,
@@ -1269,17 +1292,12 @@ bi_status prefill_launch(const void* q, const void* kc, const void* vc, const in
   BI_TIMED(::bi::kTagAttnPlan, s, BI_PDL_CHECK(launch_pdl(prefill_plan_kernel, dim3(1), dim3(1024), 0, s, q_start, q_pos0, B, T, static_cast<int>(mode), target, w.plan)));
   BI_LAUNCH_CHECK();
   const size_t smem = sizeof(PrefillSmem<HD, G>);
-  static bool attr_set = false;
-  if (!attr_set) {
-    BI_CUDA_TRY(cudaFuncSetAttribute(prefill_split_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)));
-    attr_set = true;
-  }
+  BI_CUDA_TRY(ensure_smem_limit(reinterpret_cast<const void*>(prefill_split_kernel<HD, G>), static_cast<int>(smem)));
   const float sl2 = dm->scale * kLog2e;
   BI_TIMED(::bi::kTagAttnPrefillSplit, s, BI_PDL_CHECK(launch_pdl(prefill_split_kernel<HD, G>, dim3(num_sms()), dim3(kGroupThreads * kPrefillGroups), smem, s, 
       qf ? nullptr : static_cast<const __nv_bfloat16*>(q), qf ? static_cast<const float*>(q) : nullptr,
       static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt, q_pos0, q_start,
-      dm->num_q_heads, dm->num_kv_heads, dm->max_pages, sl2, w.plan, w.part)));
+      dm->num_q_heads, dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part)));
   BI_LAUNCH_CHECK();
   BI_TIMED(::bi::kTagAttnPrefillMerge, s, BI_PDL_CHECK(launch_pdl(prefill_merge_kernel, dim3(T * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part, w.plan, q_start, q_pos0, B,
                                                                out, dm->num_q_heads, dm->num_kv_heads, HD)));
@@ -1372,33 +1390,63 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per GPU tha
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mutex;
-std::vector<void*> g_noalloc_address;  // device address of the scratch, per device
+// device address of the scratch, per (device, CUDA context): a context created
+// after a device reset gets its own lookup
+std::vector<std::pair<std::pair<int, void*>, void*>> g_noalloc_address;
+
+// The current CUDA context (the driver's cuCtxGetCurrent, reached through the
+// runtime's entry-point query), or null if it cannot be read.
+void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(p);
+  });
+  void* ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
 
 // Device address of the scratch array on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device and context (with that device current) and cached.
 bi_status noalloc_scratch_address(void** out) {
   int dev = 0;
   BI_CUDA_TRY(cudaGetDevice(&dev));
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (dev >= static_cast<int>(g_noalloc_address.size())) g_noalloc_address.resize(dev + 1, nullptr);
-  if (g_noalloc_address[dev] == nullptr) {
-    void* p = nullptr;
-    BI_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
-    g_noalloc_address[dev] = p;
-  }
-  *out = g_noalloc_address[dev];
+  const auto key = std::make_pair(dev, current_context());
+  for (const auto& e : g_noalloc_address)
+    if (e.first == key && key.second != nullptr) {
+      *out = e.second;
+      return BI_OK;
+    }
+  void* p = nullptr;
+  BI_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));  // also makes the device's context current
+  g_noalloc_address.emplace_back(std::make_pair(dev, current_context()), p);
+  *out = p;
   return BI_OK;
 }
 
 // Scratch layout of one call: the same plan and partial-state arrays as the
-// workspace path, with the partial states sized for the units `mode` can plan
-// (INVARIANT: one per 256 tokens of the longest allowed request).
-DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode mode) {
+// workspace path, with the partial states sized for the units `mode` can plan:
+// INVARIANT one per 256 tokens of the longest allowed request; FAST at most
+// f = min(64, fast_units_wanted) per request (the value decode_launch passes to
+// the plan kernel, computed by the same function); PROTECTED f per request
+// plus the target's invariant units.
+DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode mode, int target) {
   DecodeWs r;
   const size_t pb = carve_decode_plan(base, B, dm->num_kv_heads, &r.plan);
-  const int inv = (dm->max_pages * kPage + kSplit - 1) / kSplit;
-  const size_t units = static_cast<size_t>(B) * (mode_invariant(mode) ? inv : std::max(inv, kMaxFastUnits));
+  const size_t inv = static_cast<size_t>((dm->max_pages * kPage + kSplit - 1) / kSplit);
+  const size_t f = static_cast<size_t>(std::min(kMaxFastUnits, fast_units_wanted(B, dm->num_kv_heads)));
+  size_t units;
+  if (mode_invariant(mode)) units = static_cast<size_t>(B) * inv;
+  else if (mode == BI_MODE_PROTECTED && target >= 0) units = static_cast<size_t>(B - 1) * f + std::max(inv, f);
+  else units = static_cast<size_t>(B) * f;
   const size_t qb = carve_decode_parts(base ? static_cast<char*>(base) + pb : nullptr, units, dm, &r.part);
   r.bytes = pb + qb;
   return r;
@@ -1419,17 +1467,17 @@ bi_status decode_attention_noalloc_impl(const void* q, const void* kc, const voi
   BI_REQUIRE(q && kc && vc && bt && kv_lens && out, BI_ERR_INVALID_ARG, "bi_decode_attention_noalloc: null pointer");
   BI_REQUIRE(aligned16(q) && aligned16(kc) && aligned16(vc) && aligned16(out), BI_ERR_INVALID_ARG,
              "bi_decode_attention_noalloc: q/caches/out must be 16-byte aligned");
-  const size_t need = attn::carve_decode_noalloc(nullptr, B, dims, mode).bytes;
+  const int tgt = mode == BI_MODE_PROTECTED ? target : -1;
+  const size_t need = attn::carve_decode_noalloc(nullptr, B, dims, mode, tgt).bytes;
   BI_REQUIRE(need <= attn::kNoAllocScratchBytes, BI_ERR_UNSUPPORTED,
              "bi_decode_attention_noalloc: this batch needs %zu bytes of scratch but the fixed scratch holds %zu "
              "bytes; use bi_decode_attention with a caller workspace",
              need, attn::kNoAllocScratchBytes);
   void* base = nullptr;
   BI_TRY(attn::noalloc_scratch_address(&base));
-  attn::DecodeWs w = attn::carve_decode_noalloc(base, B, dims, mode);
+  attn::DecodeWs w = attn::carve_decode_noalloc(base, B, dims, mode, tgt);
   const ActDst od{out, 0, dims->act_f32 ? kActF32 : kActBF16};
-  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, od, mode,
-                   mode == BI_MODE_PROTECTED ? target : -1, w, s);
+  BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, od, mode, tgt, w, s);
 }
 
 // Decode attention for the layer loop: the plan lives in `plan_ws` (sized by

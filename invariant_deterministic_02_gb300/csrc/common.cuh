@@ -19,6 +19,13 @@ namespace bi {
 void set_error(const char* fmt, ...);
 void clear_error();
 int num_sms();  // SM count of the current device (cached per device)
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); thread-safe.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+// Resident CTAs per SM of `kernel` at `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device (after ensure_smem_limit),
+// cached per (kernel, device); 1 if the query fails.
+int occupancy_per_sm(const void* kernel, int threads, size_t smem);
 
 #define BI_REQUIRE(cond, code, ...)     \
   do {                                  \

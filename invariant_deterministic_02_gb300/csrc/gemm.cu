@@ -88,6 +88,8 @@ struct Args {
   int out_kind;
   int plane_rows;          // rows of each A plane (three planes for fp32 A; the kernel's PL)
   const float* Rf;         // fp32 residual (fp32 output) or null
+  unsigned long long wait_ns;  // limit of every bounded wait (2 s; shorter only under the test hook below)
+  int drop_first_stage;        // test hook: CTA 0 issues no copies for its first stage (its waits then run out)
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -129,7 +131,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Bounded wait, slow path.  Returns false (after recording `site`) when the
 // limit runs out or another role has already aborted.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site) {
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site,
+                                       uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -138,7 +141,7 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
       const uint64_t now = global_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns) {
         atomicCAS(&g_err_word, 0u, static_cast<unsigned>(site));
         *abort_flag = 1;
         return false;
@@ -147,9 +150,10 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site) {
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int site,
+                                             uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, abort_flag, site);
+  return wait_slow(bar, parity, abort_flag, site, limit_ns);
 }
 
 // Time-bounded wait that ignores the abort flag (used while draining after an abort).
@@ -367,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // ------------------------------------------------------------ TMA producer
     // One thread issues A then B of every stage in consumption order.
     if (lane == 0) {
-      uint32_t issued_mask = 0, issued_par = 0;
+      // the stages whose weight copies went out before the wait (first use, parity 0)
+      uint32_t issued_mask = pre_stages >= 32 ? ~0u : ((1u << pre_stages) - 1u), issued_par = 0;
       bool ok = true;
       int st = 0;        // stage slot and its phase parity, advanced in the same
       uint32_t ph = 0;   // sequence as the MMA thread's
@@ -390,9 +395,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 else tma_load_2d(sa + pl * a_plane, &tmA, fb, kb * kBK, pl * a.plane_rows + mt * kBM);
               }
             } else {
-              if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1)) {
+              if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 1, a.wait_ns)) {
                 ok = false;
                 break;
+              }
+              if (a.drop_first_stage && blockIdx.x == 0 && u == static_cast<int>(blockIdx.x) && kb == kb0 &&
+                  q == 0) {
+                // test hook: this stage's barrier is never armed and nothing lands in it, so the MMA
+                // thread's wait for it runs out (the stage is not counted as issued: nothing to drain)
+                if (++st == kStages) {
+                  st = 0;
+                  ph ^= 1u;
+                }
+                continue;
               }
               mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
               if (a.map3d) {
@@ -416,11 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
         }
       }
-      if (*abort_flag) {
-        // let copies already in flight land before shared memory is released
-        for (int i = 0; i < kStages; ++i)
-          if (issued_mask & (1u << i)) wait_drain(full0 + 8 * i, (issued_par >> i) & 1u);
-      }
+      // Let every copy issued land before shared memory is released.  After a
+      // normal run the MMA thread has already waited on each of them, so these
+      // return at once; after an abort (which another role may raise after this
+      // loop has ended) they keep the CTA alive until its copies are done.
+      for (int i = 0; i < kStages; ++i)
+        if (issued_mask & (1u << i)) wait_drain(full0 + 8 * i, (issued_par >> i) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -443,14 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           int kb0, kb1;
           if (seq > 1) k_range(a.kb_total, q, seq, kb0, kb1);
           else k_range(a.kb_total, s, ns, kb0, kb1);
-          if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 2)) {
+          if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 2, a.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * TN);
           for (int kb = kb0; kb < kb1; kb += kbs) {
-            if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3)) {
+            if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -526,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       const int row = mt * kBM + row_in_tile;
       const bool row_ok = row < a.M;
       for (int q = 0; q < seq; ++q) {
-        if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 4)) {
+        if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 4, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -901,11 +917,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
 
 template <int TN, int PL>
 bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    BI_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<TN, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
-    attr = true;
-  }
+  BI_CUDA_TRY(ensure_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<TN, PL>), kSmemLimit));
   const size_t smem = smem_bytes(args.stages, args.stage_bytes, args.a_rows);
   const int grid = std::min(args.units, num_sms());
   BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<TN, PL>, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
@@ -941,6 +953,10 @@ size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode, int planes) {
 size_t gemm_ws(int64_t M, int64_t N, int64_t K, bi_mode mode) { return gemm_ws(M, N, K, mode, 1); }
 
 namespace {
+
+// Test hook state (bi_debug_arm_gemm_stall): the next GEMM launch of this host
+// thread drops its first stage's copies in CTA 0 and uses a short wait limit.
+thread_local unsigned long long t_stall_wait_ns = 0;
 
 // Shared body of the bf16-A and fp32-A (planes) GEMMs.  A: [M][K] bf16, or
 // three bf16 planes [3][M][K] when planes == 3.  R: bf16 residual (bf16 out);
@@ -1001,6 +1017,14 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   args.plane_rows = static_cast<int>(M);
   args.out_kind = out_dtype == BI_F32 ? gemm::kOutF32 : gemm::kOutBF16;
   args.partial = nullptr;
+  args.wait_ns = gemm::kWaitLimitNs;
+  args.drop_first_stage = 0;
+  if (t_stall_wait_ns != 0) {
+    args.wait_ns = t_stall_wait_ns;
+    args.drop_first_stage = 1;
+    args.prefetch_w = 0;
+    t_stall_wait_ns = 0;
+  }
   if (p.splits > 1) {
     const size_t need = static_cast<size_t>(p.splits) * M * N * sizeof(float);
     BI_REQUIRE(ws != nullptr && ws_bytes >= need && aligned16(ws), BI_ERR_WORKSPACE,
@@ -1110,6 +1134,14 @@ extern "C" bi_status bi_gemm_f32a(const float* A, const void* W, float* C, const
                                   void* workspace, size_t ws_bytes, bi_stream s) {
   return bi::gemm_f32a_impl(A, W, C, residual, M, N, K, mode, target_row, target_count, workspace, ws_bytes,
                             reinterpret_cast<cudaStream_t>(s));
+}
+
+extern "C" bi_status bi_debug_arm_gemm_stall(int64_t wait_ns) {
+  bi::clear_error();
+  BI_REQUIRE(wait_ns >= 1000000 && wait_ns <= 2000000000, BI_ERR_INVALID_ARG,
+             "bi_debug_arm_gemm_stall: wait limit %lld ns outside [1e6, 2e9]", static_cast<long long>(wait_ns));
+  bi::t_stall_wait_ns = static_cast<unsigned long long>(wait_ns);
+  return BI_OK;
 }
 
 extern "C" int32_t bi_gemm_ksplit(int64_t N, int64_t K) {

@@ -39,7 +39,7 @@ bi_status prefill_attention_layer(const void*, const void*, const void*, const i
 size_t prefill_attention_ws(int32_t, int32_t, const bi_attn_dims*);
 bi_status qkv_rope_store_impl(const void*, const float*, const float*, const int32_t*, const int32_t*,
                               const int32_t*, int32_t, const bi_attn_dims*, void*, void*, void*, cudaStream_t,
-                              const void* q_norm, const void* k_norm, float eps, bool act_f32);
+                              const void* q_norm, const void* k_norm, float eps, bool act_f32, int max_pos);
 bi_status swiglu_impl(const void*, void*, int64_t, int64_t, cudaStream_t);
 bi_status swiglu_planes_impl(const void*, void*, int64_t, int64_t, cudaStream_t);
 bi_status embed_impl(const int32_t*, const void*, void*, int64_t, int64_t, int64_t, cudaStream_t);
@@ -219,7 +219,7 @@ bi_status layer_body_f32(const bi_model_dims* dm, const bi_layer_weights* w, con
   BI_TRY(rmsnorm_planes_impl(hidden, w->attn_norm, L.x, T, d, dm->rms_eps, mode, trow, tcnt, L.sub, L.sub_bytes, s));
   BI_TRY(gemm_planes_impl(L.x, w->w_qkv, qkv, nullptr, T, qkvw, d, mode, trow, tcnt, L.sub, L.sub_bytes, s, true));
   BI_TRY(qkv_rope_store_impl(qkv, rc, rs, L.token_pos, L.token_req, b->block_table, static_cast<int32_t>(T), &ad,
-                             L.q, kc, vc, s, w->q_norm, w->k_norm, dm->rms_eps, true));
+                             L.q, kc, vc, s, w->q_norm, w->k_norm, dm->rms_eps, true, dm->max_pos));
   const ActDst att{L.att, static_cast<size_t>(T * hq), kActPlanes};
   if (b->max_q_len == 1 && T == b->num_requests) {
     BI_TRY(decode_attention_layer(L.q, kc, vc, b->block_table, L.kv_len, b->num_requests, &ad, att, mode, treq,
@@ -255,7 +255,7 @@ bi_status layer_body(const bi_model_dims* dm, const bi_layer_weights* w, const f
   BI_TRY(rmsnorm_impl(hidden, w->attn_norm, L.x, T, d, BI_BF16, dm->rms_eps, mode, trow, tcnt, L.sub, L.sub_bytes, s));
   BI_TRY(gemm_impl(L.x, w->w_qkv, L.qkv, nullptr, T, qkvw, d, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s, true));
   BI_TRY(qkv_rope_store_impl(L.qkv, rc, rs, L.token_pos, L.token_req, b->block_table, static_cast<int32_t>(T), &ad,
-                             L.q, kc, vc, s, w->q_norm, w->k_norm, dm->rms_eps, false));
+                             L.q, kc, vc, s, w->q_norm, w->k_norm, dm->rms_eps, false, dm->max_pos));
   if (b->max_q_len == 1 && T == b->num_requests) {
     BI_TRY(decode_attention_layer(L.q, kc, vc, b->block_table, L.kv_len, b->num_requests, &ad,
                                   ActDst{L.att, 0, kActBF16}, mode, treq, L.dplan, plan_attention, L.sub, L.sub_bytes,

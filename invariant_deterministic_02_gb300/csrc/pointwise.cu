@@ -68,11 +68,31 @@ struct QkvIo {
   }
 };
 
+// Error word of this file: 21 a K/V store whose position lies past the
+// block-table row or whose page lies outside the cache (the store is skipped);
+// 22 a position outside the RoPE table (the last row is used).
+__device__ unsigned int g_pw_err_word = 0;
+constexpr unsigned kSiteBadStore = 21;
+constexpr unsigned kSiteBadPos = 22;
+
+// Cache page of position `pos` of request `req`, or -1 (reported) when the
+// position lies past the block-table row or the entry lies outside the cache.
+__device__ __forceinline__ int store_page(const int32_t* __restrict__ block_table, int req, int pos, int max_pages,
+                                          int num_pages) {
+  const int pi = pos / BI_PAGE_SIZE;
+  const int pg = (pos >= 0 && pi < max_pages) ? block_table[static_cast<size_t>(req) * max_pages + pi] : -1;
+  if (pg < 0 || pg >= num_pages) {
+    atomicCAS(&g_pw_err_word, 0u, kSiteBadStore);
+    return -1;
+  }
+  return pg;
+}
+
 template <bool F32>
 __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
     const typename QkvIo<F32>::T* __restrict__ qkv, const float* __restrict__ rc, const float* __restrict__ rs,
     const int32_t* __restrict__ token_pos, const int32_t* __restrict__ token_req,
-    const int32_t* __restrict__ block_table, int max_pages, int hq, int hkv, int hd,
+    const int32_t* __restrict__ block_table, int max_pages, int num_pages, int max_pos, int hq, int hkv, int hd,
     typename QkvIo<F32>::T* __restrict__ q_out, __nv_bfloat16* __restrict__ kc, __nv_bfloat16* __restrict__ vc,
     const __nv_bfloat16* __restrict__ qn, const __nv_bfloat16* __restrict__ kn, float eps) {
   using T = typename QkvIo<F32>::T;
@@ -88,8 +108,8 @@ __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
   if (task >= hq + hkv) {
     // v row of kv head h: stored in the cache (rounded to bf16 from fp32 activations)
     const int h = task - hq - hkv;
-    const int req = token_req[t];
-    const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
+    const int page = store_page(block_table, token_req[t], pos, max_pages, num_pages);
+    if (page < 0) return;
     const T* src = row + (hq + hkv + h) * hd;
     uint4* dst = reinterpret_cast<uint4*>(vc + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE +
                                                 pos % BI_PAGE_SIZE) * hd);
@@ -114,13 +134,18 @@ __global__ void __launch_bounds__(256) qkv_rope_store_kernel(
   if (is_q) {
     qdst = q_out + (static_cast<size_t>(t) * hq + h) * hd;
   } else {
-    const int req = token_req[t];
-    const int page = block_table[static_cast<size_t>(req) * max_pages + pos / BI_PAGE_SIZE];
+    const int page = store_page(block_table, token_req[t], pos, max_pages, num_pages);
+    if (page < 0) return;
     kdst = reinterpret_cast<uint16_t*>(kc) + ((static_cast<size_t>(page) * hkv + h) * BI_PAGE_SIZE +
                                               pos % BI_PAGE_SIZE) * hd;
   }
-  const float* c_row = rc + static_cast<size_t>(pos) * half;
-  const float* s_row = rs + static_cast<size_t>(pos) * half;
+  int tpos = pos;  // row of the RoPE tables
+  if (tpos < 0 || tpos >= max_pos) {
+    if (lane == 0) atomicCAS(&g_pw_err_word, 0u, kSiteBadPos);
+    tpos = tpos < 0 ? 0 : max_pos - 1;
+  }
+  const float* c_row = rc + static_cast<size_t>(tpos) * half;
+  const float* s_row = rs + static_cast<size_t>(tpos) * half;
   const __nv_bfloat16* g = is_q ? qn : kn;
   float r = 0.f;
   if (g != nullptr) {
@@ -256,7 +281,7 @@ bi_status embed_impl(const int32_t* ids, const void* table, void* out, int64_t T
 bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs, const int32_t* token_pos,
                               const int32_t* token_req, const int32_t* block_table, int32_t T,
                               const bi_attn_dims* dm, void* q_out, void* kc, void* vc, cudaStream_t s,
-                              const void* q_norm, const void* k_norm, float eps, bool act_f32) {
+                              const void* q_norm, const void* k_norm, float eps, bool act_f32, int max_pos) {
   BI_REQUIRE(dm && T >= 0, BI_ERR_INVALID_ARG, "bi_qkv_rope_store: dims/T");
   BI_REQUIRE(dm->head_dim % 16 == 0 && dm->head_dim >= 16 && dm->num_kv_heads >= 1 && dm->num_q_heads >= 1,
              BI_ERR_UNSUPPORTED, "bi_qkv_rope_store: head_dim %d", dm->head_dim);
@@ -271,13 +296,15 @@ bi_status qkv_rope_store_impl(const void* qkv, const float* rc, const float* rs,
   const dim3 grid(T, (dm->num_q_heads + 2 * dm->num_kv_heads + 7) / 8);
   if (act_f32) {
     BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel<true>, grid, dim3(256), 0, s, static_cast<const float*>(qkv), rc, rs, token_pos, token_req,
-                                            block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
+                                            block_table, dm->max_pages, dm->num_pages, max_pos, dm->num_q_heads,
+                                            dm->num_kv_heads, dm->head_dim,
                                             static_cast<float*>(q_out), static_cast<__nv_bfloat16*>(kc),
                                             static_cast<__nv_bfloat16*>(vc), static_cast<const __nv_bfloat16*>(q_norm),
                                             static_cast<const __nv_bfloat16*>(k_norm), eps)));
   } else {
     BI_TIMED(::bi::kTagQkvRope, s, BI_PDL_CHECK(launch_pdl(qkv_rope_store_kernel<false>, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(qkv), rc, rs, token_pos, token_req,
-                                            block_table, dm->max_pages, dm->num_q_heads, dm->num_kv_heads, dm->head_dim,
+                                            block_table, dm->max_pages, dm->num_pages, max_pos, dm->num_q_heads,
+                                            dm->num_kv_heads, dm->head_dim,
                                             static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(kc),
                                             static_cast<__nv_bfloat16*>(vc), static_cast<const __nv_bfloat16*>(q_norm),
                                             static_cast<const __nv_bfloat16*>(k_norm), eps)));
@@ -353,13 +380,31 @@ extern "C" bi_status bi_rope_table(double theta, int32_t head_dim, int32_t max_p
   return bi::rope_table_impl(theta, head_dim, max_pos, cos_out, sin_out, reinterpret_cast<cudaStream_t>(s));
 }
 
+namespace bi {
+
+int take_pointwise_device_error(cudaStream_t s, int32_t* code) {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_pw_err_word, sizeof(v), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess) return 1;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return 1;
+  if (v != 0) {
+    unsigned zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_pw_err_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return 1;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return 1;
+  }
+  *code = static_cast<int32_t>(v);
+  return 0;
+}
+
+}  // namespace bi
+
 extern "C" bi_status bi_qkv_rope_store(const void* qkv, const float* rope_cos, const float* rope_sin,
                                        const int32_t* token_pos, const int32_t* token_req, const int32_t* block_table,
                                        int32_t T, const bi_attn_dims* dims, void* q_out, void* k_cache, void* v_cache,
                                        bi_stream s) {
   bi::clear_error();
   return bi::qkv_rope_store_impl(qkv, rope_cos, rope_sin, token_pos, token_req, block_table, T, dims, q_out, k_cache,
-                                 v_cache, reinterpret_cast<cudaStream_t>(s), nullptr, nullptr, 0.f, false);
+                                 v_cache, reinterpret_cast<cudaStream_t>(s), nullptr, nullptr, 0.f, false, INT32_MAX);
 }
 
 extern "C" bi_status bi_swiglu(const void* gu, void* out, int64_t T, int64_t F, bi_stream s) {

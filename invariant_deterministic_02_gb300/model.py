@@ -12,21 +12,35 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-import synth
 from . import (PROTECTED, Batch, LayerWeights, ModelDims, ModelWeights, PAGE_SIZE, bi_model_forward, bi_model_workspace,
                bi_rope_table, INVARIANT)
+from .shapes import LLAMA31_8B_LAYER, QWEN3_8B_LAYER, LayerShape
 
 
 @dataclass
 class ModelShape:
-    layer: synth.LayerShape
+    layer: LayerShape  # any object with LayerShape's fields
     n_layers: int
     vocab: int
     max_pos: int = 32768
 
 
-QWEN3_8B = ModelShape(synth.QWEN3_8B_LAYER, 36, 151936)
-LLAMA31_8B = ModelShape(synth.LLAMA31_8B_LAYER, 32, 128256)
+QWEN3_8B = ModelShape(QWEN3_8B_LAYER, 36, 151936)
+LLAMA31_8B = ModelShape(LLAMA31_8B_LAYER, 32, 128256)
+
+
+def _normal(shape, seed: int, std: float, mean: float, device, on_host: bool) -> torch.Tensor:
+    """Seeded N(mean, std^2) bf16 tensor for random-init weights, drawn in fp32 by
+    torch's generator on the host or on the device."""
+    gdev = "cpu" if on_host else device
+    g = torch.Generator(device=gdev)
+    g.manual_seed(int(seed) & 0x7FFFFFFFFFFFFFFF)
+    t = torch.randn(tuple(shape), generator=g, dtype=torch.float32, device=gdev)
+    if std != 1.0:
+        t.mul_(std)
+    if mean != 0.0:
+        t.add_(mean)
+    return t.to(torch.bfloat16).to(device)
 
 
 @dataclass
@@ -94,35 +108,33 @@ class BiModel:
     # ------------------------------------------------------------ construction
     @staticmethod
     def random_weights(shape: ModelShape, seed: int, device="cuda", std: float = 0.02, on_host: bool | None = None):
+        """Random-init bf16 weights ~N(0, std^2) (the linear-layer [out][in] layout;
+        w_gate_up stacks gate over up).  Small models draw on the host, large ones
+        with the device's generator.  RMSNorm weights are 1 except Qwen3's q/k head
+        norms, ~N(1, 0.1^2)."""
         L = shape.layer
         if on_host is None:
             on_host = L.d_model * L.ffn_dim * shape.n_layers < 64 * 1024 * 1024
-        if on_host:
-            layers = []
-            for i in range(shape.n_layers):
-                lw = synth.layer_weights(L, seed + 100 * (i + 1), std=std)
-                layers.append({k: v.to(device) for k, v in lw.items()})
-            embed = synth.normal((shape.vocab, L.d_model), seed + 1, std=std).to(device)
-            head = synth.normal((shape.vocab, L.d_model), seed + 2, std=std).to(device)
-        else:
-            layers = []
-            for i in range(shape.n_layers):
-                s = seed + 100 * (i + 1)
-                layers.append({
-                    "attn_norm": torch.ones(L.d_model, dtype=torch.bfloat16, device=device),
-                    "w_qkv": synth.normal_device((L.qkv_dim, L.d_model), s + 2, std=std, device=device),
-                    "w_o": synth.normal_device((L.d_model, L.n_q_heads * L.head_dim), s + 3, std=std, device=device),
-                    "ffn_norm": torch.ones(L.d_model, dtype=torch.bfloat16, device=device),
-                    "w_gate_up": synth.normal_device((2 * L.ffn_dim, L.d_model), s + 5, std=std, device=device),
-                    "w_down": synth.normal_device((L.d_model, L.ffn_dim), s + 6, std=std, device=device),
-                })
-                if L.qk_norm:
-                    layers[-1]["q_norm"] = synth.normal_device((L.head_dim,), s + 7, std=0.1, mean=1.0, device=device)
-                    layers[-1]["k_norm"] = synth.normal_device((L.head_dim,), s + 8, std=0.1, mean=1.0, device=device)
-            embed = synth.normal_device((shape.vocab, L.d_model), seed + 1, std=std, device=device)
-            head = synth.normal_device((shape.vocab, L.d_model), seed + 2, std=std, device=device)
-        return {"embed": embed, "layers": layers, "final_norm": torch.ones(L.d_model, dtype=torch.bfloat16,
-                                                                            device=device), "lm_head": head}
+        nrm = lambda dims, s, sd=std, mean=0.0: _normal(dims, s, sd, mean, device, on_host)
+        ones = lambda n: torch.ones(n, dtype=torch.bfloat16, device=device)
+        layers = []
+        for i in range(shape.n_layers):
+            s = seed + 100 * (i + 1)
+            lw = {
+                "attn_norm": ones(L.d_model),
+                "w_qkv": nrm((L.qkv_dim, L.d_model), s + 2),
+                "w_o": nrm((L.d_model, L.n_q_heads * L.head_dim), s + 3),
+                "ffn_norm": ones(L.d_model),
+                "w_gate_up": nrm((2 * L.ffn_dim, L.d_model), s + 5),
+                "w_down": nrm((L.d_model, L.ffn_dim), s + 6),
+            }
+            if L.qk_norm:
+                lw["q_norm"] = nrm((L.head_dim,), s + 7, 0.1, 1.0)
+                lw["k_norm"] = nrm((L.head_dim,), s + 8, 0.1, 1.0)
+            layers.append(lw)
+        embed = nrm((shape.vocab, L.d_model), seed + 1)
+        head = nrm((shape.vocab, L.d_model), seed + 2)
+        return {"embed": embed, "layers": layers, "final_norm": ones(L.d_model), "lm_head": head}
 
     @classmethod
     def random(cls, shape: ModelShape, seed: int, device="cuda", num_pages: int = 512, page_seed: int | None = 3,

@@ -138,6 +138,43 @@ def test_protected_target_tile_keeps_invariant_bits():
     assert bits_equal(p2[7:8], inv[141:142])
 
 
+@pytest.mark.parametrize("N,out_dtype", [(4096, torch.float32), (14336, torch.bfloat16)])
+def test_multiwave_large_m_elementwise_parity(N, out_dtype):
+    # M = 4096 spans several waves of the persistent tile loop, so CTAs reuse both tensor-memory
+    # accumulators and flip every stage's phase many times; 64 sampled rows >= 128 (every column) are
+    # compared with the float64 product
+    M, K = 4096, 4096
+    A = synth.normal_device((M, K), 70)
+    W = synth.normal_device((N, K), 71, std=0.02)
+    C = gemm(A, W, out_dtype=out_dtype)
+    rows = torch.randperm(M - 128, generator=torch.Generator().manual_seed(72))[:63] + 128
+    rows = torch.cat([rows, torch.tensor([M - 1])]).sort().values
+    exact = oracle.gemm(f64(A[rows.to("cuda")]), f64(W))
+    got = f64(C[rows.to("cuda")])
+    if out_dtype == torch.bfloat16:
+        assert max_rel_err(got, oracle.round_bf16(exact)) <= TOL_BF16
+    else:
+        assert np.max(np.abs(got - exact)) <= 1e-4 * np.max(np.abs(exact))
+
+
+def test_bounded_wait_runs_out_and_the_next_call_is_clean():
+    # The test hook drops the copies of one stage in CTA 0 and shortens every wait of that launch to
+    # 100 ms: the wait for the missing stage runs out, the kernel stops all roles, drains and frees its
+    # tensor memory, and reports a GEMM site code; the next launch is unaffected.
+    M, N, K = 256, 1024, 2048
+    A = cuda(synth.normal((M, K), 80))
+    W = cuda(synth.normal((N, K), 81, std=0.02))
+    ref = gemm(A, W, out_dtype=torch.float32)
+    assert bi.bi_device_error() == 0
+    bi.bi_debug_arm_gemm_stall(100_000_000)
+    gemm(A, W, out_dtype=torch.float32)
+    code = bi.bi_device_error()
+    assert code in (1, 2, 3, 4), code
+    again = gemm(A, W, out_dtype=torch.float32)
+    assert bi.bi_device_error() == 0
+    assert bits_equal(again, ref)
+
+
 def test_device_error_word_clear_after_normal_runs():
     A = cuda(synth.normal((5, 64), 1))
     W = cuda(synth.normal((64, 64), 2))

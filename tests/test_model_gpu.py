@@ -121,28 +121,49 @@ def test_tiny_model_greedy_bit_exact_across_compositions():
     assert_same(refk, got, "ksplit")
 
 
+def _oracle_steps(m, steps):
+    """Oracle logits of one request computed alone: `steps` is a list of token
+    arrays fed in order (a prefill, then decode tokens); returns the last-token
+    logits of each step."""
+    w = m.host_weights()
+    sh = m.shape
+    kv = oracle.OracleKV(sh.n_layers, sh.layer.n_kv_heads, sh.layer.head_dim)
+    out, pos = [], 0
+    for toks in steps:
+        toks = np.asarray(toks, dtype=np.int32)
+        lg = oracle.model_forward(toks, w["embed"], w["layers"], w["final_norm"], w["lm_head"], sh.layer, kv,
+                                  [(0, len(toks))], [pos])
+        out.append(lg[-1])
+        pos += len(toks)
+    return out
+
+
 def test_blocklock_pack_target_bits_equal_invariant_alone():
     """BlockLock-Pack reading: the protected request is packed last behind a dummy
     segment that aligns it to a 128-row tile, the shared prefill runs PROTECTED
     (the neighbours FAST), then the target decodes alone.  Its tokens and top-20
     bits equal those of the target computed alone in INVARIANT mode, whatever the
-    neighbours are."""
+    neighbours are, and its logits (packed prefill and the first decode step) agree
+    with the oracle of the target computed alone (zhaixingw.cn BlockLock post, the
+    Pack mode in "BlockLock 只锁住被保护的那条请求")."""
     shape = tiny_shape()
     m = BiModel.random(shape, seed=31, num_pages=4096, page_seed=11)
     V = shape.vocab
     prompt = synth.token_ids(90, V, 300)
 
     def decode_alone(req, first_tok, steps=12):
-        toks, tops = [first_tok], []
+        toks, tops, logits = [first_tok], [], []
         for _ in range(steps):
             res = m.forward_batch([(req, np.array([toks[-1]], dtype=np.int32))], mode=bi.INVARIANT)
             toks.append(int(res.top_i[0, 0]))
             tops.append(res.top_v[0].cpu().numpy().view(np.uint32).copy())
-        return toks, tops
+            logits.append(res.logits[0].double().cpu().numpy())
+        return toks, tops, logits
 
     res = m.forward_batch([("t", prompt)], mode=bi.INVARIANT)
     ref_first = (int(res.top_i[0, 0]), res.top_v[0].cpu().numpy().view(np.uint32).copy())
     ref = decode_alone("t", ref_first[0])
+    orc = _oracle_steps(m, [prompt, [ref_first[0]]])
     m.reset()
     for trial, lens in enumerate([(37, 200), (5,), (130, 64, 300)]):
         items = [("n%d" % j, synth.token_ids(n, V, 400 + 10 * trial + j)) for j, n in enumerate(lens)]
@@ -150,6 +171,7 @@ def test_blocklock_pack_target_bits_equal_invariant_alone():
         out, row = m.pack_prefill(items, "t")
         assert out.top_i[row, 0].item() == ref_first[0]
         assert np.array_equal(out.top_v[row].cpu().numpy().view(np.uint32), ref_first[1])
+        assert max_rel_err(out.logits[row].double().cpu().numpy(), orc[0]) <= 2e-2, trial
         for r, _ in items:
             if r != "t":
                 m.release(r)
@@ -157,13 +179,17 @@ def test_blocklock_pack_target_bits_equal_invariant_alone():
         assert got[0] == ref[0], trial
         for a, b in zip(got[1], ref[1]):
             assert np.array_equal(a, b), trial
+        assert max_rel_err(got[2][0], orc[1]) <= 2e-2, trial
         m.reset()
 
 
 def test_prefix_kv_reuse_across_batches_bitwise():
     """A prompt's K/V computed inside one batch, reused by a new request in another
     batch composition (a prefix-cache hit), continues with exactly the bits of a
-    request that computed everything alone."""
+    request that computed everything alone, and its logits (suffix prefill and the
+    first decode step) agree with the oracle of the request computed alone
+    (zhaixingw.cn BlockLock post, the use cases in "batch 里换个邻居"; devpress
+    digest section 3.3 on the KV cache)."""
     shape = tiny_shape()
     m = BiModel.random(shape, seed=21, num_pages=4096, page_seed=9)
     V = shape.vocab
@@ -176,6 +202,7 @@ def test_prefix_kv_reuse_across_batches_bitwise():
         res = m.forward_batch(first_items)
         slot = [r for r, _ in first_items].index(req)
         toks, tops = [int(res.top_i[slot, 0])], [res.top_v[slot].cpu().numpy().view(np.uint32).copy()]
+        logits = [res.logits[slot].double().cpu().numpy()]
         for _ in range(steps):
             items = [(req, np.array([toks[-1]], dtype=np.int32))]
             if "nb" in m.lengths:
@@ -183,7 +210,8 @@ def test_prefix_kv_reuse_across_batches_bitwise():
             res = m.forward_batch(items)
             toks.append(int(res.top_i[0, 0]))
             tops.append(res.top_v[0].cpu().numpy().view(np.uint32).copy())
-        return toks, tops
+            logits.append(res.logits[0].double().cpu().numpy())
+        return toks, tops, logits
 
     # reference: prompt and suffix prefilled by the request alone, then decode alone
     m.forward_batch([("ref", prompt)])
@@ -201,6 +229,9 @@ def test_prefix_kv_reuse_across_batches_bitwise():
     assert got[0] == ref[0]
     for a, b in zip(got[1], ref[1]):
         assert np.array_equal(a, b)
+    orc = _oracle_steps(m, [prompt, suffix, [ref[0][0]]])
+    assert max_rel_err(got[2][0], orc[1]) <= 2e-2
+    assert max_rel_err(got[2][1], orc[2]) <= 2e-2
 
 
 @pytest.mark.slow

@@ -75,3 +75,39 @@ def test_noalloc_refuses_batches_beyond_its_scratch():
     assert st == bi.BI_ERR_UNSUPPORTED
     msg = bi.lib().bi_last_error_message().decode()
     assert "scratch" in msg and "bi_decode_attention" in msg
+
+
+def test_noalloc_fast_mode_at_decode_batch_64():
+    # FAST plans about four work items per SM over the batch (a few splits per request at B = 64), so its
+    # scratch fits easily; it is sized from the same split count the plan kernel uses
+    lens = [int(v) for v in synth.uniform_ints(64, 128, 4096, 8)]
+    q, kc, vc, bt, kl, dims = build_batch(lens, 32, 8, 128, 9)
+    for mode, target in ((bi.FAST, -1), (bi.PROTECTED, 5)):
+        ref = torch.empty_like(q)
+        bi.bi_decode_attention(q, kc, vc, bt, kl, dims, ref, mode=mode, target_request=target)
+        out = torch.full_like(q, float("nan"))
+        assert call_noalloc(q, kc, vc, bt, kl, dims, out, mode, target) == bi.BI_OK, \
+            bi.lib().bi_last_error_message()
+        torch.cuda.synchronize()
+        assert bits_equal(out, ref), mode
+
+
+def test_noalloc_kv_len_beyond_block_table_is_clamped_and_reported():
+    # a kv_len one past the block table's reach (max_pages * 16 + 1) is clamped by the plan kernel and
+    # reported; no access leaves the caller's buffers or the scratch, and the next call is unaffected
+    lens = [300, 100]
+    q, kc, vc, bt, kl, dims = build_batch(lens, 32, 8, 128, 21)
+    assert bi.bi_device_error() == 0
+    bad = kl.clone()
+    bad[0] = dims.max_pages * PS + 1
+    out = torch.empty_like(q)
+    assert call_noalloc(q, kc, vc, bt, bad, dims, out) == bi.BI_OK
+    torch.cuda.synchronize()
+    assert bi.bi_device_error() == 16
+    ref = torch.empty_like(q)
+    bi.bi_decode_attention(q, kc, vc, bt, kl, dims, ref)
+    out2 = torch.full_like(q, float("nan"))
+    assert call_noalloc(q, kc, vc, bt, kl, dims, out2) == bi.BI_OK
+    torch.cuda.synchronize()
+    assert bi.bi_device_error() == 0
+    assert bits_equal(out2, ref)
