@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 #include <unordered_map>
 
 #include "common.cuh"
@@ -637,6 +638,364 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   }
 }
 
+// ------------------------------------------------------------------ two-SM tiles (INVARIANT, M > 128)
+// A cluster of two CTAs (an SM pair) computes 256 x TN2 output tiles with
+// tcgen05.mma.cta_group::2 (instruction M = 256, N = TN2, K = 16).  CTA rank r
+// loads A rows [256 i + 128 r, +128) and B rows [TN2 j + r TN2/2, +TN2/2) of
+// every k-tile into its own shared memory; the even CTA issues the MMAs, which
+// read both CTAs' operands and accumulate rows 128 r .. of the tile in CTA r's
+// tensor memory.  Per SM a k-tile moves 16 KiB of A and TN2/2 rows of B, two
+// thirds of what a one-SM 128 x 256 tile moves for the same flops, which is
+// what lets the copy engines keep the tensor cores busy.  Per element the
+// instruction sequence (ascending k-tiles, four K = 16 steps each, the first
+// overwriting the accumulator) is the one of the one-SM kernel, so the bits
+// are the same.
+//
+// Synchronisation (every wait bounded; a wait that runs out records a site
+// code and the kernel winds down):
+//   * full[s] lives in the even CTA and counts both CTAs' copy bytes (armed by
+//     the even CTA's producer); the odd CTA's copies signal it remotely;
+//   * the MMA commits arrive on empty[s] and tfull[a] of both CTAs (multicast);
+//   * both CTAs' epilogue warps arrive on the even CTA's tempty[a];
+//   * a handshake barrier in each CTA, armed by the other CTA, orders the
+//     pair's tensor-memory allocation before the first MMA and keeps each CTA
+//     alive at the end until the other no longer addresses it.
+// The kernel waits for its predecessor before doing anything (no prologue
+// overlaps another kernel), is launched without programmatic serialisation,
+// and lets its successor start only when it exits.
+constexpr int kPairTmemCols = 512;   // two accumulators of up to 256 columns
+constexpr int kPairStagesMax = 16;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared variable in CTA `cta` of this cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(cta));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait on a barrier that the other CTA of the pair arrives on; records `site` when it runs out.
+__device__ __noinline__ bool wait_pair(uint32_t bar, uint32_t parity, int site, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (global_ns() - t0 > limit_ns) {
+      atomicCAS(&g_err_word, 0u, static_cast<unsigned>(site));
+      return false;
+    }
+  }
+  return true;
+}
+// Time-bounded wait that records `site` when it runs out (end-of-kernel drains).
+__device__ __noinline__ void wait_drain_rec(uint32_t bar, uint32_t parity, int site) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(&g_err_word, 0u, static_cast<unsigned>(site));
+      return;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the barrier at this shared offset in the CTAs of `mask` (bit r = rank r)
+// once every MMA issued so far has completed
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+// Instruction descriptor of the pair: fp32 accumulator, bf16 A and B, K-major, M = 256, N = n.
+__host__ __device__ constexpr uint32_t idesc_pair(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(256 >> 4) << 24);
+}
+
+template <int TN2>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const Args a) {
+  static_assert(TN2 == 256 || TN2 == 128, "pair tile widths");
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int kStages = a.stages;
+  constexpr int a_tile = kBM * kBK * 2;             // this CTA's 128 A rows of a k-tile
+  constexpr int kStageBytes = a_tile + (TN2 / 2) * kBK * 2;  // + its TN2/2 B rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  unsigned char* tiles = smem + kBarBlock;
+  // bars: full[16], empty[16], tfull[2], tempty[2], drain, sync; then the tensor-memory slot and the abort word
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kPairStagesMax;
+  const uint32_t tfull0 = empty0 + 8 * kPairStagesMax;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain_bar = tempty0 + 16;
+  const uint32_t sync_bar = drain_bar + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStagesMax + 6);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+  pdl_wait();  // nothing below overlaps the previous kernel
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);  // the even CTA's producer; bytes of both CTAs
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(sync_bar, 1);  // phase 0: the other CTA's allocation is done; phase 1: it has finished
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+  }
+  // Both CTAs' barriers are initialised before either addresses the other's.
+  // Nothing above can block, and the two CTAs of a cluster run together.
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kPairTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  bool pair_ok = true;
+  if (threadIdx.x == 0) {
+    // handshake 1: both CTAs hold the pair's tensor memory before the first MMA
+    mbar_arrive_cluster(peer_addr(sync_bar, rank ^ 1u));
+    pair_ok = wait_pair(sync_bar, 0, 30, a.wait_ns);
+    uint32_t peer_base = 0;
+    if (pair_ok) {
+      asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(peer_base) : "r"(peer_addr(smem_u32(tmem_slot), rank ^ 1u))
+                   : "memory");
+      if (peer_base != *tmem_slot) {
+        atomicCAS(&g_err_word, 0u, 31u);
+        pair_ok = false;
+      }
+    }
+    if (!pair_ok) *abort_flag = 1;
+  }
+  __syncthreads();
+  const uint32_t tmem_base = *tmem_slot;
+  const int m_tiles2 = (a.M + 255) / 256;
+  // no work at all when the handshake failed (both CTAs fail it together or time out)
+  const int units = *abort_flag ? 0 : m_tiles2 * a.n_tiles;
+
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t issued_mask = 0, issued_par = 0;
+      const uint32_t full_leader0 = peer_addr(full0, 0);
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = cid; u < units && ok; u += nclusters) {
+        const int nt = u / m_tiles2, mt2 = u % m_tiles2;
+        const int arow = mt2 * 256 + static_cast<int>(rank) * kBM;
+        const int brow = nt * TN2 + static_cast<int>(rank) * (TN2 / 2);
+        for (int kb = 0; kb < a.kb_total; ++kb) {
+          if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 21, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(tiles + st * kStageBytes);
+          if (leader) mbar_expect_tx(full0 + 8 * st, static_cast<uint32_t>(2 * kStageBytes));
+          tma_load_2d_pair(sa, &tmA, full_leader0 + 8 * st, kb * kBK, arow);
+          tma_load_2d_pair(sa + a_tile, &tmW, full_leader0 + 8 * st, kb * kBK, brow);
+          issued_mask |= 1u << st;
+          issued_par = (issued_par & ~(1u << st)) | (ph << st);
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (leader) {
+        // the copies of both CTAs complete on these barriers
+        for (int i = 0; i < kStages; ++i)
+          if (issued_mask & (1u << i)) wait_drain_rec(full0 + 8 * i, (issued_par >> i) & 1u, 25);
+      }
+      // the even CTA's commits for the last use of each stage arrive in this
+      // CTA's shared memory: let them land before the CTA may leave
+      if (!*abort_flag)
+        for (int i = 0; i < kStages; ++i)
+          if (issued_mask & (1u << i)) wait_drain_rec(empty0 + 8 * i, (issued_par >> i) & 1u, 26);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      const uint64_t desc0 = sw128_desc(smem_u32(tiles));
+      constexpr uint32_t kIdesc = idesc_pair(TN2);
+      int st = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      uint32_t acc_used = 0, acc_par = 0;  // accumulators committed, and the parity of their last commit
+      bool ok = true;
+      bool any = false;
+      for (int u = cid; u < units && ok; u += nclusters) {
+        if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 22, a.wait_ns)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * TN2);
+        for (int kb = 0; kb < a.kb_total; ++kb) {
+          if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 23, a.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+          const uint64_t bdesc = adesc + static_cast<uint64_t>(a_tile >> 4);
+#pragma unroll
+          for (int k = 0; k < kBK / kUK; ++k)
+            tc_mma_pair(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc,
+                        (k > 0 || kb > 0) ? 1u : 0u);
+          tc_commit_pair(empty0 + 8 * st, 3);
+          any = true;
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair(tfull0 + 8 * acc, 3);
+        acc_used |= 1u << acc;
+        acc_par = (acc_par & ~(1u << acc)) | (acc_ph << acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
+      }
+      if (*abort_flag && any) {
+        tc_commit_pair(drain_bar, 1);
+        wait_drain(drain_bar, 0);
+      }
+      // both CTAs' epilogues release each accumulator on this CTA's tempty: let
+      // their last arrivals land before this CTA may leave
+      if (!*abort_flag)
+        for (int i = 0; i < 2; ++i)
+          if (acc_used & (1u << i)) wait_drain_rec(tempty0 + 8 * i, (acc_par >> i) & 1u, 27);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (4 warps, both CTAs)
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tempty_leader0 = peer_addr(tempty0, 0);
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int u = cid; u < units; u += nclusters) {
+      const int nt = u / m_tiles2, mt2 = u % m_tiles2;
+      if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 24, a.wait_ns)) break;
+      __syncwarp();  // lanes leave the wait at different times; tcgen05.ld needs the whole warp
+      tc_fence_after();
+      const int row = mt2 * 256 + static_cast<int>(rank) * kBM + row_in_tile;
+      const bool row_ok = row < a.M;
+      const uint32_t tbase = lane_base + acc * TN2;
+#pragma unroll 1
+      for (int ch = 0; ch < TN2 / 32; ++ch) {
+        uint32_t r[32];
+        tc_ld32(tbase + ch * 32, r);
+        const int col0 = nt * TN2 + ch * 32;
+        if (!row_ok || col0 >= a.N) continue;
+        if (a.out_kind == kOutF32) {
+          float* dst = static_cast<float*>(a.C) + static_cast<size_t>(row) * a.N + col0;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (col0 + 4 * g < a.N)
+              *reinterpret_cast<float4*>(dst + 4 * g) =
+                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                              __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        } else {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.C) + static_cast<size_t>(row) * a.N + col0;
+          const __nv_bfloat16* res = a.R ? a.R + static_cast<size_t>(row) * a.N + col0 : nullptr;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + 8 * g >= a.N) break;
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * g + e]);
+            if (res) {
+              float rv[8];
+              unpack8(*reinterpret_cast<const uint4*>(res + 8 * g), rv);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __fadd_rn(f[e], rv[e]);
+            }
+            *reinterpret_cast<uint4*>(dst + 8 * g) = pack8(f);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_ph ^= 1u;
+      }
+    }
+  }
+
+  // Teardown: every MMA has completed once this CTA's epilogue consumed the
+  // last accumulator; handshake 2 keeps the pair's shared and tensor memory
+  // alive until the other CTA is done with them.
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && pair_ok) {
+    mbar_arrive_cluster(peer_addr(sync_bar, rank ^ 1u));
+    wait_pair(sync_bar, 1, 32, kWaitLimitNs);
+  }
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kPairTmemCols)
+                 : "memory");
+  }
+}
+
 // Second pass of split-K: element (i, j) of an unprotected tile is the
 // left-to-right sum ((0 + P_0) + P_1) + ... of its split partials (+ residual),
 // rounded once.  A thread owns four columns of one row; the partials are
@@ -787,7 +1146,44 @@ struct Plan {
   int splits;
   int tm0, tm1, seq;
   int m_tiles, n_tiles, units, kb_total;
+  int pair;  // 0: one-SM tiles; else the width of the SM-pair tiles (256 x pair)
 };
+
+// Clusters of two CTAs of the pair kernel that can be resident at once on the
+// current device (cached per device); 76 when there is no device.
+template <int TN2>
+int pair_clusters_for() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 76;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= static_cast<int>(cache.size())) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    const void* fn = reinterpret_cast<const void*>(gemm_pair_kernel<TN2>);
+    int n = 0;
+    if (ensure_smem_limit(fn, kSmemLimit) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * 76);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmemLimit;
+      if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    }
+    cache[dev] = n > 0 ? n : std::max(1, plan_sms() / 2);
+  }
+  return cache[dev];
+}
+
+int pair_clusters(int tn2) {
+  if (num_sms() <= 0) return 76;
+  return tn2 == 256 ? pair_clusters_for<256>() : pair_clusters_for<128>();
+}
+
+// Relative time of one k-tile per CTA (one-SM tile of `tn` columns) or per CTA
+// pair (256 x tn2 tile), as measured on GB300 for compute-sized GEMMs: the
+// copy engines, not the tensor cores, set the pace of the narrower tiles.
+double ktile_cost_single(int tn) { return tn >= 256 ? 645.0 : tn >= 128 ? 625.0 : tn >= 64 ? 500.0 : 450.0; }
+double ktile_cost_pair(int tn2) { return tn2 >= 256 ? 540.0 : 420.0; }
 
 // Part count of the K-only split (INVARIANT_KSPLIT): enough parts that a
 // decode-sized GEMM (one 128-row tile, 256-column tiles) gives about one unit
@@ -846,7 +1242,8 @@ int choose_width_small_m(int64_t N, int splits, int a_rows) {
 
 // planes: 1 for bf16 A, 3 for fp32 A held as three bf16 planes (each plane
 // adds an A box to every stage).
-Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te, int planes = 1) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te, int planes = 1,
+               bool allow_pair = true) {
   Plan p;
   p.a_rows = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : kBM;
   p.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
@@ -895,6 +1292,33 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   }
   if (fast_tn) p.TN = fast_tn;
   else p.TN = M <= kBM ? choose_width_small_m(N, p.splits, planes * p.a_rows) : choose_width(M, N, max_tn);
+  p.pair = 0;
+  if (mode == BI_MODE_INVARIANT && planes == 1 && M > kBM && allow_pair) {
+    // SM-pair tiles when the model says they finish sooner than the one-SM tiles
+    const int sms = plan_sms();
+    const int64_t single_units = static_cast<int64_t>(p.m_tiles) * ((N + p.TN - 1) / p.TN);
+    double best = static_cast<double>((single_units + sms - 1) / sms) * ktile_cost_single(p.TN);
+    for (int tn2 : {256, 128}) {
+      const int64_t units = ((M + 255) / 256) * ((N + tn2 - 1) / tn2);
+      const int cl = pair_clusters(tn2);
+      const double t = static_cast<double>((units + cl - 1) / cl) * ktile_cost_pair(tn2);
+      if (t < best * 0.97) {
+        best = t;
+        p.pair = tn2;
+      }
+    }
+  }
+  if (p.pair) {
+    p.TN = p.pair;
+    p.a_rows = kBM;
+    p.kbs = 1;
+    p.map3d = 0;
+    p.stage_bytes = kBM * kBK * 2 + (p.pair / 2) * kBK * 2;
+    p.stages = std::min(kPairStagesMax, (kSmemLimit - 1024 - kBarBlock) / p.stage_bytes);
+    p.n_tiles = static_cast<int>((N + p.pair - 1) / p.pair);
+    p.units = static_cast<int>(((M + 255) / 256) * p.n_tiles);
+    return p;
+  }
   // Each copy costs the copy engine a roughly fixed time, so at decode sizes a
   // stage spans several k-blocks (one 3D box of 16-32 KiB of weights per copy,
   // at most 4 k-blocks so that several stages fit).  (A 3D copy costs more
@@ -913,6 +1337,25 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   const int prot = p.tm1 - p.tm0;
   p.units = p.n_tiles * (prot + (p.m_tiles - prot) * p.splits);
   return p;
+}
+
+template <int TN2>
+bi_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
+  const void* fn = reinterpret_cast<const void*>(gemm_pair_kernel<TN2>);
+  BI_CUDA_TRY(ensure_smem_limit(fn, kSmemLimit));
+  const size_t smem = 1024 + kBarBlock + static_cast<size_t>(args.stages) * args.stage_bytes;
+  const int grid = 2 * std::min(args.units, pair_clusters(TN2));
+  // no programmatic serialisation: the pair kernel starts after its predecessor has finished
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<TN2>, ma, mw, args)));
+  BI_LAUNCH_CHECK();
+  return BI_OK;
 }
 
 template <int TN, int PL>
@@ -989,7 +1432,8 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   BI_REQUIRE(aligned16(A) && aligned16(Wt) && aligned16(C) && (R == nullptr || aligned16(R)) &&
                  (Rf == nullptr || aligned16(Rf)),
              BI_ERR_INVALID_ARG, "bi_gemm: pointers must be 16-byte aligned");
-  gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te, planes);
+  // the stall test hook exists in the one-SM kernel only
+  gemm::Plan p = gemm::make_plan(M, N, K, mode, tb, te, planes, t_stall_wait_ns == 0);
   BI_REQUIRE(p.seq == 1 || p.TN <= 128, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (merged units at width %d)",
              p.TN);
   BI_REQUIRE(p.stages >= 2, BI_ERR_UNSUPPORTED, "bi_gemm: internal plan error (%d stages)", p.stages);
@@ -1032,6 +1476,11 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
     args.partial = static_cast<float*>(ws);
   }
   CUtensorMap ma, mw;
+  if (p.pair) {
+    BI_TRY(gemm::tensor_map(A, M, K, gemm::kBM, 0, &ma));
+    BI_TRY(gemm::tensor_map(Wt, N, K, p.pair / 2, 0, &mw));
+    return p.pair == 256 ? gemm::launch_pair<256>(ma, mw, args, s) : gemm::launch_pair<128>(ma, mw, args, s);
+  }
   // the planes form one [planes*M][K] matrix; plane p's rows start at p*M
   BI_TRY(gemm::tensor_map(A, planes * M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
   BI_TRY(gemm::tensor_map(Wt, N, K, p.TN, p.map3d ? p.kbs : 0, &mw));

@@ -133,15 +133,90 @@ __device__ __forceinline__ void* out_row(void* y, int64_t r, int d) {
   else return static_cast<TX*>(y) + r * d;
 }
 
-template <typename TX, typename TG, bool PL>
+// Raw 16-byte vectors of a row (NCH per thread, chunk c = t + 256 i) and their
+// conversion: the row data stays packed in registers until it is used.
+template <typename TX>
+struct RawOf;
+template <>
+struct RawOf<float> {
+  using T = float4;
+  static __device__ __forceinline__ void unpack(const float4& v, float (&f)[4]) {
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+};
+template <>
+struct RawOf<__nv_bfloat16> {
+  using T = uint4;
+  static __device__ __forceinline__ void unpack(const uint4& v, float (&f)[8]) { unpack8(v, f); }
+};
+
+template <typename TX, int NCH>
+__device__ __forceinline__ void load_row(const TX* __restrict__ x, int nchunks, typename RawOf<TX>::T (&raw)[NCH]) {
+  using R = typename RawOf<TX>::T;
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    const int c = threadIdx.x + i * kThreads;
+    if (c < nchunks) {
+      const uint4 u = ld_stream(reinterpret_cast<const R*>(x) + c);
+      raw[i] = *reinterpret_cast<const R*>(&u);
+    }
+  }
+}
+
+// INVARIANT kernel: a grid-stride loop over rows, one row per CTA at a time,
+// the next row's vectors loaded before the current row is reduced so that two
+// rows per CTA are in flight.  NCH = 16-byte vectors per thread (d / (V * 256),
+// rounded up): the row lives in registers, so the register count, and with it
+// the number of resident CTAs, follows d.  The arithmetic is rms_row's: the
+// same per-thread order, warp butterfly and pairwise tree of warp sums.
+template <typename TX, typename TG, bool PL, int NCH>
 __global__ void __launch_bounds__(kThreads) rms_invariant_kernel(const TX* __restrict__ x, const TG* __restrict__ gamma,
                                                                  void* y, size_t plane, int64_t row_begin,
                                                                  int64_t row_end, int d, float eps) {
+  using R = typename RawOf<TX>::T;
+  constexpr int V = VecOf<TX>::N;
   pdl_wait();
   pdl_trigger();
   __shared__ float red[kWarps];
-  for (int64_t r = row_begin + blockIdx.x; r < row_end; r += gridDim.x)
-    rms_row<TX, TG, PL>(x + r * d, gamma, out_row<TX, PL>(y, r, d), plane, d, eps, red);
+  const int t = threadIdx.x;
+  const int nchunks = d / V;
+  int64_t r = row_begin + blockIdx.x;
+  R cur[NCH], nxt[NCH];
+  if (r < row_end) load_row<TX, NCH>(x + r * d, nchunks, cur);
+  for (; r < row_end; r += gridDim.x) {
+    const int64_t rn = r + gridDim.x;
+    if (rn < row_end) load_row<TX, NCH>(x + rn * d, nchunks, nxt);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      if (t + i * kThreads < nchunks) {
+        float f[V];
+        RawOf<TX>::unpack(cur[i], f);
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc = __fmaf_rn(f[e], f[e], acc);
+      }
+    }
+    acc = warp_sum(acc);
+    if ((t & 31) == 0) red[t >> 5] = acc;
+    __syncthreads();
+    const float rr = inv_rms(sum8(red), d, eps);
+    __syncthreads();  // red is reused by the next row
+    void* yr = out_row<TX, PL>(y, r, d);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int c = t + i * kThreads;
+      if (c < nchunks) {
+        float f[V], g[V], o[V];
+        RawOf<TX>::unpack(cur[i], f);
+        load_vec(gamma + static_cast<size_t>(c) * V, g);
+#pragma unroll
+        for (int e = 0; e < V; ++e) o[e] = __fmul_rn(__fmul_rn(f[e], rr), g[e]);
+        store_out<TX, PL, V>(yr, plane, static_cast<size_t>(c) * V, o);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) cur[i] = nxt[i];
+  }
 }
 
 // FAST pass 1: CTA (row, s) sums the squares of chunk range s of its row.
@@ -227,10 +302,21 @@ bi_status launch(const void* xv, const void* gv, void* y, int64_t rows, int d, f
   const int splits = mode_invariant(mode) ? 1 : fast_splits(rows, d, V);
   if (splits == 1) {
     // Unsplit: the data-parallel schedule, identical to INVARIANT for every row.
-    const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(num_sms()) * 8);
-    BI_TIMED(::bi::kTagRmsnorm, s, BI_PDL_CHECK(launch_pdl(rms_invariant_kernel<TX, TG, PL>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, x, g, y, plane, int64_t(0), rows, d, eps)));
-    BI_LAUNCH_CHECK();
-    return BI_OK;
+    const int nch = (d / V + kThreads - 1) / kThreads;
+    auto go = [&](auto kern) -> bi_status {
+      const void* fn = reinterpret_cast<const void*>(kern);
+      // every SM holds as many CTAs as its registers allow, each working through rows
+      const int64_t grid =
+          std::min<int64_t>(rows, static_cast<int64_t>(num_sms()) * occupancy_per_sm(fn, kThreads, 0));
+      BI_TIMED(::bi::kTagRmsnorm, s, BI_PDL_CHECK(launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
+                                                             s, x, g, y, plane, int64_t(0), rows, d, eps)));
+      BI_LAUNCH_CHECK();
+      return BI_OK;
+    };
+    if (nch <= 1) return go(rms_invariant_kernel<TX, TG, PL, 1>);
+    if (nch <= 2) return go(rms_invariant_kernel<TX, TG, PL, 2>);
+    if (nch <= 4) return go(rms_invariant_kernel<TX, TG, PL, 4>);
+    return go(rms_invariant_kernel<TX, TG, PL, kMaxChunks>);
   }
   const size_t need = static_cast<size_t>(rows) * splits * sizeof(float);
   BI_REQUIRE(ws != nullptr && ws_bytes >= need, BI_ERR_WORKSPACE, "bi_rmsnorm: workspace %zu < %zu bytes", ws_bytes,

@@ -110,8 +110,8 @@ class BiModel:
     def random_weights(shape: ModelShape, seed: int, device="cuda", std: float = 0.02, on_host: bool | None = None):
         """Random-init bf16 weights ~N(0, std^2) (the linear-layer [out][in] layout;
         w_gate_up stacks gate over up).  Small models draw on the host, large ones
-        with the device's generator.  RMSNorm weights are 1 except Qwen3's q/k head
-        norms, ~N(1, 0.1^2)."""
+        with the device's generator.  RMSNorm weights are 1, except the Qwen3 q/k head
+        norms of large models, ~N(1, 0.1^2)."""
         L = shape.layer
         if on_host is None:
             on_host = L.d_model * L.ffn_dim * shape.n_layers < 64 * 1024 * 1024
@@ -129,8 +129,9 @@ class BiModel:
                 "w_down": nrm((L.d_model, L.ffn_dim), s + 6),
             }
             if L.qk_norm:
-                lw["q_norm"] = nrm((L.head_dim,), s + 7, 0.1, 1.0)
-                lw["k_norm"] = nrm((L.head_dim,), s + 8, 0.1, 1.0)
+                # small models: unit head norms; large ones: ~N(1, 0.1^2)
+                lw["q_norm"] = ones(L.head_dim) if on_host else nrm((L.head_dim,), s + 7, 0.1, 1.0)
+                lw["k_norm"] = ones(L.head_dim) if on_host else nrm((L.head_dim,), s + 8, 0.1, 1.0)
             layers.append(lw)
         embed = nrm((shape.vocab, L.d_model), seed + 1)
         head = nrm((shape.vocab, L.d_model), seed + 2)

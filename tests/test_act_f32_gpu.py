@@ -264,7 +264,7 @@ def test_qwen3_layer_chunked_prefill_equals_token_by_token_decode():
 
 # ---------------------------------------------------------------- model
 def tiny_shape(layer=synth.TINY_QK_LAYER):
-    return ModelShape(layer=layer, n_layers=2, vocab=512, max_pos=2048)
+    return ModelShape(layer=layer, n_layers=2, vocab=512, max_pos=8448)  # decode neighbours reach 8000 + steps
 
 
 def test_tiny_model_parity():

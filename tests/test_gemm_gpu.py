@@ -164,6 +164,7 @@ def test_bounded_wait_runs_out_and_the_next_call_is_clean():
     M, N, K = 256, 1024, 2048
     A = cuda(synth.normal((M, K), 80))
     W = cuda(synth.normal((N, K), 81, std=0.02))
+    bi.bi_device_error()  # start from clear error words
     ref = gemm(A, W, out_dtype=torch.float32)
     assert bi.bi_device_error() == 0
     bi.bi_debug_arm_gemm_stall(100_000_000)

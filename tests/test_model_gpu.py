@@ -15,7 +15,7 @@ from invariant_deterministic_02_gb300.model import QWEN3_8B, BiModel, ModelShape
 
 
 def tiny_shape(layer=synth.TINY_LAYER):
-    return ModelShape(layer=layer, n_layers=2, vocab=512, max_pos=2048)
+    return ModelShape(layer=layer, n_layers=2, vocab=512, max_pos=8448)  # decode neighbours reach 8000 + steps
 
 
 @pytest.mark.parametrize("layer", [synth.TINY_LAYER, synth.TINY_QK_LAYER], ids=["plain", "qk_norm"])
@@ -93,6 +93,8 @@ def greedy_run(m: BiModel, prompt, steps, prefill_chunks, neighbours, target_slo
         tok = int(ti[slot])
         tokens.append(tok)
         tops.append((res.top_v[slot].cpu().numpy().view(np.uint32).copy(), res.top_i[slot].cpu().numpy().copy()))
+    # every position, page and KV length the kernels met was in range
+    assert bi.bi_device_error() == 0
     return tokens, tops
 
 
