@@ -54,9 +54,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None, help="keep the raw SM clock samples of the timed region here")
-    ap.add_argument("--case", choices=["model", "attn", "gemm", "topk"], default="model",
-                    help="model: the decode-step workload; attn/gemm/topk: one kernel on a small single-layer "
-                         "case (for profiler captures), printing that kernel's timing")
+    ap.add_argument("--case", choices=["model", "attn", "gemm", "topk", "rmsnorm"], default="model",
+                    help="model: the decode-step workload; attn/gemm/topk/rmsnorm: one kernel on a small case "
+                         "(for profiler captures), printing that kernel's timing")
     ap.add_argument("--gemm-shape", default="64,24576,4096", help="M,N,K of --case gemm")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the GEMM sweep, RMSNorm roofline and smaller decode batches")
@@ -175,9 +175,10 @@ def run_ours(args, rank, world, local_rank):
                if args.mode == "invariant" else [])
     act32 = args.mode == "invariant"  # also time the fp32-activation variant of the same step
     sweep_b = [b for b in SWEEP_BATCHES if b < B] if args.mode == "invariant" and not args.no_extras else []
-    # warm-up, timed, profiled, end-to-end, other modes, fp32 activations, smaller decode batches
+    tune = "fast" in compare
+    # warm-up, timed, profiled, end-to-end, other modes, fp32 activations, smaller decode batches, FAST tuning
     total_steps = (W + 2 * K + K + len(compare) * (K + 1) + (K + 1 if act32 else 0) +
-                   len(sweep_b) * (W + K))
+                   len(sweep_b) * (W + K) + (3 * (K + 1) if tune else 0))
     pages = int(sum((int(L) + total_steps + 16) // 16 + 1 for L in Ls)) + 16
     model = BiModel(shape, BiModel.random_weights(shape, seed=seeds["weights"]), num_pages=pages,
                     page_seed=args.seed + 3)
@@ -373,6 +374,67 @@ def run_ours(args, rank, world, local_rank):
         modes["invariant_over_fast_time"] = round(ms_per_step / modes["fast"]["ms_per_step"], 4)
     if "protected" in modes:
         modes["protected"]["target_request"] = 0
+
+    # ---------------------------------------------------------------- FAST tuned by timing
+    # The non-invariant schedule at its best: every GEMM shape of the step takes whichever of FAST's
+    # split-K rule and INVARIANT's tile plan times faster here, and decode attention whichever of the
+    # occupancy-chosen split count and the 256-token splits gives the faster FAST step.
+    if tune:
+        L = shape.layer
+        shapes_nk = [(L.qkv_dim, L.d_model), (L.d_model, L.n_q_heads * L.head_dim), (2 * L.ffn_dim, L.d_model),
+                     (L.d_model, L.ffn_dim), (shape.vocab, L.d_model)]
+        flush = L2Flush(torch)
+        gemm_choice = {}
+        for N, Kd in shapes_nk:
+            A = synth.normal_device((B, Kd), 700 + N)
+            Wt = synth.normal_device((N, Kd), 701 + N, std=0.02)
+            C = torch.empty((B, N), dtype=torch.float32 if N == shape.vocab else torch.bfloat16, device=dev)
+            gws = torch.empty(max(1, bi.lib().bi_gemm_workspace(B, N, Kd, bi.FAST)), dtype=torch.uint8, device=dev)
+            t = {}
+            for plan in (0, 1):
+                bi.bi_fast_gemm_plan(B, N, Kd, plan)
+                f = lambda: bi.bi_gemm(A, Wt, C, mode=bi.FAST, workspace=gws)
+                for _ in range(3):
+                    f()
+                t[plan] = time_launches(torch, f, 10, flush)
+            best = min(t, key=t.get)
+            bi.bi_fast_gemm_plan(B, N, Kd, best)
+            gemm_choice["%dx%dx%d" % (B, N, Kd)] = {"plan": ["split_k", "tile_plan"][best],
+                                                   "ms": {"split_k": round(t[0], 4), "tile_plan": round(t[1], 4)}}
+            del A, Wt, C, gws
+        step_ms = {}
+        for plan in (0, 1):
+            bi.bi_fast_attention_plan(plan)
+            one_step(bi.FAST)
+            torch.cuda.synchronize()
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for _ in range(K):
+                one_step(bi.FAST)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            step_ms[plan] = c0.elapsed_time(c1) / K
+        attn_best = min(step_ms, key=step_ms.get)
+        bi.bi_fast_attention_plan(attn_best)
+        one_step(bi.FAST)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(K):
+            one_step(bi.FAST)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cms = max_over_ranks(c0.elapsed_time(c1), dist, dev)
+        modes["fast_tuned"] = {"value": round(job_throughput(B, world, K, cms / 1000.0), 2), "unit": "tok/s",
+                               "ms_per_step": round(cms / K, 4), "gemm_plans": gemm_choice,
+                               "attention_plan": ["occupancy_split_count", "splits_of_256"][attn_best],
+                               "attention_step_ms": {"occupancy_split_count": round(step_ms[0], 4),
+                                                     "splits_of_256": round(step_ms[1], 4)}}
+        modes["invariant_over_fast_tuned_time"] = round(ms_per_step / modes["fast_tuned"]["ms_per_step"], 4)
+        # back to FAST's own rules
+        bi.bi_fast_attention_plan(0)
+        for N, Kd in shapes_nk:
+            bi.bi_fast_gemm_plan(B, N, Kd, 0)
 
     # ---------------------------------------------------------------- smaller decode batches (B = 1, 8)
     # the first nb requests of the same model and caches; roofline: the weights every step streams
@@ -629,6 +691,13 @@ def run_case(args):
             kernel, work, unit, peak = "gemm", flops, "TFLOP/s", pk["bf16_tflops"]
         else:
             kernel, work, unit, peak = "gemm", byts, "GB/s", pk["hbm_gbs"]
+    elif args.case == "rmsnorm":
+        rows, d = 16384, 4096
+        x = synth.normal_device((rows, d), args.seed + 8)
+        g = synth.normal_device((d,), args.seed + 9, std=0.1, mean=1.0)
+        y = torch.empty_like(x)
+        fn = lambda: bi.bi_rmsnorm(x, g, y, 1e-5, mode=mode)
+        kernel, work, unit, peak = "rmsnorm", 4.0 * rows * d + 2 * d, "GB/s", pk["hbm_gbs"]
     else:
         V = 151936
         x = synth.normal_device((B, V), args.seed + 7, dtype=torch.float32)

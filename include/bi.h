@@ -113,6 +113,21 @@ bi_status bi_device_error(int32_t* code, bi_stream s);
  * next launch is unaffected.  wait_ns in [1e6, 2e9], else BI_ERR_INVALID_ARG. */
 bi_status bi_debug_arm_gemm_stall(int64_t wait_ns);
 
+/* Tuning of the non-invariant schedules (FAST mode; the pages have no
+ * counterpart: it exists so that the cost of invariance can be measured
+ * against the best non-invariant schedule these kernels offer).
+ * bi_fast_gemm_plan: FAST GEMMs of shape (M, N, K) (bf16 or fp32 activations)
+ * take INVARIANT's tile plan, with no split-K, when plan = 1; plan = 0 restores
+ * FAST's own rule (split K over CTAs when there are fewer tiles than SMs).
+ * bi_fast_attention_plan: plan = 1 makes FAST decode attention cut every request
+ * into the 256-token splits of INVARIANT (combined left to right) instead of
+ * the occupancy-chosen unit count of plan = 0.  Process-wide host-side settings
+ * (bi_fast_gemm_plan keeps one entry per shape); they change no INVARIANT,
+ * INVARIANT_KSPLIT or PROTECTED schedule.  Workspace queries made while a
+ * setting is in force size for it.  Any other plan is BI_ERR_INVALID_ARG. */
+bi_status bi_fast_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t plan);
+bi_status bi_fast_attention_plan(int32_t plan);
+
 /* Kernel timing (off by default).  bi_profile_start creates 2*max_launches CUDA
  * events up front; while it is on, every kernel launch of the library is
  * bracketed by two events recorded on the launching stream (launches beyond

@@ -38,7 +38,7 @@ TOPK_MAX = 32
 
 EXPORTED = [
     "bi_status_string", "bi_last_error_message", "bi_version", "bi_num_sms", "bi_device_error",
-    "bi_debug_arm_gemm_stall",
+    "bi_debug_arm_gemm_stall", "bi_fast_gemm_plan", "bi_fast_attention_plan",
     "bi_rmsnorm_workspace", "bi_rmsnorm", "bi_gemm_workspace", "bi_gemm_ksplit", "bi_gemm",
     "bi_gemm_f32a_workspace", "bi_gemm_f32a",
     "bi_decode_attention_workspace", "bi_decode_attention", "bi_decode_attention_noalloc",
@@ -107,6 +107,8 @@ def _declare(lib):
         "bi_num_sms": (c_i32, []),
         "bi_device_error": (c_i32, [P(c_i32), vp]),
         "bi_debug_arm_gemm_stall": (c_i32, [c_i64]),
+        "bi_fast_gemm_plan": (c_i32, [c_i64, c_i64, c_i64, c_i32]),
+        "bi_fast_attention_plan": (c_i32, [c_i32]),
         "bi_rmsnorm_workspace": (c_sz, [c_i64, c_i64, c_i32]),
         "bi_rmsnorm": (c_i32, [vp, vp, vp, c_i64, c_i64, c_i32, c_f, c_i32, c_i32, c_i32, vp, c_sz, vp]),
         "bi_gemm_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
@@ -203,6 +205,16 @@ def bi_device_error(stream=None) -> int:
     if st not in (BI_OK, BI_ERR_TIMEOUT, BI_ERR_INVALID_ARG) or (st != BI_OK and code.value == 0):
         _check(st, "bi_device_error")
     return int(code.value)
+
+
+def bi_fast_gemm_plan(M: int, N: int, K: int, plan: int):
+    """FAST-mode GEMMs of shape (M, N, K): 1 = INVARIANT's tile plan (no split-K), 0 = FAST's own rule."""
+    _check(lib().bi_fast_gemm_plan(M, N, K, plan), "bi_fast_gemm_plan")
+
+
+def bi_fast_attention_plan(plan: int):
+    """FAST decode attention: 1 = the 256-token splits, 0 = the occupancy-chosen unit count."""
+    _check(lib().bi_fast_attention_plan(plan), "bi_fast_attention_plan")
 
 
 def bi_debug_arm_gemm_stall(wait_ns: int):

@@ -23,6 +23,7 @@
 // of values: per-lane FMA chain over the slot's 16 positions in order, xor 8
 // then 16 across slots, then the four warp sums added warp 0 + 1 + 2 + 3.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -621,6 +622,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict
     int ul, n;
     if (inv) {
       ul = kSplit;
+      n = (L + kSplit - 1) / kSplit;
+    } else if (fast_units_wanted <= 0) {
+      ul = kSplit;  // tuned FAST: the invariant splits, combined left to right
       n = (L + kSplit - 1) / kSplit;
     } else {
       const int pages = (L + kPage - 1) / kPage;
@@ -1248,9 +1252,18 @@ bi_status decode_grid(int* grid) {
   return BI_OK;
 }
 
+// Tuning of the non-invariant decode schedule (bi_fast_attention_plan): 0 =
+// the occupancy-chosen unit count below; 1 = fixed 256-token units (the
+// invariant splits) combined left to right.
+std::atomic<int> g_fast_attn_plan{0};
+
 // Units per request the FAST plan asks for (the plan kernel caps it at 64 and
-// at the request's page count): about four work items per SM over the batch.
-int fast_units_wanted(int B, int hkv) { return std::max(1, (4 * num_sms() + B * hkv - 1) / (B * hkv)); }
+// at the request's page count): about four work items per SM over the batch;
+// 0 asks the plan kernel for fixed 256-token units.
+int fast_units_wanted(int B, int hkv) {
+  if (g_fast_attn_plan.load() == 1) return 0;
+  return std::max(1, (4 * num_sms() + B * hkv - 1) / (B * hkv));
+}
 
 template <int HD, int G>
 bi_status decode_launch(const void* q, const void* kc, const void* vc, const int32_t* bt, const int32_t* kv_lens,
@@ -1442,7 +1455,8 @@ DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode
   DecodeWs r;
   const size_t pb = carve_decode_plan(base, B, dm->num_kv_heads, &r.plan);
   const size_t inv = static_cast<size_t>((dm->max_pages * kPage + kSplit - 1) / kSplit);
-  const size_t f = static_cast<size_t>(std::min(kMaxFastUnits, fast_units_wanted(B, dm->num_kv_heads)));
+  const int fw = fast_units_wanted(B, dm->num_kv_heads);
+  const size_t f = fw <= 0 ? inv : static_cast<size_t>(std::min(kMaxFastUnits, fw));
   size_t units;
   if (mode_invariant(mode)) units = static_cast<size_t>(B) * inv;
   else if (mode == BI_MODE_PROTECTED && target >= 0) units = static_cast<size_t>(B - 1) * f + std::max(inv, f);
@@ -1534,6 +1548,13 @@ int take_attn_device_error(cudaStream_t s, int32_t* code) {
 }
 
 }  // namespace bi
+
+extern "C" bi_status bi_fast_attention_plan(int32_t plan) {
+  bi::clear_error();
+  BI_REQUIRE(plan == 0 || plan == 1, BI_ERR_INVALID_ARG, "bi_fast_attention_plan: plan %d", plan);
+  bi::attn::g_fast_attn_plan.store(plan);
+  return BI_OK;
+}
 
 extern "C" size_t bi_decode_attention_workspace(int32_t B, const bi_attn_dims* dims, bi_mode) {
   return bi::decode_attention_ws(B, dims);

@@ -42,7 +42,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 #include <unordered_map>
 
@@ -1240,6 +1242,18 @@ int choose_width_small_m(int64_t N, int splits, int a_rows) {
   return btn;
 }
 
+// Tuning of the non-invariant schedule (bi_fast_gemm_plan): per (M, N, K,
+// planes), 1 = FAST takes the tile plan of INVARIANT (no split-K) instead of
+// its own split-K rule.  A host-side table, set by a caller that has timed both.
+std::mutex g_fast_mutex;
+std::map<std::tuple<int64_t, int64_t, int64_t, int>, int> g_fast_plan;
+
+int fast_plan_hint(int64_t M, int64_t N, int64_t K, int planes) {
+  std::lock_guard<std::mutex> lock(g_fast_mutex);
+  auto it = g_fast_plan.find(std::make_tuple(M, N, K, planes));
+  return it == g_fast_plan.end() ? 0 : it->second;
+}
+
 // planes: 1 for bf16 A, 3 for fp32 A held as three bf16 planes (each plane
 // adds an A box to every stage).
 Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_t te, int planes = 1,
@@ -1253,6 +1267,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   p.seq = 1;
   // A protected target in the only m-tile makes the whole launch INVARIANT.
   if (mode == BI_MODE_PROTECTED && te > tb && p.m_tiles == 1) mode = BI_MODE_INVARIANT;
+  // FAST tuned to the invariant tile plan for this shape
+  if (mode == BI_MODE_FAST && fast_plan_hint(M, N, K, planes) == 1) mode = BI_MODE_INVARIANT;
   int max_tn = 256;
   if (mode == BI_MODE_INVARIANT_KSPLIT) {
     const int ks = ksplit_count(N, K);
@@ -1583,6 +1599,20 @@ extern "C" bi_status bi_gemm_f32a(const float* A, const void* W, float* C, const
                                   void* workspace, size_t ws_bytes, bi_stream s) {
   return bi::gemm_f32a_impl(A, W, C, residual, M, N, K, mode, target_row, target_count, workspace, ws_bytes,
                             reinterpret_cast<cudaStream_t>(s));
+}
+
+extern "C" bi_status bi_fast_gemm_plan(int64_t M, int64_t N, int64_t K, int32_t plan) {
+  bi::clear_error();
+  BI_REQUIRE(M > 0 && N > 0 && K > 0 && (plan == 0 || plan == 1), BI_ERR_INVALID_ARG,
+             "bi_fast_gemm_plan: M=%lld N=%lld K=%lld plan=%d", static_cast<long long>(M), static_cast<long long>(N),
+             static_cast<long long>(K), plan);
+  std::lock_guard<std::mutex> lock(bi::gemm::g_fast_mutex);
+  for (int planes : {1, 3}) {
+    const auto key = std::make_tuple(M, N, K, planes);
+    if (plan == 0) bi::gemm::g_fast_plan.erase(key);
+    else bi::gemm::g_fast_plan[key] = plan;
+  }
+  return BI_OK;
 }
 
 extern "C" bi_status bi_debug_arm_gemm_stall(int64_t wait_ns) {
