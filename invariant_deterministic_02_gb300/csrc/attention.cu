@@ -22,9 +22,13 @@
 // L adds positions 8L..8L+7 in order, then a 32-lane butterfly.  Weighted sum
 // of values: per-lane FMA chain over the slot's 16 positions in order, xor 8
 // then 16 across slots, then the four warp sums added warp 0 + 1 + 2 + 3.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "common.cuh"
@@ -147,38 +151,45 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// Loaders return the 16-byte pieces of position `pp` (0..255 within the split)
-// that lane c owns: dims [8c, 8c+8) and, for head_dim 128, [64+8c, 64+8c+8).
-// The before_*/after_* hooks bracket a warp's reads of its quarter (positions
-// [64w, 64w+64)); they synchronise with the copy engine but do no arithmetic.
+// Shared-memory layout of K and V (decode ring stages and prefill staging
+// alike): a split is four quarters of 64 positions, a quarter four pages of 16
+// positions, and a page is stored as HD/64 halves of [16 positions][64 dims]
+// (128-byte rows) with the 128-byte swizzle: the 16-byte chunk c of row r sits
+// at chunk position c ^ (r & 7).  This is the layout a TMA tensor copy of one
+// page writes (box {64 dims, 16 positions, HD/64 halves}), and it lets the
+// warp-level MMA fragments (ldmatrix over 8 consecutive positions) read
+// shared memory without bank conflicts.
+template <int HD>
+struct PageLayout {
+  static constexpr int kPageBytes = 16 * HD * 2;    // one page of one kv head
+  static constexpr int kQuarterBytes = 4 * kPageBytes;
+  // byte offset, within a quarter, of the 16-byte chunk `c` (dims 8c .. 8c+7) of position q (0..63)
+  static __device__ __forceinline__ int chunk(int q, int c) {
+    const int pos = q & 15;
+    return (q >> 4) * kPageBytes + (c >> 3) * 2048 + pos * 128 + (((c & 7) ^ (pos & 7)) << 4);
+  }
+};
+
+// Loaders hand out the K and V pieces of a split; the before_*/after_* hooks
+// bracket a warp's reads of its quarter (positions [64w, 64w+64)); they
+// synchronise with the copy engine but do no arithmetic.
 //
 // Decode: quarters of the split stream through a ring of shared-memory stages,
-// filled page by page with bulk copies; order K0..K3, V0..V3 per split.
+// filled page by page with TMA tensor copies; order K0..K3, V0..V3 per split.
 template <int HD>
 struct RingKV {
-  const __nv_bfloat16* ring;  // [stages][64*HD]
+  const unsigned char* ring;  // [stages][quarter bytes], 1024-byte aligned
   uint32_t full0, empty0;     // mbarrier arrays
   int n0;                     // linear stage index of K0 of this split
   int stages;
   volatile int* abort_flag;
   __device__ __forceinline__ int slot(int j) const { return (n0 + j) % stages; }
   __device__ __forceinline__ uint32_t parity(int j) const { return static_cast<uint32_t>(((n0 + j) / stages) & 1); }
-  __device__ __forceinline__ void k(int pp, int c, uint4 (&out)[HD / 64]) const {
-    const __nv_bfloat16* r = ring + static_cast<size_t>(slot(pp >> 6)) * 64 * HD + (pp & 63) * HD;
-#pragma unroll
-    for (int i = 0; i < HD / 64; ++i) out[i] = *reinterpret_cast<const uint4*>(r + 64 * i + 8 * c);
+  __device__ __forceinline__ const unsigned char* kq(int w) const {
+    return ring + static_cast<size_t>(slot(w)) * PageLayout<HD>::kQuarterBytes;
   }
-  // the HD/64 words (HD/32 values) of value row pp that lane `lane` owns in the weighted sum
-  __device__ __forceinline__ void vpiece(int pp, int lane, uint32_t (&w)[HD / 64]) const {
-    const __nv_bfloat16* r =
-        ring + static_cast<size_t>(slot(4 + (pp >> 6))) * 64 * HD + (pp & 63) * HD + lane * (HD / 32);
-    if constexpr (HD == 128) {
-      const uint2 u = *reinterpret_cast<const uint2*>(r);
-      w[0] = u.x;
-      w[1] = u.y;
-    } else {
-      w[0] = *reinterpret_cast<const uint32_t*>(r);
-    }
+  __device__ __forceinline__ const unsigned char* vq(int w) const {
+    return ring + static_cast<size_t>(slot(4 + w)) * PageLayout<HD>::kQuarterBytes;
   }
   __device__ __forceinline__ void before_k(int w) const { wait_bounded(full0 + 8 * slot(w), parity(w), abort_flag, 11); }
   __device__ __forceinline__ void after_k(int w) const {
@@ -194,30 +205,43 @@ struct RingKV {
   }
 };
 
-// Prefill: the split's keys and values are staged whole in shared memory.
+// Prefill: the split's keys and values are staged whole in shared memory, in
+// the same layout (quarter w at w * quarter bytes).
 template <int HD>
 struct SmemKV {
-  const __nv_bfloat16* ks;  // [256][HD] positions start .. start+255
-  const __nv_bfloat16* vs;
+  const unsigned char* ks;
+  const unsigned char* vs;
+  __device__ __forceinline__ const unsigned char* kq(int w) const { return ks + w * PageLayout<HD>::kQuarterBytes; }
+  __device__ __forceinline__ const unsigned char* vq(int w) const { return vs + w * PageLayout<HD>::kQuarterBytes; }
   __device__ __forceinline__ void before_k(int) const {}
   __device__ __forceinline__ void after_k(int) const {}
   __device__ __forceinline__ void before_v(int) const {}
   __device__ __forceinline__ void after_v(int) const {}
-  __device__ __forceinline__ void k(int pp, int c, uint4 (&out)[HD / 64]) const {
-#pragma unroll
-    for (int i = 0; i < HD / 64; ++i) out[i] = *reinterpret_cast<const uint4*>(ks + pp * HD + 64 * i + 8 * c);
-  }
-  __device__ __forceinline__ void vpiece(int pp, int lane, uint32_t (&w)[HD / 64]) const {
-    const __nv_bfloat16* r = vs + pp * HD + lane * (HD / 32);
-    if constexpr (HD == 128) {
-      const uint2 u = *reinterpret_cast<const uint2*>(r);
-      w[0] = u.x;
-      w[1] = u.y;
-    } else {
-      w[0] = *reinterpret_cast<const uint32_t*>(r);
-    }
-  }
 };
+
+// The 16-byte pieces of position pp (0..255 within the split) that lane c owns
+// in the fp32-query score loop: dims [8c, 8c+8) and, for head_dim 128, [64+8c, 64+8c+8).
+template <int HD, class KV>
+__device__ __forceinline__ void k_pieces(const KV& kv, int pp, int c, uint4 (&out)[HD / 64]) {
+  const unsigned char* q = kv.kq(pp >> 6);
+#pragma unroll
+  for (int i = 0; i < HD / 64; ++i)
+    out[i] = *reinterpret_cast<const uint4*>(q + PageLayout<HD>::chunk(pp & 63, 8 * i + c));
+}
+// the HD/64 words (HD/32 values) of value row pp that lane `lane` owns in the fp32-query weighted sum
+template <int HD, class KV>
+__device__ __forceinline__ void v_piece(const KV& kv, int pp, int lane, uint32_t (&w)[HD / 64]) {
+  const unsigned char* q = kv.vq(pp >> 6);
+  if constexpr (HD == 128) {
+    // dims 4 lane .. 4 lane + 3: half of chunk lane / 2
+    const uint2 u = *reinterpret_cast<const uint2*>(q + PageLayout<HD>::chunk(pp & 63, lane >> 1) + (lane & 1) * 8);
+    w[0] = u.x;
+    w[1] = u.y;
+  } else {
+    // dims 2 lane, 2 lane + 1: a quarter of chunk lane / 4
+    w[0] = *reinterpret_cast<const uint32_t*>(q + PageLayout<HD>::chunk(pp & 63, lane >> 2) + (lane & 3) * 4);
+  }
+}
 
 // Query registers of one lane for the score phase: the dims lane c owns
 // (64i + 8c + 2m, 64i + 8c + 2m + 1) of each head, as fp32 pairs.
@@ -341,7 +365,7 @@ __device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& k
     float dot[G];
     if (pp < valid) {
       uint4 kr[HD / 64];
-      kv.k(pp, c, kr);
+      k_pieces<HD>(kv, pp, c, kr);
       float2 kf[NW];
 #pragma unroll
       for (int j = 0; j < HD / 64; ++j) {
@@ -403,7 +427,7 @@ __device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& k
   for (int j = 0; j < nv; ++j) {
     const int pp = 64 * w + j;
     uint32_t vw[HD / 64];
-    kv.vpiece(pp, lane, vw);
+    v_piece<HD>(kv, pp, lane, vw);
     const float4 e4 = *reinterpret_cast<const float4*>(&sm.e[pp][0]);
     const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
@@ -424,6 +448,194 @@ __device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& k
       *reinterpret_cast<float2*>(dst) = acc[hh][0];
     }
   }
+  group_sync(group);
+#pragma unroll
+  for (int j = 0; j < outputs_per_thread(HD, G); ++j) {
+    const int k = tid + kGroupThreads * j;
+    if (k < G * HD) {
+      const int hh = k / HD, d = k % HD;
+      out[j] = __fadd_rn(__fadd_rn(__fadd_rn(sm.o[0][hh][d], sm.o[1][hh][d]), sm.o[2][hh][d]), sm.o[3][hh][d]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ warp-level MMA split reduction
+// bf16 queries: the two products of a split run on the tensor cores as
+// warp-level MMAs (mma.sync m16n8k16, bf16 operands, fp32 accumulation),
+// reading K and V straight from the swizzled pages with ldmatrix.
+//   scores  S^T[pos][head] = K[pos][:] . q[head][:]   (A = K, 16 positions x 16 dims; B = q^T, heads padded to 8)
+//   values  O^T[dim][head] = sum_pos V[pos][dim] P[head][pos]   (A = V^T via ldmatrix.trans; B = P^T)
+// The softmax between them is the CUDA-core code of split_reduce, except that
+// the weights exp2(z - m) are rounded to bf16 (the MMA's operand type) and l
+// sums the rounded weights, so o / l is a weighted mean of V with exactly the
+// weights the MMA used.  Every sum has one fixed order (the MMA's k steps in
+// ascending order, then the four warps' partial sums 0+1+2+3), whoever calls it:
+// decode and prefill give the same bits.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// d = a * b + d (m16n8k16, bf16 in, fp32 accumulate)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float round_bf16f_(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// B operand of the score MMAs: q^T, 16 dims x 8 columns (query heads g*G.., zero past G).
+template <int HD>
+struct QFrags {
+  uint32_t b[HD / 16][2];
+};
+
+// qrow: the G query rows [G][HD] (bf16) of the item, in shared or global memory.
+template <int HD, int G>
+__device__ __forceinline__ void load_qfrags(const __nv_bfloat16* qrow, QFrags<HD>& qf) {
+  const int lane = threadIdx.x & 31;
+  const int n = lane >> 2;          // column = query head
+  const int k0 = (lane & 3) * 2;   // first of the two k values this lane holds
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    if (n < G) {
+      qf.b[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + n * HD + 16 * ks + k0);
+      qf.b[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + n * HD + 16 * ks + 8 + k0);
+    } else {
+      qf.b[ks][0] = 0u;
+      qf.b[ks][1] = 0u;
+    }
+  }
+}
+
+template <int HD, int G, class KV>
+__device__ __forceinline__ void split_reduce_tc(const QFrags<HD>& qf, const KV& kv, int valid, float scale_log2,
+                                                SplitSmem<HD, G>& sm, int group, float (&out)[outputs_per_thread(HD, G)]) {
+  const int tid = threadIdx.x % kGroupThreads;
+  const int w = tid >> 5;
+  const int lane = tid & 31;
+  const int g8 = lane >> 2;        // fragment row group
+  const int c4 = lane & 3;         // fragment column pair
+  const int mi = lane >> 3;        // ldmatrix: the matrix this lane addresses
+  const int mr = lane & 7;         //           and its row
+  const int base = 64 * w;         // this warp's positions [base, base + 64) = quarter w
+  const int nvalid = min(64, valid - base);  // positions of this warp that take part (warp-uniform)
+
+  // ---- scores: one m16 tile of 16 positions per page of the quarter
+  kv.before_k(w);
+  {
+    const uint32_t kq = static_cast<uint32_t>(__cvta_generic_to_shared(kv.kq(w)));
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      if (16 * mt >= nvalid) break;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      // matrices: (pos 0-7, dims 0-7), (pos 8-15, dims 0-7), (pos 0-7, dims 8-15), (pos 8-15, dims 8-15)
+      const int qpos = 16 * mt + (mi & 1) * 8 + mr;
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kq + PageLayout<HD>::chunk(qpos, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+        mma_bf16(d, a0, a1, a2, a3, qf.b[ks][0], qf.b[ks][1]);
+      }
+      // d: (pos g8, head 2c4), (pos g8, head 2c4+1), (pos g8+8, head 2c4), (pos g8+8, head 2c4+1)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int hh = 2 * c4 + (e & 1);
+        const int pp = base + 16 * mt + g8 + (e >> 1) * 8;
+        if (hh < G) sm.z[hh][pp] = (pp < valid) ? __fmul_rn(d[e], scale_log2) : -INFINITY;
+      }
+    }
+    // positions of this warp past the split's valid ones
+    for (int pp = base + max(nvalid, 0) + lane; pp < base + 64; pp += 32)
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) sm.z[hh][pp] = -INFINITY;
+  }
+  kv.after_k(w);
+  group_sync(group);
+
+  // ---- per-head max (exact, order-free) and sum of the bf16-rounded exponentials (fixed order)
+  for (int hh = w; hh < G; hh += 4) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, sm.z[hh][lane + 32 * j]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int pp = lane + 32 * j;
+      const float e = (pp < valid) ? round_bf16f_(exp2f(__fsub_rn(sm.z[hh][pp], mx))) : 0.f;
+      sm.e[pp][hh] = e;
+      s = __fadd_rn(s, e);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
+    if (lane == 0) {
+      sm.m[hh] = mx;
+      sm.l[hh] = s;
+    }
+  }
+  group_sync(group);
+
+  // ---- weighted sum of values: O^T (HD dims x 8 columns) over this warp's positions
+  float acc[HD / 16][4];
+#pragma unroll
+  for (int mt = 0; mt < HD / 16; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+  kv.before_v(w);
+  {
+    const uint32_t vq = static_cast<uint32_t>(__cvta_generic_to_shared(kv.vq(w)));
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {  // 16 positions per step: page ks of the quarter
+      if (16 * ks >= nvalid) break;
+      // B = P^T: (pos 2c4, 2c4+1 | +8) x column g8 (a query head, zero past G)
+      uint32_t b0 = 0u, b1 = 0u;
+      if (g8 < G) {
+        const int p0 = base + 16 * ks + 2 * c4;
+        b0 = pack_bf16x2(sm.e[p0][g8], sm.e[p0 + 1][g8]);
+        b1 = pack_bf16x2(sm.e[p0 + 8][g8], sm.e[p0 + 9][g8]);
+      }
+      const bool partial = 16 * ks + 16 > nvalid;
+      // the A fragment's positions: 2c4, 2c4+1 (a0, a1) and 8+2c4, 8+2c4+1 (a2, a3)
+      const int lim = nvalid - 16 * ks;
+#pragma unroll
+      for (int mt = 0; mt < HD / 16; ++mt) {
+        // A = V^T: matrices (dims 0-7, pos 0-7), (dims 8-15, pos 0-7), (dims 0-7, pos 8-15), (dims 8-15, pos 8-15),
+        // each read as 8 rows of positions and transposed
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vq + PageLayout<HD>::chunk(16 * ks + (mi >> 1) * 8 + mr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        if (partial) {
+          // positions past the valid ones hold stale or never-written data: take no part (0 x NaN would)
+          const uint32_t lo0 = (2 * c4 < lim) ? 0x0000ffffu : 0u, hi0 = (2 * c4 + 1 < lim) ? 0xffff0000u : 0u;
+          const uint32_t lo1 = (8 + 2 * c4 < lim) ? 0x0000ffffu : 0u, hi1 = (8 + 2 * c4 + 1 < lim) ? 0xffff0000u : 0u;
+          a0 &= lo0 | hi0;
+          a1 &= lo0 | hi0;
+          a2 &= lo1 | hi1;
+          a3 &= lo1 | hi1;
+        }
+        mma_bf16(acc[mt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+  kv.after_v(w);
+  group_sync(group);  // every warp is done with e before o overwrites it
+  // acc[mt]: (dim 16mt + g8, head 2c4), (.., head 2c4+1), (dim 16mt + g8 + 8, head 2c4), (.., 2c4+1)
+#pragma unroll
+  for (int mt = 0; mt < HD / 16; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int hh = 2 * c4 + (e & 1);
+      if (hh < G) sm.o[w][hh][16 * mt + g8 + (e >> 1) * 8] = acc[mt][e];
+    }
   group_sync(group);
 #pragma unroll
   for (int j = 0; j < outputs_per_thread(HD, G); ++j) {
@@ -688,7 +900,7 @@ constexpr int kItemSlots = 2;
 
 template <int HD, int G>
 struct DecodeSmem {
-  __nv_bfloat16 ring[kDecodeStages][64 * HD];
+  __align__(1024) unsigned char ring[kDecodeStages][PageLayout<HD>::kQuarterBytes];  // TMA tensor copies land swizzled
   SplitSmem<HD, G> sm;
   __align__(16) __nv_bfloat16 qbuf[kItemSlots][G * HD];
   int4 item[kItemSlots];  // {unit u, kv head g, first position, end position}
@@ -699,15 +911,28 @@ struct DecodeSmem {
   int abort_flag;
 };
 
-template <int HD, int G>
+// One TMA tensor copy of a page of one kv head: box {64 dims, 16 positions, HD/64
+// halves} of the cache viewed as [pages * kv heads][16][HD/64][64], landing as
+// [half][position][64 dims] with the 128-byte swizzle.
+__device__ __forceinline__ void tma_page(uint32_t dst, const CUtensorMap* map, uint32_t bar, int page_head) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(0), "r"(0), "r"(page_head)
+      : "memory");
+}
+
+template <int HD, int G, bool TC>
 __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
-    const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const __nv_bfloat16* __restrict__ kc,
-    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, int B, int hq, int hkv, int max_pages,
-    int num_pages, float scale_log2, DecodePlan plan, Partials part) {
-  // qf: fp32 queries (fp32-activation layers; q unused).  The consumers then
+    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+    const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const int* __restrict__ block_table, int B,
+    int hq, int hkv, int max_pages, int num_pages, float scale_log2, DecodePlan plan, Partials part) {
+  // TC: bf16 queries, the split's products on the tensor cores (split_reduce_tc).
+  // qf: fp32 queries (fp32-activation layers; q unused, TC false).  The consumers then
   // read q from global memory and the item ring carries the descriptor only.
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>(smem_raw);
+  DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                              ~uintptr_t(1023));
   const uint32_t full0 = smem_u32(&S.full[0]);
   const uint32_t empty0 = smem_u32(&S.empty[0]);
   const uint32_t ifull0 = smem_u32(&S.item_full[0]);
@@ -809,10 +1034,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
           }
           __syncwarp();
           if (plane < npg) {
-            const __nv_bfloat16* cache = (j < 4) ? kc : vc;
             const int page = checked_page(brow, (bs + q0) / kPage + plane, max_pages, num_pages);
-            const __nv_bfloat16* src = cache + (static_cast<size_t>(page) * hkv + g) * kPage * HD;
-            bulk_g2s(smem_u32(&S.ring[st][plane * kPage * HD]), src, kPage * HD * 2, fb);
+            tma_page(smem_u32(&S.ring[st][plane * PageLayout<HD>::kPageBytes]), (j < 4) ? &kmap : &vmap, fb,
+                     page * hkv + g);
           }
           issued |= 1u << st;
           ipar = (ipar & ~(1u << st)) | (ph << st);
@@ -850,7 +1074,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const int ustart = desc.z;
     const int uend = desc.w;
     QRegs<HD, G> qr;
-    if (qf != nullptr) {
+    QFrags<HD> qfr;
+    if constexpr (TC) {
+      load_qfrags<HD, G>(&S.qbuf[islot][0], qfr);
+    } else if (qf != nullptr) {
       const int b = find_row(plan.prefix, B, u);
       load_q<HD, G>(qf + (static_cast<size_t>(b) * hq + g * G) * HD, c, qr);
     } else {
@@ -871,7 +1098,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
       const int valid = min(kSplit, uend - bs);
       RingKV<HD> kv{&S.ring[0][0], full0, empty0, n0, kDecodeStages, abort_flag};
       float bo[OPT];
-      split_reduce<HD, G>(qr, kv, valid, scale_log2, S.sm, 0, bo);
+      if constexpr (TC) split_reduce_tc<HD, G>(qfr, kv, valid, scale_log2, S.sm, 0, bo);
+      else split_reduce<HD, G>(qr, kv, valid, scale_log2, S.sm, 0, bo);
 #pragma unroll
       for (int j = 0; j < OPT; ++j) {
         const int k = tid + kGroupThreads * j;
@@ -1054,12 +1282,12 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int* __restric
 
 template <int HD, int G>
 struct PrefillSmem {
-  __nv_bfloat16 k[kSplit][HD];
-  __nv_bfloat16 v[kSplit][HD];
+  __align__(16) unsigned char k[4 * PageLayout<HD>::kQuarterBytes];  // the split's keys, page layout of the ring
+  __align__(16) unsigned char v[4 * PageLayout<HD>::kQuarterBytes];
   SplitSmem<HD, G> grp[kPrefillGroups];
 };
 
-template <int HD, int G>
+template <int HD, int G, bool TC>
 __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_kernel(
     const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, const int* __restrict__ q_pos0,
@@ -1098,11 +1326,12 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
       const int pos = st + r;
       const int pg = checked_page(block_table + static_cast<size_t>(b) * max_pages, pos / kPage, max_pages, num_pages);
       const size_t off = ((static_cast<size_t>(pg) * hkv + g) * kPage + (pos % kPage)) * HD + ch * 8;
-      *reinterpret_cast<uint4*>(&sm.k[r][ch * 8]) = *reinterpret_cast<const uint4*>(kc + off);
-      *reinterpret_cast<uint4*>(&sm.v[r][ch * 8]) = *reinterpret_cast<const uint4*>(vc + off);
+      const int so = (r >> 6) * PageLayout<HD>::kQuarterBytes + PageLayout<HD>::chunk(r & 63, ch);
+      *reinterpret_cast<uint4*>(&sm.k[so]) = *reinterpret_cast<const uint4*>(kc + off);
+      *reinterpret_cast<uint4*>(&sm.v[so]) = *reinterpret_cast<const uint4*>(vc + off);
     }
     __syncthreads();
-    SmemKV<HD> kv{&sm.k[0][0], &sm.v[0][0]};
+    SmemKV<HD> kv{&sm.k[0], &sm.v[0]};
     for (int qi = group; qi < ntok; qi += kPrefillGroups) {
       const int tok = tok0 + qi;
       const int p = p_first + qi;
@@ -1110,11 +1339,17 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
       int st_t, en_t;
       split_range(inv, pos0, s, p, st_t, en_t);
       const int valid = en_t - st_t;  // >= 1; same origin st as the staged rows
-      QRegs<HD, G> qr;
-      if (qf != nullptr) load_q<HD, G>(qf + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
-      else load_q<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
       float bo[OPT];
-      split_reduce<HD, G>(qr, kv, valid, scale_log2, sm.grp[group], group, bo);
+      if constexpr (TC) {
+        QFrags<HD> qfr;
+        load_qfrags<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, qfr);
+        split_reduce_tc<HD, G>(qfr, kv, valid, scale_log2, sm.grp[group], group, bo);
+      } else {
+        QRegs<HD, G> qr;
+        if (qf != nullptr) load_q<HD, G>(qf + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
+        else load_q<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
+        split_reduce<HD, G>(qr, kv, valid, scale_log2, sm.grp[group], group, bo);
+      }
       const size_t pidx = (static_cast<size_t>(plan.tok_prefix[tok]) + s) * hq + g * G;
 #pragma unroll
       for (int j = 0; j < OPT; ++j) {
@@ -1243,12 +1478,66 @@ PrefillWs carve_prefill(void* ws, size_t cap, int B, int T, const bi_attn_dims* 
   return r;
 }
 
+// Dynamic shared memory of the decode split kernel (the ring is aligned to 1024 bytes inside it).
 template <int HD, int G>
+constexpr size_t decode_smem() { return sizeof(DecodeSmem<HD, G>) + 1024; }
+
+template <int HD, int G, bool TC>
 bi_status decode_grid(int* grid) {
-  const size_t smem = sizeof(DecodeSmem<HD, G>);
-  const void* fn = reinterpret_cast<const void*>(decode_split_kernel<HD, G>);
+  const size_t smem = decode_smem<HD, G>();
+  const void* fn = reinterpret_cast<const void*>(decode_split_kernel<HD, G, TC>);
   BI_CUDA_TRY(ensure_smem_limit(fn, static_cast<int>(smem)));
   *grid = occupancy_per_sm(fn, kDecodeThreads, smem) * num_sms();
+  return BI_OK;
+}
+
+// Tensor map of a paged K or V cache [pages][kv heads][16][HD] bf16 for the
+// decode loader: viewed as [pages * kv heads][16 positions][HD/64 halves][64]
+// (strides 16*HD*2, HD*2 and 128 bytes), box {64, 16, HD/64, 1} = one page of
+// one kv head, 128-byte swizzle.  Cached per (pointer, shape, device).
+PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+std::mutex g_cache_map_mutex;
+std::vector<std::pair<std::tuple<const void*, int, int, int, int>, CUtensorMap>> g_cache_maps;
+
+bi_status cache_map(const void* cache, int num_pages, int hkv, int hd, CUtensorMap* out) {
+  int dev = 0;
+  BI_CUDA_TRY(cudaGetDevice(&dev));
+  const auto key = std::make_tuple(cache, num_pages, hkv, hd, dev);
+  {
+    std::lock_guard<std::mutex> lock(g_cache_map_mutex);
+    for (const auto& e : g_cache_maps)
+      if (e.first == key) {
+        *out = e.second;
+        return BI_OK;
+      }
+  }
+  auto fn = attn_encode_fn();
+  BI_REQUIRE(fn != nullptr, BI_ERR_CUDA, "attention: cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[4] = {64, 16, static_cast<cuuint64_t>(hd / 64),
+                        static_cast<cuuint64_t>(num_pages) * static_cast<cuuint64_t>(hkv)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(hd) * 2, 128, static_cast<cuuint64_t>(16 * hd * 2)};
+  cuuint32_t box[4] = {64, 16, static_cast<cuuint32_t>(hd / 64), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  BI_REQUIRE(r == CUDA_SUCCESS, BI_ERR_CUDA, "attention: cuTensorMapEncodeTiled failed for the KV cache (%d)",
+             static_cast<int>(r));
+  std::lock_guard<std::mutex> lock(g_cache_map_mutex);
+  if (g_cache_maps.size() > 1024) g_cache_maps.clear();
+  g_cache_maps.emplace_back(key, *out);
   return BI_OK;
 }
 
@@ -1280,14 +1569,25 @@ bi_status decode_launch(const void* q, const void* kc, const void* vc, const int
     BI_LAUNCH_CHECK();
   }
   const float sl2 = dm->scale * kLog2e;
+  CUtensorMap kmap, vmap;
+  BI_TRY(cache_map(kc, dm->num_pages, dm->num_kv_heads, HD, &kmap));
+  BI_TRY(cache_map(vc, dm->num_pages, dm->num_kv_heads, HD, &vmap));
   int grid = 0;
-  BI_TRY((decode_grid<HD, G>(&grid)));
-  const size_t dsmem = sizeof(DecodeSmem<HD, G>);
-  BI_TIMED(::bi::kTagAttnDecodeSplit, s,
-           BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G>, dim3(grid), dim3(kDecodeThreads), dsmem, s, 
-               qf ? nullptr : static_cast<const __nv_bfloat16*>(q), qf ? static_cast<const float*>(q) : nullptr,
-               static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt, B,
-               dm->num_q_heads, dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part)));
+  const size_t dsmem = decode_smem<HD, G>();
+  if (qf) {
+    BI_TRY((decode_grid<HD, G, false>(&grid)));
+    BI_TIMED(::bi::kTagAttnDecodeSplit, s,
+             BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, false>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
+                                     kmap, vmap, nullptr, static_cast<const float*>(q), bt, B, dm->num_q_heads,
+                                     dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part)));
+  } else {
+    BI_TRY((decode_grid<HD, G, true>(&grid)));
+    BI_TIMED(::bi::kTagAttnDecodeSplit, s,
+             BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, true>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
+                                     kmap, vmap, static_cast<const __nv_bfloat16*>(q), nullptr, bt, B,
+                                     dm->num_q_heads, dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan,
+                                     w.part)));
+  }
   BI_LAUNCH_CHECK();
   BI_TIMED(::bi::kTagAttnDecodeMerge, s,
            BI_PDL_CHECK(launch_pdl(decode_merge_kernel, dim3(B * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part,
@@ -1305,13 +1605,21 @@ bi_status prefill_launch(const void* q, const void* kc, const void* vc, const in
   BI_TIMED(::bi::kTagAttnPlan, s, BI_PDL_CHECK(launch_pdl(prefill_plan_kernel, dim3(1), dim3(1024), 0, s, q_start, q_pos0, B, T, static_cast<int>(mode), target, w.plan)));
   BI_LAUNCH_CHECK();
   const size_t smem = sizeof(PrefillSmem<HD, G>);
-  BI_CUDA_TRY(ensure_smem_limit(reinterpret_cast<const void*>(prefill_split_kernel<HD, G>), static_cast<int>(smem)));
   const float sl2 = dm->scale * kLog2e;
-  BI_TIMED(::bi::kTagAttnPrefillSplit, s, BI_PDL_CHECK(launch_pdl(prefill_split_kernel<HD, G>, dim3(num_sms()), dim3(kGroupThreads * kPrefillGroups), smem, s, 
-      qf ? nullptr : static_cast<const __nv_bfloat16*>(q), qf ? static_cast<const float*>(q) : nullptr,
-      static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt, q_pos0, q_start,
-      dm->num_q_heads, dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part)));
-  BI_LAUNCH_CHECK();
+  auto go = [&](auto kern) -> bi_status {
+    BI_CUDA_TRY(ensure_smem_limit(reinterpret_cast<const void*>(kern), static_cast<int>(smem)));
+    BI_TIMED(::bi::kTagAttnPrefillSplit, s,
+             BI_PDL_CHECK(launch_pdl(kern, dim3(num_sms()), dim3(kGroupThreads * kPrefillGroups), smem, s,
+                                     qf ? nullptr : static_cast<const __nv_bfloat16*>(q),
+                                     qf ? static_cast<const float*>(q) : nullptr,
+                                     static_cast<const __nv_bfloat16*>(kc), static_cast<const __nv_bfloat16*>(vc), bt,
+                                     q_pos0, q_start, dm->num_q_heads, dm->num_kv_heads, dm->max_pages,
+                                     dm->num_pages, sl2, w.plan, w.part)));
+    BI_LAUNCH_CHECK();
+    return BI_OK;
+  };
+  // bf16 queries: the products on the tensor cores, as in decode (same function, same bits)
+  BI_TRY(qf ? go(prefill_split_kernel<HD, G, false>) : go(prefill_split_kernel<HD, G, true>));
   BI_TIMED(::bi::kTagAttnPrefillMerge, s, BI_PDL_CHECK(launch_pdl(prefill_merge_kernel, dim3(T * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part, w.plan, q_start, q_pos0, B,
                                                                out, dm->num_q_heads, dm->num_kv_heads, HD)));
   BI_LAUNCH_CHECK();
