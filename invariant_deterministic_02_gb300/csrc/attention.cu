@@ -73,7 +73,7 @@ struct SplitSmem {
   union {
     struct {
       float z[G][kSplit];               // scores (log2 domain), -inf where masked
-      __align__(16) float e[kSplit][4]; // exp2(z - m), position-major, heads padded to 4
+      __align__(16) uint32_t e[kSplit][4]; // weights exp2(z - m) as bf16 (hi, lo) pairs, position-major, heads padded to 4
     };
     __align__(16) float o[4][G][HD];  // per-warp partial weighted sums
   };
@@ -219,257 +219,23 @@ struct SmemKV {
   __device__ __forceinline__ void after_v(int) const {}
 };
 
-// The 16-byte pieces of position pp (0..255 within the split) that lane c owns
-// in the fp32-query score loop: dims [8c, 8c+8) and, for head_dim 128, [64+8c, 64+8c+8).
-template <int HD, class KV>
-__device__ __forceinline__ void k_pieces(const KV& kv, int pp, int c, uint4 (&out)[HD / 64]) {
-  const unsigned char* q = kv.kq(pp >> 6);
-#pragma unroll
-  for (int i = 0; i < HD / 64; ++i)
-    out[i] = *reinterpret_cast<const uint4*>(q + PageLayout<HD>::chunk(pp & 63, 8 * i + c));
-}
-// the HD/64 words (HD/32 values) of value row pp that lane `lane` owns in the fp32-query weighted sum
-template <int HD, class KV>
-__device__ __forceinline__ void v_piece(const KV& kv, int pp, int lane, uint32_t (&w)[HD / 64]) {
-  const unsigned char* q = kv.vq(pp >> 6);
-  if constexpr (HD == 128) {
-    // dims 4 lane .. 4 lane + 3: half of chunk lane / 2
-    const uint2 u = *reinterpret_cast<const uint2*>(q + PageLayout<HD>::chunk(pp & 63, lane >> 1) + (lane & 1) * 8);
-    w[0] = u.x;
-    w[1] = u.y;
-  } else {
-    // dims 2 lane, 2 lane + 1: a quarter of chunk lane / 4
-    w[0] = *reinterpret_cast<const uint32_t*>(q + PageLayout<HD>::chunk(pp & 63, lane >> 2) + (lane & 3) * 4);
-  }
-}
-
-// Query registers of one lane for the score phase: the dims lane c owns
-// (64i + 8c + 2m, 64i + 8c + 2m + 1) of each head, as fp32 pairs.
-template <int HD, int G>
-struct QRegs {
-  float2 q[G][HD / 16];
-};
-
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-template <int HD, int G>
-__device__ __forceinline__ void load_q(const __nv_bfloat16* qrow /* [Hq][HD] at head g*G */, int c, QRegs<HD, G>& qr) {
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-#pragma unroll
-    for (int i = 0; i < HD / 64; ++i) {
-      const uint4 u = *reinterpret_cast<const uint4*>(qrow + hh * HD + 64 * i + 8 * c);
-      qr.q[hh][4 * i + 0] = bf16x2_to_float2(u.x);
-      qr.q[hh][4 * i + 1] = bf16x2_to_float2(u.y);
-      qr.q[hh][4 * i + 2] = bf16x2_to_float2(u.z);
-      qr.q[hh][4 * i + 3] = bf16x2_to_float2(u.w);
-    }
-  }
-}
-
-// The same registers from fp32 query rows (fp32-activation layers).
-template <int HD, int G>
-__device__ __forceinline__ void load_q(const float* qrow /* [Hq][HD] at head g*G */, int c, QRegs<HD, G>& qr) {
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-#pragma unroll
-    for (int i = 0; i < HD / 64; ++i) {
-      const float4 a = *reinterpret_cast<const float4*>(qrow + hh * HD + 64 * i + 8 * c);
-      const float4 b = *reinterpret_cast<const float4*>(qrow + hh * HD + 64 * i + 8 * c + 4);
-      qr.q[hh][4 * i + 0] = make_float2(a.x, a.y);
-      qr.q[hh][4 * i + 1] = make_float2(a.z, a.w);
-      qr.q[hh][4 * i + 2] = make_float2(b.x, b.y);
-      qr.q[hh][4 * i + 3] = make_float2(b.z, b.w);
-    }
-  }
-}
-
-// Sum of the 8 partial dot products of one position held by lanes 8s..8s+7
-// (one per head in dot[]), reduced with halving exchanges: lane c ends with the
-// full sum of head head_of_lane(c).  The additions are those of a xor-butterfly
-// (offsets 4, 2, 1), so every lane that holds a head's sum holds the same bits.
-template <int G>
-__device__ __forceinline__ float reduce_scatter8(const float (&dot)[G], int c) {
-  if constexpr (G == 4) {
-    const bool hi = (c & 4) != 0;
-    const float k0 = hi ? dot[2] : dot[0], k1 = hi ? dot[3] : dot[1];
-    const float s0 = hi ? dot[0] : dot[2], s1 = hi ? dot[1] : dot[3];
-    const float a0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, s0, 4));
-    const float a1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, s1, 4));
-    const bool mid = (c & 2) != 0;
-    const float k = mid ? a1 : a0, snd = mid ? a0 : a1;
-    const float b = __fadd_rn(k, __shfl_xor_sync(0xffffffffu, snd, 2));
-    return __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, 1));
-  } else if constexpr (G == 2) {
-    const bool hi = (c & 4) != 0;
-    const float k = hi ? dot[1] : dot[0], snd = hi ? dot[0] : dot[1];
-    float a = __fadd_rn(k, __shfl_xor_sync(0xffffffffu, snd, 4));
-    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    return __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
-  } else {
-    float a = dot[0];
-    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    return __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
-  }
-}
-
-template <int G>
-__device__ __forceinline__ int head_of_lane(int c) {
-  if constexpr (G == 4) return ((c >> 2) & 1) * 2 + ((c >> 1) & 1);
-  else if constexpr (G == 2) return (c >> 2) & 1;
-  else return 0;
-}
-
-template <int G>
-__device__ __forceinline__ bool writes_score(int c) {
-  if constexpr (G == 4) return (c & 1) == 0;
-  else if constexpr (G == 2) return (c & 3) == 0;
-  else return c == 0;
-}
-
-__host__ __device__ constexpr int outputs_per_thread(int HD, int G) { return (G * HD + kGroupThreads - 1) / kGroupThreads; }
-
-// The split reduction.  Executed by one 128-thread group; `valid` (1..256)
-// positions starting at the loader's origin take part.  On return every thread
-// holds its assigned weighted-sum outputs k = tid + 128*j (head k / HD, dim
-// k % HD) in `out`, and sm.m / sm.l hold the per-head max and sum.
-//
-// Fixed arithmetic order (the same whoever calls it):
-//  * score of position pp, head h: lane (slot, c) with pp = 64w + 4i + slot
-//    forms two interleaved FMA chains over its 16 (8 for head_dim 64) dims,
-//    even and odd dims (packed fp32 FMA), adds them, then the 8 lanes of the
-//    position are summed as a xor-butterfly 4, 2, 1; times scale*log2(e);
-//  * m = max of the scores (exact); e = exp2(z - m); l: lane L adds positions
-//    L, L+32, ..., L+224 in order, then a 32-lane butterfly;
-//  * o[h][d]: lane L owns dims (HD/32)L .. +HD/32; warp w adds e*v over its
-//    positions 64w .. 64w+63 in order; the four warp sums are added 0+1+2+3.
-template <int HD, int G, class KV>
-__device__ __forceinline__ void split_reduce(const QRegs<HD, G>& qr, const KV& kv, int valid, float scale_log2,
-                                             SplitSmem<HD, G>& sm, int group, float (&out)[outputs_per_thread(HD, G)]) {
-  constexpr int NW = HD / 16;  // bf16 pairs per lane in the score phase
-  constexpr int DPO = HD / 32; // dims per lane in the weighted sum
-  const int tid = threadIdx.x % kGroupThreads;
-  const int w = tid >> 5;
-  const int lane = tid & 31;
-  const int slot = lane >> 3;
-  const int c = lane & 7;
-
-  // ---- scores
-  kv.before_k(w);
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
-    const int pp = 64 * w + 4 * i + slot;
-    float dot[G];
-    if (pp < valid) {
-      uint4 kr[HD / 64];
-      k_pieces<HD>(kv, pp, c, kr);
-      float2 kf[NW];
-#pragma unroll
-      for (int j = 0; j < HD / 64; ++j) {
-        kf[4 * j + 0] = bf16x2_to_float2(kr[j].x);
-        kf[4 * j + 1] = bf16x2_to_float2(kr[j].y);
-        kf[4 * j + 2] = bf16x2_to_float2(kr[j].z);
-        kf[4 * j + 3] = bf16x2_to_float2(kr[j].w);
-      }
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < NW; ++e) a = __ffma2_rn(qr.q[hh][e], kf[e], a);
-        dot[hh] = __fadd_rn(a.x, a.y);
-      }
-    } else {
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) dot[hh] = 0.f;
-    }
-    const float full = reduce_scatter8<G>(dot, c);
-    if (writes_score<G>(c)) sm.z[head_of_lane<G>(c)][pp] = (pp < valid) ? __fmul_rn(full, scale_log2) : -INFINITY;
-  }
-  kv.after_k(w);
-  group_sync(group);
-
-  // ---- per-head max (exact, order-free) and sum of exponentials (fixed order)
-  for (int hh = w; hh < G; hh += 4) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, sm.z[hh][lane + 32 * j]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int pp = lane + 32 * j;
-      const float e = (pp < valid) ? exp2f(__fsub_rn(sm.z[hh][pp], mx)) : 0.f;
-      sm.e[pp][hh] = e;
-      s = __fadd_rn(s, e);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
-    if (lane == 0) {
-      sm.m[hh] = mx;
-      sm.l[hh] = s;
-    }
-  }
-  group_sync(group);
-
-  // ---- weighted sum of values
-  float2 acc[G][DPO / 2];
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-    for (int e = 0; e < DPO / 2; ++e) acc[hh][e] = make_float2(0.f, 0.f);
-  kv.before_v(w);
-  const int nv = min(64, valid - 64 * w);  // positions of this warp (uniform across the warp)
-#pragma unroll 4
-  for (int j = 0; j < nv; ++j) {
-    const int pp = 64 * w + j;
-    uint32_t vw[HD / 64];
-    v_piece<HD>(kv, pp, lane, vw);
-    const float4 e4 = *reinterpret_cast<const float4*>(&sm.e[pp][0]);
-    const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const float2 p2 = make_float2(ev[hh], ev[hh]);
-#pragma unroll
-      for (int e = 0; e < DPO / 2; ++e) acc[hh][e] = __ffma2_rn(p2, bf16x2_to_float2(vw[e]), acc[hh][e]);
-    }
-  }
-  kv.after_v(w);
-  group_sync(group);  // every warp is done with e before o overwrites it
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-    float* dst = &sm.o[w][hh][lane * DPO];
-    if constexpr (DPO == 4) {
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[hh][0].x, acc[hh][0].y, acc[hh][1].x, acc[hh][1].y);
-    } else {
-      *reinterpret_cast<float2*>(dst) = acc[hh][0];
-    }
-  }
-  group_sync(group);
-#pragma unroll
-  for (int j = 0; j < outputs_per_thread(HD, G); ++j) {
-    const int k = tid + kGroupThreads * j;
-    if (k < G * HD) {
-      const int hh = k / HD, d = k % HD;
-      out[j] = __fadd_rn(__fadd_rn(__fadd_rn(sm.o[0][hh][d], sm.o[1][hh][d]), sm.o[2][hh][d]), sm.o[3][hh][d]);
-    }
-  }
-}
-
 // ------------------------------------------------------------------ warp-level MMA split reduction
-// bf16 queries: the two products of a split run on the tensor cores as
-// warp-level MMAs (mma.sync m16n8k16, bf16 operands, fp32 accumulation),
-// reading K and V straight from the swizzled pages with ldmatrix.
-//   scores  S^T[pos][head] = K[pos][:] . q[head][:]   (A = K, 16 positions x 16 dims; B = q^T, heads padded to 8)
-//   values  O^T[dim][head] = sum_pos V[pos][dim] P[head][pos]   (A = V^T via ldmatrix.trans; B = P^T)
-// The softmax between them is the CUDA-core code of split_reduce, except that
-// the weights exp2(z - m) are rounded to bf16 (the MMA's operand type) and l
-// sums the rounded weights, so o / l is a weighted mean of V with exactly the
-// weights the MMA used.  Every sum has one fixed order (the MMA's k steps in
-// ascending order, then the four warps' partial sums 0+1+2+3), whoever calls it:
+// The two products of a split run on the tensor cores as warp-level MMAs
+// (mma.sync m16n8k16, bf16 operands, fp32 accumulation), reading K and V
+// straight from the swizzled pages with ldmatrix:
+//   scores  S^T[pos][head] = K[pos][:] . q[head][:]          (A = K: 16 positions x 16 dims; B = q^T, heads padded to 8)
+//   values  O^T[dim][head] = sum_pos V[pos][dim] P[head][pos] (A = V^T, read by ldmatrix.trans; B = P^T)
+// Operands the MMA cannot take exactly in one bf16 value are split into bf16
+// terms whose sum is the value, and one MMA is issued per term on the same A
+// fragment, in term order (every bf16 x bf16 product is exact in fp32):
+//   * fp32 queries (fp32-activation layers): three terms hi, mid, lo (exact,
+//     as in the fp32-activation GEMM); bf16 queries: one;
+//   * the softmax weights p = exp2(z - m): two terms p_hi = bf16(p),
+//     p_lo = bf16(p - p_hi); the weight used is p_hi + p_lo (exact in fp32,
+//     within 2^-16 of p) and l sums those, so o / l is a weighted mean of V with
+//     exactly the weights the MMAs used.
+// Every sum has one fixed order (per k step the terms in order, k steps
+// ascending, then the four warps' partial sums 0+1+2+3), whoever calls it:
 // decode and prefill give the same bits.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -490,35 +256,54 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ float round_bf16f_(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-// B operand of the score MMAs: q^T, 16 dims x 8 columns (query heads g*G.., zero past G).
-template <int HD>
+// Outputs per thread of the split function: thread t of the group holds the
+// weighted sums k = t + 128 j (head k / HD, dim k % HD).
+__host__ __device__ constexpr int outputs_per_thread(int HD, int G) { return (G * HD + kGroupThreads - 1) / kGroupThreads; }
+
+// B operand of the score MMAs: q^T, 16 dims x 8 columns (query heads g*G.., zero
+// past G), per k step of 16 dims, per term.
+template <int HD, int PL>
 struct QFrags {
-  uint32_t b[HD / 16][2];
+  uint32_t b[PL][HD / 16][2];
 };
 
-// qrow: the G query rows [G][HD] (bf16) of the item, in shared or global memory.
+// The G query rows [G][HD] of the item (bf16, in shared or global memory).
 template <int HD, int G>
-__device__ __forceinline__ void load_qfrags(const __nv_bfloat16* qrow, QFrags<HD>& qf) {
+__device__ __forceinline__ void load_qfrags(const __nv_bfloat16* qrow, QFrags<HD, 1>& qf) {
   const int lane = threadIdx.x & 31;
-  const int n = lane >> 2;          // column = query head
+  const int n = lane >> 2;         // column = query head
   const int k0 = (lane & 3) * 2;   // first of the two k values this lane holds
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks) {
-    if (n < G) {
-      qf.b[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + n * HD + 16 * ks + k0);
-      qf.b[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + n * HD + 16 * ks + 8 + k0);
-    } else {
-      qf.b[ks][0] = 0u;
-      qf.b[ks][1] = 0u;
-    }
+    qf.b[0][ks][0] = n < G ? *reinterpret_cast<const uint32_t*>(qrow + n * HD + 16 * ks + k0) : 0u;
+    qf.b[0][ks][1] = n < G ? *reinterpret_cast<const uint32_t*>(qrow + n * HD + 16 * ks + 8 + k0) : 0u;
   }
 }
+// The same from fp32 query rows (global memory), each value split into three bf16 terms.
+template <int HD, int G>
+__device__ __forceinline__ void load_qfrags(const float* qrow, QFrags<HD, 3>& qf) {
+  const int lane = threadIdx.x & 31;
+  const int n = lane >> 2;
+  const int k0 = (lane & 3) * 2;
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float2 v = make_float2(0.f, 0.f);
+      if (n < G) v = *reinterpret_cast<const float2*>(qrow + n * HD + 16 * ks + 8 * half + k0);
+      float h0, m0, l0, h1, m1, l1;
+      split3(v.x, h0, m0, l0);
+      split3(v.y, h1, m1, l1);
+      qf.b[0][ks][half] = pack_bf16x2(h0, h1);
+      qf.b[1][ks][half] = pack_bf16x2(m0, m1);
+      qf.b[2][ks][half] = pack_bf16x2(l0, l1);
+    }
+}
 
-template <int HD, int G, class KV>
-__device__ __forceinline__ void split_reduce_tc(const QFrags<HD>& qf, const KV& kv, int valid, float scale_log2,
-                                                SplitSmem<HD, G>& sm, int group, float (&out)[outputs_per_thread(HD, G)]) {
+template <int HD, int G, int PL, class KV>
+__device__ __forceinline__ void split_reduce(const QFrags<HD, PL>& qf, const KV& kv, int valid, float scale_log2,
+                                             SplitSmem<HD, G>& sm, int group, float (&out)[outputs_per_thread(HD, G)]) {
   const int tid = threadIdx.x % kGroupThreads;
   const int w = tid >> 5;
   const int lane = tid & 31;
@@ -543,7 +328,8 @@ __device__ __forceinline__ void split_reduce_tc(const QFrags<HD>& qf, const KV& 
       for (int ks = 0; ks < HD / 16; ++ks) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(kq + PageLayout<HD>::chunk(qpos, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-        mma_bf16(d, a0, a1, a2, a3, qf.b[ks][0], qf.b[ks][1]);
+#pragma unroll
+        for (int pl = 0; pl < PL; ++pl) mma_bf16(d, a0, a1, a2, a3, qf.b[pl][ks][0], qf.b[pl][ks][1]);
       }
       // d: (pos g8, head 2c4), (pos g8, head 2c4+1), (pos g8+8, head 2c4), (pos g8+8, head 2c4+1)
 #pragma unroll
@@ -561,7 +347,7 @@ __device__ __forceinline__ void split_reduce_tc(const QFrags<HD>& qf, const KV& 
   kv.after_k(w);
   group_sync(group);
 
-  // ---- per-head max (exact, order-free) and sum of the bf16-rounded exponentials (fixed order)
+  // ---- per-head max (exact, order-free), the weights as two bf16 terms, and their sum (fixed order)
   for (int hh = w; hh < G; hh += 4) {
     float mx = -INFINITY;
 #pragma unroll
@@ -572,9 +358,11 @@ __device__ __forceinline__ void split_reduce_tc(const QFrags<HD>& qf, const KV& 
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int pp = lane + 32 * j;
-      const float e = (pp < valid) ? round_bf16f_(exp2f(__fsub_rn(sm.z[hh][pp], mx))) : 0.f;
-      sm.e[pp][hh] = e;
-      s = __fadd_rn(s, e);
+      const float e = (pp < valid) ? exp2f(__fsub_rn(sm.z[hh][pp], mx)) : 0.f;
+      const float hi = __bfloat162float(__float2bfloat16_rn(e));
+      const float lo = __bfloat162float(__float2bfloat16_rn(__fsub_rn(e, hi)));
+      sm.e[pp][hh] = pack_bf16x2(hi, lo);
+      s = __fadd_rn(s, __fadd_rn(hi, lo));
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
@@ -597,12 +385,15 @@ __device__ __forceinline__ void split_reduce_tc(const QFrags<HD>& qf, const KV& 
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {  // 16 positions per step: page ks of the quarter
       if (16 * ks >= nvalid) break;
-      // B = P^T: (pos 2c4, 2c4+1 | +8) x column g8 (a query head, zero past G)
-      uint32_t b0 = 0u, b1 = 0u;
+      // B = P^T, hi and lo terms: (pos 2c4, 2c4+1 | +8) x column g8 (a query head, zero past G)
+      uint32_t bh0 = 0u, bh1 = 0u, bl0 = 0u, bl1 = 0u;
       if (g8 < G) {
         const int p0 = base + 16 * ks + 2 * c4;
-        b0 = pack_bf16x2(sm.e[p0][g8], sm.e[p0 + 1][g8]);
-        b1 = pack_bf16x2(sm.e[p0 + 8][g8], sm.e[p0 + 9][g8]);
+        const uint32_t e0 = sm.e[p0][g8], e1 = sm.e[p0 + 1][g8], e8 = sm.e[p0 + 8][g8], e9 = sm.e[p0 + 9][g8];
+        bh0 = (e0 & 0xffffu) | (e1 << 16);
+        bl0 = (e0 >> 16) | (e1 & 0xffff0000u);
+        bh1 = (e8 & 0xffffu) | (e9 << 16);
+        bl1 = (e8 >> 16) | (e9 & 0xffff0000u);
       }
       const bool partial = 16 * ks + 16 > nvalid;
       // the A fragment's positions: 2c4, 2c4+1 (a0, a1) and 8+2c4, 8+2c4+1 (a2, a3)
@@ -615,14 +406,15 @@ __device__ __forceinline__ void split_reduce_tc(const QFrags<HD>& qf, const KV& 
         ldsm_x4_t(vq + PageLayout<HD>::chunk(16 * ks + (mi >> 1) * 8 + mr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
         if (partial) {
           // positions past the valid ones hold stale or never-written data: take no part (0 x NaN would)
-          const uint32_t lo0 = (2 * c4 < lim) ? 0x0000ffffu : 0u, hi0 = (2 * c4 + 1 < lim) ? 0xffff0000u : 0u;
-          const uint32_t lo1 = (8 + 2 * c4 < lim) ? 0x0000ffffu : 0u, hi1 = (8 + 2 * c4 + 1 < lim) ? 0xffff0000u : 0u;
-          a0 &= lo0 | hi0;
-          a1 &= lo0 | hi0;
-          a2 &= lo1 | hi1;
-          a3 &= lo1 | hi1;
+          const uint32_t m0 = ((2 * c4 < lim) ? 0x0000ffffu : 0u) | ((2 * c4 + 1 < lim) ? 0xffff0000u : 0u);
+          const uint32_t m1 = ((8 + 2 * c4 < lim) ? 0x0000ffffu : 0u) | ((8 + 2 * c4 + 1 < lim) ? 0xffff0000u : 0u);
+          a0 &= m0;
+          a1 &= m0;
+          a2 &= m1;
+          a3 &= m1;
         }
-        mma_bf16(acc[mt], a0, a1, a2, a3, b0, b1);
+        mma_bf16(acc[mt], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16(acc[mt], a0, a1, a2, a3, bl0, bl1);
       }
     }
   }
@@ -922,14 +714,14 @@ __device__ __forceinline__ void tma_page(uint32_t dst, const CUtensorMap* map, u
       : "memory");
 }
 
-template <int HD, int G, bool TC>
+template <int HD, int G, int PL>
 __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const int* __restrict__ block_table, int B,
     int hq, int hkv, int max_pages, int num_pages, float scale_log2, DecodePlan plan, Partials part) {
-  // TC: bf16 queries, the split's products on the tensor cores (split_reduce_tc).
-  // qf: fp32 queries (fp32-activation layers; q unused, TC false).  The consumers then
-  // read q from global memory and the item ring carries the descriptor only.
+  // PL = 1: bf16 queries, staged with the item; PL = 3: fp32 queries qf
+  // (fp32-activation layers; q unused), which the consumers read from global
+  // memory (the item ring then carries the descriptor only).
   extern __shared__ __align__(128) unsigned char smem_raw[];
   DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                               ~uintptr_t(1023));
@@ -1059,7 +851,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
   // ------------------------------------------------------------------ consumers
   constexpr int OPT = outputs_per_thread(HD, G);
   const int tid = threadIdx.x;
-  const int c = (tid & 31) & 7;
   int n0 = 0;
   // items in the order the producer announces them, up to its end marker (a
   // CTA never gets more than `total`; a wait that gave up ends the loop too)
@@ -1073,15 +864,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const int g = desc.y;
     const int ustart = desc.z;
     const int uend = desc.w;
-    QRegs<HD, G> qr;
-    QFrags<HD> qfr;
-    if constexpr (TC) {
+    QFrags<HD, PL> qfr;
+    if constexpr (PL == 1) {
       load_qfrags<HD, G>(&S.qbuf[islot][0], qfr);
-    } else if (qf != nullptr) {
-      const int b = find_row(plan.prefix, B, u);
-      load_q<HD, G>(qf + (static_cast<size_t>(b) * hq + g * G) * HD, c, qr);
     } else {
-      load_q<HD, G>(&S.qbuf[islot][0], c, qr);
+      const int b = find_row(plan.prefix, B, u);
+      load_qfrags<HD, G>(qf + (static_cast<size_t>(b) * hq + g * G) * HD, qfr);
     }
     __syncwarp();
     if ((tid & 31) == 0) mbar_arrive(iempty0 + 8 * islot);  // descriptor and q are in registers
@@ -1098,8 +886,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
       const int valid = min(kSplit, uend - bs);
       RingKV<HD> kv{&S.ring[0][0], full0, empty0, n0, kDecodeStages, abort_flag};
       float bo[OPT];
-      if constexpr (TC) split_reduce_tc<HD, G>(qfr, kv, valid, scale_log2, S.sm, 0, bo);
-      else split_reduce<HD, G>(qr, kv, valid, scale_log2, S.sm, 0, bo);
+      split_reduce<HD, G, PL>(qfr, kv, valid, scale_log2, S.sm, 0, bo);
 #pragma unroll
       for (int j = 0; j < OPT; ++j) {
         const int k = tid + kGroupThreads * j;
@@ -1287,7 +1074,7 @@ struct PrefillSmem {
   SplitSmem<HD, G> grp[kPrefillGroups];
 };
 
-template <int HD, int G, bool TC>
+template <int HD, int G, int PL>
 __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_kernel(
     const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ block_table, const int* __restrict__ q_pos0,
@@ -1340,16 +1127,10 @@ __global__ void __launch_bounds__(kGroupThreads* kPrefillGroups) prefill_split_k
       split_range(inv, pos0, s, p, st_t, en_t);
       const int valid = en_t - st_t;  // >= 1; same origin st as the staged rows
       float bo[OPT];
-      if constexpr (TC) {
-        QFrags<HD> qfr;
-        load_qfrags<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, qfr);
-        split_reduce_tc<HD, G>(qfr, kv, valid, scale_log2, sm.grp[group], group, bo);
-      } else {
-        QRegs<HD, G> qr;
-        if (qf != nullptr) load_q<HD, G>(qf + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
-        else load_q<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, c, qr);
-        split_reduce<HD, G>(qr, kv, valid, scale_log2, sm.grp[group], group, bo);
-      }
+      QFrags<HD, PL> qfr;
+      if constexpr (PL == 1) load_qfrags<HD, G>(q + (static_cast<size_t>(tok) * hq + g * G) * HD, qfr);
+      else load_qfrags<HD, G>(qf + (static_cast<size_t>(tok) * hq + g * G) * HD, qfr);
+      split_reduce<HD, G, PL>(qfr, kv, valid, scale_log2, sm.grp[group], group, bo);
       const size_t pidx = (static_cast<size_t>(plan.tok_prefix[tok]) + s) * hq + g * G;
 #pragma unroll
       for (int j = 0; j < OPT; ++j) {
@@ -1482,10 +1263,10 @@ PrefillWs carve_prefill(void* ws, size_t cap, int B, int T, const bi_attn_dims* 
 template <int HD, int G>
 constexpr size_t decode_smem() { return sizeof(DecodeSmem<HD, G>) + 1024; }
 
-template <int HD, int G, bool TC>
+template <int HD, int G, int PL>
 bi_status decode_grid(int* grid) {
   const size_t smem = decode_smem<HD, G>();
-  const void* fn = reinterpret_cast<const void*>(decode_split_kernel<HD, G, TC>);
+  const void* fn = reinterpret_cast<const void*>(decode_split_kernel<HD, G, PL>);
   BI_CUDA_TRY(ensure_smem_limit(fn, static_cast<int>(smem)));
   *grid = occupancy_per_sm(fn, kDecodeThreads, smem) * num_sms();
   return BI_OK;
@@ -1575,15 +1356,15 @@ bi_status decode_launch(const void* q, const void* kc, const void* vc, const int
   int grid = 0;
   const size_t dsmem = decode_smem<HD, G>();
   if (qf) {
-    BI_TRY((decode_grid<HD, G, false>(&grid)));
+    BI_TRY((decode_grid<HD, G, 3>(&grid)));
     BI_TIMED(::bi::kTagAttnDecodeSplit, s,
-             BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, false>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
+             BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, 3>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
                                      kmap, vmap, nullptr, static_cast<const float*>(q), bt, B, dm->num_q_heads,
                                      dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part)));
   } else {
-    BI_TRY((decode_grid<HD, G, true>(&grid)));
+    BI_TRY((decode_grid<HD, G, 1>(&grid)));
     BI_TIMED(::bi::kTagAttnDecodeSplit, s,
-             BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, true>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
+             BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, 1>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
                                      kmap, vmap, static_cast<const __nv_bfloat16*>(q), nullptr, bt, B,
                                      dm->num_q_heads, dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan,
                                      w.part)));
@@ -1618,8 +1399,8 @@ bi_status prefill_launch(const void* q, const void* kc, const void* vc, const in
     BI_LAUNCH_CHECK();
     return BI_OK;
   };
-  // bf16 queries: the products on the tensor cores, as in decode (same function, same bits)
-  BI_TRY(qf ? go(prefill_split_kernel<HD, G, false>) : go(prefill_split_kernel<HD, G, true>));
+  // the same split function as decode (same bits): one query term (bf16) or three (fp32)
+  BI_TRY(qf ? go(prefill_split_kernel<HD, G, 3>) : go(prefill_split_kernel<HD, G, 1>));
   BI_TIMED(::bi::kTagAttnPrefillMerge, s, BI_PDL_CHECK(launch_pdl(prefill_merge_kernel, dim3(T * dm->num_kv_heads), dim3(G * HD / 4), 0, s, w.part, w.plan, q_start, q_pos0, B,
                                                                out, dm->num_q_heads, dm->num_kv_heads, HD)));
   BI_LAUNCH_CHECK();
