@@ -722,14 +722,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
-                                                 int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
@@ -753,27 +745,15 @@ __host__ __device__ constexpr uint32_t idesc_pair(int n) {
          (static_cast<uint32_t>(256 >> 4) << 24);
 }
 
-// Decode-sized M (M <= 128, one row block): the rows are split between the
-// pair instead, CTA r holding A rows [r h, r h + h) (h = a.a_rows, a box of 16,
-// 32 or 64 rows) at the start of its 128-row operand, so each CTA loads half of
-// A and half of the B tile per k-tile, and the two CTAs' tensor memory hold the
-// accumulator rows 0..h-1 of their halves.  The instruction's remaining A rows
-// read whatever follows in shared memory (as in the one-SM kernel at decode
-// sizes) and give accumulator rows that are never stored.  A stage then spans
-// a.kbs k-tiles (3D boxes) so that every copy is 8-16 KiB or more.
 template <int TN2>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const Args a) {
-  static_assert(TN2 == 256 || TN2 == 128 || TN2 == 96 || TN2 == 64, "pair tile widths");
+  static_assert(TN2 == 256 || TN2 == 128, "pair tile widths");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int kStages = a.stages;
-  const bool msplit = a.M <= kBM;                  // decode sizes: rows split between the pair
-  const int kbs = a.kbs;                            // k-tiles per stage
-  const int a_tile = a.a_rows * kBK * 2;            // this CTA's A rows of a k-tile (128, or h when msplit)
-  constexpr int b_tile = (TN2 / 2) * kBK * 2;       // its TN2/2 B rows of a k-tile
-  const int a_bytes = kbs * a_tile;
-  const int kStageBytes = a.stage_bytes;            // kbs * (a_tile + b_tile)
+  constexpr int a_tile = kBM * kBK * 2;             // this CTA's 128 A rows of a k-tile
+  constexpr int kStageBytes = a_tile + (TN2 / 2) * kBK * 2;  // + its TN2/2 B rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   unsigned char* tiles = smem + kBarBlock;
   // bars: full[16], empty[16], tfull[2], tempty[2], drain, sync; then the tensor-memory slot and the abort word
@@ -856,22 +836,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = cid; u < units && ok; u += nclusters) {
         const int nt = u / m_tiles2, mt2 = u % m_tiles2;
-        const int arow = msplit ? static_cast<int>(rank) * a.a_rows : mt2 * 256 + static_cast<int>(rank) * kBM;
+        const int arow = mt2 * 256 + static_cast<int>(rank) * kBM;
         const int brow = nt * TN2 + static_cast<int>(rank) * (TN2 / 2);
-        for (int kb = 0; kb < a.kb_total; kb += kbs) {
+        for (int kb = 0; kb < a.kb_total; ++kb) {
           if (!wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 21, a.wait_ns)) {
             ok = false;
             break;
           }
           const uint32_t sa = smem_u32(tiles + st * kStageBytes);
           if (leader) mbar_expect_tx(full0 + 8 * st, static_cast<uint32_t>(2 * kStageBytes));
-          if (a.map3d) {
-            tma_load_3d_pair(sa, &tmA, full_leader0 + 8 * st, 0, arow, kb);
-            tma_load_3d_pair(sa + a_bytes, &tmW, full_leader0 + 8 * st, 0, brow, kb);
-          } else {
-            tma_load_2d_pair(sa, &tmA, full_leader0 + 8 * st, kb * kBK, arow);
-            tma_load_2d_pair(sa + a_bytes, &tmW, full_leader0 + 8 * st, kb * kBK, brow);
-          }
+          tma_load_2d_pair(sa, &tmA, full_leader0 + 8 * st, kb * kBK, arow);
+          tma_load_2d_pair(sa + a_tile, &tmW, full_leader0 + 8 * st, kb * kBK, brow);
           issued_mask |= 1u << st;
           issued_par = (issued_par & ~(1u << st)) | (ph << st);
           if (++st == kStages) {
@@ -907,22 +882,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 22, a.wait_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * TN2);
-        for (int kb = 0; kb < a.kb_total; kb += kbs) {
+        for (int kb = 0; kb < a.kb_total; ++kb) {
           if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 23, a.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t sdesc = desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
-          const int nkb = min(kbs, a.kb_total - kb);  // k-tiles of this stage inside K
-          for (int j = 0; j < nkb; ++j) {
-            const uint64_t adesc = sdesc + static_cast<uint64_t>((j * a_tile) >> 4);
-            const uint64_t bdesc = sdesc + static_cast<uint64_t>((a_bytes + j * b_tile) >> 4);
+          const uint64_t adesc = desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+          const uint64_t bdesc = adesc + static_cast<uint64_t>(a_tile >> 4);
 #pragma unroll
-            for (int k = 0; k < kBK / kUK; ++k)
-              tc_mma_pair(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc,
-                          (k > 0 || kb + j > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < kBK / kUK; ++k)
+            tc_mma_pair(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc,
+                        (k > 0 || kb > 0) ? 1u : 0u);
           tc_commit_pair(empty0 + 8 * st, 3);
           any = true;
           if (++st == kStages) {
@@ -962,9 +933,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 24, a.wait_ns)) break;
       __syncwarp();  // lanes leave the wait at different times; tcgen05.ld needs the whole warp
       tc_fence_after();
-      const int row = msplit ? static_cast<int>(rank) * a.a_rows + row_in_tile
-                             : mt2 * 256 + static_cast<int>(rank) * kBM + row_in_tile;
-      const bool row_ok = row < a.M && (!msplit || row_in_tile < a.a_rows);
+      const int row = mt2 * 256 + static_cast<int>(rank) * kBM + row_in_tile;
+      const bool row_ok = row < a.M;
       const uint32_t tbase = lane_base + acc * TN2;
 #pragma unroll 1
       for (int ch = 0; ch < TN2 / 32; ++ch) {
@@ -1208,12 +1178,7 @@ int pair_clusters_for() {
 
 int pair_clusters(int tn2) {
   if (num_sms() <= 0) return 76;
-  switch (tn2) {
-    case 256: return pair_clusters_for<256>();
-    case 128: return pair_clusters_for<128>();
-    case 96: return pair_clusters_for<96>();
-    default: return pair_clusters_for<64>();
-  }
+  return tn2 == 256 ? pair_clusters_for<256>() : pair_clusters_for<128>();
 }
 
 // Relative time of one k-tile per CTA (one-SM tile of `tn` columns) or per CTA
@@ -1344,42 +1309,6 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
   if (fast_tn) p.TN = fast_tn;
   else p.TN = M <= kBM ? choose_width_small_m(N, p.splits, planes * p.a_rows) : choose_width(M, N, max_tn);
   p.pair = 0;
-  if (mode == BI_MODE_INVARIANT && planes == 1 && M <= kBM && allow_pair && K % kBK == 0) {
-    // Decode sizes: SM pairs that split the rows (each CTA loads half of A and
-    // half of the B tile) when they cut the bytes a CTA moves per k-tile enough:
-    // every CTA of a one-SM tile re-reads all a_rows rows of A, a pair reads
-    // them once between its two CTAs.  The pair starts only after its
-    // predecessor (no early weight prefetch), hence the margin.
-    const int sms = plan_sms();
-    const int h = M <= 32 ? 16 : M <= 64 ? 32 : 64;  // A rows per CTA of the pair
-    const int64_t su = (N + p.TN - 1) / p.TN;
-    const double single = static_cast<double>((su + sms - 1) / sms) * (p.a_rows + p.TN);
-    double best = single * 0.8;
-    for (int tn2 : {256, 128, 96, 64}) {
-      if (N % tn2 != 0 && tn2 != 256) continue;
-      const int64_t units = (N + tn2 - 1) / tn2;
-      const int cl = pair_clusters(tn2);
-      const double t = static_cast<double>((units + cl - 1) / cl) * (h + tn2 / 2);
-      if (t < best) {
-        best = t;
-        p.pair = tn2;
-        p.a_rows = h;
-      }
-    }
-    if (p.pair) {
-      p.TN = p.pair;
-      // k-tiles per stage: each copy at least 8 KiB, at most 4 k-tiles, and at least 4 stages
-      const int kb_bytes = (p.a_rows + p.pair / 2) * kBK * 2;
-      p.kbs = 4;
-      while (p.kbs > 1 && (kSmemLimit - 1024 - kBarBlock - kOverreadSlack) / (p.kbs * kb_bytes) < 4) p.kbs /= 2;
-      p.map3d = p.kbs > 1 ? 1 : 0;
-      p.stage_bytes = p.kbs * kb_bytes;
-      p.stages = std::min(kPairStagesMax, (kSmemLimit - 1024 - kBarBlock - kOverreadSlack) / p.stage_bytes);
-      p.n_tiles = static_cast<int>((N + p.pair - 1) / p.pair);
-      p.units = p.n_tiles;
-      return p;
-    }
-  }
   if (mode == BI_MODE_INVARIANT && planes == 1 && M > kBM && allow_pair) {
     // SM-pair tiles when the model says they finish sooner than the one-SM tiles
     const int sms = plan_sms();
@@ -1430,9 +1359,7 @@ template <int TN2>
 bi_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mw, const Args& args, cudaStream_t s) {
   const void* fn = reinterpret_cast<const void*>(gemm_pair_kernel<TN2>);
   BI_CUDA_TRY(ensure_smem_limit(fn, kSmemLimit));
-  // decode sizes: the instruction reads 128 A rows from a stage that holds fewer (over-read slack)
-  const size_t smem = 1024 + kBarBlock + static_cast<size_t>(args.stages) * args.stage_bytes +
-                      (args.a_rows < kBM ? kOverreadSlack : 0);
+  const size_t smem = 1024 + kBarBlock + static_cast<size_t>(args.stages) * args.stage_bytes;
   const int grid = 2 * std::min(args.units, pair_clusters(TN2));
   // no programmatic serialisation: the pair kernel starts after its predecessor has finished
   cudaLaunchConfig_t cfg = {};
@@ -1566,14 +1493,9 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   }
   CUtensorMap ma, mw;
   if (p.pair) {
-    BI_TRY(gemm::tensor_map(A, M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
-    BI_TRY(gemm::tensor_map(Wt, N, K, p.pair / 2, p.map3d ? p.kbs : 0, &mw));
-    switch (p.pair) {
-      case 256: return gemm::launch_pair<256>(ma, mw, args, s);
-      case 128: return gemm::launch_pair<128>(ma, mw, args, s);
-      case 96: return gemm::launch_pair<96>(ma, mw, args, s);
-      default: return gemm::launch_pair<64>(ma, mw, args, s);
-    }
+    BI_TRY(gemm::tensor_map(A, M, K, gemm::kBM, 0, &ma));
+    BI_TRY(gemm::tensor_map(Wt, N, K, p.pair / 2, 0, &mw));
+    return p.pair == 256 ? gemm::launch_pair<256>(ma, mw, args, s) : gemm::launch_pair<128>(ma, mw, args, s);
   }
   // the planes form one [planes*M][K] matrix; plane p's rows start at p*M
   BI_TRY(gemm::tensor_map(A, planes * M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
