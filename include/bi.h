@@ -94,12 +94,14 @@ int32_t bi_num_sms(void);
  *   16    decode attention: a kv_len outside [0, max_pages*16]; it was clamped
  *   17    attention: a block-table entry outside [0, num_pages), or a position
  *         past the request's block-table row; page 0 was read instead
+ *   18    decode attention: its dynamic shared memory did not start 1024-byte
+ *         aligned, so nothing was computed              -> BI_ERR_UNSUPPORTED
  *   21    K/V store: a position past the block-table row or a page outside the
  *         cache; that token's K/V were not stored
  *   22    K/V store: a position outside the RoPE tables; the last row was used
  *                                                        -> BI_ERR_INVALID_ARG
- * (16-22: the kernels check these device-side inputs so that no access leaves
- * the caller's buffers; the outputs of the affected rows are undefined.) */
+ * (16, 17, 21, 22: the kernels check these device-side inputs so that no access
+ * leaves the caller's buffers; the outputs of the affected rows are undefined.) */
 bi_status bi_device_error(int32_t* code, bi_stream s);
 
 /* Test hook for the failure path of the bounded in-kernel waits (the pages have

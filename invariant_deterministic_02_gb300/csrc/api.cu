@@ -194,6 +194,10 @@ extern "C" bi_status bi_device_error(int32_t* code, bi_stream s) {
   const int32_t c = cg != 0 ? cg : ca != 0 ? ca : cp;
   *code = c;
   if (c == 0) return BI_OK;
+  if (c == 18) {
+    bi::set_error("decode attention: its dynamic shared memory was not 1024-byte aligned; nothing was computed");
+    return BI_ERR_UNSUPPORTED;
+  }
   if (c >= 16) {
     bi::set_error("a kernel met an out-of-range KV length, block-table entry or position (site code %d)", c);
     return BI_ERR_INVALID_ARG;

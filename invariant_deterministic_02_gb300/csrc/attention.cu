@@ -591,6 +591,7 @@ struct DecodePlan {
 // [0, num_pages) or a position past the block-table row (page 0 read instead).
 constexpr unsigned kSiteBadLength = 16;
 constexpr unsigned kSiteBadPage = 17;
+constexpr unsigned kSiteSmemAlign = 18;  // the decode kernel's shared memory is not 1024-byte aligned (output not written)
 
 // Page of position-block `pi` of a request's block-table row, checked: an entry
 // past the row or outside the cache is reported and replaced by page 0, so no
@@ -692,7 +693,10 @@ constexpr int kItemSlots = 2;
 
 template <int HD, int G>
 struct DecodeSmem {
-  __align__(1024) unsigned char ring[kDecodeStages][PageLayout<HD>::kQuarterBytes];  // TMA tensor copies land swizzled
+  // TMA tensor copies land here with the 128-byte swizzle, which wants 1024-byte aligned pages: the ring is the
+  // first member and the dynamic shared memory window starts 1024-byte aligned (checked at kernel entry).  No
+  // alignment attribute on the struct: padding it to 1024 bytes would cost the third CTA per SM.
+  __align__(128) unsigned char ring[kDecodeStages][PageLayout<HD>::kQuarterBytes];
   SplitSmem<HD, G> sm;
   __align__(16) __nv_bfloat16 qbuf[kItemSlots][G * HD];
   int4 item[kItemSlots];  // {unit u, kv head g, first position, end position}
@@ -722,9 +726,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
   // PL = 1: bf16 queries, staged with the item; PL = 3: fp32 queries qf
   // (fp32-activation layers; q unused), which the consumers read from global
   // memory (the item ring then carries the descriptor only).
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                              ~uintptr_t(1023));
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    // the swizzled TMA copies need 1024-byte aligned pages; report instead of copying misaligned
+    if (threadIdx.x == 0) atomicCAS(&g_attn_err_word, 0u, kSiteSmemAlign);
+    return;
+  }
+  DecodeSmem<HD, G>& S = *reinterpret_cast<DecodeSmem<HD, G>*>(smem_raw);
   const uint32_t full0 = smem_u32(&S.full[0]);
   const uint32_t empty0 = smem_u32(&S.empty[0]);
   const uint32_t ifull0 = smem_u32(&S.item_full[0]);
@@ -1259,9 +1267,9 @@ PrefillWs carve_prefill(void* ws, size_t cap, int B, int T, const bi_attn_dims* 
   return r;
 }
 
-// Dynamic shared memory of the decode split kernel (the ring is aligned to 1024 bytes inside it).
+// Dynamic shared memory of the decode split kernel (three CTAs per SM at head_dim 128).
 template <int HD, int G>
-constexpr size_t decode_smem() { return sizeof(DecodeSmem<HD, G>) + 1024; }
+constexpr size_t decode_smem() { return sizeof(DecodeSmem<HD, G>); }
 
 template <int HD, int G, int PL>
 bi_status decode_grid(int* grid) {
