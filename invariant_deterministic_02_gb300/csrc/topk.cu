@@ -8,11 +8,18 @@
 // order are unique and do not depend on how the scan is parallelised.
 //
 // One CTA of 32 warps per row.  Each warp scans a contiguous segment of the row
-// (four consecutive elements per lane per step, 16-byte loads) and keeps its
-// best k in a sorted list spread over its lanes (lane j holds entry j); an
-// element enters only if it beats the list's last entry, so after the first few
-// steps almost every step is one compare and one ballot.  Warp 0 then folds the
-// 32 warp lists into one with the same insertion.
+// (8 consecutive elements per lane per step as two 16-byte loads, the next
+// step's loads issued before the current step is examined) and keeps its best k
+// in a sorted list spread over its lanes (lane j holds entry j).  Elements are
+// offered to the list only when they beat a filter: a lower bound on the row's
+// k-th entry.  Any warp's own k-th entry is such a bound (that warp alone holds k
+// entries at least as good), so the warps publish theirs to a shared maximum
+// after every step; before its list fills, a warp uses the k-th largest of its
+// lanes' maxima over the first step (k distinct elements reach it).  An element
+// that fails the filter cannot be among the row's k best, so skipping it changes
+// nothing, and almost every step is two loads, eight compares and one vote.
+// The 32 warp lists are then folded pairwise in five rounds (16, 8, 4, 2, 1
+// warps), each warp offering its partner's list to its own.
 #include <climits>
 
 #include "common.cuh"
@@ -22,7 +29,36 @@ namespace {
 
 constexpr int kTopkWarps = 32;
 
+__device__ __forceinline__ float4 ld_stream_f4(const float* p) {
+  const uint4 u = ld_stream(p);
+  return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+
 __device__ __forceinline__ bool better(float av, int ai, float bv, int bi) { return av > bv || (av == bv && ai < bi); }
+
+// 64-bit key ordered like `better` for non-NaN values: the float's bits mapped to
+// an unsigned integer of the same order (-0 taken as +0, which compare equal),
+// then the index reversed so that the lower index is the larger key.
+__device__ __forceinline__ unsigned long long entry_key(float v, int i) {
+  unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<unsigned long long>(u) << 32) | (0xffffffffu - static_cast<unsigned>(i));
+}
+
+// Descending bitonic sort of one value per lane across the warp.
+__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool lower = (lane & stride) == 0;     // this lane keeps the larger value if descending here
+      const bool desc = (lane & size) == 0 || size == 32;
+      v = (lower == desc) ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return v;
+}
 
 // Insert (v, i) into the warp's sorted list (lanes < k hold entries, best first);
 // the caller has checked that it beats entry k-1.
@@ -62,49 +98,101 @@ __device__ __forceinline__ void warp_offer(float& lv, int& li, float& tv, int& t
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits, int64_t V, int k,
                                                                float* __restrict__ top_v, int32_t* __restrict__ top_i,
                                                                int32_t* __restrict__ greedy) {
-  pdl_wait();
-  pdl_trigger();
+  constexpr int kU = 2;               // 16-byte loads per lane per step
+  constexpr int kStep = kU * 4 * 32;  // elements per warp step
   __shared__ float sv[kTopkWarps][32];
   __shared__ int si[kTopkWarps][32];
+  __shared__ unsigned long long s_filter;  // the best k-th entry any warp has published (a key)
+  if (threadIdx.x == 0) s_filter = 0ull;
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
   const int64_t row = blockIdx.x;
   const float* x = logits + row * V;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   float lv = -INFINITY, tv = -INFINITY;
   int li = INT_MAX, ti = INT_MAX;
-  // segment of this warp: a multiple of 128 elements
-  const int64_t per = ((V + kTopkWarps - 1) / kTopkWarps + 127) / 128 * 128;
-  const int64_t s0 = warp * per, s1 = min(V, s0 + per);
+  unsigned long long filter = 0ull, published = 0ull;
+  // segment of this warp: a multiple of kStep elements
+  const int64_t per = ((V + kTopkWarps - 1) / kTopkWarps + kStep - 1) / kStep * kStep;
+  const int64_t s0 = min(V, warp * per), s1 = min(V, s0 + per);
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
   int64_t e = s0;
-  if (vec) {
-    for (; e + 128 <= s1; e += 128) {
-      const float4 f = *reinterpret_cast<const float4*>(x + e + 4 * lane);
-      const int base = static_cast<int>(e) + 4 * lane;
-      warp_offer(lv, li, tv, ti, f.x, base, lane, k);
-      warp_offer(lv, li, tv, ti, f.y, base + 1, lane, k);
-      warp_offer(lv, li, tv, ti, f.z, base + 2, lane, k);
-      warp_offer(lv, li, tv, ti, f.w, base + 3, lane, k);
+  if (vec && e + kStep <= s1) {
+    float4 cur[kU], nxt[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) cur[u] = ld_stream_f4(x + e + 128 * u + 4 * lane);
+    {
+      // first filter: the k-th largest lane maximum of the first step (NaNs are never kept)
+      float m = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) m = fmaxf(m, fmaxf(fmaxf(cur[u].x, cur[u].y), fmaxf(cur[u].z, cur[u].w)));
+      const float t = __shfl_sync(0xffffffffu, warp_sort_desc(m == m ? m : -INFINITY, lane), k - 1);
+      filter = entry_key(t, INT_MAX);
+    }
+    for (;;) {
+      const int64_t en = e + kStep;
+      const bool more = en + kStep <= s1;
+      if (more) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) nxt[u] = ld_stream_f4(x + en + 128 * u + 4 * lane);
+      }
+      bool any = false;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int base = static_cast<int>(e) + 128 * u + 4 * lane;
+        any |= (entry_key(cur[u].x, base) > filter) | (entry_key(cur[u].y, base + 1) > filter) |
+               (entry_key(cur[u].z, base + 2) > filter) | (entry_key(cur[u].w, base + 3) > filter);
+      }
+      if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int base = static_cast<int>(e) + 128 * u + 4 * lane;
+          const float c[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const bool pass = entry_key(c[q], base + q) > filter;
+            warp_offer(lv, li, tv, ti, pass ? c[q] : -INFINITY, pass ? base + q : INT_MAX, lane, k);
+          }
+        }
+        if (ti != INT_MAX) {
+          // the list is full: its k-th entry bounds the row's from below
+          const unsigned long long key = entry_key(tv, ti);
+          if (key > published) {
+            published = key;
+            if (lane == 0) atomicMax(&s_filter, key);
+          }
+        }
+      }
+      filter = max(filter, max(published, *reinterpret_cast<volatile unsigned long long*>(&s_filter)));
+      e = en;
+      if (!more) break;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
     }
   }
   for (; e < s1; e += 32) {
     const int64_t idx = e + lane;
     const float v = idx < s1 ? x[idx] : -INFINITY;
-    warp_offer(lv, li, tv, ti, v, idx < s1 ? static_cast<int>(idx) : INT_MAX, lane, k);
+    const bool pass = idx < s1 && entry_key(v, static_cast<int>(idx)) > filter;
+    warp_offer(lv, li, tv, ti, pass ? v : -INFINITY, pass ? static_cast<int>(idx) : INT_MAX, lane, k);
   }
   sv[warp][lane] = lv;
   si[warp][lane] = li;
   __syncthreads();
-  if (warp == 0) {
-    lv = sv[0][lane];
-    li = si[0][lane];
-    tv = __shfl_sync(0xffffffffu, lv, k - 1);
-    ti = __shfl_sync(0xffffffffu, li, k - 1);
-    for (int w = 1; w < kTopkWarps; ++w) {
-      const float cv = lane < k ? sv[w][lane] : -INFINITY;
-      const int ci = lane < k ? si[w][lane] : INT_MAX;
+  // pairwise folds: in the round of h warps, warp w < h takes list w + h into its own
+  for (int h = kTopkWarps / 2; h >= 1; h >>= 1) {
+    if (warp < h) {
+      const float cv = lane < k ? sv[warp + h][lane] : -INFINITY;
+      const int ci = lane < k ? si[warp + h][lane] : INT_MAX;
       warp_offer(lv, li, tv, ti, cv, ci, lane, k);
+      sv[warp][lane] = lv;
+      si[warp][lane] = li;
     }
+    __syncthreads();
+  }
+  if (warp == 0) {
     if (lane < k) {
       top_v[row * k + lane] = lv;
       top_i[row * k + lane] = li;

@@ -44,3 +44,17 @@ def test_tie_example_from_page():
     x = torch.tensor([g["run1"], g["run2"]], dtype=torch.float32)
     _, ti = topk(cuda(x), 1)
     assert ti[:, 0].tolist() == g["expected_argmax_lowest_index"]
+
+
+@pytest.mark.parametrize("V", [1, 7, 100, 513, 16385, 65536, 151935])
+def test_topk_ragged_lengths(V):
+    # lengths that leave warps without a segment, partial vector steps and (odd V) rows that
+    # start off a 16-byte boundary, so the scalar tail path runs for whole rows
+    k = min(20, V)
+    x = synth.normal((5, V), 11, dtype=torch.float32)
+    x = torch.round(x * 16) / 16
+    x[4, :] = 0.5
+    tv, ti = topk(cuda(x), k)
+    ov, oi = oracle.topk(x.double().numpy(), k)
+    assert np.array_equal(ti, oi)
+    assert np.array_equal(tv.astype(np.float64), ov)
