@@ -73,6 +73,7 @@ enum OutKind : int { kOutBF16 = 0, kOutF32 = 1 };
 struct Args {
   int M, N, K;
   int a_rows;       // rows of A per TMA box (16, 32, 64 or 128)
+  int m64;          // 1 (M <= 64): instructions of M = 64, accumulator row r in tensor-memory lane 32 (r / 16) + r % 16
   int kbs;          // k-blocks per stage (one TMA box spans them when map3d)
   int map3d;        // tensor maps are [kblock][rows][64] views (K % 64 == 0)
   int stage_bytes;  // kbs x (A box + TN rows of B)
@@ -199,6 +200,30 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// The same two instructions issued by one elected lane of a warp whose lanes
+// all execute the call with the same operands: the warp's control flow and the
+// descriptors stay uniform, and a small-N MMA issues in about 40 cycles instead
+// of about 55 from a single-lane branch (measured on this GB300 with a probe of
+// back-to-back M=128, N=32 instructions).
+__device__ __forceinline__ void tc_mma_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -237,10 +262,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_for(int n) {
+// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M = m (128 or 64), N = n.
+// An M = 64 instruction costs the tensor pipe less than an M = 128 one at decode widths (N <= 64: about 31
+// against 40 cycles per instruction issued back to back, measured on this GB300); every accumulator element
+// is the same chain of K = 16 steps either way.
+__host__ __device__ constexpr uint32_t idesc_for(int n, int m = kBM) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(kBM >> 4) << 24);
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // unit -> (m tile, n tile, split index, split count)
@@ -445,10 +473,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // ------------------------------------------------------------ MMA issuer
     // Every pass over a K range (a whole tile, one split unit, or one of the
     // in-CTA partials of a merged unit) goes into the next of the two
-    // accumulators and is handed to the epilogue on its own.
-    if (lane == 0) {
+    // accumulators and is handed to the epilogue on its own.  The whole warp
+    // runs the loop; one elected lane issues each MMA and commit.  Every lane
+    // waits on the barriers itself and the warp goes on only if all of them saw
+    // the phase complete, so the loop stays uniform even when a wait runs out.
+    {
+      auto wait_all = [&](uint32_t bar, uint32_t par, int site) -> bool {
+        const bool r = wait_bounded(bar, par, abort_flag, site, a.wait_ns);
+        return __all_sync(0xffffffffu, r);
+      };
       const uint64_t desc0 = sw128_desc(smem_u32(tiles));
-      constexpr uint32_t kIdescW = idesc_for(TN);
+      const uint32_t kIdescW = a.m64 ? idesc_for(TN, 64) : idesc_for(TN);
       int st = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -462,14 +497,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           int kb0, kb1;
           if (seq > 1) k_range(a.kb_total, q, seq, kb0, kb1);
           else k_range(a.kb_total, s, ns, kb0, kb1);
-          if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 2, a.wait_ns)) {
+          if (!wait_all(tempty0 + 8 * acc, acc_ph ^ 1u, 2)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * TN);
           for (int kb = kb0; kb < kb1; kb += kbs) {
-            if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 3, a.wait_ns)) {
+            if (!wait_all(full0 + 8 * st, ph, 3)) {
               ok = false;
               break;
             }
@@ -488,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                   // one instruction spans the tile's TN columns: the B rows of a stage are
                   // contiguous 128-byte swizzle rows, 1024 bytes per 8-row group
                   const uint32_t accum = (k > 0 || !first) ? 1u : 0u;
-                  tc_mma(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdescW,
-                         accum);
+                  tc_mma_elect(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                               kIdescW, accum);
                 }
               } else {
                 // fp32 A: per k16 step the planes hi, mid, lo in order, same B operand
@@ -498,13 +533,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                   for (int pl = 0; pl < PL; ++pl) {
                     const uint32_t accum = (k > 0 || pl > 0 || !first) ? 1u : 0u;
-                    tc_mma(d0, adesc + static_cast<uint64_t>(((pl * a_plane) >> 4) + 2 * k),
-                           bdesc + static_cast<uint64_t>(2 * k), kIdescW, accum);
+                    tc_mma_elect(d0, adesc + static_cast<uint64_t>(((pl * a_plane) >> 4) + 2 * k),
+                                 bdesc + static_cast<uint64_t>(2 * k), kIdescW, accum);
                   }
                 }
               }
             }
-            tc_commit(empty0 + 8 * st);  // stage free once these MMAs have read it
+            tc_commit_elect(empty0 + 8 * st);  // stage free once these MMAs have read it
             any = true;
             if (++st == kStages) {
               st = 0;
@@ -512,16 +547,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             }
           }
           if (!ok) break;
-          tc_commit(tfull0 + 8 * acc);
+          tc_commit_elect(tfull0 + 8 * acc);
           if (++acc == 2) {
             acc = 0;
             acc_ph ^= 1u;
           }
         }
       }
-      if (*abort_flag && any) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0) && any) {
         // a commit arrives once every MMA issued above has completed
-        tc_commit(drain_bar);
+        tc_commit_elect(drain_bar);
         wait_drain(drain_bar, 0);
       }
     }
@@ -532,8 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // tensor-memory buffer, sum = ((0 + P0) + P1) + ..., rounded once at the end;
     // the second-pass reduction of split units adds the same partials in the
     // same order, so both give the same bits.
+    // With M = 64 instructions the accumulator holds 16 rows per lane quarter
+    // (lanes 32 w .. 32 w + 15); the warp's other lanes load and store nothing.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const int row_in_tile = quarter * 32 + lane;
+    const bool lane_live = !a.m64 || lane < 16;
+    const int row_in_tile = a.m64 ? quarter * 16 + lane : quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t sum_base = lane_base + 2 * TN;  // running-sum buffer (merged units only)
     int acc = 0;
@@ -543,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       int mt, nt, s, ns, seq;
       unit_coords(a, u, mt, nt, s, ns, seq);
       const int row = mt * kBM + row_in_tile;
-      const bool row_ok = row < a.M;
+      const bool row_ok = lane_live && row < a.M;
       for (int q = 0; q < seq; ++q) {
         if (!wait_bounded(tfull0 + 8 * acc, acc_ph, abort_flag, 4, a.wait_ns)) {
           ok = false;
@@ -1457,6 +1495,7 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   gemm::Args args{};
   args.M = static_cast<int>(M);
   args.a_rows = p.a_rows;
+  args.m64 = M <= 64 ? 1 : 0;
   args.kbs = p.kbs;
   args.map3d = p.map3d;
   args.stage_bytes = p.stage_bytes;
