@@ -186,22 +186,8 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two instructions issued by one elected lane of a warp whose lanes
-// all execute the call with the same operands: the warp's control flow and the
+// An MMA and a commit issued by one elected lane of a warp whose lanes all
+// execute the call with the same operands: the warp's control flow and the
 // descriptors stay uniform, and a small-N MMA issues in about 40 cycles instead
 // of about 55 from a single-lane branch (measured on this GB300 with a probe of
 // back-to-back M=128, N=32 instructions).
@@ -760,20 +746,25 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
-__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
+// The pair's MMA and commit, issued by one elected lane of a warp whose lanes all
+// make the call (see tc_mma_elect).  The commit arrives on the barrier at this
+// shared offset in the CTAs of `mask` (bit r = rank r) once every MMA issued so
+// far has completed.
+__device__ __forceinline__ void tc_mma_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// arrive on the barrier at this shared offset in the CTAs of `mask` (bit r = rank r)
-// once every MMA issued so far has completed
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+__device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar, uint16_t mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
       "h"(mask)
       : "memory");
 }
@@ -906,7 +897,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (lane == 0 && leader) {
+    // The whole warp runs the loop and an elected lane issues (as in the one-SM
+    // kernel); the warp goes on only if all lanes saw each barrier phase complete.
+    if (leader) {
+      auto wait_all = [&](uint32_t bar, uint32_t par, int site) -> bool {
+        const bool r = wait_bounded(bar, par, abort_flag, site, a.wait_ns);
+        return __all_sync(0xffffffffu, r);
+      };
       const uint64_t desc0 = sw128_desc(smem_u32(tiles));
       constexpr uint32_t kIdesc = idesc_pair(TN2);
       int st = 0;
@@ -917,11 +914,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool any = false;
       for (int u = cid; u < units && ok; u += nclusters) {
-        if (!wait_bounded(tempty0 + 8 * acc, acc_ph ^ 1u, abort_flag, 22, a.wait_ns)) break;
+        if (!wait_all(tempty0 + 8 * acc, acc_ph ^ 1u, 22)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * TN2);
         for (int kb = 0; kb < a.kb_total; ++kb) {
-          if (!wait_bounded(full0 + 8 * st, ph, abort_flag, 23, a.wait_ns)) {
+          if (!wait_all(full0 + 8 * st, ph, 23)) {
             ok = false;
             break;
           }
@@ -930,9 +927,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = adesc + static_cast<uint64_t>(a_tile >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / kUK; ++k)
-            tc_mma_pair(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc,
-                        (k > 0 || kb > 0) ? 1u : 0u);
-          tc_commit_pair(empty0 + 8 * st, 3);
+            tc_mma_pair_elect(d0, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k), kIdesc,
+                              (k > 0 || kb > 0) ? 1u : 0u);
+          tc_commit_pair_elect(empty0 + 8 * st, 3);
           any = true;
           if (++st == kStages) {
             st = 0;
@@ -940,7 +937,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit_pair(tfull0 + 8 * acc, 3);
+        tc_commit_pair_elect(tfull0 + 8 * acc, 3);
         acc_used |= 1u << acc;
         acc_par = (acc_par & ~(1u << acc)) | (acc_ph << acc);
         if (++acc == 2) {
@@ -948,13 +945,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           acc_ph ^= 1u;
         }
       }
-      if (*abort_flag && any) {
-        tc_commit_pair(drain_bar, 1);
+      const bool aborted = __any_sync(0xffffffffu, *abort_flag != 0);
+      if (aborted && any) {
+        tc_commit_pair_elect(drain_bar, 1);
         wait_drain(drain_bar, 0);
       }
       // both CTAs' epilogues release each accumulator on this CTA's tempty: let
       // their last arrivals land before this CTA may leave
-      if (!*abort_flag)
+      if (!aborted)
         for (int i = 0; i < 2; ++i)
           if (acc_used & (1u << i)) wait_drain_rec(tempty0 + 8 * i, (acc_par >> i) & 1u, 27);
     }
