@@ -39,8 +39,8 @@ def test_one_hot_weights_select_columns_exactly():
         assert bits_equal(C[:, j].cpu(), A[:, (j * 5) % K])
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 512, 512), (8, 512, 512), (16, 512, 512), (97, 4096, 4096),
-                                   (256, 1024, 4096), (513, 640, 1536)])
+@pytest.mark.parametrize("M,N,K", [(1, 512, 512), (8, 512, 512), (16, 512, 512), (33, 512, 512), (64, 4096, 4096),
+                                   (48, 1024, 12288), (97, 4096, 4096), (256, 1024, 4096), (513, 640, 1536)])
 def test_random_parity_bf16(M, N, K):
     A = synth.normal((M, K), 20 + M)
     W = synth.normal((N, K), 21 + N, std=0.02)
@@ -93,6 +93,19 @@ def test_row0_bitwise_across_M_sweep(N):
     if N != 151936:
         exact = oracle.round_bf16(exact)
     assert max_rel_err(got, exact) <= TOL_BF16
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (6144, 4096), (4096, 12288)])
+def test_every_row_bitwise_across_instruction_heights(N, K):
+    # M <= 64 runs M = 64 instructions (16 accumulator rows per lane quarter), 64 < M <= 128 M = 128
+    # instructions on one SM, larger M the SM-pair kernel: every row of the small product must come out
+    # of all three with the same bits (a wrong row-to-lane map would move rows 16..63)
+    W = synth.normal_device((N, K), 70 + N + K, std=0.02)
+    big = synth.normal_device((300, K), 71)
+    ref = gemm(big, W, out_dtype=torch.float32)
+    for M in (17, 40, 64, 100, 128):
+        C = gemm(big[:M].contiguous(), W, out_dtype=torch.float32)
+        assert bits_equal(C, ref[:M]), "rows changed at M=%d" % M
 
 
 def test_run_to_run_deterministic_2048():
