@@ -763,20 +763,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const int plane = threadIdx.x - kGroupThreads;
     int n = 0;
     uint32_t issued = 0, ipar = 0;
-    // Work items are claimed from a counter shared by the launch's CTAs, one
-    // item ahead, so a CTA that finishes early takes more; which CTA reduces
-    // an item changes nothing in its arithmetic.
+    // Work items: each CTA's first is its own index, the rest are claimed from
+    // a counter shared by the launch's CTAs (the next one as soon as the current
+    // one's copies are all issued), so a CTA that finishes early takes more;
+    // which CTA reduces an item changes nothing in its arithmetic.
     auto claim = [&]() -> int {
       int it = 0;
-      if (plane == 0) it = atomicAdd(plan.counter, 1);
+      if (plane == 0) it = static_cast<int>(gridDim.x) + atomicAdd(plan.counter, 1);
       return __shfl_sync(0xffffffffu, it, 0);
     };
     // item k's descriptor and q go to slot k % 2; an item is announced while
     // the item before it is still being streamed; a claim past the last item
-    // is announced as an end marker (u = -1)
+    // is announced as an end marker (u = -1).  Returns the item's request row
+    // (every lane), which the loop below reuses.
     int ann = 0;
     uint32_t ann_issued = 0;
-    auto announce = [&](int it) {
+    auto announce = [&](int it) -> int {
+      const int u = it < total ? it / hkv : 0;
+      const int g = it % hkv;
+      const int b = it < total ? find_row(plan.prefix, B, u) : 0;
       if (plane == 0) {
         const int slot = ann % kItemSlots;
         const uint32_t ph = static_cast<uint32_t>((ann / kItemSlots) & 1);
@@ -785,34 +790,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
           S.item[slot] = make_int4(-1, 0, 0, 0);
           mbar_arrive(ifull0 + 8 * slot);  // release: the descriptor store
           ann_issued &= ~(1u << slot);
-          ++ann;
-          return;
-        }
-        const int u = it / hkv;
-        const int g = it % hkv;
-        const int b = find_row(plan.prefix, B, u);
-        const int ul = plan.ulen[b];
-        const int us = (u - plan.prefix[b]) * ul;
-        S.item[slot] = make_int4(u, g, us, min(plan.len[b], us + ul));
-        if (qf != nullptr) {
-          mbar_arrive(ifull0 + 8 * slot);  // release: the descriptor store
         } else {
-          mbar_expect_tx(ifull0 + 8 * slot, static_cast<uint32_t>(G * HD * 2));  // release: the descriptor store
-          bulk_g2s(smem_u32(&S.qbuf[slot][0]), q + (static_cast<size_t>(b) * hq + g * G) * HD, G * HD * 2,
-                   ifull0 + 8 * slot);
-          ann_issued |= 1u << slot;
+          const int ul = plan.ulen[b];
+          const int us = (u - plan.prefix[b]) * ul;
+          S.item[slot] = make_int4(u, g, us, min(plan.len[b], us + ul));
+          if (qf != nullptr) {
+            mbar_arrive(ifull0 + 8 * slot);  // release: the descriptor store
+          } else {
+            mbar_expect_tx(ifull0 + 8 * slot, static_cast<uint32_t>(G * HD * 2));  // release: the descriptor store
+            bulk_g2s(smem_u32(&S.qbuf[slot][0]), q + (static_cast<size_t>(b) * hq + g * G) * HD, G * HD * 2,
+                     ifull0 + 8 * slot);
+            ann_issued |= 1u << slot;
+          }
         }
       }
       ++ann;
+      return b;
     };
-    int item = claim();
-    announce(item);
+    int item = static_cast<int>(blockIdx.x);
+    int b = announce(item);
     while (item < total) {
-      const int next = claim();
-      announce(next);
       const int u = item / hkv;
       const int g = item % hkv;
-      const int b = find_row(plan.prefix, B, u);
       const int s = u - plan.prefix[b];
       const int L = plan.len[b];
       const int ul = plan.ulen[b];
@@ -821,6 +820,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
       const int* brow = block_table + static_cast<size_t>(b) * max_pages;
       for (int bs = ustart; bs < uend; bs += kSplit) {
         const int valid = min(kSplit, uend - bs);
+        // the block's (up to 16) page indices, one per lane, fetched together
+        // before its copies rather than one dependent load per quarter
+        const int npages = (valid + kPage - 1) / kPage;
+        const int pg = plane < npages ? checked_page(brow, bs / kPage + plane, max_pages, num_pages) : 0;
         for (int j = 0; j < 8; ++j, ++n) {
           const int st = n % kDecodeStages;
           const uint32_t ph = static_cast<uint32_t>((n / kDecodeStages) & 1);
@@ -828,21 +831,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
           const int nv = max(0, min(64, valid - q0));
           const int npg = (nv + kPage - 1) / kPage;
           const uint32_t fb = full0 + 8 * st;
+          const int page = __shfl_sync(0xffffffffu, pg, ((j & 3) * 4 + plane) & 31);
           if (plane == 0) {
             wait_bounded(empty0 + 8 * st, ph ^ 1u, abort_flag, 13);
             mbar_expect_tx(fb, static_cast<uint32_t>(npg * kPage * HD * 2));
           }
           __syncwarp();
-          if (plane < npg) {
-            const int page = checked_page(brow, (bs + q0) / kPage + plane, max_pages, num_pages);
+          if (plane < npg)
             tma_page(smem_u32(&S.ring[st][plane * PageLayout<HD>::kPageBytes]), (j < 4) ? &kmap : &vmap, fb,
                      page * hkv + g);
-          }
           issued |= 1u << st;
           ipar = (ipar & ~(1u << st)) | (ph << st);
         }
       }
-      item = next;
+      // the next item is claimed once this one's copies are all issued, not
+      // before: a CTA then holds at most one item that no copy has started
+      // for, which keeps the launch's last items from queueing behind busy CTAs
+      item = claim();
+      b = announce(item);
     }
     // keep the CTA resident until every copy it issued has landed
     if (plane == 0) {
