@@ -267,8 +267,8 @@ bi_status bi_decode_attention(const void* q, const void* k_cache, const void* v_
  *     address (cudaGetSymbolAddress, with that device current) and caches it;
  *     make that first call before any stream capture.
  *   - Batches whose scratch need exceeds 16 MiB are rejected with
- *     BI_ERR_UNSUPPORTED and a message naming the need: U * num_q_heads *
- *     (head_dim+2) * 4 bytes plus a few int32 per request, for U split units:
+ *     BI_ERR_UNSUPPORTED and a message naming the need: U * (num_q_heads *
+ *     (head_dim+2) + 1) * 4 bytes plus a few int32 per request, for U split units:
  *     INVARIANT U = B * ceil(max_pages*16/256); FAST U = B * f with
  *     f = min(64, ceil(4 * SMs / (B * num_kv_heads))); PROTECTED
  *     U = (B-1) * f + max(f, ceil(max_pages*16/256)).

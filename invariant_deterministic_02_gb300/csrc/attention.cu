@@ -584,6 +584,7 @@ struct DecodePlan {
   int* nunits;   // [B]
   int* prefix;   // [B+1]
   int* counter;  // [1] next unclaimed work item of the split kernel (0 between launches)
+  int* unit_row; // [units] request row of each unit (one load instead of a search over prefix)
 };
 
 // Error-word site codes of this file: 11-15 a bounded wait ran out; 16 a KV
@@ -655,6 +656,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int* __restrict
   int run = part[t] - local;
   for (int b = b0; b < b1; ++b) {
     plan.prefix[b] = run;
+    for (int u = 0; u < plan.nunits[b]; ++u) plan.unit_row[run + u] = b;
     run += plan.nunits[b];
   }
   if (t == 1023) plan.prefix[B] = part[1023];
@@ -781,7 +783,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     auto announce = [&](int it) -> int {
       const int u = it < total ? it / hkv : 0;
       const int g = it % hkv;
-      const int b = it < total ? find_row(plan.prefix, B, u) : 0;
+      const int b = it < total ? plan.unit_row[u] : 0;
       if (plane == 0) {
         const int slot = ann % kItemSlots;
         const uint32_t ph = static_cast<uint32_t>((ann / kItemSlots) & 1);
@@ -882,7 +884,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     if constexpr (PL == 1) {
       load_qfrags<HD, G>(&S.qbuf[islot][0], qfr);
     } else {
-      const int b = find_row(plan.prefix, B, u);
+      const int b = plan.unit_row[u];
       load_qfrags<HD, G>(qf + (static_cast<size_t>(b) * hq + g * G) * HD, qfr);
     }
     __syncwarp();
@@ -1216,7 +1218,7 @@ struct DecodeWs {
 };
 
 // Plan arrays of a decode batch (small; reusable by every layer of a step).
-size_t carve_decode_plan(void* base, int B, int hkv, DecodePlan* plan) {
+size_t carve_decode_plan(void* base, int B, int hkv, size_t units, DecodePlan* plan) {
   WsCarver cv(base, 0);
   plan->len = cv.take<int>(B);
   plan->mode = cv.take<int>(B);
@@ -1224,6 +1226,7 @@ size_t carve_decode_plan(void* base, int B, int hkv, DecodePlan* plan) {
   plan->nunits = cv.take<int>(B);
   plan->prefix = cv.take<int>(B + 1);
   plan->counter = cv.take<int>(1);
+  plan->unit_row = cv.take<int>(units);
   return align_up(cv.used, 256);
 }
 
@@ -1237,8 +1240,8 @@ size_t carve_decode_parts(void* base, size_t units, const bi_attn_dims* dm, Part
 
 DecodeWs carve_decode(void* ws, size_t, int B, const bi_attn_dims* dm) {
   DecodeWs r;
-  const size_t pb = carve_decode_plan(ws, B, dm->num_kv_heads, &r.plan);
   const size_t units = static_cast<size_t>(B) * max_units_per_request(dm);
+  const size_t pb = carve_decode_plan(ws, B, dm->num_kv_heads, units, &r.plan);
   const size_t qb = carve_decode_parts(ws ? static_cast<char*>(ws) + pb : nullptr, units, dm, &r.part);
   r.bytes = pb + qb;
   return r;
@@ -1556,7 +1559,6 @@ bi_status noalloc_scratch_address(void** out) {
 // plus the target's invariant units.
 DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode mode, int target) {
   DecodeWs r;
-  const size_t pb = carve_decode_plan(base, B, dm->num_kv_heads, &r.plan);
   const size_t inv = static_cast<size_t>((dm->max_pages * kPage + kSplit - 1) / kSplit);
   const int fw = fast_units_wanted(B, dm->num_kv_heads);
   const size_t f = fw <= 0 ? inv : static_cast<size_t>(std::min(kMaxFastUnits, fw));
@@ -1564,6 +1566,7 @@ DecodeWs carve_decode_noalloc(void* base, int B, const bi_attn_dims* dm, bi_mode
   if (mode_invariant(mode)) units = static_cast<size_t>(B) * inv;
   else if (mode == BI_MODE_PROTECTED && target >= 0) units = static_cast<size_t>(B - 1) * f + std::max(inv, f);
   else units = static_cast<size_t>(B) * f;
+  const size_t pb = carve_decode_plan(base, B, dm->num_kv_heads, units, &r.plan);
   const size_t qb = carve_decode_parts(base ? static_cast<char*>(base) + pb : nullptr, units, dm, &r.part);
   r.bytes = pb + qb;
   return r;
@@ -1600,9 +1603,10 @@ bi_status decode_attention_noalloc_impl(const void* q, const void* kc, const voi
 // Decode attention for the layer loop: the plan lives in `plan_ws` (sized by
 // decode_plan_bytes) and is built only when make_plan is set, so the layers of
 // one step share it; the partial states live in `part_ws`.
-size_t decode_plan_bytes(int32_t B, int32_t hkv) {
+size_t decode_plan_bytes(int32_t B, const bi_attn_dims* dims) {
   attn::DecodePlan p;
-  return attn::carve_decode_plan(nullptr, B, hkv, &p);
+  return attn::carve_decode_plan(nullptr, B, dims->num_kv_heads,
+                                 static_cast<size_t>(B) * attn::max_units_per_request(dims), &p);
 }
 
 size_t decode_parts_bytes(int32_t B, const bi_attn_dims* dims) {
@@ -1618,7 +1622,8 @@ bi_status decode_attention_layer(const void* q, const void* kc, const void* vc, 
   BI_REQUIRE(B >= 1 && plan_ws && part_ws && part_bytes >= decode_parts_bytes(B, dims), BI_ERR_WORKSPACE,
              "decode attention: workspace");
   attn::DecodeWs w;
-  attn::carve_decode_plan(plan_ws, B, dims->num_kv_heads, &w.plan);
+  attn::carve_decode_plan(plan_ws, B, dims->num_kv_heads, static_cast<size_t>(B) * attn::max_units_per_request(dims),
+                          &w.plan);
   attn::carve_decode_parts(part_ws, static_cast<size_t>(B) * attn::max_units_per_request(dims), dims, &w.part);
   BI_ATTN_DISPATCH(attn::decode_launch, q, kc, vc, bt, kv_lens, B, dims, out, mode,
                    mode == BI_MODE_PROTECTED ? target : -1, w, s, make_plan);

@@ -28,7 +28,7 @@ bi_status prefill_attention_impl(const void*, const void*, const void*, const in
                                  const int32_t*, int32_t, int32_t, const bi_attn_dims*, void*, bi_mode, int32_t,
                                  void*, size_t, cudaStream_t);
 size_t decode_attention_ws(int32_t, const bi_attn_dims*);
-size_t decode_plan_bytes(int32_t, int32_t);
+size_t decode_plan_bytes(int32_t, const bi_attn_dims*);
 size_t decode_parts_bytes(int32_t, const bi_attn_dims*);
 bi_status decode_attention_layer(const void*, const void*, const void*, const int32_t*, const int32_t*, int32_t,
                                  const bi_attn_dims*, const ActDst&, bi_mode, int32_t, void*, bool, void*, size_t,
@@ -164,7 +164,10 @@ LayerBufs carve(void* ws, size_t cap, const bi_model_dims* dm, const bi_batch* b
     r.gu = cv.take<__nv_bfloat16>(T * 2 * F);
     r.act = cv.take<__nv_bfloat16>(T * F);
   }
-  r.dplan = cv.take<unsigned char>(decode_plan_bytes(static_cast<int32_t>(B), dm->num_kv_heads));
+  {
+    const bi_attn_dims ad = attn_dims(dm, b);
+    r.dplan = cv.take<unsigned char>(decode_plan_bytes(static_cast<int32_t>(B), &ad));
+  }
   if (model) {
     const size_t es = dm->act_f32 ? sizeof(float) : sizeof(__nv_bfloat16);
     r.hidden = cv.take<unsigned char>(T * d * es);
