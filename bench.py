@@ -7,7 +7,9 @@ of 64 requests whose cached KV lengths are drawn uniform on [128, 4096]:
 embedding, per layer RMSNorm -> QKV GEMM -> q/k head RMSNorm + RoPE + paged KV
 store -> split-KV attention + merge tree -> O GEMM (+residual) -> RMSNorm ->
 gate|up GEMM -> SwiGLU -> down GEMM (+residual), then final RMSNorm, lm-head
-(fp32 logits) and top-20.  All of it runs in libbi's kernels through bi_model_forward.
+(fp32 logits) and top-20.  All of it runs in libbi's kernels through bi_model_forward; timed steps replay
+a CUDA graph captured from one bi_model_forward call (the step's positions and ids staged into its fixed
+buffers), the per-kernel profile pass calls it eagerly.
 
 Prints one JSON line (rank 0).  --impl reference times the float64 CPU oracle
 on a bounded sample of the same workload instead.
@@ -218,12 +220,40 @@ def run_ours(args, rank, world, local_rank):
     sp = stream.cuda_stream
     step = [0]
 
-    def one_step(m=mode, dims=model.dims, nb=B):
+    # Timed decode steps replay a CUDA graph of bi_model_forward, captured once per (mode, activations, batch
+    # size) on fixed buffers: the step's positions are copied into a fixed buffer before the replay and its
+    # greedy ids fed back after it (two small device copies).  The profiled pass runs the same steps eagerly.
+    d_pos1 = d_pos[0].clone()
+    d_in = ids[0].clone()
+    d_next = torch.empty(B, dtype=torch.int32, device=dev)
+    graphs = {}
+
+    def graph_for(m, dims, nb):
+        key = (m, int(dims.act_f32), nb)
+        if key not in graphs:
+            t = 0 if m == bi.PROTECTED else -1
+            bat = bi.Batch(nb, nb, 1, d_qs.data_ptr(), d_pos1.data_ptr(), d_bt.data_ptr(), max_pages, pages,
+                           t, 0 if t >= 0 else -1, 1 if t >= 0 else 0)
+
+            def call(st, bat=bat, m=m, dims=dims):
+                bi.bi_model_forward(dims, model.mw, model.rope_cos, model.rope_sin, d_in, bat, model.k_ptrs,
+                                    model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=d_next, mode=m, workspace=ws,
+                                    ws_bytes=ws_bytes, stream=st)
+            graphs[key] = (StepGraph(torch, call), bat)
+        return graphs[key][0]
+
+    def one_step(m=mode, dims=model.dims, nb=B, eager=False):
         s = step[0]
-        src, dst = ids[s % 2], ids[(s + 1) % 2]
-        bi.bi_model_forward(dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s, m, nb), model.k_ptrs,
-                            model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=dst, mode=m, workspace=ws,
-                            ws_bytes=ws_bytes, stream=sp)
+        if eager:
+            src, dst = ids[s % 2], ids[(s + 1) % 2]
+            bi.bi_model_forward(dims, model.mw, model.rope_cos, model.rope_sin, src, batch_for(s, m, nb),
+                                model.k_ptrs, model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=dst, mode=m,
+                                workspace=ws, ws_bytes=ws_bytes, stream=sp)
+        else:
+            d_pos1.copy_(d_pos[s])
+            g = graph_for(m, dims, nb)
+            g.replay()
+            d_in.copy_(d_next)
         step[0] += 1
 
     dist = None
@@ -260,7 +290,7 @@ def run_ours(args, rank, world, local_rank):
     bi.bi_profile_start(K * 600)
     p_step0 = step[0]
     for _ in range(K):
-        one_step()
+        one_step(eager=True)
     torch.cuda.synchronize()
     bi.bi_profile_stop()
     kern = {}
@@ -322,8 +352,15 @@ def run_ours(args, rank, world, local_rank):
     h_out_i = torch.empty((B, TOPK), dtype=torch.int32).pin_memory()
     h_out_v = torch.empty((B, TOPK), dtype=torch.float32).pin_memory()
     h_pos_all = pin(pos_all)
-    d_ids = torch.empty(B, dtype=torch.int32, device=dev)
-    d_pos1 = torch.empty(B, dtype=torch.int32, device=dev)
+    # the step's inputs land in fixed device buffers that a CUDA graph of bi_model_forward reads
+    d_ids = h_ids.to(dev)
+    d_pos_e = h_pos_all[step[0]].to(dev)
+    b_e = bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos_e.data_ptr(), d_bt.data_ptr(), max_pages, pages, target,
+                   0 if target >= 0 else -1, 1 if target >= 0 else 0)
+    g_e = StepGraph(torch, lambda st: bi.bi_model_forward(model.dims, model.mw, model.rope_cos, model.rope_sin,
+                                                          d_ids, b_e, model.k_ptrs, model.v_ptrs, logits, TOPK, tv,
+                                                          ti, greedy_ids=None, mode=mode, workspace=ws,
+                                                          ws_bytes=ws_bytes, stream=st))
     h2d = d2h = 0
     torch.cuda.synchronize()
     if dist:
@@ -332,15 +369,11 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(K):
         s = step[0]
         d_ids.copy_(h_ids, non_blocking=True)
-        d_pos1.copy_(h_pos_all[s], non_blocking=True)
+        d_pos_e.copy_(h_pos_all[s], non_blocking=True)
         d_qs.copy_(h_qs, non_blocking=True)
         d_bt.copy_(h_bt, non_blocking=True)
         h2d = 4 * (B + B + (B + 1)) + bt.nbytes
-        b_ = bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos1.data_ptr(), d_bt.data_ptr(), max_pages, pages, target,
-                      0 if target >= 0 else -1, 1 if target >= 0 else 0)
-        bi.bi_model_forward(model.dims, model.mw, model.rope_cos, model.rope_sin, d_ids, b_, model.k_ptrs,
-                            model.v_ptrs, logits, TOPK, tv, ti, greedy_ids=None, mode=mode, workspace=ws,
-                            ws_bytes=ws_bytes, stream=sp)
+        g_e.replay()
         h_out_i.copy_(ti, non_blocking=True)
         h_out_v.copy_(tv, non_blocking=True)
         d2h = h_out_i.numel() * 4 + h_out_v.numel() * 4
@@ -399,12 +432,14 @@ def run_ours(args, rank, world, local_rank):
                 t[plan] = time_launches(torch, f, 10, flush)
             best = min(t, key=t.get)
             bi.bi_fast_gemm_plan(B, N, Kd, best)
+            graphs.clear()  # captured FAST steps carry the plans they were captured with
             gemm_choice["%dx%dx%d" % (B, N, Kd)] = {"plan": ["split_k", "tile_plan"][best],
                                                    "ms": {"split_k": round(t[0], 4), "tile_plan": round(t[1], 4)}}
             del A, Wt, C, gws
         step_ms = {}
         for plan in (0, 1):
             bi.bi_fast_attention_plan(plan)
+            graphs.clear()
             one_step(bi.FAST)
             torch.cuda.synchronize()
             c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -416,6 +451,7 @@ def run_ours(args, rank, world, local_rank):
             step_ms[plan] = c0.elapsed_time(c1) / K
         attn_best = min(step_ms, key=step_ms.get)
         bi.bi_fast_attention_plan(attn_best)
+        graphs.clear()
         one_step(bi.FAST)
         torch.cuda.synchronize()
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -435,6 +471,7 @@ def run_ours(args, rank, world, local_rank):
         bi.bi_fast_attention_plan(0)
         for N, Kd in shapes_nk:
             bi.bi_fast_gemm_plan(B, N, Kd, 0)
+        graphs.clear()
 
     # ---------------------------------------------------------------- smaller decode batches (B = 1, 8)
     # the first nb requests of the same model and caches; roofline: the weights every step streams
@@ -472,6 +509,8 @@ def run_ours(args, rank, world, local_rank):
             "config": {"workload": WORKLOAD, "batch_per_gpu": B, "kv_len": "U{%d..%d} seed %d" % (KV_LO, KV_HI,
                                                                                             args.seed),
                        "mode": args.mode, "parallelism": "replicas" if world > 1 else "single",
+                       "launch": "each step replays a CUDA graph of one bi_model_forward call (stream capture of "
+                                 "the public call, same kernels); the per-kernel profile runs the steps eagerly",
                        "l2": "inputs larger than L2: ~15 GB weights + ~20 GB KV streamed per step"},
             "clocks": ck, "e2e": e2e, "gpu_launches": int(round(launches_per_step * K)),
             "roofline": roofline, "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
@@ -499,6 +538,27 @@ def weight_bytes_per_step(shape) -> float:
     per_layer = (L.qkv_dim * L.d_model + L.d_model * L.n_q_heads * L.head_dim + 2 * L.ffn_dim * L.d_model +
                  L.d_model * L.ffn_dim + 2 * L.d_model + (2 * L.head_dim if L.qk_norm else 0))
     return 2.0 * (shape.n_layers * per_layer + L.d_model + shape.vocab * L.d_model)
+
+
+class StepGraph:
+    """One call of the public bi_model_forward captured in a CUDA graph (stream capture) on fixed buffers and
+    replayed on the current stream: the same kernels with the same arguments, launched as one graph.  The call
+    runs once eagerly on the capture stream first (lazy initialisation happens outside the capture)."""
+
+    def __init__(self, torch, call):
+        cur = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            call(side.cuda_stream)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            call(torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
 
 
 class L2Flush:
