@@ -724,7 +724,8 @@ template <int HD, int G, int PL>
 __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __nv_bfloat16* __restrict__ q, const float* __restrict__ qf, const int* __restrict__ block_table, int B,
-    int hq, int hkv, int max_pages, int num_pages, float scale_log2, DecodePlan plan, Partials part) {
+    int hq, int hkv, int max_pages, int num_pages, float scale_log2, DecodePlan plan, Partials part,
+    int plan_ready) {
   // PL = 1: bf16 queries, staged with the item; PL = 3: fp32 queries qf
   // (fp32-activation layers; q unused), which the consumers read from global
   // memory (the item ring then carries the descriptor only).
@@ -753,6 +754,39 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // plan_ready: the plan was built by a kernel that finished before the
+  // previous one started (the layers after the first of a decode step).  The
+  // producer then issues the key quarters of its first item before waiting for
+  // the previous kernel, as far as they hold no page of the request's newest
+  // position (the one that kernel stores); `pre` counts them.
+  int pre = 0;
+  uint32_t pre_issued = 0;
+  if (plan_ready && threadIdx.x >= kGroupThreads) {
+    const int lane = threadIdx.x - kGroupThreads;
+    const int it = static_cast<int>(blockIdx.x);
+    if (it < plan.prefix[B] * hkv) {
+      const int u = it / hkv, g = it % hkv;
+      const int b = plan.unit_row[u];
+      const int L = plan.len[b], ul = plan.ulen[b];
+      const int bs = (u - plan.prefix[b]) * ul;  // the first block of the item
+      const int valid = min(kSplit, min(L, bs + ul) - bs);
+      const int newest_page_start = ((L - 1) / kPage) * kPage;
+      while (pre < 4 && 64 * pre < valid && bs + 64 * pre + 64 <= newest_page_start) ++pre;
+      const int* brow = block_table + static_cast<size_t>(b) * max_pages;
+      const int npages = (min(valid, 64 * pre) + kPage - 1) / kPage;
+      const int pg = lane < npages ? checked_page(brow, bs / kPage + lane, max_pages, num_pages) : 0;
+      for (int j = 0; j < pre; ++j) {
+        const int nv = min(64, valid - 64 * j);
+        const int npg = (nv + kPage - 1) / kPage;
+        const uint32_t fb = full0 + 8 * j;  // fresh stages: nothing to wait for
+        const int page = __shfl_sync(0xffffffffu, pg, (j * 4 + lane) & 31);
+        if (lane == 0) mbar_expect_tx(fb, static_cast<uint32_t>(npg * kPage * HD * 2));
+        __syncwarp();
+        if (lane < npg) tma_page(smem_u32(&S.ring[j][lane * PageLayout<HD>::kPageBytes]), &kmap, fb, page * hkv + g);
+        pre_issued |= 1u << j;
+      }
+    }
+  }
   pdl_wait();
   pdl_trigger();
   const int total = plan.prefix[B] * hkv;
@@ -764,7 +798,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
     // of a stage are in flight together.
     const int plane = threadIdx.x - kGroupThreads;
     int n = 0;
-    uint32_t issued = 0, ipar = 0;
+    uint32_t issued = pre_issued, ipar = 0;  // quarters issued before the wait: stages 0.., phase 0
+    int skip = pre;
     // Work items: each CTA's first is its own index, the rest are claimed from
     // a counter shared by the launch's CTAs (the next one as soon as the current
     // one's copies are all issued), so a CTA that finishes early takes more;
@@ -827,6 +862,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
         const int npages = (valid + kPage - 1) / kPage;
         const int pg = plane < npages ? checked_page(brow, bs / kPage + plane, max_pages, num_pages) : 0;
         for (int j = 0; j < 8; ++j, ++n) {
+          if (skip > 0) {  // issued before the wait
+            --skip;
+            continue;
+          }
           const int st = n % kDecodeStages;
           const uint32_t ph = static_cast<uint32_t>((n / kDecodeStages) & 1);
           const int q0 = (j & 3) * 64;
@@ -1377,14 +1416,15 @@ bi_status decode_launch(const void* q, const void* kc, const void* vc, const int
     BI_TIMED(::bi::kTagAttnDecodeSplit, s,
              BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, 3>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
                                      kmap, vmap, nullptr, static_cast<const float*>(q), bt, B, dm->num_q_heads,
-                                     dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part)));
+                                     dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan, w.part,
+                                     make_plan ? 0 : 1)));
   } else {
     BI_TRY((decode_grid<HD, G, 1>(&grid)));
     BI_TIMED(::bi::kTagAttnDecodeSplit, s,
              BI_PDL_CHECK(launch_pdl(decode_split_kernel<HD, G, 1>, dim3(grid), dim3(kDecodeThreads), dsmem, s,
                                      kmap, vmap, static_cast<const __nv_bfloat16*>(q), nullptr, bt, B,
                                      dm->num_q_heads, dm->num_kv_heads, dm->max_pages, dm->num_pages, sl2, w.plan,
-                                     w.part)));
+                                     w.part, make_plan ? 0 : 1)));
   }
   BI_LAUNCH_CHECK();
   BI_TIMED(::bi::kTagAttnDecodeMerge, s,
