@@ -345,40 +345,47 @@ def run_ours(args, rank, world, local_rank):
                                                                                     1000.0) / 1e12, 2)
 
     # ---------------------------------------------------------------- end to end through host buffers
+    # The step's inputs (token ids, positions, the batch's row starts and block table) travel in one pinned
+    # host buffer and one copy to one device buffer that the batch descriptor points into; the step's top-20
+    # values and ids come back in one copy; the next step's ids are the top-1 of this one.
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_ids = pin(synth.token_ids(B, shape.vocab, args.seed + 6))
-    h_qs = pin(np.arange(B + 1, dtype=np.int32))
-    h_bt = pin(bt)
-    h_out_i = torch.empty((B, TOPK), dtype=torch.int32).pin_memory()
-    h_out_v = torch.empty((B, TOPK), dtype=torch.float32).pin_memory()
     h_pos_all = pin(pos_all)
-    # the step's inputs land in fixed device buffers that a CUDA graph of bi_model_forward reads
-    d_ids = h_ids.to(dev)
-    d_pos_e = h_pos_all[step[0]].to(dev)
-    b_e = bi.Batch(B, B, 1, d_qs.data_ptr(), d_pos_e.data_ptr(), d_bt.data_ptr(), max_pages, pages, target,
+    al = lambda n: (n + 3) // 4 * 4  # int32 offsets kept 16-byte aligned
+    o_ids, o_pos, o_qs = 0, al(B), 2 * al(B)
+    o_bt = o_qs + al(B + 1)
+    n_in = o_bt + bt.size
+    h_in = torch.empty(n_in, dtype=torch.int32).pin_memory()
+    h_in[o_ids:o_ids + B] = torch.from_numpy(synth.token_ids(B, shape.vocab, args.seed + 6))
+    h_in[o_qs:o_qs + B + 1] = torch.arange(B + 1, dtype=torch.int32)
+    h_in[o_bt:o_bt + bt.size] = torch.from_numpy(np.ascontiguousarray(bt).reshape(-1))
+    h_in[o_pos:o_pos + B] = h_pos_all[step[0]]
+    d_in_e = h_in.to(dev)
+    out_e = torch.empty(2 * B * TOPK, dtype=torch.int32, device=dev)  # [top-20 values as fp32 bits | top-20 ids]
+    tv_e = out_e[:B * TOPK].view(torch.float32).view(B, TOPK)
+    ti_e = out_e[B * TOPK:].view(B, TOPK)
+    h_out = torch.empty(2 * B * TOPK, dtype=torch.int32).pin_memory()
+    h_out_i = h_out[B * TOPK:].view(B, TOPK)
+    base = d_in_e.data_ptr()
+    b_e = bi.Batch(B, B, 1, base + 4 * o_qs, base + 4 * o_pos, base + 4 * o_bt, max_pages, pages, target,
                    0 if target >= 0 else -1, 1 if target >= 0 else 0)
+    d_ids = d_in_e[o_ids:o_ids + B]
     g_e = StepGraph(torch, lambda st: bi.bi_model_forward(model.dims, model.mw, model.rope_cos, model.rope_sin,
-                                                          d_ids, b_e, model.k_ptrs, model.v_ptrs, logits, TOPK, tv,
-                                                          ti, greedy_ids=None, mode=mode, workspace=ws,
+                                                          d_ids, b_e, model.k_ptrs, model.v_ptrs, logits, TOPK, tv_e,
+                                                          ti_e, greedy_ids=None, mode=mode, workspace=ws,
                                                           ws_bytes=ws_bytes, stream=st))
-    h2d = d2h = 0
+    h2d = 4 * n_in
+    d2h = 4 * 2 * B * TOPK
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(K):
-        s = step[0]
-        d_ids.copy_(h_ids, non_blocking=True)
-        d_pos_e.copy_(h_pos_all[s], non_blocking=True)
-        d_qs.copy_(h_qs, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        h2d = 4 * (B + B + (B + 1)) + bt.nbytes
+        h_in[o_pos:o_pos + B] = h_pos_all[step[0]]
+        d_in_e.copy_(h_in, non_blocking=True)
         g_e.replay()
-        h_out_i.copy_(ti, non_blocking=True)
-        h_out_v.copy_(tv, non_blocking=True)
-        d2h = h_out_i.numel() * 4 + h_out_v.numel() * 4
+        h_out.copy_(out_e, non_blocking=True)
         stream.synchronize()
-        h_ids[:] = h_out_i[:, 0]
+        h_in[o_ids:o_ids + B] = h_out_i[:, 0]
         step[0] += 1
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     e2e = {"value": round(job_throughput(B, world, K, e2e_s), 2), "unit": "tok/s", "h2d_bytes_per_step": h2d,
