@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       uint32_t issued_mask = pre_stages >= 32 ? ~0u : ((1u << pre_stages) - 1u), issued_par = 0;
       bool ok = true;
       int st = 0;        // stage slot and its phase parity, advanced in the same
-      uint32_t ph = 0;   // sequence as the MMA thread's
+      uint32_t ph = 0;   // sequence as the MMA warp's
       for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         int mt, nt, s, ns, seq;
         unit_coords(a, u, mt, nt, s, ns, seq);
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
       }
       // Let every copy issued land before shared memory is released.  After a
-      // normal run the MMA thread has already waited on each of them, so these
+      // normal run the MMA warp has already waited on each of them, so these
       // return at once; after an abort (which another role may raise after this
       // loop has ended) they keep the CTA alive until its copies are done.
       for (int i = 0; i < kStages; ++i)
@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
   // Normal exit: the epilogue has consumed the last accumulator commit, so every
   // MMA has completed and every load was consumed.  After an abort the producer
-  // and the MMA thread drained their own work above.
+  // and the MMA warp drained their own work above.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
