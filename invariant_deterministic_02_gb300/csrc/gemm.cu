@@ -666,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
 // ------------------------------------------------------------------ two-SM tiles (INVARIANT, M > 128)
 // A cluster of two CTAs (an SM pair) computes 256 x TN2 output tiles (TN2 = 256,
-// 224 or 128; 224 makes N = 4096 exactly 19 column tiles, so 4 row tiles fill the
-// 76 pairs of a 152-SM part in whole waves) with tcgen05.mma.cta_group::2
+// 224, 192 or 128; 224 makes N = 4096 exactly 19 column tiles, so 4 row tiles fill
+// the 76 pairs of a 152-SM part in whole waves, and 192 makes N = 14336 75 column
+// tiles, one wave for 256 rows) with tcgen05.mma.cta_group::2
 // (instruction M = 256, N = TN2, K = 16).  CTA rank r
 // loads A rows [256 i + 128 r, +128) and B rows [TN2 j + r TN2/2, +TN2/2) of
 // every k-tile into its own shared memory; the even CTA issues the MMAs, which
@@ -779,7 +780,7 @@ __host__ __device__ constexpr uint32_t idesc_pair(int n) {
 template <int TN2>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const Args a) {
-  static_assert(TN2 == 256 || TN2 == 224 || TN2 == 128, "pair tile widths");
+  static_assert(TN2 == 256 || TN2 == 224 || TN2 == 192 || TN2 == 128, "pair tile widths");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int kStages = a.stages;
@@ -1216,14 +1217,19 @@ int pair_clusters_for() {
 
 int pair_clusters(int tn2) {
   if (num_sms() <= 0) return 76;
-  return tn2 == 256 ? pair_clusters_for<256>() : tn2 == 224 ? pair_clusters_for<224>() : pair_clusters_for<128>();
+  switch (tn2) {
+    case 256: return pair_clusters_for<256>();
+    case 224: return pair_clusters_for<224>();
+    case 192: return pair_clusters_for<192>();
+    default: return pair_clusters_for<128>();
+  }
 }
 
 // Relative time of one k-tile per CTA (one-SM tile of `tn` columns) or per CTA
 // pair (256 x tn2 tile), as measured on GB300 for compute-sized GEMMs: the
 // copy engines, not the tensor cores, set the pace of the narrower tiles.
 double ktile_cost_single(int tn) { return tn >= 256 ? 645.0 : tn >= 128 ? 625.0 : tn >= 64 ? 500.0 : 450.0; }
-double ktile_cost_pair(int tn2) { return tn2 >= 256 ? 540.0 : tn2 >= 224 ? 495.0 : 420.0; }
+double ktile_cost_pair(int tn2) { return tn2 >= 256 ? 540.0 : tn2 >= 224 ? 495.0 : tn2 >= 192 ? 470.0 : 420.0; }
 
 // Part count of the K-only split (INVARIANT_KSPLIT): enough parts that a
 // decode-sized GEMM (one 128-row tile, 256-column tiles) gives about one unit
@@ -1352,7 +1358,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
     const int sms = plan_sms();
     const int64_t single_units = static_cast<int64_t>(p.m_tiles) * ((N + p.TN - 1) / p.TN);
     double best = static_cast<double>((single_units + sms - 1) / sms) * ktile_cost_single(p.TN);
-    for (int tn2 : {256, 224, 128}) {
+    for (int tn2 : {256, 224, 192, 128}) {
       const int64_t units = ((M + 255) / 256) * ((N + tn2 - 1) / tn2);
       const int cl = pair_clusters(tn2);
       const double t = static_cast<double>((units + cl - 1) / cl) * ktile_cost_pair(tn2);
@@ -1535,9 +1541,12 @@ bi_status gemm_core(const void* A, int planes, const void* Wt, void* C, const vo
   if (p.pair) {
     BI_TRY(gemm::tensor_map(A, M, K, gemm::kBM, 0, &ma));
     BI_TRY(gemm::tensor_map(Wt, N, K, p.pair / 2, 0, &mw));
-    return p.pair == 256   ? gemm::launch_pair<256>(ma, mw, args, s)
-           : p.pair == 224 ? gemm::launch_pair<224>(ma, mw, args, s)
-                           : gemm::launch_pair<128>(ma, mw, args, s);
+    switch (p.pair) {
+      case 256: return gemm::launch_pair<256>(ma, mw, args, s);
+      case 224: return gemm::launch_pair<224>(ma, mw, args, s);
+      case 192: return gemm::launch_pair<192>(ma, mw, args, s);
+      default: return gemm::launch_pair<128>(ma, mw, args, s);
+    }
   }
   // the planes form one [planes*M][K] matrix; plane p's rows start at p*M
   BI_TRY(gemm::tensor_map(A, planes * M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
