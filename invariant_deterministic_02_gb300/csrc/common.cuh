@@ -166,6 +166,13 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
 }
 
+// SwiGLU of one (gate, up) pair: silu(g) * u = g / (1 + e^-g) * u, each
+// operation rounded once (the one definition the SwiGLU kernels and the
+// gate|up GEMM's fused epilogue share, so both give the same bits).
+__device__ __forceinline__ float swiglu1(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                     pack_bf16x2(f[6], f[7]));

@@ -92,6 +92,11 @@ struct Args {
   int out_kind;
   int plane_rows;          // rows of each A plane (three planes for fp32 A; the kernel's PL)
   const float* Rf;         // fp32 residual (fp32 output) or null
+  int swiglu;                  // 1: gate|up GEMM with SwiGLU in the epilogue: a tile's first TN/2 B rows are
+                               // gate rows nt*TN/2.., the next TN/2 the up rows F + nt*TN/2.. of the same outputs;
+                               // the epilogue writes act[row][nt*TN/2 + j] = swiglu(bf16(gate), bf16(up))
+  int F;                       // ... output width (half of N)
+  __nv_bfloat16* act;          // ... output [M][F]
   unsigned long long wait_ns;  // limit of every bounded wait (2 s; shorter only under the test hook below)
   int drop_first_stage;        // test hook: CTA 0 issues no copies for its first stage (its waits then run out)
 };
@@ -172,6 +177,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
           "r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 
@@ -367,6 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   // except the weight copies of the first stages when a.prefetch_w is set: the
   // producer issues those first (their stages are fresh, so no empty-wait is
   // needed) and only then waits, so weight latency overlaps the previous kernel.
+  // B part of a stage: the tile's TN weight rows (for the SwiGLU GEMM TN/2 gate
+  // rows then the TN/2 up rows of the same outputs, one box of a row-pair map)
+  auto load_w = [&](uint32_t dst, uint32_t bar, int nt, int kb) {
+    if (a.swiglu) {
+      if (a.map3d) tma_load_4d(dst, &tmW, bar, 0, nt * (TN / 2), 0, kb);
+      else tma_load_3d(dst, &tmW, bar, kb * kBK, nt * (TN / 2), 0);
+    } else if (a.map3d) {
+      tma_load_3d(dst, &tmW, bar, 0, nt * TN, kb);
+    } else {
+      tma_load_2d(dst, &tmW, bar, kb * kBK, nt * TN);
+    }
+  };
   int pre_stages = 0;  // stages whose W copy (and transaction count) was issued early
   if (warp < kProducerWarps && lane == 0 && a.prefetch_w && blockIdx.x < a.units) {
     int mt, nt, s, ns, seq, kb0, kb1;
@@ -377,8 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       const uint32_t fb = full0 + 8 * pre_stages;
       const uint32_t sa = smem_u32(tiles + pre_stages * kStageBytes);
       mbar_expect_tx(fb, static_cast<uint32_t>(kStageBytes));
-      if (a.map3d) tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
-      else tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
+      load_w(sa + a_bytes, fb, nt, kb);
     }
   }
   pdl_wait();
@@ -431,12 +456,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                 for (int pl = 0; pl < PL; ++pl)
                   tma_load_3d(sa + pl * a_plane, &tmA, fb, 0, pl * a.plane_rows + mt * kBM, kb);
-                tma_load_3d(sa + a_bytes, &tmW, fb, 0, nt * TN, kb);
+                load_w(sa + a_bytes, fb, nt, kb);
               } else {
 #pragma unroll
                 for (int pl = 0; pl < PL; ++pl)
                   tma_load_2d(sa + pl * a_plane, &tmA, fb, kb * kBK, pl * a.plane_rows + mt * kBM);
-                tma_load_2d(sa + a_bytes, &tmW, fb, kb * kBK, nt * TN);
+                load_w(sa + a_bytes, fb, nt, kb);
               }
             }
             issued_mask |= 1u << st;
@@ -577,6 +602,74 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         tc_fence_after();
         const uint32_t tbase = lane_base + acc * TN;
         const bool last = q == seq - 1;
+        if constexpr (TN % 64 == 0) {
+          if (a.swiglu) {
+            // gate chunk ch and up chunk ch of the tile give 32 outputs of a row: each accumulator value is
+            // rounded to bf16 as the plain GEMM stores it, then the SwiGLU kernel's own function.  With M = 64
+            // instructions the warp's 16 rows sit in lanes 0..15, so lanes 16..31 take the upper 16 columns
+            // of the row of lane - 16 (shuffled over) and every lane computes 16 outputs.
+#pragma unroll 1
+            for (int ch = 0; ch < TN / 64; ++ch) {
+              uint32_t g[32], v[32];
+              tc_ld32(tbase + ch * 32, g);
+              tc_ld32(tbase + TN / 2 + ch * 32, v);
+              const int col0 = nt * (TN / 2) + ch * 32;
+              if (a.m64) {
+                const int src = lane & 15;
+                const bool upper = lane >= 16;
+                float o[16];
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                  const uint32_t g0 = __shfl_sync(0xffffffffu, g[16 + e], src);
+                  const uint32_t g1 = __shfl_sync(0xffffffffu, g[17 + e], src);
+                  const uint32_t v0 = __shfl_sync(0xffffffffu, v[16 + e], src);
+                  const uint32_t v1 = __shfl_sync(0xffffffffu, v[17 + e], src);
+                  const uint32_t gp = pack_bf16x2(__uint_as_float(upper ? g0 : g[e]), __uint_as_float(upper ? g1 : g[e + 1]));
+                  const uint32_t up = pack_bf16x2(__uint_as_float(upper ? v0 : v[e]), __uint_as_float(upper ? v1 : v[e + 1]));
+                  o[e] = swiglu1(bf16_lo(gp), bf16_lo(up));
+                  o[e + 1] = swiglu1(bf16_hi(gp), bf16_hi(up));
+                }
+                const int orow = mt * kBM + quarter * 16 + src;
+                const int c0 = col0 + (upper ? 16 : 0);
+                if (orow < a.M) {
+                  __nv_bfloat16* dst = a.act + static_cast<size_t>(orow) * a.F + c0;
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    if (c0 + 8 * h >= a.F) break;
+                    float o8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o8[e] = o[8 * h + e];
+                    *reinterpret_cast<uint4*>(dst + 8 * h) = pack8(o8);
+                  }
+                }
+              } else {
+                if (!row_ok || col0 >= a.F) continue;
+                __nv_bfloat16* dst = a.act + static_cast<size_t>(row) * a.F + col0;
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                  if (col0 + 8 * q8 >= a.F) break;
+                  float o[8];
+#pragma unroll
+                  for (int e = 0; e < 8; e += 2) {
+                    const uint32_t gp = pack_bf16x2(__uint_as_float(g[8 * q8 + e]), __uint_as_float(g[8 * q8 + e + 1]));
+                    const uint32_t up = pack_bf16x2(__uint_as_float(v[8 * q8 + e]), __uint_as_float(v[8 * q8 + e + 1]));
+                    o[e] = swiglu1(bf16_lo(gp), bf16_lo(up));
+                    o[e + 1] = swiglu1(bf16_hi(gp), bf16_hi(up));
+                  }
+                  *reinterpret_cast<uint4*>(dst + 8 * q8) = pack8(o);
+                }
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) {
+              acc = 0;
+              acc_ph ^= 1u;
+            }
+            continue;
+          }
+        }
 #pragma unroll 1
         for (int ch = 0; ch < TN / 32; ++ch) {
           uint32_t r[32];
@@ -1110,9 +1203,11 @@ struct MapKey {
   int64_t rows, K;
   int box_rows;
   int kbs;  // 0: 2D map; >0: 3D [kblock][rows][64] view with boxes spanning kbs k-blocks
+  int halves;  // 1: the matrix taken as two stacked [rows][K] halves, one box from each
   int dev;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && kbs == o.kbs && dev == o.dev;
+    return ptr == o.ptr && rows == o.rows && K == o.K && box_rows == o.box_rows && kbs == o.kbs &&
+           halves == o.halves && dev == o.dev;
   }
 };
 struct MapKeyHash {
@@ -1120,7 +1215,7 @@ struct MapKeyHash {
     size_t h = reinterpret_cast<size_t>(k.ptr);
     h ^= static_cast<size_t>(k.rows) * 0x9E3779B97F4A7C15ull;
     h ^= static_cast<size_t>(k.K) * 0xC2B2AE3D27D4EB4Full;
-    h ^= static_cast<size_t>(k.box_rows * 131 + k.dev + k.kbs * 7919);
+    h ^= static_cast<size_t>(k.box_rows * 131 + k.dev + k.kbs * 7919 + k.halves * 104729);
     return h;
   }
 };
@@ -1133,10 +1228,15 @@ std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 // multiple of 64): the matrix viewed as [K/64][rows][64] (k-block stride 128
 // bytes), box 64 x box_rows x kbs, so one copy brings kbs consecutive k-blocks,
 // each landing as its own swizzled box_rows x 128-byte tile.
-bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, int kbs, CUtensorMap* out) {
+// halves == 1: the matrix is [2][rows][K] (two stacked matrices) and every box
+// takes box_rows rows of the first half followed by the same rows of the
+// second, landing as one 2*box_rows-row tile (one more map dimension of extent
+// 2 and stride rows*K elements).
+bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, int kbs, CUtensorMap* out,
+                     int halves = 0) {
   int dev = 0;
   cudaGetDevice(&dev);
-  MapKey key{ptr, rows, K, box_rows, kbs, dev};
+  MapKey key{ptr, rows, K, box_rows, kbs, halves, dev};
   {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     auto it = g_maps.find(key);
@@ -1148,7 +1248,18 @@ bi_status tensor_map(const void* ptr, int64_t rows, int64_t K, int box_rows, int
   auto fn = encode_fn();
   BI_REQUIRE(fn != nullptr, BI_ERR_CUDA, "bi_gemm: cuTensorMapEncodeTiled is not available from the driver");
   CUresult r;
-  if (kbs == 0) {
+  if (halves != 0) {
+    const cuuint64_t half = static_cast<cuuint64_t>(rows) * K * 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(kbs == 0 ? K : kBK), static_cast<cuuint64_t>(rows), 2,
+                          static_cast<cuuint64_t>(K / kBK)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(K) * 2, half, static_cast<cuuint64_t>(kBK) * 2};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows), 2,
+                         static_cast<cuuint32_t>(kbs)};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kbs == 0 ? 3 : 4, const_cast<void*>(ptr), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (kbs == 0) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
@@ -1598,6 +1709,65 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
   clear_error();
   return gemm_core(A, 1, Wt, C, R, nullptr, M, N, K, out_dtype, mode, target_row, target_count, ws, ws_bytes, s,
                    weights_constant);
+}
+
+// Gate|up GEMM with SwiGLU in its epilogue: act[M][F] = swiglu(A Wgu^T) for Wgu
+// [2F][K] (gate rows then up rows).  Runs only where the plan of the plain
+// [M][2F] GEMM is one-SM tiles, one split, one unit per tile and a tile width
+// that is a multiple of 64; then every product is the plain GEMM's own (the
+// same per-element k order) and the output equals that GEMM followed by the
+// SwiGLU kernel, bit for bit.  *used says whether it ran; when it is false
+// nothing was launched and the caller runs the two kernels.
+bi_status gemm_swiglu_impl(const void* A, const void* Wgu, void* act, int64_t M, int64_t F, int64_t K, bi_mode mode,
+                           int32_t target_row, int32_t target_count, cudaStream_t s, bool* used) {
+  *used = false;
+  if (M <= 0 || F <= 0 || K < 8 || K % 8 != 0 || F % 8 != 0 || M > gemm::kBM || t_stall_wait_ns != 0) return BI_OK;
+  if (!mode_valid(mode) || M >= (int64_t(1) << 31) || 2 * F >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return BI_OK;
+  if (!aligned16(A) || !aligned16(Wgu) || !aligned16(act)) return BI_OK;
+  int64_t tb = 0, te = 0;
+  if (mode == BI_MODE_PROTECTED && target_row >= 0) {
+    if (target_count < 1 || target_row + static_cast<int64_t>(target_count) > M) return BI_OK;
+    tb = target_row;
+    te = target_row + static_cast<int64_t>(target_count);
+  }
+  const gemm::Plan p = gemm::make_plan(M, 2 * F, K, mode, tb, te, 1, true);
+  if (p.pair || p.splits != 1 || p.seq != 1 || p.TN % 64 != 0 || p.stages < 2) return BI_OK;
+  gemm::Args args{};
+  args.M = static_cast<int>(M);
+  args.a_rows = p.a_rows;
+  args.m64 = M <= 64 ? 1 : 0;
+  args.kbs = p.kbs;
+  args.map3d = p.map3d;
+  args.stage_bytes = p.stage_bytes;
+  args.stages = p.stages;
+  args.N = static_cast<int>(2 * F);
+  args.K = static_cast<int>(K);
+  args.m_tiles = p.m_tiles;
+  args.n_tiles = p.n_tiles;
+  args.splits = 1;
+  args.tm0 = p.tm0;
+  args.tm1 = p.tm1;
+  args.seq = 1;
+  args.prefetch_w = 1;
+  args.units = p.units;
+  args.kb_total = p.kb_total;
+  args.plane_rows = static_cast<int>(M);
+  args.out_kind = gemm::kOutBF16;
+  args.swiglu = 1;
+  args.F = static_cast<int>(F);
+  args.act = static_cast<__nv_bfloat16*>(act);
+  args.wait_ns = gemm::kWaitLimitNs;
+  CUtensorMap ma, mw;
+  BI_TRY(gemm::tensor_map(A, M, K, p.a_rows, p.map3d ? p.kbs : 0, &ma));
+  BI_TRY(gemm::tensor_map(Wgu, F, K, p.TN / 2, p.map3d ? p.kbs : 0, &mw, 1));
+  bi_status st;
+  if (p.TN == 256) st = gemm::launch_w<256, 1>(ma, mw, args, s);
+  else if (p.TN == 192) st = gemm::launch_w<192, 1>(ma, mw, args, s);
+  else if (p.TN == 128) st = gemm::launch_w<128, 1>(ma, mw, args, s);
+  else st = gemm::launch_w<64, 1>(ma, mw, args, s);
+  if (st == BI_OK) *used = true;
+  return st;
 }
 
 // fp32-activation layers: A already split into three bf16 planes [3][M][K] by

@@ -214,10 +214,7 @@ __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, __nv_bfloat1
     unpack8(gv, g);
     unpack8(uv, u);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float sg = __fdiv_rn(g[e], __fadd_rn(1.0f, expf(-g[e])));
-      o[e] = __fmul_rn(sg, u[e]);
-    }
+    for (int e = 0; e < 8; ++e) o[e] = swiglu1(g[e], u[e]);
     *reinterpret_cast<uint4*>(out + t * F + c * 8) = pack8(o);
   }
 }
@@ -239,10 +236,7 @@ __global__ void swiglu_planes_kernel(const float* __restrict__ gu, uint16_t* __r
     const float u[4] = {uv.x, uv.y, uv.z, uv.w};
     float o[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float sg = __fdiv_rn(g[e], __fadd_rn(1.0f, expf(-g[e])));
-      o[e] = __fmul_rn(sg, u[e]);
-    }
+    for (int e = 0; e < 4; ++e) o[e] = swiglu1(g[e], u[e]);
     store_planes4(out + t * F + c * 4, plane, o[0], o[1], o[2], o[3]);
   }
 }
