@@ -6,7 +6,7 @@ layers, d 4096, 32/8 heads, head_dim 128, FFN 12288, vocab 151936) for a batch
 of 64 requests whose cached KV lengths are drawn uniform on [128, 4096]:
 embedding, per layer RMSNorm -> QKV GEMM -> q/k head RMSNorm + RoPE + paged KV
 store -> split-KV attention + merge tree -> O GEMM (+residual) -> RMSNorm ->
-gate|up GEMM -> SwiGLU -> down GEMM (+residual), then final RMSNorm, lm-head
+gate|up GEMM with SwiGLU in its epilogue -> down GEMM (+residual), then final RMSNorm, lm-head
 (fp32 logits) and top-20.  All of it runs in libbi's kernels through bi_model_forward; timed steps replay
 a CUDA graph captured from one bi_model_forward call (the step's positions and ids staged into its fixed
 buffers), the per-kernel profile pass calls it eagerly.
@@ -56,10 +56,11 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None, help="keep the raw SM clock samples of the timed region here")
-    ap.add_argument("--case", choices=["model", "attn", "gemm", "topk", "rmsnorm"], default="model",
-                    help="model: the decode-step workload; attn/gemm/topk/rmsnorm: one kernel on a small case "
-                         "(for profiler captures), printing that kernel's timing")
-    ap.add_argument("--gemm-shape", default="64,24576,4096", help="M,N,K of --case gemm")
+    ap.add_argument("--case", choices=["model", "attn", "gemm", "gemm_swiglu", "topk", "rmsnorm"], default="model",
+                    help="model: the decode-step workload; attn/gemm/gemm_swiglu/topk/rmsnorm: one kernel on a "
+                         "small case (for profiler captures), printing that kernel's timing")
+    ap.add_argument("--gemm-shape", default="64,24576,4096",
+                    help="M,N,K of --case gemm (gemm_swiglu: N = 2F, the gate and up rows)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the GEMM sweep, RMSNorm roofline and smaller decode batches")
     return ap.parse_args()
@@ -311,8 +312,12 @@ def run_ours(args, rank, world, local_rank):
     gemm_shapes = [(L.qkv_dim, L.d_model), (L.d_model, L.n_q_heads * L.head_dim), (2 * L.ffn_dim, L.d_model),
                    (L.d_model, L.ffn_dim)]
     gemm_bytes_step, gemm_flops_step = 0.0, 0.0
+    # with no SwiGLU launch the gate|up GEMM applied it in its epilogue and wrote only the [B][F] activation
+    swiglu_fused = "swiglu" not in kern
     for N, Kd in gemm_shapes:
-        gemm_bytes_step += shape.n_layers * (2 * (B * Kd + N * Kd) + 2 * B * N + (2 * B * N if N == L.d_model else 0))
+        n_out = N // 2 if (swiglu_fused and N == 2 * L.ffn_dim) else N
+        gemm_bytes_step += shape.n_layers * (2 * (B * Kd + N * Kd) + 2 * B * n_out +
+                                             (2 * B * N if N == L.d_model else 0))
         gemm_flops_step += shape.n_layers * 2.0 * B * N * Kd
     gemm_bytes_step += 2 * (B * L.d_model + shape.vocab * L.d_model) + 4 * B * shape.vocab
     gemm_flops_step += 2.0 * B * shape.vocab * L.d_model
@@ -760,14 +765,23 @@ def run_case(args):
         fn = lambda: bi.bi_decode_attention(q, kc, vc, bt, kl, dims, out, mode=mode, workspace=ws)
         kernel, work, unit = "attn_decode_split", float(Ls.sum()) * hkv * hd * 2 * 2 + 2 * B * hq * hd * 2, "GB/s"
         peak = pk["hbm_gbs"]
-    elif args.case == "gemm":
+    elif args.case in ("gemm", "gemm_swiglu"):
         M, N, Kd = (int(v) for v in args.gemm_shape.split(","))
         A = synth.normal_device((M, Kd), args.seed + 5)
         Wt = synth.normal_device((N, Kd), args.seed + 6, std=0.02)
-        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        fn = lambda: bi.bi_gemm(A, Wt, C, mode=mode)
+        if args.case == "gemm":
+            C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: bi.bi_gemm(A, Wt, C, mode=mode)
+            n_out = N
+        else:
+            # the one-call form: the SwiGLU output [M][N/2] is all that is written
+            act = torch.empty((M, N // 2), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(1, bi.lib().bi_gemm_swiglu_workspace(M, N // 2, Kd, mode)), dtype=torch.uint8,
+                             device=dev)
+            fn = lambda: bi.bi_gemm_swiglu(A, Wt, act, mode=mode, workspace=ws)
+            n_out = N // 2
         flops = 2.0 * M * N * Kd
-        byts = 2.0 * (M * Kd + N * Kd + M * N)
+        byts = 2.0 * (M * Kd + N * Kd + M * n_out)
         if flops / byts > pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9):
             kernel, work, unit, peak = "gemm", flops, "TFLOP/s", pk["bf16_tflops"]
         else:
@@ -804,7 +818,7 @@ def run_case(args):
     return {"case": args.case, "kernel": kernel, "launches": n, "launch_ms": round(per, 5),
             "achieved": round(achieved, 2), "unit": unit, "peak": peak, "frac": round(achieved / peak, 4),
             "work_per_launch": work, "batch": B, "mode": args.mode,
-            "shape": args.gemm_shape if args.case == "gemm" else None}
+            "shape": args.gemm_shape if args.case in ("gemm", "gemm_swiglu") else None}
 
 
 def main():

@@ -317,6 +317,25 @@ bi_status bi_qkv_rope_store(const void* qkv, const float* rope_cos, const float*
 /* out[t][j] = bf16( silu(gu[t][j]) * gu[t][F + j] ), gu device [T][2F] bf16, out [T][F]. */
 bi_status bi_swiglu(const void* gu, void* out, int64_t T, int64_t F, bi_stream s);
 
+/* Gate|up projection followed by SwiGLU, as one call:
+ *   act[m][j] = bi_swiglu of the bf16 result of bi_gemm(A, W_gate_up) (INVARIANT
+ *   etc. as bi_gemm), i.e. bf16(silu(g) * u) with g = C[m][j], u = C[m][F + j]
+ *   and C = A W_gate_up^T rounded to bf16.
+ * A: device [M][K] bf16.  W_gate_up: device [2F][K] bf16, the F gate rows then
+ * the F up rows.  act: device [M][F] bf16.  Same modes, targets and size rules
+ * as bi_gemm (K, F multiples of 8; M = 0 or F = 0 is a no-op).
+ * Where the plain [M][2F] GEMM's plan is one CTA per tile with the whole K range
+ * (M <= 128 and no split), the SwiGLU runs in that GEMM's epilogue: each tile
+ * reads gate and up rows of the same outputs and the [M][2F] product never
+ * reaches memory.  Otherwise the call runs bi_gemm into the workspace and then
+ * bi_swiglu.  Both give the same bits, which are those of the two separate calls.
+ * workspace: device, >= bi_gemm_swiglu_workspace(M, F, K, mode) bytes, 16-byte
+ * aligned; it may be NULL when the fused plan applies (M <= 128 in INVARIANT). */
+size_t bi_gemm_swiglu_workspace(int64_t M, int64_t F, int64_t K, bi_mode mode);
+bi_status bi_gemm_swiglu(const void* A, const void* W_gate_up, void* act, int64_t M, int64_t F, int64_t K,
+                         bi_mode mode, int32_t target_row, int32_t target_count, void* workspace, size_t ws_bytes,
+                         bi_stream s);
+
 /* Per row, the k largest logits ordered by (value descending, index ascending):
  * ties go to the lowest index, so the result is unique [BlockLock "坑清单" 2, 5].
  * logits: device float [rows][V]; top_v: device float [rows][k]; top_i: device

@@ -43,7 +43,8 @@ EXPORTED = [
     "bi_gemm_f32a_workspace", "bi_gemm_f32a",
     "bi_decode_attention_workspace", "bi_decode_attention", "bi_decode_attention_noalloc",
     "bi_prefill_attention_workspace",
-    "bi_prefill_attention", "bi_embed", "bi_rope_table", "bi_qkv_rope_store", "bi_swiglu", "bi_topk",
+    "bi_prefill_attention", "bi_embed", "bi_rope_table", "bi_qkv_rope_store", "bi_swiglu", "bi_gemm_swiglu_workspace",
+    "bi_gemm_swiglu", "bi_topk",
     "bi_layer_workspace", "bi_layer_forward", "bi_model_workspace", "bi_model_forward",
     "bi_profile_start", "bi_profile_stop", "bi_profile_read", "bi_profile_kernel_name", "bi_profile_kernel_count",
 ]
@@ -126,6 +127,8 @@ def _declare(lib):
         "bi_rope_table": (c_i32, [c_d, c_i32, c_i32, vp, vp, vp]),
         "bi_qkv_rope_store": (c_i32, [vp, vp, vp, vp, vp, vp, c_i32, P(AttnDims), vp, vp, vp, vp]),
         "bi_swiglu": (c_i32, [vp, vp, c_i64, c_i64, vp]),
+        "bi_gemm_swiglu_workspace": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
+        "bi_gemm_swiglu": (c_i32, [vp, vp, vp, c_i64, c_i64, c_i64, c_i32, c_i32, c_i32, vp, c_sz, vp]),
         "bi_topk": (c_i32, [vp, c_i64, c_i64, c_i32, vp, vp, vp]),
         "bi_layer_workspace": (c_sz, [P(ModelDims), P(Batch), c_i32]),
         "bi_layer_forward": (c_i32, [P(ModelDims), P(LayerWeights), vp, vp, vp, P(Batch), vp, vp, c_i32, vp, c_sz,
@@ -340,6 +343,19 @@ def bi_swiglu(gu, out, stream=None):
     T, F2 = gu.shape
     _check(lib().bi_swiglu(_p(gu), _p(out), T, F2 // 2, _stream(stream)), "bi_swiglu")
     return out
+
+
+def bi_gemm_swiglu(A, W_gate_up, act, mode=INVARIANT, target_row=-1, target_count=0, workspace=None,
+                   stream=None):
+    """act [M][F] = SwiGLU of A [M][K] times W_gate_up [2F][K] (gate rows, then up rows), bf16."""
+    M, K = A.shape
+    F = W_gate_up.shape[0] // 2
+    m = _mode(mode)
+    need = lib().bi_gemm_swiglu_workspace(M, F, K, m)
+    ws, nb = _ws(need, A.device, workspace)
+    _check(lib().bi_gemm_swiglu(_p(A), _p(W_gate_up), _p(act), M, F, K, m, target_row, target_count, _p(ws), nb,
+                                _stream(stream)), "bi_gemm_swiglu")
+    return act
 
 
 def bi_topk(logits, k: int, top_v, top_i, stream=None):

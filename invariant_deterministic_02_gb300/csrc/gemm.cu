@@ -1711,6 +1711,8 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
                    weights_constant);
 }
 
+bi_status swiglu_impl(const void* gu, void* out, int64_t T, int64_t F, cudaStream_t s);  // pointwise.cu
+
 // Gate|up GEMM with SwiGLU in its epilogue: act[M][F] = swiglu(A Wgu^T) for Wgu
 // [2F][K] (gate rows then up rows).  Runs only where the plan of the plain
 // [M][2F] GEMM is one-SM tiles, one split, one unit per tile and a tile width
@@ -1719,7 +1721,8 @@ bi_status gemm_impl(const void* A, const void* Wt, void* C, const void* R, int64
 // SwiGLU kernel, bit for bit.  *used says whether it ran; when it is false
 // nothing was launched and the caller runs the two kernels.
 bi_status gemm_swiglu_impl(const void* A, const void* Wgu, void* act, int64_t M, int64_t F, int64_t K, bi_mode mode,
-                           int32_t target_row, int32_t target_count, cudaStream_t s, bool* used) {
+                           int32_t target_row, int32_t target_count, cudaStream_t s, bool* used,
+                           bool weights_constant) {
   *used = false;
   if (M <= 0 || F <= 0 || K < 8 || K % 8 != 0 || F % 8 != 0 || M > gemm::kBM || t_stall_wait_ns != 0) return BI_OK;
   if (!mode_valid(mode) || M >= (int64_t(1) << 31) || 2 * F >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
@@ -1749,7 +1752,7 @@ bi_status gemm_swiglu_impl(const void* A, const void* Wgu, void* act, int64_t M,
   args.tm0 = p.tm0;
   args.tm1 = p.tm1;
   args.seq = 1;
-  args.prefetch_w = 1;
+  args.prefetch_w = weights_constant ? 1 : 0;
   args.units = p.units;
   args.kb_total = p.kb_total;
   args.plane_rows = static_cast<int>(M);
@@ -1854,4 +1857,41 @@ extern "C" bi_status bi_gemm(const void* A, const void* W, void* C, const void* 
                              void* workspace, size_t ws_bytes, bi_stream s) {
   return bi::gemm_impl(A, W, C, residual, M, N, K, out_dtype, mode, target_row, target_count, workspace, ws_bytes,
                        reinterpret_cast<cudaStream_t>(s), false);
+}
+
+extern "C" size_t bi_gemm_swiglu_workspace(int64_t M, int64_t F, int64_t K, bi_mode mode) {
+  if (M <= 0 || F <= 0 || K <= 0) return 0;
+  return bi::align_up(static_cast<size_t>(M) * 2 * F * 2, 256) + bi::gemm_ws(M, 2 * F, K, mode);
+}
+
+extern "C" bi_status bi_gemm_swiglu(const void* A, const void* W_gate_up, void* act, int64_t M, int64_t F, int64_t K,
+                                    bi_mode mode, int32_t target_row, int32_t target_count, void* workspace,
+                                    size_t ws_bytes, bi_stream s) {
+  bi::clear_error();
+  BI_REQUIRE(M >= 0 && F >= 0 && K >= 8, BI_ERR_INVALID_ARG, "bi_gemm_swiglu: M=%lld F=%lld K=%lld",
+             static_cast<long long>(M), static_cast<long long>(F), static_cast<long long>(K));
+  BI_REQUIRE(K % 8 == 0 && F % 8 == 0, BI_ERR_UNSUPPORTED, "bi_gemm_swiglu: K (%lld) and F (%lld) must be multiples of 8",
+             static_cast<long long>(K), static_cast<long long>(F));
+  BI_REQUIRE(bi::mode_valid(mode), BI_ERR_INVALID_ARG, "bi_gemm_swiglu: mode %d", static_cast<int>(mode));
+  if (mode == BI_MODE_PROTECTED && target_row >= 0)
+    BI_REQUIRE(target_count >= 1 && target_row + static_cast<int64_t>(target_count) <= M, BI_ERR_INVALID_ARG,
+               "bi_gemm_swiglu: target rows [%d, %d) outside [0, %lld)", target_row, target_row + target_count,
+               static_cast<long long>(M));
+  if (M == 0 || F == 0) return BI_OK;
+  BI_REQUIRE(A && W_gate_up && act, BI_ERR_INVALID_ARG, "bi_gemm_swiglu: null pointer");
+  BI_REQUIRE(bi::aligned16(A) && bi::aligned16(W_gate_up) && bi::aligned16(act), BI_ERR_INVALID_ARG,
+             "bi_gemm_swiglu: pointers must be 16-byte aligned");
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  bool used = false;
+  BI_TRY(bi::gemm_swiglu_impl(A, W_gate_up, act, M, F, K, mode, target_row, target_count, st, &used, false));
+  if (used) return BI_OK;
+  const size_t gu_bytes = bi::align_up(static_cast<size_t>(M) * 2 * F * 2, 256);
+  const size_t need = bi_gemm_swiglu_workspace(M, F, K, mode);
+  BI_REQUIRE(workspace != nullptr && bi::aligned16(workspace) && ws_bytes >= need, BI_ERR_WORKSPACE,
+             "bi_gemm_swiglu: workspace %zu < %zu bytes", ws_bytes, need);
+  void* gu = workspace;
+  void* sub = static_cast<char*>(workspace) + gu_bytes;
+  BI_TRY(bi::gemm_impl(A, W_gate_up, gu, nullptr, M, 2 * F, K, BI_BF16, mode, target_row, target_count,
+                       ws_bytes > gu_bytes ? sub : nullptr, ws_bytes - gu_bytes, st, false));
+  return bi::swiglu_impl(gu, act, M, F, st);
 }

@@ -42,7 +42,7 @@ bi_status qkv_rope_store_impl(const void*, const float*, const float*, const int
                               const void* q_norm, const void* k_norm, float eps, bool act_f32, int max_pos);
 bi_status swiglu_impl(const void*, void*, int64_t, int64_t, cudaStream_t);
 bi_status gemm_swiglu_impl(const void*, const void*, void*, int64_t, int64_t, int64_t, bi_mode, int32_t, int32_t,
-                           cudaStream_t, bool*);
+                           cudaStream_t, bool*, bool);
 bi_status swiglu_planes_impl(const void*, void*, int64_t, int64_t, cudaStream_t);
 bi_status embed_impl(const int32_t*, const void*, void*, int64_t, int64_t, int64_t, cudaStream_t);
 bi_status embed_f32_impl(const int32_t*, const void*, void*, int64_t, int64_t, int64_t, cudaStream_t);
@@ -272,7 +272,7 @@ bi_status layer_body(const bi_model_dims* dm, const bi_layer_weights* w, const f
   BI_TRY(gemm_impl(L.att, w->w_o, hidden, hidden, T, d, hq, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s, true));
   BI_TRY(rmsnorm_impl(hidden, w->ffn_norm, L.x, T, d, BI_BF16, dm->rms_eps, mode, trow, tcnt, L.sub, L.sub_bytes, s));
   bool fused = false;
-  BI_TRY(gemm_swiglu_impl(L.x, w->w_gate_up, L.act, T, F, d, mode, trow, tcnt, s, &fused));
+  BI_TRY(gemm_swiglu_impl(L.x, w->w_gate_up, L.act, T, F, d, mode, trow, tcnt, s, &fused, true));
   if (!fused) {
     BI_TRY(gemm_impl(L.x, w->w_gate_up, L.gu, nullptr, T, 2 * F, d, BI_BF16, mode, trow, tcnt, L.sub, L.sub_bytes, s,
                      true));
