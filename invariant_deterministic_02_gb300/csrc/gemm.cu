@@ -1490,17 +1490,19 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, bi_mode mode, int64_t tb, int64_
     p.units = static_cast<int>(((M + 255) / 256) * p.n_tiles);
     return p;
   }
-  // Each copy costs the copy engine a roughly fixed time, so at decode sizes a
-  // stage spans several k-blocks (one 3D box of 32 KiB of weights per copy at
-  // up to 8 k-blocks; measured on GB300, 64x4096x{4096,12288}: 8 k-blocks per
-  // stage in two stages beat 4 k-blocks in four by 9-12%).  (A 3D copy costs
-  // more than a 2D box of the same bytes, so the 3D view is used only when a
-  // copy spans several k-blocks.)
+  // Each stage costs the copy engine and the barrier round trip a roughly fixed
+  // time, so at decode sizes a stage spans several k-blocks (one 3D box per
+  // operand, up to 8 k-blocks), but it also waits for its whole stage before the
+  // MMAs start, so the ring keeps at least three stages.  Measured on GB300,
+  // 64x4096x12288: 4 k-blocks x 4 stages (48 KiB each) 31.0 us against 8 x 2
+  // (96 KiB) 33.7 us; 1x4096x12288: 8 x 4 (48 KiB) 27.0 us against 4 x 8 31.0 us
+  // and 2 k-blocks per stage 42 us at either size.  (A 3D copy costs more than a
+  // 2D box of the same bytes, so the 3D view is used only when a copy spans
+  // several k-blocks.)
   p.kbs = (K % kBK == 0 && M <= kBM) ? std::min(8, std::max(1, 256 / p.TN)) : 1;
   const int budget = kSmemLimit - 1024 - kBarBlock - (p.a_rows < kBM ? kOverreadSlack : 0);
-  // at least two stages in flight; fp32 A triples the A part of a stage: keep three there
   const int kblock_bytes = (planes * p.a_rows + p.TN) * kBK * 2;
-  const int min_stages = planes > 1 ? 3 : 2;
+  const int min_stages = 3;
   while (p.kbs > 1 && budget / (p.kbs * kblock_bytes) < min_stages) p.kbs /= 2;
   p.map3d = p.kbs > 1 ? 1 : 0;
   p.stage_bytes = p.kbs * kblock_bytes;
