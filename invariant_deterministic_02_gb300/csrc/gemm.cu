@@ -59,7 +59,11 @@ constexpr int kBK = 64;         // k-tile (128 bytes of bf16: one swizzle row)
 constexpr int kUK = 16;         // instruction K
 constexpr int kProducerWarps = 1;
 constexpr int kMmaWarp = kProducerWarps;
-constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
+constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;  // SM-pair kernel
+// one-SM kernel: two epilogue warps per tensor-memory lane quarter, each taking
+// half of a tile's columns (or half of each SwiGLU chunk's outputs)
+constexpr int kEpiWarpsTc = 8;
+constexpr int kThreadsTc = (kProducerWarps + 1 + kEpiWarpsTc) * 32;
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kSmemLimit = 227 * 1024;     // dynamic shared memory per CTA
 constexpr int kMaxStages = 16;
@@ -324,7 +328,7 @@ __host__ __device__ constexpr size_t smem_bytes(int stages, int stage_bytes, int
 // PL: planes of A (1: bf16 A; 3: fp32 A as three bf16 planes).  A compile-time
 // count keeps the one-plane kernel free of the plane loops on its latency path.
 template <int TN, int PL>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+__global__ void __launch_bounds__(kThreadsTc, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                               const __grid_constant__ CUtensorMap tmW, const Args a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -359,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull0 + 8 * i, 1);
-      mbar_init(tempty0 + 8 * i, 4);
+      mbar_init(tempty0 + 8 * i, kEpiWarpsTc);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -572,8 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (4 warps)
-    // Thread = one accumulator row (tensor-memory lane), 32 columns per load.
+    // ------------------------------------------------------------ epilogue (8 warps)
+    // Thread = one accumulator row (tensor-memory lane), 32 columns per load;
+    // the two warps of a lane quarter take alternate 32-column chunks.
     // Merged units: partial q is added into a running sum kept in a third
     // tensor-memory buffer, sum = ((0 + P0) + P1) + ..., rounded once at the end;
     // the second-pass reduction of split units adds the same partials in the
@@ -581,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     // With M = 64 instructions the accumulator holds 16 rows per lane quarter
     // (lanes 32 w .. 32 w + 15); the warp's other lanes load and store nothing.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int half = (warp - kProducerWarps - 1) >> 2;  // 0 or 1: which of the quarter's two warps
     const bool lane_live = !a.m64 || lane < 16;
     const int row_in_tile = a.m64 ? quarter * 16 + lane : quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -605,9 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if constexpr (TN % 64 == 0) {
           if (a.swiglu) {
             // gate chunk ch and up chunk ch of the tile give 32 outputs of a row: each accumulator value is
-            // rounded to bf16 as the plain GEMM stores it, then the SwiGLU kernel's own function.  With M = 64
-            // instructions the warp's 16 rows sit in lanes 0..15, so lanes 16..31 take the upper 16 columns
-            // of the row of lane - 16 (shuffled over) and every lane computes 16 outputs.
+            // rounded to bf16 as the plain GEMM stores it, then the SwiGLU kernel's own function.  Both warps
+            // of the lane quarter load the chunk pair and each computes half of the outputs.  With M = 64
+            // instructions the quarter's 16 rows sit in lanes 0..15, so lanes 16..31 take the upper 16 columns
+            // of the row of lane - 16 (shuffled over): every lane computes 8 outputs per chunk.
 #pragma unroll 1
             for (int ch = 0; ch < TN / 64; ++ch) {
               uint32_t g[32], v[32];
@@ -615,44 +622,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
               tc_ld32(tbase + TN / 2 + ch * 32, v);
               const int col0 = nt * (TN / 2) + ch * 32;
               if (a.m64) {
+                // this warp's 8 of the lane's 16 outputs: columns 8 half .. 8 half + 7 of its 16
                 const int src = lane & 15;
                 const bool upper = lane >= 16;
-                float o[16];
+                float o[8];
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                  const uint32_t g0 = __shfl_sync(0xffffffffu, g[16 + e], src);
-                  const uint32_t g1 = __shfl_sync(0xffffffffu, g[17 + e], src);
-                  const uint32_t v0 = __shfl_sync(0xffffffffu, v[16 + e], src);
-                  const uint32_t v1 = __shfl_sync(0xffffffffu, v[17 + e], src);
-                  const uint32_t gp = pack_bf16x2(__uint_as_float(upper ? g0 : g[e]), __uint_as_float(upper ? g1 : g[e + 1]));
-                  const uint32_t up = pack_bf16x2(__uint_as_float(upper ? v0 : v[e]), __uint_as_float(upper ? v1 : v[e + 1]));
+                for (int e = 0; e < 8; e += 2) {
+                  // register indices stay compile-time: pick between the two halves' values
+                  const uint32_t ga = half ? g[8 + e] : g[e], gb = half ? g[9 + e] : g[e + 1];
+                  const uint32_t va = half ? v[8 + e] : v[e], vb = half ? v[9 + e] : v[e + 1];
+                  const uint32_t gA = half ? g[24 + e] : g[16 + e], gB = half ? g[25 + e] : g[17 + e];
+                  const uint32_t vA = half ? v[24 + e] : v[16 + e], vB = half ? v[25 + e] : v[17 + e];
+                  const uint32_t g0 = __shfl_sync(0xffffffffu, gA, src);
+                  const uint32_t g1 = __shfl_sync(0xffffffffu, gB, src);
+                  const uint32_t v0 = __shfl_sync(0xffffffffu, vA, src);
+                  const uint32_t v1 = __shfl_sync(0xffffffffu, vB, src);
+                  const uint32_t gp = pack_bf16x2(__uint_as_float(upper ? g0 : ga), __uint_as_float(upper ? g1 : gb));
+                  const uint32_t up = pack_bf16x2(__uint_as_float(upper ? v0 : va), __uint_as_float(upper ? v1 : vb));
                   o[e] = swiglu1(bf16_lo(gp), bf16_lo(up));
                   o[e + 1] = swiglu1(bf16_hi(gp), bf16_hi(up));
                 }
                 const int orow = mt * kBM + quarter * 16 + src;
-                const int c0 = col0 + (upper ? 16 : 0);
-                if (orow < a.M) {
-                  __nv_bfloat16* dst = a.act + static_cast<size_t>(orow) * a.F + c0;
-#pragma unroll
-                  for (int h = 0; h < 2; ++h) {
-                    if (c0 + 8 * h >= a.F) break;
-                    float o8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o8[e] = o[8 * h + e];
-                    *reinterpret_cast<uint4*>(dst + 8 * h) = pack8(o8);
-                  }
-                }
+                const int c0 = col0 + (upper ? 16 : 0) + 8 * half;
+                if (orow < a.M && c0 < a.F)
+                  *reinterpret_cast<uint4*>(a.act + static_cast<size_t>(orow) * a.F + c0) = pack8(o);
               } else {
                 if (!row_ok || col0 >= a.F) continue;
                 __nv_bfloat16* dst = a.act + static_cast<size_t>(row) * a.F + col0;
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
+                for (int h = 0; h < 2; ++h) {
+                  const int q8 = 2 * half + h;
                   if (col0 + 8 * q8 >= a.F) break;
                   float o[8];
 #pragma unroll
                   for (int e = 0; e < 8; e += 2) {
-                    const uint32_t gp = pack_bf16x2(__uint_as_float(g[8 * q8 + e]), __uint_as_float(g[8 * q8 + e + 1]));
-                    const uint32_t up = pack_bf16x2(__uint_as_float(v[8 * q8 + e]), __uint_as_float(v[8 * q8 + e + 1]));
+                    const int i0 = 8 * h + e;  // compile-time; the other half's values sit 16 further on
+                    const uint32_t gp = pack_bf16x2(__uint_as_float(half ? g[16 + i0] : g[i0]),
+                                                    __uint_as_float(half ? g[17 + i0] : g[i0 + 1]));
+                    const uint32_t up = pack_bf16x2(__uint_as_float(half ? v[16 + i0] : v[i0]),
+                                                    __uint_as_float(half ? v[17 + i0] : v[i0 + 1]));
                     o[e] = swiglu1(bf16_lo(gp), bf16_lo(up));
                     o[e + 1] = swiglu1(bf16_hi(gp), bf16_hi(up));
                   }
@@ -671,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
         }
 #pragma unroll 1
-        for (int ch = 0; ch < TN / 32; ++ch) {
+        for (int ch = half; ch < TN / 32; ch += 2) {
           uint32_t r[32];
           tc_ld32(tbase + ch * 32, r);
           if (seq > 1) {
@@ -1537,7 +1545,7 @@ bi_status launch_w(const CUtensorMap& ma, const CUtensorMap& mw, const Args& arg
   BI_CUDA_TRY(ensure_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<TN, PL>), kSmemLimit));
   const size_t smem = smem_bytes(args.stages, args.stage_bytes, args.a_rows);
   const int grid = std::min(args.units, num_sms());
-  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<TN, PL>, dim3(grid), dim3(kThreads), smem, s, ma, mw, args)));
+  BI_TIMED(::bi::kTagGemm, s, BI_PDL_CHECK(launch_pdl(gemm_tc_kernel<TN, PL>, dim3(grid), dim3(kThreadsTc), smem, s, ma, mw, args)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
