@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
   __shared__ float sv[kTopkWarps][32];
   __shared__ int si[kTopkWarps][32];
   __shared__ unsigned long long s_filter;  // the best k-th entry any warp has published (a key)
+  __shared__ float s_wmax[kTopkWarps];     // each warp's maximum over its first step
   if (threadIdx.x == 0) s_filter = 0ull;
   pdl_wait();
   pdl_trigger();
@@ -119,18 +120,28 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
   const int64_t s0 = min(V, warp * per), s1 = min(V, s0 + per);
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
   int64_t e = s0;
-  if (vec && e + kStep <= s1) {
-    float4 cur[kU], nxt[kU];
+  const bool vec_run = vec && e + kStep <= s1;  // warp-uniform
+  float4 cur[kU], nxt[kU];
+  {
+    // First filter, from the first step's elements (NaNs are never kept): the k-th largest of the warp's
+    // 32 lane maxima, and the k-th largest of the CTA's 32 warp maxima.  Each is the k-th largest of
+    // maxima of disjoint groups, so at least k elements of the row reach it; the second is the much
+    // tighter one (a maximum of 256 elements), so few elements get past it before the lists fill.
+    float m = -INFINITY;
+    if (vec_run) {
 #pragma unroll
-    for (int u = 0; u < kU; ++u) cur[u] = ld_stream_f4(x + e + 128 * u + 4 * lane);
-    {
-      // first filter: the k-th largest lane maximum of the first step (NaNs are never kept)
-      float m = -INFINITY;
+      for (int u = 0; u < kU; ++u) cur[u] = ld_stream_f4(x + e + 128 * u + 4 * lane);
 #pragma unroll
       for (int u = 0; u < kU; ++u) m = fmaxf(m, fmaxf(fmaxf(cur[u].x, cur[u].y), fmaxf(cur[u].z, cur[u].w)));
-      const float t = __shfl_sync(0xffffffffu, warp_sort_desc(m == m ? m : -INFINITY, lane), k - 1);
-      filter = entry_key(t, INT_MAX);
     }
+    const float sorted = warp_sort_desc(m == m ? m : -INFINITY, lane);
+    const float tw = __shfl_sync(0xffffffffu, sorted, k - 1);
+    if (lane == 0) s_wmax[warp] = sorted;  // lane 0 holds the largest after the descending sort
+    __syncthreads();
+    const float tc = __shfl_sync(0xffffffffu, warp_sort_desc(s_wmax[lane], lane), k - 1);
+    filter = entry_key(fmaxf(tw, tc), INT_MAX);
+  }
+  if (vec_run) {
     for (;;) {
       const int64_t en = e + kStep;
       const bool more = en + kStep <= s1;
