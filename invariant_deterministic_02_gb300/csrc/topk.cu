@@ -7,7 +7,8 @@
 // descending, index ascending): a total order, so the selected set and its
 // order are unique and do not depend on how the scan is parallelised.
 //
-// One CTA of 32 warps per row.  Each warp scans a contiguous segment of the row
+// A cluster of four CTAs of 16 warps per row (the row's 64 warps on up to four
+// SMs, whose load capacity they share).  Each warp scans a contiguous segment of the row
 // (8 consecutive elements per lane per step as two 16-byte loads, the next
 // step's loads issued before the current step is examined) and keeps its best k
 // in a sorted list spread over its lanes (lane j holds entry j).  Elements are
@@ -18,16 +19,22 @@
 // lanes' maxima over the first step (k distinct elements reach it).  An element
 // that fails the filter cannot be among the row's k best, so skipping it changes
 // nothing, and almost every step is two loads, eight compares and one vote.
-// The 32 warp lists are then folded pairwise in five rounds (16, 8, 4, 2, 1
-// warps), each warp offering its partner's list to its own.
+// The 16 warp lists of a CTA are then folded pairwise in four rounds (8, 4, 2,
+// 1 warps), each warp offering its partner's list to its own, and the first CTA
+// of the cluster offers the other three CTAs' lists (read from their shared
+// memory) to its own.  The selected set and its order are unique under the
+// total order, so how the row is cut up does not change the result.
 #include <climits>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 
 namespace bi {
 namespace {
 
-constexpr int kTopkWarps = 32;
+constexpr int kTopkWarps = 16;
+constexpr int kTopkCtas = 4;  // CTAs (one cluster) per row
 
 __device__ __forceinline__ float4 ld_stream_f4(const float* p) {
   const uint4 u = ld_stream(p);
@@ -95,50 +102,67 @@ __device__ __forceinline__ void warp_offer(float& lv, int& li, float& tv, int& t
   }
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits, int64_t V, int k,
-                                                               float* __restrict__ top_v, int32_t* __restrict__ top_i,
-                                                               int32_t* __restrict__ greedy) {
+__global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkWarps * 32)
+    topk_kernel(const float* __restrict__ logits, int64_t V, int k, float* __restrict__ top_v,
+                int32_t* __restrict__ top_i, int32_t* __restrict__ greedy) {
   constexpr int kU = 2;               // 16-byte loads per lane per step
   constexpr int kStep = kU * 4 * 32;  // elements per warp step
+  static_assert(kU * kTopkWarps == 32, "one first-step group maximum per lane of the sorting warp");
   __shared__ float sv[kTopkWarps][32];
   __shared__ int si[kTopkWarps][32];
   __shared__ unsigned long long s_filter;  // the best k-th entry any warp has published (a key)
-  __shared__ float s_wmax[kTopkWarps];     // each warp's maximum over its first step
+  __shared__ float s_gmax[kU * kTopkWarps];  // maxima of the 128-element groups of every warp's first step
   if (threadIdx.x == 0) s_filter = 0ull;
   pdl_wait();
   pdl_trigger();
   __syncthreads();
-  const int64_t row = blockIdx.x;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int part = static_cast<int>(cluster.block_rank());
+  const int64_t row = blockIdx.x / kTopkCtas;
   const float* x = logits + row * V;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   float lv = -INFINITY, tv = -INFINITY;
   int li = INT_MAX, ti = INT_MAX;
   unsigned long long filter = 0ull, published = 0ull;
-  // segment of this warp: a multiple of kStep elements
-  const int64_t per = ((V + kTopkWarps - 1) / kTopkWarps + kStep - 1) / kStep * kStep;
-  const int64_t s0 = min(V, warp * per), s1 = min(V, s0 + per);
+  // segment of this warp (warp `part * 16 + warp` of the row's 64): a multiple of kStep elements
+  constexpr int kRowWarps = kTopkWarps * kTopkCtas;
+  const int64_t per = ((V + kRowWarps - 1) / kRowWarps + kStep - 1) / kStep * kStep;
+  const int64_t s0 = min(V, (part * kTopkWarps + warp) * per), s1 = min(V, s0 + per);
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
   int64_t e = s0;
   const bool vec_run = vec && e + kStep <= s1;  // warp-uniform
   float4 cur[kU], nxt[kU];
   {
     // First filter, from the first step's elements (NaNs are never kept): the k-th largest of the warp's
-    // 32 lane maxima, and the k-th largest of the CTA's 32 warp maxima.  Each is the k-th largest of
-    // maxima of disjoint groups, so at least k elements of the row reach it; the second is the much
-    // tighter one (a maximum of 256 elements), so few elements get past it before the lists fill.
-    float m = -INFINITY;
+    // 32 lane maxima, and the k-th largest of the CTA's 32 group maxima (each warp's first step is two
+    // groups of 128 consecutive elements, one per 16-byte load of its lanes).  Each is the k-th largest
+    // of maxima of disjoint groups, so at least k elements of the row reach it; the second is the much
+    // tighter one, so few elements get past it before the lists fill.
+    float m = -INFINITY, gm[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) gm[u] = -INFINITY;
     if (vec_run) {
 #pragma unroll
       for (int u = 0; u < kU; ++u) cur[u] = ld_stream_f4(x + e + 128 * u + 4 * lane);
 #pragma unroll
-      for (int u = 0; u < kU; ++u) m = fmaxf(m, fmaxf(fmaxf(cur[u].x, cur[u].y), fmaxf(cur[u].z, cur[u].w)));
+      for (int u = 0; u < kU; ++u) {
+        const float mu = fmaxf(fmaxf(cur[u].x, cur[u].y), fmaxf(cur[u].z, cur[u].w));
+        gm[u] = mu == mu ? mu : -INFINITY;
+        m = fmaxf(m, mu);
+      }
     }
-    const float sorted = warp_sort_desc(m == m ? m : -INFINITY, lane);
-    const float tw = __shfl_sync(0xffffffffu, sorted, k - 1);
-    if (lane == 0) s_wmax[warp] = sorted;  // lane 0 holds the largest after the descending sort
+    const float tw = __shfl_sync(0xffffffffu, warp_sort_desc(m == m ? m : -INFINITY, lane), k - 1);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      float g = gm[u];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, o));
+      if (lane == 0) s_gmax[kU * warp + u] = g;
+    }
     __syncthreads();
-    const float tc = __shfl_sync(0xffffffffu, warp_sort_desc(s_wmax[lane], lane), k - 1);
+    const float tc = __shfl_sync(0xffffffffu, warp_sort_desc(s_gmax[lane], lane), k - 1);
     filter = entry_key(fmaxf(tw, tc), INT_MAX);
   }
   if (vec_run) {
@@ -203,26 +227,37 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
     }
     __syncthreads();
   }
-  if (warp == 0) {
+  // every CTA's list is in its shared memory (sv[0], si[0]); the first CTA takes the others' in
+  cluster.sync();
+  if (part == 0 && warp == 0) {
+    for (int r = 1; r < kTopkCtas; ++r) {
+      const float* rv = cluster.map_shared_rank(&sv[0][0], r);
+      const int* ri = cluster.map_shared_rank(&si[0][0], r);
+      const float cv = lane < k ? rv[lane] : -INFINITY;
+      const int ci = lane < k ? ri[lane] : INT_MAX;
+      warp_offer(lv, li, tv, ti, cv, ci, lane, k);
+    }
     if (lane < k) {
       top_v[row * k + lane] = lv;
       top_i[row * k + lane] = li;
     }
     if (greedy != nullptr && lane == 0) greedy[row] = li;
   }
+  // no CTA leaves (and frees its shared memory) before the first one has read it
+  cluster.sync();
 }
 
 }  // namespace
 
 bi_status topk_impl(const float* logits, int64_t rows, int64_t V, int32_t k, float* tv, int32_t* ti,
                     int32_t* greedy, cudaStream_t s) {
-  BI_REQUIRE(rows >= 0 && V >= 1 && V < INT_MAX, BI_ERR_INVALID_ARG, "bi_topk: rows=%lld V=%lld",
-             static_cast<long long>(rows), static_cast<long long>(V));
+  BI_REQUIRE(rows >= 0 && rows <= INT_MAX / kTopkCtas && V >= 1 && V < INT_MAX, BI_ERR_INVALID_ARG,
+             "bi_topk: rows=%lld V=%lld", static_cast<long long>(rows), static_cast<long long>(V));
   BI_REQUIRE(k >= 1 && k <= BI_TOPK_MAX && k <= V, BI_ERR_UNSUPPORTED, "bi_topk: k=%d (1..%d, <= V)", k, BI_TOPK_MAX);
   if (rows == 0) return BI_OK;
   BI_REQUIRE(logits && tv && ti, BI_ERR_INVALID_ARG, "bi_topk: null pointer");
   BI_TIMED(::bi::kTagTopk, s,
-           BI_PDL_CHECK(launch_pdl(topk_kernel, dim3(static_cast<unsigned>(rows)), dim3(kTopkWarps * 32), 0, s, logits, V, k, tv, ti, greedy)));
+           BI_PDL_CHECK(launch_pdl(topk_kernel, dim3(static_cast<unsigned>(rows * kTopkCtas)), dim3(kTopkWarps * 32), 0, s, logits, V, k, tv, ti, greedy)));
   BI_LAUNCH_CHECK();
   return BI_OK;
 }
