@@ -712,11 +712,22 @@ struct DecodeSmem {
 // One TMA tensor copy of a page of one kv head: box {64 dims, 16 positions, HD/64
 // halves} of the cache viewed as [pages * kv heads][16][HD/64][64], landing as
 // [half][position][64 dims] with the 128-byte swizzle.
+// A page of keys or values is read once per pass, so its copies carry an L2
+// evict-first hint: the cache stream does not push out of L2 what is reused
+// soon after (the split states that the merge kernel reads back, the
+// activations between the layer's kernels).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void tma_page(uint32_t dst, const CUtensorMap* map, uint32_t bar, int page_head) {
+  const uint64_t pol = l2_evict_first_policy();
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
-      "[%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(0), "r"(0), "r"(page_head)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(0), "r"(0), "r"(page_head), "l"(pol)
       : "memory");
 }
 
