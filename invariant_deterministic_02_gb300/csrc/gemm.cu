@@ -201,6 +201,42 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Weight copies of a GEMM with one row tile read every weight byte once per
+// pass: they carry an L2 evict-first cache policy, so the weight stream does not
+// push out of L2 the activations that the next kernels read.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z, int w, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -387,14 +423,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) gemm_tc_kernel(const __grid_con
   // needed) and only then waits, so weight latency overlaps the previous kernel.
   // B part of a stage: the tile's TN weight rows (for the SwiGLU GEMM TN/2 gate
   // rows then the TN/2 up rows of the same outputs, one box of a row-pair map)
+  // (one row tile: every weight byte is read once, see l2_evict_first_policy)
+  const bool w_once = a.m_tiles == 1;
+  const uint64_t w_pol = l2_evict_first_policy();
   auto load_w = [&](uint32_t dst, uint32_t bar, int nt, int kb) {
     if (a.swiglu) {
-      if (a.map3d) tma_load_4d(dst, &tmW, bar, 0, nt * (TN / 2), 0, kb);
-      else tma_load_3d(dst, &tmW, bar, kb * kBK, nt * (TN / 2), 0);
+      if (a.map3d) tma_load_4d_hint(dst, &tmW, bar, 0, nt * (TN / 2), 0, kb, w_pol);
+      else tma_load_3d_hint(dst, &tmW, bar, kb * kBK, nt * (TN / 2), 0, w_pol);
     } else if (a.map3d) {
-      tma_load_3d(dst, &tmW, bar, 0, nt * TN, kb);
+      if (w_once) tma_load_3d_hint(dst, &tmW, bar, 0, nt * TN, kb, w_pol);
+      else tma_load_3d(dst, &tmW, bar, 0, nt * TN, kb);
     } else {
-      tma_load_2d(dst, &tmW, bar, kb * kBK, nt * TN);
+      if (w_once) tma_load_2d_hint(dst, &tmW, bar, kb * kBK, nt * TN, w_pol);
+      else tma_load_2d(dst, &tmW, bar, kb * kBK, nt * TN);
     }
   };
   int pre_stages = 0;  // stages whose W copy (and transaction count) was issued early
