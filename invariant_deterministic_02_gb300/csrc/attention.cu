@@ -996,8 +996,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 3) decode_split_kernel(
 // Merge of the split states of each (request, query head) in a second kernel.
 __global__ void decode_merge_kernel(const Partials part, DecodePlan plan, ActDst out, int B, int hq, int hkv,
                                     int hd) {
-  pdl_wait();
+  // The next kernel (the O projection) may launch at once: its CTAs then take
+  // the SMs that the split kernel's last CTAs free and fetch their first weight
+  // stages while this merge still waits; its own wait still covers this kernel.
   pdl_trigger();
+  pdl_wait();
   // the split kernel has finished: its work counter starts from zero for the next launch
   if (blockIdx.x == 0 && threadIdx.x == 0) *plan.counter = 0;
   const int b = blockIdx.x / hkv;
