@@ -20,9 +20,9 @@
 // that fails the filter cannot be among the row's k best, so skipping it changes
 // nothing, and almost every step is two loads, eight compares and one vote.
 // The 16 warp lists of a CTA are then folded pairwise in four rounds (8, 4, 2,
-// 1 warps), each warp offering its partner's list to its own, and the first CTA
-// of the cluster offers the other three CTAs' lists (read from their shared
-// memory) to its own.  The selected set and its order are unique under the
+// 1 warps), each warp merging its partner's list into its own with a bitonic
+// merge, and the first CTA of the cluster merges the other three CTAs' lists
+// (read from their shared memory) into its own.  The selected set and its order are unique under the
 // total order, so how the row is cut up does not change the result.
 #include <climits>
 
@@ -98,6 +98,30 @@ __device__ __forceinline__ void warp_offer(float& lv, int& li, float& tv, int& t
       warp_insert(lv, li, v, i, lane, k);
       tv = __shfl_sync(0xffffffffu, lv, k - 1);
       ti = __shfl_sync(0xffffffffu, li, k - 1);
+    }
+  }
+}
+
+// Merge of two lists of 32 entries, each sorted best first (lane j holds entry
+// j; unused entries are (-inf, INT_MAX), worse than any element), keeping the
+// 32 best in order: the better of own[j] and other[31 - j] form a bitonic
+// sequence holding the 32 best of both, which five half-cleaner stages of a
+// bitonic network sort.  `better` is a total order, so the result is unique.
+__device__ __forceinline__ void warp_merge32(float& lv, int& li, float rv, int ri, int lane) {
+  // rv, ri: the other list's entry 31 - lane
+  if (better(rv, ri, lv, li)) {
+    lv = rv;
+    li = ri;
+  }
+#pragma unroll
+  for (int stride = 16; stride >= 1; stride >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, lv, stride);
+    const int oi = __shfl_xor_sync(0xffffffffu, li, stride);
+    const bool keep_better = (lane & stride) == 0;  // the lower lane of the pair takes the better entry
+    const bool other_better = better(ov, oi, lv, li);
+    if (keep_better == other_better) {
+      lv = ov;
+      li = oi;
     }
   }
 }
@@ -216,12 +240,11 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkWarps *
   sv[warp][lane] = lv;
   si[warp][lane] = li;
   __syncthreads();
-  // pairwise folds: in the round of h warps, warp w < h takes list w + h into its own
+  // pairwise folds: in the round of h warps, warp w < h merges list w + h into its own
+  // (lists hold their k entries in lanes < k and (-inf, INT_MAX) or worse entries after them)
   for (int h = kTopkWarps / 2; h >= 1; h >>= 1) {
     if (warp < h) {
-      const float cv = lane < k ? sv[warp + h][lane] : -INFINITY;
-      const int ci = lane < k ? si[warp + h][lane] : INT_MAX;
-      warp_offer(lv, li, tv, ti, cv, ci, lane, k);
+      warp_merge32(lv, li, sv[warp + h][31 - lane], si[warp + h][31 - lane], lane);
       sv[warp][lane] = lv;
       si[warp][lane] = li;
     }
@@ -233,9 +256,7 @@ __global__ void __cluster_dims__(kTopkCtas, 1, 1) __launch_bounds__(kTopkWarps *
     for (int r = 1; r < kTopkCtas; ++r) {
       const float* rv = cluster.map_shared_rank(&sv[0][0], r);
       const int* ri = cluster.map_shared_rank(&si[0][0], r);
-      const float cv = lane < k ? rv[lane] : -INFINITY;
-      const int ci = lane < k ? ri[lane] : INT_MAX;
-      warp_offer(lv, li, tv, ti, cv, ci, lane, k);
+      warp_merge32(lv, li, rv[31 - lane], ri[31 - lane], lane);
     }
     if (lane < k) {
       top_v[row * k + lane] = lv;
